@@ -1,0 +1,394 @@
+/*
+ * oracle.c -- plain CPU oracle for DGQ KV-cache compression and INT8 paged decode
+ * attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline load this library; the product path (libdgq.so) never does, and this file
+ * shares no code, header, table or constant with it.  It is deliberately slow and
+ * single-threaded: every step is written out in the order the sources give it, one
+ * IEEE-754 operation at a time, so that it can be checked against them by eye.
+ * Build flags: -O2 -ffp-contract=off (no FMA contraction; no fast-math).
+ *
+ * Sources (cited by title and section):
+ *   [DGQ]   "DeepSeek KV-cache dynamic group quantisation (DGQ)" article, pptc.cn news 101026
+ *           §2.2  per-head variance curve along L, 16-token windows, jump detection,
+ *                 3-5 segments, independent min/max INT8 per segment, segment ids
+ *           §3.2  length-aware n_groups rule inside compress()
+ *           §3.3  storage formula (INT8 body + per-token segment marker)
+ *   [PAGED] "DeepSeek-V4 high-concurrency KV-cache bottleneck" article (deepseek.csdn.net),
+ *           "PagedAttention implementation" section: logical blocks mapped to scattered
+ *           physical blocks through a block table.
+ *   Where the articles leave a step open, the readings below are the plainest ones the
+ *   rest supports; each is marked READING.
+ *
+ * Parity pins (tests/test_oracle_*.py check this file against them):
+ *   n_groups       closed-form table of the [DGQ] §3.2 rule at its edges
+ *   variance       fp64 variance within the fp32 error bound; constant rows -> 0
+ *   window means   fp64 mean within bound; exact for partial windows of equal values
+ *   boundaries     planted variance steps recovered exactly; brute force over all
+ *                  k-subsets of windows on tiny inputs
+ *   seg min/max    brute-force numpy min/max over each segment slice
+ *   codes          min -> 0, max -> 255, |dequant - x| <= scale/2 (+fp32 slack),
+ *                  monotone in x; one segment == textbook per-tensor asymmetric uint8
+ *   paging         gather through the block table reproduces the unpaged codes;
+ *                  bytes written == 1 B/element + one 128-byte record per (request, head)
+ *   attention      numpy fp64 brute force; two-key closed form; uniform average for
+ *                  equal keys; invariance under any permutation of physical blocks
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_D 128        /* head dimension handled here */
+#define OR_WIN 16       /* window length, [DGQ] §2.2 "win_size=16" */
+#define OR_MAX_SEG 5    /* at most five segments, [DGQ] §2.2 / §3.2 */
+
+/* One segment record per (request, KV head): 128 bytes. */
+typedef struct {
+    int32_t n_seg;               /* number of segments (0 only when seq_len == 0) */
+    int32_t seq_len;             /* tokens compressed */
+    int32_t start[OR_MAX_SEG];   /* first token of each segment; unused entries = seq_len */
+    float k_min[OR_MAX_SEG];
+    float k_scale[OR_MAX_SEG];
+    float v_min[OR_MAX_SEG];
+    float v_scale[OR_MAX_SEG];
+    int32_t pad[OR_MAX_SEG];
+} oracle_seg;
+
+static float bf16_to_float(uint16_t h)
+{
+    uint32_t b = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+/* ---------------------------------------------------------------------------------
+ * a1. n_groups, [DGQ] §3.2 compress(): "if seq_len < 2048: 2; elif < 16384: 3; else
+ * min(5, int(log2(seq_len / 1024)) + 2)".  The extracted text lost the comparison
+ * operators; READING: strict "<" as the thresholds 2048 / 16384 suggest, int() = floor
+ * (the argument is >= 16 there, so truncation and floor agree).
+ * -------------------------------------------------------------------------------*/
+int32_t oracle_ngroups(int32_t L)
+{
+    if (L < 2048) return 2;
+    if (L < 16384) return 3;
+    int32_t g = (int32_t)floor(log2((double)L / 1024.0)) + 2;
+    return g < 5 ? g : 5;
+}
+
+/* Balanced pairwise sum of n = 2^k fp32 values: sum(left half) + sum(right half).
+ * READING: [DGQ] fixes neither the precision nor the order of the variance sums; the
+ * oracle fixes fp32 and this tree, so that a GPU reduction can reproduce it bit for bit
+ * (the segment boundaries are integer decisions taken on these sums). */
+static float pairwise_sum(const float *a, int n)
+{
+    if (n == 1) return a[0];
+    return pairwise_sum(a, n / 2) + pairwise_sum(a + n / 2, n / 2);
+}
+
+/* a2. Per-token variance of K over the head dimension, [DGQ] §2.2 ("for each head,
+ * compute the variance curve along the L dimension").  READING: population variance
+ * (divide by D), two-pass (mean first), of K only, as the article analyses K. */
+float oracle_token_variance(const uint16_t *k_row)
+{
+    float x[OR_D], e[OR_D];
+    for (int d = 0; d < OR_D; ++d) x[d] = bf16_to_float(k_row[d]);
+    float mean = pairwise_sum(x, OR_D) / (float)OR_D;
+    for (int d = 0; d < OR_D; ++d) {
+        float dev = x[d] - mean;
+        e[d] = dev * dev;
+    }
+    return pairwise_sum(e, OR_D) / (float)OR_D;
+}
+
+/* a3. Window means of the variance curve, [DGQ] §2.2 (window of 16 tokens).
+ * READING: non-overlapping windows [16w, 16w+16); the last, partial, window is kept
+ * and averaged over its own token count (its sum is taken over the 16-slot tree with
+ * +0 in the empty slots, which adds nothing). */
+void oracle_window_means(const float *var, int32_t L, float *means)
+{
+    int32_t W = (L + OR_WIN - 1) / OR_WIN;
+    for (int32_t w = 0; w < W; ++w) {
+        float slot[OR_WIN];
+        int32_t cnt = L - w * OR_WIN;
+        if (cnt > OR_WIN) cnt = OR_WIN;
+        for (int32_t i = 0; i < OR_WIN; ++i) slot[i] = i < cnt ? var[w * OR_WIN + i] : 0.0f;
+        means[w] = pairwise_sum(slot, OR_WIN) / (float)cnt;
+    }
+}
+
+/* a4. Segment starts from the largest jumps between adjacent window means, [DGQ] §2.2
+ * ("detect abrupt changes of the variance ... cut the sequence into 3-5 segments") with
+ * the segment count from the §3.2 rule.
+ * READINGS: jump_w = |m[w+1] - m[w]| between windows w and w+1; the n_groups-1 largest
+ * jumps are taken (ties to the earlier window); a boundary after window w starts a
+ * segment at token 16(w+1); the count is capped by the W-1 available jumps; zero jumps
+ * are still used when fewer nonzero ones exist.  Returns n_seg, writes n_seg starts. */
+int32_t oracle_boundaries(const float *means, int32_t W, int32_t L, int32_t *start)
+{
+    int32_t k = oracle_ngroups(L);
+    if (k > W) k = W;
+    k -= 1;
+    int32_t chosen[OR_MAX_SEG];
+    for (int32_t s = 0; s < k; ++s) {
+        int32_t best = -1;
+        float best_jump = 0.0f;
+        for (int32_t w = 0; w + 1 < W; ++w) {
+            int taken = 0;
+            for (int32_t c = 0; c < s; ++c)
+                if (chosen[c] == w) taken = 1;
+            if (taken) continue;
+            float jump = fabsf(means[w + 1] - means[w]);
+            if (best < 0 || jump > best_jump) { /* strict: earlier window wins ties */
+                best = w;
+                best_jump = jump;
+            }
+        }
+        chosen[s] = best;
+    }
+    /* starts: 0 followed by the chosen cut tokens in ascending order */
+    start[0] = 0;
+    for (int32_t s = 0; s < k; ++s) start[s + 1] = OR_WIN * (chosen[s] + 1);
+    for (int32_t i = 2; i <= k; ++i) {
+        int32_t v = start[i], j = i - 1;
+        while (j >= 1 && start[j] > v) {
+            start[j + 1] = start[j];
+            --j;
+        }
+        start[j + 1] = v;
+    }
+    return k + 1;
+}
+
+/* a5. fp32 min and max over all tokens x D of one segment, [DGQ] §2.2 ("each segment
+ * computes its own min/max").  READING: -0.0 results are stored as +0.0. */
+static void segment_min_max(const uint16_t *x, int64_t row_stride, int32_t t0, int32_t t1,
+                            float *mn, float *mx)
+{
+    float lo = INFINITY, hi = -INFINITY;
+    for (int32_t t = t0; t < t1; ++t)
+        for (int d = 0; d < OR_D; ++d) {
+            float v = bf16_to_float(x[(int64_t)t * row_stride + d]);
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+    if (lo == 0.0f) lo = 0.0f;
+    if (hi == 0.0f) hi = 0.0f;
+    *mn = lo;
+    *mx = hi;
+}
+
+/* Affine uint8 parameters of one segment: scale = (max-min)/255 for dequantisation and,
+ * as a separate IEEE division, inv = 255/(max-min) for encoding.  A flat segment
+ * (max == min) gets scale = inv = 0, so every code is 0 and decodes to min. */
+static void segment_affine(float mn, float mx, float *scale, float *inv)
+{
+    float r = mx - mn;
+    if (r == 0.0f) {
+        *scale = 0.0f;
+        *inv = 0.0f;
+    } else {
+        *scale = r / 255.0f;
+        *inv = 255.0f / r;
+    }
+}
+
+/* a6. One code: q = rint((x - min) * inv), round-half-even, kept in [0, 255]. */
+uint8_t oracle_encode(float x, float mn, float inv)
+{
+    float u = (x - mn) * inv;
+    float q = rintf(u);
+    if (q < 0.0f) q = 0.0f;
+    if (q > 255.0f) q = 255.0f;
+    return (uint8_t)q;
+}
+
+/* Compress one (request, KV head): L rows of K and V (bf16, rows `row_stride` elements
+ * apart).  Fills the record and, when non-null, the unpaged codes [L, 128]. */
+void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stride, int32_t L,
+                          oracle_seg *rec, uint8_t *k_codes, uint8_t *v_codes)
+{
+    memset(rec, 0, sizeof *rec);
+    rec->seq_len = L;
+    for (int i = 0; i < OR_MAX_SEG; ++i) rec->start[i] = L;
+    if (L <= 0) return;
+
+    int32_t W = (L + OR_WIN - 1) / OR_WIN;
+    float *var = (float *)malloc(sizeof(float) * (size_t)L);
+    float *means = (float *)malloc(sizeof(float) * (size_t)W);
+    float k_inv[OR_MAX_SEG], v_inv[OR_MAX_SEG];
+
+    for (int32_t t = 0; t < L; ++t) var[t] = oracle_token_variance(k + (int64_t)t * row_stride);
+    oracle_window_means(var, L, means);
+    /* READING: one segmentation per (request, KV head), derived from K and shared by K
+     * and V (the article derives the segments from K, and its storage formula counts a
+     * single marker bit per layer x head x token), with separate min/scale for K and V. */
+    int32_t n = oracle_boundaries(means, W, L, rec->start);
+    rec->n_seg = n;
+
+    for (int32_t s = 0; s < n; ++s) {
+        int32_t t0 = rec->start[s], t1 = s + 1 < n ? rec->start[s + 1] : L;
+        float mn, mx;
+        segment_min_max(k, row_stride, t0, t1, &mn, &mx);
+        rec->k_min[s] = mn;
+        segment_affine(mn, mx, &rec->k_scale[s], &k_inv[s]);
+        segment_min_max(v, row_stride, t0, t1, &mn, &mx);
+        rec->v_min[s] = mn;
+        segment_affine(mn, mx, &rec->v_scale[s], &v_inv[s]);
+    }
+
+    if (k_codes || v_codes) {
+        int32_t s = 0;
+        for (int32_t t = 0; t < L; ++t) {
+            while (s + 1 < n && rec->start[s + 1] <= t) ++s;
+            for (int d = 0; d < OR_D; ++d) {
+                if (k_codes)
+                    k_codes[(int64_t)t * OR_D + d] = oracle_encode(
+                        bf16_to_float(k[(int64_t)t * row_stride + d]), rec->k_min[s], k_inv[s]);
+                if (v_codes)
+                    v_codes[(int64_t)t * OR_D + d] = oracle_encode(
+                        bf16_to_float(v[(int64_t)t * row_stride + d]), rec->v_min[s], v_inv[s]);
+            }
+        }
+    }
+    free(var);
+    free(means);
+}
+
+/* a2-a7 for one layer of a batch.  K and V are packed variable-length [T, Hkv, 128]
+ * with request b on rows cu_seqlens[b] .. cu_seqlens[b+1]).  Token t of request b, head h
+ * is stored at pool[block_tables[b][t / bs]][h][t % bs][0..128), [PAGED]
+ * "PagedAttention implementation" (logical block -> physical block).  Slots past the
+ * sequence end in its last block are left untouched.  Pools are [num_blocks, Hkv, bs, 128]
+ * uint8, the record table [B, Hkv]. */
+void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                     int32_t B, int32_t Hkv, int32_t bs, const int32_t *block_tables,
+                     int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool, oracle_seg *table)
+{
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t L = cu_seqlens[b + 1] - cu_seqlens[b];
+        for (int32_t h = 0; h < Hkv; ++h) {
+            const int64_t row0 = ((int64_t)cu_seqlens[b] * Hkv + h) * OR_D;
+            uint8_t *kc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
+            uint8_t *vc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
+            oracle_seg *rec = &table[(int64_t)b * Hkv + h];
+            oracle_compress_pair(k + row0, v + row0, (int64_t)Hkv * OR_D, L, rec, kc, vc);
+            for (int32_t t = 0; t < L; ++t) {
+                int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
+                int64_t dst = ((blk * Hkv + h) * bs + t % bs) * OR_D;
+                memcpy(k_pool + dst, kc + (int64_t)t * OR_D, OR_D);
+                memcpy(v_pool + dst, vc + (int64_t)t * OR_D, OR_D);
+            }
+            free(kc);
+            free(vc);
+        }
+    }
+}
+
+/* Dequantised value of one code, in fp64: min + q * scale. */
+static double dequant(uint8_t q, float mn, float scale)
+{
+    return (double)mn + (double)q * (double)scale;
+}
+
+static int32_t segment_of(const oracle_seg *rec, int32_t t)
+{
+    int32_t s = 0;
+    for (int32_t i = 1; i < rec->n_seg; ++i)
+        if (rec->start[i] <= t) s = i;
+    return s;
+}
+
+/* Dequantise one (request, KV head) back to an fp64 [L, 128] array (test helper). */
+void oracle_dequant_pair(const uint8_t *pool, const oracle_seg *table, const int32_t *block_tables,
+                         int32_t b, int32_t h, int32_t Hkv, int32_t bs, int32_t max_blocks,
+                         int32_t L, int which_v, double *out)
+{
+    const oracle_seg *rec = &table[(int64_t)b * Hkv + h];
+    for (int32_t t = 0; t < L; ++t) {
+        int32_t s = segment_of(rec, t);
+        float mn = which_v ? rec->v_min[s] : rec->k_min[s];
+        float sc = which_v ? rec->v_scale[s] : rec->k_scale[s];
+        int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
+        const uint8_t *row = pool + ((blk * Hkv + h) * bs + t % bs) * OR_D;
+        for (int d = 0; d < OR_D; ++d) out[(int64_t)t * OR_D + d] = dequant(row[d], mn, sc);
+    }
+}
+
+/* a8-a10. Decode-step attention in fp64 over the dequantised paged cache plus the
+ * current step's own bf16 key/value.
+ * q [B, Hq, 128], k_new / v_new [B, Hkv, 128] (bf16 bits); out [B, Hq, 128] fp64.
+ * Query head hq reads KV head hq / (Hq / Hkv) (grouped-query attention, consecutive
+ * query heads share a KV head).  Scores are q.k / sqrt(128); softmax over the L cached
+ * positions and the current one; output = sum_t p_t v_t.
+ * READINGS: the cached tokens are exactly positions 0..L-1 (no mask, keys already
+ * rotary-embedded), the current token at position L is attended unquantised and is not
+ * part of the cache. */
+void oracle_paged_decode_attn(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                              const uint8_t *k_pool, const uint8_t *v_pool,
+                              const oracle_seg *table, const int32_t *block_tables,
+                              const int32_t *seq_lens, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t bs, int32_t max_blocks, double *out)
+{
+    const int32_t G = Hq / Hkv;
+    const double inv_sqrt_d = 1.0 / sqrt((double)OR_D);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t L = seq_lens[b];
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        for (int32_t hq = 0; hq < Hq; ++hq) {
+            const int32_t h = hq / G;
+            const oracle_seg *rec = &table[(int64_t)b * Hkv + h];
+            const uint16_t *qv = q + ((int64_t)b * Hq + hq) * OR_D;
+            for (int32_t t = 0; t < L; ++t) {
+                int32_t sg = segment_of(rec, t);
+                int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
+                const uint8_t *kr = k_pool + ((blk * Hkv + h) * bs + t % bs) * OR_D;
+                double acc = 0.0;
+                for (int d = 0; d < OR_D; ++d)
+                    acc += (double)bf16_to_float(qv[d]) * dequant(kr[d], rec->k_min[sg], rec->k_scale[sg]);
+                s[t] = acc * inv_sqrt_d;
+            }
+            {
+                const uint16_t *kn = k_new + ((int64_t)b * Hkv + h) * OR_D;
+                double acc = 0.0;
+                for (int d = 0; d < OR_D; ++d)
+                    acc += (double)bf16_to_float(qv[d]) * (double)bf16_to_float(kn[d]);
+                s[L] = acc * inv_sqrt_d;
+            }
+            double m = s[0];
+            for (int32_t t = 1; t <= L; ++t)
+                if (s[t] > m) m = s[t];
+            double l = 0.0;
+            for (int32_t t = 0; t <= L; ++t) {
+                s[t] = exp(s[t] - m);
+                l += s[t];
+            }
+            double o[OR_D];
+            for (int d = 0; d < OR_D; ++d) o[d] = 0.0;
+            for (int32_t t = 0; t < L; ++t) {
+                int32_t sg = segment_of(rec, t);
+                int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
+                const uint8_t *vr = v_pool + ((blk * Hkv + h) * bs + t % bs) * OR_D;
+                for (int d = 0; d < OR_D; ++d)
+                    o[d] += s[t] * dequant(vr[d], rec->v_min[sg], rec->v_scale[sg]);
+            }
+            {
+                const uint16_t *vn = v_new + ((int64_t)b * Hkv + h) * OR_D;
+                for (int d = 0; d < OR_D; ++d) o[d] += s[L] * (double)bf16_to_float(vn[d]);
+            }
+            double *dst = out + ((int64_t)b * Hq + hq) * OR_D;
+            for (int d = 0; d < OR_D; ++d) dst[d] = o[d] / l;
+        }
+        free(s);
+    }
+}
+
+/* Algorithmic bytes one compress call writes for a request of L tokens and Hkv heads:
+ * 1 byte per K and per V element plus one 128-byte record per head ([DGQ] §3.3 gives the
+ * INT8 body at 1 byte per element; the record replaces its per-token marker bits). */
+int64_t oracle_compress_bytes_written(int32_t L, int32_t Hkv)
+{
+    return 2LL * L * Hkv * OR_D + (int64_t)sizeof(oracle_seg) * Hkv;
+}

@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of the DGQ INT8 paged KV-cache hot path on GB300.
+
+One step = dgq_compress of every layer's K/V (bf16 -> uint8 codes in paged blocks plus
+segment records) followed by dgq_paged_decode_attn over every layer's INT8 cache, for one
+synthetic workload (default: the Llama-3-8B-shaped decode batch, 32 layers, 32 requests of
+2048 tokens, Hq 32 / Hkv 8, block size 16).  Inputs are generated on the GPU by the seeded
+generator before timing and stay resident in HBM; each layer has its own buffers, so one
+step touches far more than L2 (no flush needed).
+
+Prints ONE JSON line (rank 0).  `value` is decode-attention algorithmic GB/s over all ranks;
+`compress_gbs` the same for dgq_compress.  `--impl reference` times the CPU oracle instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT8 paged decode-attn HBM GB/s (% of peak); dgq_compress GB/s"
+D = 128
+REC = 128  # bytes per segment record
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(cfg):
+    from synth import configs
+    key = int(cfg) if cfg.isdigit() else cfg
+    w = configs.WORKLOADS[key]
+    lens = configs.seq_lens(w)
+    bt, nb = configs.block_tables(w, lens)
+    return w, lens, bt, nb, configs.cu_seqlens(lens)
+
+
+def algorithmic_bytes(w, lens):
+    """Per layer: (decode bytes, compress bytes), from the shapes."""
+    dec = 0
+    for L in lens:
+        L = int(L)
+        dec += w.hkv * (2 * L * D + REC) + 4 * ((L + w.block_size - 1) // w.block_size)
+        dec += w.hq * D * 2 * 2 + 2 * w.hkv * D * 2  # q in, out, k_new, v_new
+    elems = 2 * int(sum(lens)) * w.hkv * D          # K and V elements
+    comp = elems * 2 + elems * 1 + len(lens) * w.hkv * REC + 4 * len(lens)  # read bf16, write codes + records
+    return dec, comp
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def src_hash(name):
+    with open(os.path.join(ROOT, "int8_group_quantized_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def ncu_traffic(kernel_src, workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    h = src_hash(kernel_src)
+    with open(p) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split("\t")
+            if len(parts) >= 4 and parts[0] == kernel_src and parts[1] == workload_name and parts[2] == h:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.proc = None
+        self.dev = dev_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """A bounded sample of the workload (the first `requests` requests of the first `layers`
+    layers), generated once on the host; run() times the oracle's compress and fp64 decode
+    attention over it."""
+
+    def __init__(self, w, lens, layers=4, requests=8):
+        import numpy as np
+        import synth
+        from synth import configs
+        self.w = w
+        self.sub = np.asarray(lens[:requests], dtype=np.int32)
+        self.cu = configs.cu_seqlens(self.sub)
+        nblk = [(int(L) + w.block_size - 1) // w.block_size for L in self.sub]
+        self.bt = np.zeros((len(self.sub), max(1, max(nblk))), dtype=np.int32)
+        off = 0
+        for b, n in enumerate(nblk):
+            self.bt[b, :n] = np.arange(off, off + n)
+            off += n
+        self.nb = max(off, 1)
+        self.dec_b, self.comp_b = algorithmic_bytes(w, self.sub)
+        self.layers = []
+        for layer in range(layers):
+            tabs = synth.span_tables(w.seed, layer, self.sub, w.hkv, w.rule)
+            B = len(self.sub)
+            self.layers.append((
+                synth.fill_layer(w.seed, synth.STREAM_K, layer, self.cu, w.hkv, tabs),
+                synth.fill_layer(w.seed, synth.STREAM_V, layer, self.cu, w.hkv, tabs),
+                synth.fill_heads(w.seed, synth.STREAM_Q, layer, B, w.hq, 1.0),
+                synth.fill_heads(w.seed, synth.STREAM_KNEW, layer, B, w.hkv, 0.15),
+                synth.fill_heads(w.seed, synth.STREAM_VNEW, layer, B, w.hkv, 0.15)))
+        self.desc = (f"oracle (single-threaded C) on {requests} of {len(lens)} requests x {layers} of "
+                     f"{w.layers} layers of workload '{w.name}'")
+
+    def run(self):
+        """Returns (decode_bytes, decode_s, compress_bytes, compress_s)."""
+        import oracle
+        td = tc = 0.0
+        for k, v, q, kn, vn in self.layers:
+            t0 = time.perf_counter()
+            kp, vp, table = oracle.compress(k, v, self.cu, self.w.hkv, self.w.block_size, self.bt, self.nb)
+            t1 = time.perf_counter()
+            oracle.paged_decode_attn(q, kn, vn, kp, vp, table, self.bt, self.sub)
+            t2 = time.perf_counter()
+            tc += t1 - t0
+            td += t2 - t1
+        n = len(self.layers)
+        return self.dec_b * n, td, self.comp_b * n, tc
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w, lens, _, _, _ = workload(args.config)
+    tot_d = tot_c = bd = bc = 0.0
+    sample = OracleSample(w, lens, layers=1, requests=4)
+    desc = sample.desc
+    for i in range(args.warmup + args.steps):
+        db, dt, cb, ct = sample.run()
+        if i >= args.warmup:
+            bd += db
+            tot_d += dt
+            bc += cb
+            tot_c += ct
+    value = bd / tot_d / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * (tot_d + tot_c) / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": "4 requests x 1 layer per step"},
+        "compress_gbs": round(bc / tot_c / 1e9, 4),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU path
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import int8_group_quantized_gb300 as dgq
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dgq.lib()
+
+    w, lens, bt, nb, cu = workload(args.config)
+    B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
+    T = int(cu[-1])
+    max_seqlen = int(lens.max())
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    d_cu = torch.from_numpy(cu).to(dev)
+    d_bt = torch.from_numpy(bt).to(dev)
+    d_lens = torch.from_numpy(lens).to(dev)
+    layers = []
+    for l in range(nl):
+        n, st, sg = synth.span_tables(w.seed, l, lens, Hkv, w.rule)
+        tabs = tuple(torch.from_numpy(x).to(dev) for x in (n, st, sg))
+        k = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+        v = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+        synth.dev_fill_layer(w.seed, synth.STREAM_K, l, d_cu, Hkv, tabs, T, k, sp)
+        synth.dev_fill_layer(w.seed, synth.STREAM_V, l, d_cu, Hkv, tabs, T, v, sp)
+        q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        kn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+        vn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+        synth.dev_fill_heads(w.seed, synth.STREAM_Q, l, B, Hq, 1.0, q, sp)
+        synth.dev_fill_heads(w.seed, synth.STREAM_KNEW, l, B, Hkv, 0.15, kn, sp)
+        synth.dev_fill_heads(w.seed, synth.STREAM_VNEW, l, B, Hkv, 0.15, vn, sp)
+        layers.append(dict(
+            k=k, v=v, q=q, kn=kn, vn=vn,
+            kp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
+            vp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
+            table=torch.zeros((B, Hkv, REC), dtype=torch.uint8, device=dev),
+            out=torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)))
+    cws = torch.zeros(dgq.dgq_compress_workspace_size(B, max_seqlen, Hkv), dtype=torch.uint8, device=dev)
+    aws = torch.zeros(dgq.dgq_attn_workspace_size(B, Hq, Hkv, max_seqlen), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def compress_all():
+        for L in layers:
+            dgq.dgq_compress(L["k"], L["v"], d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"], cws, sp)
+
+    def decode_all():
+        for L in layers:
+            dgq.dgq_paged_decode_attn(L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], d_bt, d_lens,
+                                      max_seqlen, L["out"], aws, sp)
+
+    for _ in range(args.warmup):
+        compress_all()
+        decode_all()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, each = compress all layers + decode all layers
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for e0, e1, e2 in evs:
+        e0.record(stream)
+        compress_all()
+        e1.record(stream)
+        decode_all()
+        e2.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    comp_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in evs)
+    dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in evs)
+    err = dgq.dgq_workspace_error(cws, sp) or dgq.dgq_workspace_error(aws, sp)
+
+    dec_b, comp_b = algorithmic_bytes(w, lens)
+    dec_b_step, comp_b_step = dec_b * nl, comp_b * nl
+
+    # ---- end-to-end through the public API: per step the step's decode inputs (q, k_new, v_new
+    # of every layer) come from pinned host memory and the outputs go back to pinned host memory.
+    hq_in = [torch.empty_like(L["q"], device="cpu").pin_memory() for L in layers]
+    hk_in = [torch.empty_like(L["kn"], device="cpu").pin_memory() for L in layers]
+    hv_in = [torch.empty_like(L["vn"], device="cpu").pin_memory() for L in layers]
+    h_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
+    for i, L in enumerate(layers):
+        hq_in[i].copy_(L["q"])
+        hk_in[i].copy_(L["kn"])
+        hv_in[i].copy_(L["vn"])
+    h2d = sum(t.numel() * t.element_size() for t in hq_in + hk_in + hv_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for i, L in enumerate(layers):
+            L["q"].copy_(hq_in[i], non_blocking=True)
+            L["kn"].copy_(hk_in[i], non_blocking=True)
+            L["vn"].copy_(hv_in[i], non_blocking=True)
+        decode_all()
+        for i, L in enumerate(layers):
+            h_out[i].copy_(L["out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(5, min(args.steps, 50))
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+
+    # ---- parity spot check outside the timed region: one (request, head) of layer 0 vs the oracle
+    checked = spot_check(w, lens, cu, bt, layers[0], rank)
+
+    stats = torch.tensor([total_ms, comp_ms, dec_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
+    total_ms, comp_ms, dec_ms, e2e_ms = stats.tolist()
+
+    if rank == 0:
+        K = args.steps
+        dec_gbs = world * dec_b_step * K / (dec_ms / 1e3) / 1e9
+        comp_gbs = world * comp_b_step * K / (comp_ms / 1e3) / 1e9
+        peak, peak_src = measured_peak()
+        dec_launch_us = dec_ms / (K * nl) * 1e3
+        comp_launch_us = comp_ms / (K * nl) * 1e3
+        kernels = {
+            "attn_kernel": {"bytes_per_launch": dec_b, "avg_launch_us": round(dec_launch_us, 2),
+                            "achieved_gbs": round(dec_b / dec_launch_us / 1e3, 1), "src": "dgq_attn.cu"},
+            "compress_kernel": {"bytes_per_launch": comp_b, "avg_launch_us": round(comp_launch_us, 2),
+                                "achieved_gbs": round(comp_b / comp_launch_us / 1e3, 1), "src": "dgq_compress.cu"},
+        }
+        dom = max(kernels, key=lambda k: kernels[k]["avg_launch_us"])
+        ach = kernels[dom]["achieved_gbs"]
+        roofline = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "traffic": ncu_traffic(kernels[dom]["src"], w.name), "kernel": dom, "peak_source": peak_src}
+        line = {
+            "metric": METRIC, "value": round(dec_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": w.name, "layers": nl, "batch": B, "q_heads": Hq, "kv_heads": Hkv,
+                       "head_dim": D, "block_size": bs, "seq_len": int(max_seqlen) if len(set(lens.tolist())) == 1
+                       else f"{int(lens.min())}..{int(lens.max())}", "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (each layer has its own buffers; one step reads "
+                             f"{(dec_b_step + comp_b_step) / 1e9:.1f} GB)"},
+            "decode_frac_of_peak": round(dec_gbs / world / peak, 4),
+            "compress_gbs": round(comp_gbs, 1),
+            "compress_frac_of_peak": round(comp_gbs / world / peak, 4),
+            "decode_token_heads_per_s": round(world * sum(int(L) + 1 for L in lens) * Hq * nl * K / (dec_ms / 1e3), 1),
+            "roofline": roofline,
+            "kernels": kernels,
+            "e2e": {"value": round(world * dec_b_step / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "what": "decode step via the C ABI: host->device copy of q/k_new/v_new, 32-layer decode, "
+                            "device->host copy of the outputs"},
+            "gpu_launches": 2 * nl * K,
+            "clocks": clk,
+            "device_error": err,
+            "parity_spot_check": checked,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            sample = OracleSample(w, lens)
+            db = dt = cb = ct = 0.0
+            while dt + ct < 10.0:  # about 10 s of single-core oracle work
+                a_, b_, c_, d_ = sample.run()
+                db, dt, cb, ct = db + a_, dt + b_, cb + c_, ct + d_
+            line["cpu_baseline"] = {"value": round(db / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": sample.desc + f", repeated for {dt + ct:.1f} s",
+                                    "compress_gbs": round(cb / ct / 1e9, 4)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def spot_check(w, lens, cu, bt, layer0, rank):
+    """Compress codes of request 0 / head 0 of layer 0 bit-exact vs the oracle (host-generated)."""
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    import synth
+    L = int(lens[0])
+    n, st, sg = synth.spans(w.seed, 0, 0, 0, L, w.rule)
+    k = synth.fill_pair(w.seed, synth.STREAM_K, 0, 0, 0, L, n, st, sg)
+    v = synth.fill_pair(w.seed, synth.STREAM_V, 0, 0, 0, L, n, st, sg)
+    rec, kc, vc = oracle.compress_pair(k, v)
+    kp = layer0["kp"].cpu().numpy()
+    t = np.arange(L)
+    gk = kp[bt[0, t // w.block_size], 0, t % w.block_size]
+    grec = layer0["table"][0, 0].cpu().numpy().tobytes()
+    return bool(np.array_equal(gk, kc) and grec == rec.tobytes())
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

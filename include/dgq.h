@@ -1,0 +1,186 @@
+/*
+ * dgq.h -- C ABI of libdgq.so: an LLM decoder's KV cache compressed to INT8 by dynamic
+ * group quantisation (DGQ), stored in fixed-size paged blocks, and read by decode-step
+ * attention.  sm_103a (GB300) only.
+ *
+ * Sources, cited by title and section:
+ *   [DGQ]   "DeepSeek KV-cache dynamic group quantisation (DGQ)" article (pptc.cn news
+ *           101026): section 2.2 (per-head variance curve along L, 16-token windows,
+ *           boundaries at abrupt variance changes, 3-5 segments, independent min/max INT8
+ *           per segment, per-token segment id used at decode), section 3.2 (length-aware
+ *           n_groups in compress(); decompress is the hot part and belongs in CUDA),
+ *           section 3.3 (storage formula).
+ *   [PAGED] "DeepSeek-V4 high-concurrency KV-cache bottleneck" article (deepseek.csdn.net),
+ *           "PagedAttention implementation" section (logical blocks mapped to scattered
+ *           physical blocks via a page table with a free list) and its modified forward()
+ *           that passes block_tables to paged_attention().
+ *
+ * Conventions for every call below:
+ *   - Head dimension D is 128; block_size (tokens per physical block) is 16, 32 or 64.
+ *   - Device pointers are raw CUDA device addresses; the caller owns every buffer.  The
+ *     library allocates no device memory.  Pointers must be 16-byte aligned.
+ *   - `cuda_stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls enqueue work on it and return without synchronising.
+ *   - All argument checks happen on the host, before any launch; a failed check launches
+ *     nothing and returns a negative dgq_status.  Block-table entries and sequence lengths
+ *     live on the device and are trusted (each entry < num_blocks; seq_lens[b] <=
+ *     max_seqlen).
+ *   - A workspace is a caller-owned device buffer of at least the queried size.  It must be
+ *     zero-filled before its first use (dgq_workspace_init); every call leaves it ready for
+ *     the next one.  Calls that share a workspace must be ordered on one stream.  Device-side
+ *     failures (a wait that timed out) are recorded in the workspace and read with
+ *     dgq_workspace_error.
+ *   - bf16 values are IEEE bfloat16 bit patterns; fp32 is IEEE binary32.
+ */
+#ifndef DGQ_H
+#define DGQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DGQ_HEAD_DIM 128
+#define DGQ_WINDOW 16   /* variance-smoothing window, [DGQ] section 2.2 */
+#define DGQ_MAX_SEG 5   /* segments per (request, KV head), [DGQ] sections 2.2 and 3.2 */
+
+typedef enum dgq_status {
+    DGQ_OK = 0,
+    DGQ_ERR_INVALID_ARG = -1,    /* null pointer, bad size, misaligned pointer */
+    DGQ_ERR_UNSUPPORTED = -2,    /* shape outside what the kernels handle (D, block size, G) */
+    DGQ_ERR_WORKSPACE = -3,      /* workspace missing or smaller than the queried size */
+    DGQ_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed */
+    DGQ_ERR_POOL_EXHAUSTED = -5, /* block pool has fewer free blocks than requested */
+    DGQ_ERR_DEVICE = -6          /* a device-side wait timed out (see dgq_workspace_error) */
+} dgq_status;
+
+/*
+ * Segment record of one (request, KV head): exactly 128 bytes.
+ * [DGQ] section 2.2 keeps one segment id per token and looks up the segment's min/max at
+ * decode; here the id is implicit: token t belongs to segment s = max{i : start[i] <= t}.
+ * Dequantised value of code q in segment s: x = min[s] + q * scale[s] (fp32 values; the
+ * decode kernel evaluates it in fp32).  Entries i >= n_seg hold start = seq_len, min =
+ * scale = 0.  A record with seq_len == 0 has n_seg == 0.
+ */
+typedef struct dgq_seg_record {
+    int32_t n_seg;              /* 1..5 (0 when seq_len == 0) */
+    int32_t seq_len;            /* tokens compressed into the cache for this (request, head) */
+    int32_t start[DGQ_MAX_SEG]; /* start[0] = 0, ascending, multiples of 16 */
+    float k_min[DGQ_MAX_SEG];
+    float k_scale[DGQ_MAX_SEG]; /* (max - min) / 255, or 0 for a flat segment */
+    float v_min[DGQ_MAX_SEG];
+    float v_scale[DGQ_MAX_SEG];
+    int32_t pad[DGQ_MAX_SEG];   /* zero */
+} dgq_seg_record;
+
+/* ---------------------------------------------------------------------------------------
+ * dgq_compress -- DGQ encode of one layer for a batch of requests into a paged cache.
+ *
+ * Computes, per (request b, KV head h), [DGQ] section 2.2 / 3.2:
+ *   1. per-token variance of K over D (fp32, population, mean first; the sums use the
+ *      balanced pairwise order sum(left half) + sum(right half));
+ *   2. the mean of that variance over each non-overlapping 16-token window (the last,
+ *      partial, window averaged over its own token count);
+ *   3. n_groups(L) = 2 if L < 2048, 3 if L < 16384, else min(5, floor(log2(L/1024)) + 2),
+ *      and the n_groups-1 largest jumps |m[w+1] - m[w]| between adjacent window means
+ *      (ties to the earlier window; at most W-1 of them), each starting a segment at
+ *      token 16(w+1); one segmentation per (request, head), shared by K and V;
+ *   4. fp32 min/max of K and of V over each segment (all tokens x D), scale = (max-min)/255,
+ *      and codes q = rint((x - min) * (255 / (max - min))) (two rounded fp32 operations,
+ *      round-half-even), 0 for a flat segment;
+ *   5. stores the codes of token t at pool[block_tables[b][t / bs]][h][t % bs][0..128)
+ *      ([PAGED] PagedAttention: logical block t / bs -> physical block), and the record.
+ *
+ * k_bf16, v_bf16   [T, Hkv, 128] bf16, device.  Packed variable length: request b owns
+ *                  rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (T = cu_seqlens[batch]).
+ * cu_seqlens_dev   [batch+1] int32, device, non-decreasing, cu_seqlens[0] = 0.
+ * max_seqlen       host upper bound on every request length (sizes the workspace).
+ * block_tables_dev [batch, max_blocks_per_seq] int32, device.  The first ceil(L_b / bs)
+ *                  entries of row b name distinct physical blocks < num_blocks; requests
+ *                  of one call use disjoint blocks.  max_seqlen <= max_blocks_per_seq * bs.
+ * k_pool, v_pool   [num_blocks, Hkv, block_size, 128] uint8, device; only the slots of
+ *                  tokens 0..L_b-1 are written (the rest of a last block is untouched).
+ * seg_table        [batch, Hkv] dgq_seg_record, device, written in full.
+ * workspace        >= dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads) bytes.
+ * Inputs must be finite; requests may be empty (L = 0 writes a record with n_seg = 0).
+ * The call launches one cooperative kernel; the whole GPU takes part in it.
+ */
+dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, const int32_t *cu_seqlens_dev,
+                        int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                        int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool,
+                        int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                        size_t workspace_bytes, void *cuda_stream);
+
+size_t dgq_compress_workspace_size(int32_t batch, int32_t max_seqlen, int32_t num_kv_heads);
+
+/* ---------------------------------------------------------------------------------------
+ * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
+ * paged cache plus the step's own (unquantised) key and value.
+ *
+ * For request b and query head hq (KV head h = hq / G, G = Hq / Hkv, consecutive query
+ * heads share a KV head): scores s_t = q . x_K(t) / sqrt(128) for the cached tokens
+ * t < L_b, where x_K(t) = k_min[s] + code * k_scale[s] from the record of (b, h) and the
+ * codes gathered through the block table ([DGQ] section 2.2: segment lookup per token;
+ * section 3.2: dequantisation on the GPU; [PAGED] paged_attention(q, k, v, block_tables)),
+ * plus s_L = q . k_new / sqrt(128) for the current token; out = softmax(s) . [x_V ; v_new].
+ * The softmax is computed online in fp32 over splits of the sequence that run on different
+ * thread blocks and are merged in a fixed order (bitwise reproducible for a given GPU).
+ *
+ * q_bf16           [batch, Hq, 128] bf16, device, |q| < 65504.
+ * k_new_bf16, v_new_bf16  [batch, Hkv, 128] bf16, device: the step's own key / value.
+ * k_pool, v_pool, seg_table, block_tables_dev: as written by dgq_compress.
+ * seq_lens_dev     [batch] int32, device: cached tokens per request (0 allowed); must not
+ *                  exceed the record's seq_len.
+ * out_bf16         [batch, Hq, 128] bf16, device.
+ * Supported: Hq % Hkv == 0 with G = Hq / Hkv in {1, 2, 4, 8}.
+ * workspace        >= dgq_attn_workspace_size(batch, Hq, Hkv, max_seqlen) bytes.
+ */
+dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16,
+                                 const void *v_new_bf16, const uint8_t *k_pool,
+                                 const uint8_t *v_pool, const dgq_seg_record *seg_table,
+                                 const int32_t *block_tables_dev, const int32_t *seq_lens_dev,
+                                 int32_t max_seqlen, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
+                                 void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t max_seqlen);
+
+/* Zero-fill a workspace (cudaMemsetAsync on the stream). */
+dgq_status dgq_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/* Synchronise the stream and read the device-side error word of a workspace into
+ * *device_error (0 = none; otherwise an internal code naming the wait that timed out).
+ * Returns DGQ_ERR_DEVICE when the word is non-zero.  The workspace must be re-initialised
+ * after a device-side error. */
+dgq_status dgq_workspace_error(const void *workspace, void *cuda_stream, int32_t *device_error);
+
+/* ---------------------------------------------------------------------------------------
+ * Host block bookkeeping ([PAGED] BlockTable: physical blocks handed out from a free list
+ * and returned when a request ends).  Plain host memory; not thread-safe.
+ */
+typedef struct dgq_pool dgq_pool;
+
+dgq_pool *dgq_pool_create(int32_t num_blocks);          /* NULL on bad size / no memory */
+void dgq_pool_destroy(dgq_pool *pool);
+/* Takes n blocks (all or nothing); ids in ascending order of availability. */
+dgq_status dgq_pool_alloc(dgq_pool *pool, int32_t n, int32_t *out_ids);
+/* Returns blocks; an id out of range or already free is DGQ_ERR_INVALID_ARG (nothing freed). */
+dgq_status dgq_pool_free(dgq_pool *pool, const int32_t *ids, int32_t n);
+int32_t dgq_pool_num_free(const dgq_pool *pool);
+/* Fills row `row` of a host block table [*, max_blocks_per_seq] with blocks for `len`
+ * tokens taken from the pool (ceil(len / block_size) of them); unused entries set to 0. */
+dgq_status dgq_pool_alloc_table_row(dgq_pool *pool, int32_t len, int32_t block_size,
+                                    int32_t *table, int32_t row, int32_t max_blocks_per_seq);
+
+const char *dgq_status_str(dgq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGQ_H */

@@ -1,0 +1,196 @@
+"""DGQ INT8 paged KV cache on GB300: Python binding of ``libdgq.so``.
+
+Argument marshalling only.  Every step of compression and decode attention runs in the
+library's CUDA kernels; the functions here take torch CUDA tensors (or raw device
+addresses), pass pointers and sizes through the C ABI declared in ``include/dgq.h`` and
+raise :class:`DGQError` on a non-OK status.  There is no CPU fallback: if ``libdgq.so``
+is missing the import of any entry point fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+HEAD_DIM = 128
+MAX_SEG = 5
+SEG_RECORD_BYTES = 128
+
+__all__ = [
+    "DGQError", "lib", "dgq_compress", "dgq_compress_workspace_size", "dgq_paged_decode_attn",
+    "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
+    "seg_record_dtype",
+]
+
+
+class DGQError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = lib().dgq_status_str(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})" if what else f"{msg} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdgq.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is not built: run __graft_entry__.build() first")
+        L = ctypes.CDLL(_build.LIB)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.dgq_status_str.argtypes = [ctypes.c_int]
+        L.dgq_status_str.restype = ctypes.c_char_p
+        L.dgq_compress.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
+        L.dgq_compress.restype = ctypes.c_int
+        L.dgq_compress_workspace_size.argtypes = [i32, i32, i32]
+        L.dgq_compress_workspace_size.restype = sz
+        L.dgq_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                            P, P, sz, P]
+        L.dgq_paged_decode_attn.restype = ctypes.c_int
+        L.dgq_attn_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.dgq_attn_workspace_size.restype = sz
+        L.dgq_workspace_init.argtypes = [P, sz, P]
+        L.dgq_workspace_init.restype = ctypes.c_int
+        L.dgq_workspace_error.argtypes = [P, P, ctypes.POINTER(i32)]
+        L.dgq_workspace_error.restype = ctypes.c_int
+        L.dgq_pool_create.argtypes = [i32]
+        L.dgq_pool_create.restype = P
+        L.dgq_pool_destroy.argtypes = [P]
+        L.dgq_pool_destroy.restype = None
+        L.dgq_pool_alloc.argtypes = [P, i32, P]
+        L.dgq_pool_alloc.restype = ctypes.c_int
+        L.dgq_pool_free.argtypes = [P, P, i32]
+        L.dgq_pool_free.restype = ctypes.c_int
+        L.dgq_pool_num_free.argtypes = [P]
+        L.dgq_pool_num_free.restype = i32
+        L.dgq_pool_alloc_table_row.argtypes = [P, i32, i32, P, i32, i32]
+        L.dgq_pool_alloc_table_row.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int:
+    """Device address of a torch tensor (or a raw integer address)."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _nbytes(x) -> int:
+    return x.numel() * x.element_size()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise DGQError(status, what)
+
+
+def seg_record_dtype():
+    """numpy structured dtype of one dgq_seg_record (128 bytes)."""
+    import numpy as np
+    dt = np.dtype([("n_seg", "<i4"), ("seq_len", "<i4"), ("start", "<i4", (MAX_SEG,)),
+                   ("k_min", "<f4", (MAX_SEG,)), ("k_scale", "<f4", (MAX_SEG,)),
+                   ("v_min", "<f4", (MAX_SEG,)), ("v_scale", "<f4", (MAX_SEG,)),
+                   ("pad", "<i4", (MAX_SEG,))])
+    assert dt.itemsize == SEG_RECORD_BYTES
+    return dt
+
+
+def dgq_compress_workspace_size(batch: int, max_seqlen: int, num_kv_heads: int) -> int:
+    return int(lib().dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads))
+
+
+def dgq_attn_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_seqlen: int) -> int:
+    return int(lib().dgq_attn_workspace_size(batch, num_q_heads, num_kv_heads, max_seqlen))
+
+
+def dgq_workspace_init(workspace, stream=None) -> None:
+    _check(lib().dgq_workspace_init(_ptr(workspace), _nbytes(workspace), _stream(stream)), "dgq_workspace_init")
+
+
+def dgq_workspace_error(workspace, stream=None) -> int:
+    """Synchronises the stream; returns the device-side error word (0 = none)."""
+    code = ctypes.c_int32(0)
+    st = lib().dgq_workspace_error(_ptr(workspace), _stream(stream), ctypes.byref(code))
+    if st not in (0, -6):
+        raise DGQError(st, "dgq_workspace_error")
+    return int(code.value)
+
+
+def dgq_compress(k, v, cu_seqlens, max_seqlen, block_size, block_tables, k_pool, v_pool, seg_table,
+                 workspace, stream=None) -> None:
+    """k, v: bf16 [T, Hkv, 128]; cu_seqlens int32 [B+1]; block_tables int32 [B, max_blocks];
+    k_pool, v_pool uint8 [num_blocks, Hkv, bs, 128]; seg_table uint8 [B, Hkv, 128] (records);
+    workspace uint8 (dgq_compress_workspace_size bytes).  All CUDA tensors."""
+    B = cu_seqlens.shape[0] - 1
+    Hkv = k.shape[1]
+    _check(lib().dgq_compress(_ptr(k), _ptr(v), _ptr(cu_seqlens), B, int(max_seqlen), Hkv, k.shape[2],
+                              int(block_size), _ptr(block_tables), block_tables.shape[1], _ptr(k_pool),
+                              _ptr(v_pool), k_pool.shape[0], _ptr(seg_table), _ptr(workspace),
+                              _nbytes(workspace), _stream(stream)), "dgq_compress")
+
+
+def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens, max_seqlen,
+                          out, workspace, stream=None) -> None:
+    """q bf16 [B, Hq, 128]; k_new, v_new bf16 [B, Hkv, 128]; pools / seg_table / block_tables as
+    written by dgq_compress; seq_lens int32 [B]; out bf16 [B, Hq, 128]."""
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    _check(lib().dgq_paged_decode_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                       _ptr(seg_table), _ptr(block_tables), _ptr(seq_lens), int(max_seqlen),
+                                       B, Hq, Hkv, D, k_pool.shape[2], block_tables.shape[1], k_pool.shape[0],
+                                       _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dgq_paged_decode_attn")
+
+
+class BlockPool:
+    """Host free list of physical block ids (dgq_pool_*)."""
+
+    def __init__(self, num_blocks: int):
+        self._h = lib().dgq_pool_create(num_blocks)
+        if not self._h:
+            raise DGQError(-1, "dgq_pool_create")
+
+    def close(self) -> None:
+        if self._h:
+            lib().dgq_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int) -> list[int]:
+        buf = (ctypes.c_int32 * max(n, 1))()
+        _check(lib().dgq_pool_alloc(self._h, n, buf), "dgq_pool_alloc")
+        return list(buf[:n])
+
+    def free(self, ids) -> None:
+        ids = list(ids)
+        buf = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(lib().dgq_pool_free(self._h, buf, len(ids)), "dgq_pool_free")
+
+    def num_free(self) -> int:
+        return int(lib().dgq_pool_num_free(self._h))
+
+    def alloc_table_row(self, length: int, block_size: int, table, row: int) -> None:
+        """table: C-contiguous int32 numpy array [rows, max_blocks]."""
+        _check(lib().dgq_pool_alloc_table_row(self._h, length, block_size, table.ctypes.data, row,
+                                              table.shape[1]), "dgq_pool_alloc_table_row")

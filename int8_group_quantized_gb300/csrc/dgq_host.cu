@@ -1,0 +1,221 @@
+// dgq_host.cu -- the C ABI of libdgq.so: argument checks, workspace sizing, launch,
+// device error read-back, and the host block pool.  Every check runs before any launch.
+#include "dgq.h"
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "dgq_launch.h"
+
+static_assert(sizeof(dgq_seg_record) == 128, "dgq_seg_record must be 128 bytes");
+
+namespace {
+
+constexpr int32_t kMaxBatch = 8192;  // per-call limit (the kernels keep per-request prefixes on chip)
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64; }
+
+int device_sm_count(int *nsm)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dgq_status_str(dgq_status s)
+{
+    switch (s) {
+    case DGQ_OK: return "ok";
+    case DGQ_ERR_INVALID_ARG: return "invalid argument";
+    case DGQ_ERR_UNSUPPORTED: return "unsupported shape";
+    case DGQ_ERR_WORKSPACE: return "workspace too small or missing";
+    case DGQ_ERR_CUDA: return "CUDA error";
+    case DGQ_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+    case DGQ_ERR_DEVICE: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t dgq_compress_workspace_size(int32_t batch, int32_t max_seqlen, int32_t num_kv_heads)
+{
+    if (batch <= 0 || max_seqlen < 0 || num_kv_heads <= 0) return 0;
+    return dgq::compress_layout(batch, max_seqlen, num_kv_heads).total;
+}
+
+dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, const int32_t *cu_seqlens_dev, int32_t batch,
+                        int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                        uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                        size_t workspace_bytes, void *cuda_stream)
+{
+    if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    if ((int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size) return DGQ_ERR_INVALID_ARG;
+    // flat window index and pool row index are 32-bit on the device
+    const int64_t windows = (int64_t)batch * num_kv_heads * ((max_seqlen + DGQ_WINDOW - 1) / DGQ_WINDOW);
+    if (windows >= INT32_MAX || (int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX)
+        return DGQ_ERR_UNSUPPORTED;
+    if (!k_bf16 || !v_bf16 || !cu_seqlens_dev || !block_tables_dev || !k_pool || !v_pool || !seg_table)
+        return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(seg_table) || !aligned16(cu_seqlens_dev) || !aligned16(block_tables_dev))
+        return DGQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads))
+        return DGQ_ERR_WORKSPACE;
+    cudaError_t e = dgq::launch_compress(k_bf16, v_bf16, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
+                                         block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table, workspace,
+                                         static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seqlen)
+{
+    (void)max_seqlen;
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    int nsm = 0;
+    if (device_sm_count(&nsm) != 0) return 0;
+    return dgq::attn_layout(batch, num_q_heads, num_kv_heads, nsm).total;
+}
+
+dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                                 const uint8_t *k_pool, const uint8_t *v_pool, const dgq_seg_record *seg_table,
+                                 const int32_t *block_tables_dev, const int32_t *seq_lens_dev, int32_t max_seqlen,
+                                 int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
+                                 void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return DGQ_ERR_INVALID_ARG;
+    const int32_t G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return DGQ_ERR_UNSUPPORTED;
+    if ((int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size) return DGQ_ERR_INVALID_ARG;
+    const int64_t chunks = (int64_t)batch * num_kv_heads * ((max_seqlen + 63) / 64 + 1);
+    if (chunks >= INT32_MAX || (int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX)
+        return DGQ_ERR_UNSUPPORTED;
+    if (!q_bf16 || !k_new_bf16 || !v_new_bf16 || !k_pool || !v_pool || !seg_table || !block_tables_dev ||
+        !seq_lens_dev || !out_bf16)
+        return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(k_new_bf16) || !aligned16(v_new_bf16) || !aligned16(k_pool) ||
+        !aligned16(v_pool) || !aligned16(seg_table) || !aligned16(out_bf16) || !aligned16(block_tables_dev) ||
+        !aligned16(seq_lens_dev))
+        return DGQ_ERR_INVALID_ARG;
+    int nsm = 0;
+    if (device_sm_count(&nsm) != 0) return DGQ_ERR_CUDA;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < dgq::attn_layout(batch, num_q_heads, num_kv_heads, nsm).total)
+        return DGQ_ERR_WORKSPACE;
+    bool map_failed = false;
+    cudaError_t e = dgq::launch_attn(q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table, block_tables_dev,
+                                     seq_lens_dev, max_seqlen, batch, num_q_heads, num_kv_heads, block_size,
+                                     max_blocks_per_seq, num_blocks, out_bf16, workspace, nsm, &map_failed,
+                                     static_cast<cudaStream_t>(cuda_stream));
+    if (map_failed) return DGQ_ERR_INVALID_ARG;
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+dgq_status dgq_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (!workspace || workspace_bytes == 0) return DGQ_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+dgq_status dgq_workspace_error(const void *workspace, void *cuda_stream, int32_t *device_error)
+{
+    if (!workspace || !device_error) return DGQ_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DGQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DGQ_ERR_CUDA;
+    *device_error = (int32_t)word;
+    return word ? DGQ_ERR_DEVICE : DGQ_OK;
+}
+
+// ---- host block pool --------------------------------------------------------------------
+
+struct dgq_pool {
+    int32_t num_blocks;
+    std::vector<int32_t> free_list;  // stack of free ids
+    std::vector<uint8_t> is_free;
+};
+
+dgq_pool *dgq_pool_create(int32_t num_blocks)
+{
+    if (num_blocks <= 0) return nullptr;
+    dgq_pool *p = new (std::nothrow) dgq_pool;
+    if (!p) return nullptr;
+    p->num_blocks = num_blocks;
+    p->free_list.resize(num_blocks);
+    p->is_free.assign(num_blocks, 1);
+    for (int32_t i = 0; i < num_blocks; ++i) p->free_list[i] = num_blocks - 1 - i;  // pops 0, 1, 2, ...
+    return p;
+}
+
+void dgq_pool_destroy(dgq_pool *pool) { delete pool; }
+
+dgq_status dgq_pool_alloc(dgq_pool *pool, int32_t n, int32_t *out_ids)
+{
+    if (!pool || n < 0 || (n > 0 && !out_ids)) return DGQ_ERR_INVALID_ARG;
+    if ((size_t)n > pool->free_list.size()) return DGQ_ERR_POOL_EXHAUSTED;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t id = pool->free_list.back();
+        pool->free_list.pop_back();
+        pool->is_free[id] = 0;
+        out_ids[i] = id;
+    }
+    return DGQ_OK;
+}
+
+dgq_status dgq_pool_free(dgq_pool *pool, const int32_t *ids, int32_t n)
+{
+    if (!pool || n < 0 || (n > 0 && !ids)) return DGQ_ERR_INVALID_ARG;
+    std::vector<uint8_t> seen;
+    for (int32_t i = 0; i < n; ++i) {  // validate all first: nothing is freed on error
+        int32_t id = ids[i];
+        if (id < 0 || id >= pool->num_blocks || pool->is_free[id]) return DGQ_ERR_INVALID_ARG;
+        if (seen.empty()) seen.assign(pool->num_blocks, 0);
+        if (seen[id]) return DGQ_ERR_INVALID_ARG;
+        seen[id] = 1;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        pool->is_free[ids[i]] = 1;
+        pool->free_list.push_back(ids[i]);
+    }
+    return DGQ_OK;
+}
+
+int32_t dgq_pool_num_free(const dgq_pool *pool) { return pool ? (int32_t)pool->free_list.size() : -1; }
+
+dgq_status dgq_pool_alloc_table_row(dgq_pool *pool, int32_t len, int32_t block_size, int32_t *table, int32_t row,
+                                    int32_t max_blocks_per_seq)
+{
+    if (!pool || !table || len < 0 || row < 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    const int32_t n = (len + block_size - 1) / block_size;
+    if (n > max_blocks_per_seq) return DGQ_ERR_INVALID_ARG;
+    int32_t *dst = table + (int64_t)row * max_blocks_per_seq;
+    dgq_status s = dgq_pool_alloc(pool, n, dst);
+    if (s != DGQ_OK) return s;
+    for (int32_t i = n; i < max_blocks_per_seq; ++i) dst[i] = 0;
+    return DGQ_OK;
+}
+
+}  // extern "C"

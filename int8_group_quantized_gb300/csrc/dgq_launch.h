@@ -1,0 +1,29 @@
+// dgq_launch.h -- internal declarations shared by the host ABI and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dgq.h"
+
+namespace dgq {
+
+struct CompressLayout {
+    size_t off_count, off_flag, off_params, off_mean, off_mm, total;
+};
+CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
+cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
+                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+                            uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream);
+
+struct AttnLayout {
+    size_t off_count, off_part, total;
+};
+AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm);
+cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const uint8_t *kpool, const uint8_t *vpool,
+                        const dgq_seg_record *table, const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen,
+                        int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
+                        void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+
+}  // namespace dgq

@@ -118,7 +118,7 @@ SYNTH_FN float synth_cos2pi(float x)
     }
     float t = y * 0x1.921fb6p+2f; /* 2*pi*y in [0, pi/2] */
     float t2 = t * t;
-    float p = 0x1.1ee9ebp-29f;          /*  1/12! */
+    float p = 0x1.1ee9ecp-29f;          /*  1/12! */
     p = p * t2 - 0x1.27e4fcp-22f;       /* -1/10! */
     p = p * t2 + 0x1.a01a02p-16f;       /*  1/8!  */
     p = p * t2 - 0x1.6c16c2p-10f;       /* -1/6!  */

@@ -1,0 +1,135 @@
+"""The C ABI on the host: the library loads, exports every function include/dgq.h declares,
+rejects bad arguments before any launch, and keeps the block pool consistent.  CPU only."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from int8_group_quantized_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, POOL_EXHAUSTED = 0, -1, -2, -3, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    import int8_group_quantized_gb300 as dgq
+    return dgq.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dgq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(dgq_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"dgq_compress", "dgq_paged_decode_attn", "dgq_pool_alloc"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert L.dgq_status_str(s)
+    assert L.dgq_status_str(-99) == b"unknown status"
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: checks fail first
+
+
+def _compress(L, **kw):
+    a = dict(k=FAKE, v=FAKE, cu=FAKE, batch=2, max_seqlen=300, hkv=2, d=128, bs=16, bt=FAKE,
+             max_blocks=19, kp=FAKE, vp=FAKE, nb=32, table=FAKE, ws=FAKE, wsb=1 << 30, stream=0)
+    a.update(kw)
+    return L.dgq_compress(a["k"], a["v"], a["cu"], a["batch"], a["max_seqlen"], a["hkv"], a["d"], a["bs"],
+                          a["bt"], a["max_blocks"], a["kp"], a["vp"], a["nb"], a["table"], a["ws"], a["wsb"],
+                          a["stream"])
+
+
+def test_compress_rejects_bad_arguments_before_launch(L):
+    assert _compress(L, d=64) == UNSUPPORTED
+    assert _compress(L, bs=8) == UNSUPPORTED
+    assert _compress(L, bs=128) == UNSUPPORTED
+    assert _compress(L, k=0) == INVALID
+    assert _compress(L, table=0) == INVALID
+    assert _compress(L, k=FAKE + 2) == INVALID           # misaligned
+    assert _compress(L, batch=0) == INVALID
+    assert _compress(L, max_seqlen=305) == INVALID       # > max_blocks * bs
+    assert _compress(L, ws=0) == WORKSPACE
+    need = L.dgq_compress_workspace_size(2, 300, 2)
+    assert need > 0
+    assert _compress(L, wsb=need - 1) == WORKSPACE
+
+
+def _attn(L, **kw):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, kp=FAKE, vp=FAKE, table=FAKE, bt=FAKE, lens=FAKE, max_seqlen=300,
+             batch=2, hq=4, hkv=2, d=128, bs=16, max_blocks=19, nb=32, out=FAKE, ws=FAKE, wsb=1 << 30, stream=0)
+    a.update(kw)
+    return L.dgq_paged_decode_attn(a["q"], a["kn"], a["vn"], a["kp"], a["vp"], a["table"], a["bt"], a["lens"],
+                                   a["max_seqlen"], a["batch"], a["hq"], a["hkv"], a["d"], a["bs"],
+                                   a["max_blocks"], a["nb"], a["out"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_attn_rejects_bad_arguments_before_launch(L):
+    assert _attn(L, d=256) == UNSUPPORTED
+    assert _attn(L, bs=48) == UNSUPPORTED
+    assert _attn(L, hq=6, hkv=4) == INVALID              # Hq not a multiple of Hkv
+    assert _attn(L, hq=48, hkv=3) == UNSUPPORTED         # G = 16
+    assert _attn(L, q=0) == INVALID
+    assert _attn(L, out=FAKE + 8) == INVALID
+    assert _attn(L, max_seqlen=400) == INVALID
+    assert _attn(L, batch=-1) == INVALID
+
+
+def test_workspace_size_is_monotone(L):
+    a = L.dgq_compress_workspace_size(4, 1000, 8)
+    b = L.dgq_compress_workspace_size(4, 2000, 8)
+    c = L.dgq_compress_workspace_size(8, 2000, 8)
+    assert 0 < a < b < c
+    assert L.dgq_compress_workspace_size(0, 10, 1) == 0
+
+
+def test_block_pool_alloc_free_exhaust():
+    import int8_group_quantized_gb300 as dgq
+    _build.build()
+    pool = dgq.BlockPool(10)
+    assert pool.num_free() == 10
+    a = pool.alloc(4)
+    assert a == [0, 1, 2, 3] and pool.num_free() == 6
+    with pytest.raises(dgq.DGQError) as e:
+        pool.alloc(7)  # all or nothing
+    assert e.value.status == POOL_EXHAUSTED and pool.num_free() == 6
+    b = pool.alloc(6)
+    assert sorted(a + b) == list(range(10)) and pool.num_free() == 0
+    pool.free([3, 1])
+    assert pool.num_free() == 2
+    with pytest.raises(dgq.DGQError):
+        pool.free([3])        # already free
+    with pytest.raises(dgq.DGQError):
+        pool.free([0, 0])     # duplicate id: nothing freed
+    with pytest.raises(dgq.DGQError):
+        pool.free([10])       # out of range
+    assert pool.num_free() == 2
+    assert sorted(pool.alloc(2)) == [1, 3]
+    pool.close()
+
+
+def test_block_pool_table_rows():
+    import int8_group_quantized_gb300 as dgq
+    _build.build()
+    pool = dgq.BlockPool(32)
+    table = np.full((2, 19), -1, dtype=np.int32)
+    pool.alloc_table_row(37, 16, table, 0)
+    pool.alloc_table_row(300, 16, table, 1)
+    used = np.concatenate([table[0, :3], table[1, :19]])
+    assert len(set(used.tolist())) == 22 and pool.num_free() == 10
+    assert np.all(table[0, 3:] == 0)
+    with pytest.raises(dgq.DGQError):
+        pool.alloc_table_row(400, 16, table, 0)  # 25 blocks > 19 columns

@@ -1,0 +1,84 @@
+"""dgq_compress on the GPU against the CPU oracle: codes, segment records and block gathers
+bit-exact, across lengths that hit every n_groups branch, ragged tails, empty requests and
+all block sizes."""
+import numpy as np
+import pytest
+
+from dgq_cases import Case, assert_compress_equal, table_to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+def run(case, fill=0):
+    kp, vp, table = case.oracle_compress()
+    case.gpu_compress(fill=fill)
+    assert_compress_equal(case, kp, vp, table, case.d_kp.cpu().numpy(), case.d_vp.cpu().numpy(),
+                          table_to_numpy(case.d_table))
+    return kp, vp, table
+
+
+def test_tiny_workload():
+    run(Case([37, 300], hq=4, hkv=2, bs=16, seed=0, rule=0))
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_lengths_across_ngroups_branches(bs):
+    lens = [1, 15, 16, 17, 37, 300, 2047, 2048, 2049, 5000, 16383, 16384, 20000]
+    run(Case(lens, hq=8, hkv=2, bs=bs, seed=bs))
+
+
+def test_empty_requests_and_single_tokens():
+    case = Case([0, 1, 0, 33, 0], hq=2, hkv=2, bs=16, seed=5)
+    run(case)
+    tab = table_to_numpy(case.d_table)
+    assert tab[0, 0]["n_seg"] == 0 and tab[1, 0]["n_seg"] == 1 and tab[3, 1]["n_seg"] == 2
+
+
+def test_untouched_slots_keep_their_bytes():
+    case = Case([37, 300], hq=4, hkv=2, bs=16, seed=7)
+    run(case, fill=0xA5)
+    kp = case.d_kp.cpu().numpy()
+    touched = np.zeros(kp.shape[:3], dtype=bool)
+    for b, L in enumerate(case.lens):
+        for t in range(L):
+            touched[case.bt[b, t // 16], :, t % 16] = True
+    assert np.all(kp[~touched] == 0xA5)
+
+
+def test_many_pairs_several_super_groups():
+    # 64 requests x 8 heads x ~1.5K tokens: ~1.5 M windows-worth of work spread over super-groups
+    rng = np.random.default_rng(1)
+    lens = rng.integers(1, 3000, 64).tolist()
+    run(Case(lens, hq=32, hkv=8, bs=16, seed=11))
+
+
+def test_repeated_calls_reuse_workspace():
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    case = Case([100, 2500, 40], hq=4, hkv=4, bs=32, seed=13)
+    kp, vp, table = run(case)
+    for _ in range(3):  # same workspace, the epoch/flag protocol must reset itself
+        case.d_kp.zero_()
+        case.d_vp.zero_()
+        dgq.dgq_compress(case.d_k, case.d_v, case.d_cu, case.max_seqlen, case.bs, case.d_bt, case.d_kp,
+                         case.d_vp, case.d_table, case.d_cws)
+        torch.cuda.synchronize()
+        assert dgq.dgq_workspace_error(case.d_cws) == 0
+        assert_compress_equal(case, kp, vp, table, case.d_kp.cpu().numpy(), case.d_vp.cpu().numpy(),
+                              table_to_numpy(case.d_table))
+
+
+def test_planted_boundaries_on_gpu():
+    # K with sigma steps at window-aligned tokens (0.03 / 0.47 / 0.15 as in the DGQ example)
+    import torch
+    case = Case([4096], hq=1, hkv=1, bs=64, seed=3)
+    rng = np.random.default_rng(0)
+    k = np.zeros((4096, 1, 128), dtype=np.float32)
+    for (s, e, sg) in ((0, 1024, 0.03), (1024, 2560, 0.47), (2560, 4096, 0.15)):
+        k[s:e] = rng.standard_normal((e - s, 1, 128)) * sg
+    bits = k.view(np.uint32)
+    case.k = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+    case.v = case.k.copy()
+    run(case)
+    tab = table_to_numpy(case.d_table)
+    assert tab[0, 0]["n_seg"] == 3 and list(tab[0, 0]["start"][:3]) == [0, 1024, 2560]

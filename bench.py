@@ -40,6 +40,8 @@ def parse_args():
     ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (profiling captures; 0 = all of the workload's layers)")
     return ap.parse_args()
 
 
@@ -240,6 +242,8 @@ def run_ours(args):
 
     w, lens, bt, nb, cu = workload(args.config)
     B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
+    if args.layers:
+        nl = min(nl, args.layers)
     T = int(cu[-1])
     max_seqlen = int(lens.max())
     stream = torch.cuda.current_stream()

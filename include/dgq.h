@@ -94,7 +94,9 @@ typedef struct dgq_seg_record {
  *      ([PAGED] PagedAttention: logical block t / bs -> physical block), and the record.
  *
  * k_bf16, v_bf16   [T, Hkv, 128] bf16, device.  Packed variable length: request b owns
- *                  rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (T = cu_seqlens[batch]).
+ *                  rows cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ * total_tokens     T, the number of rows the K and V buffers hold (>= cu_seqlens[batch]);
+ *                  the kernels never read past row T.
  * cu_seqlens_dev   [batch+1] int32, device, non-decreasing, cu_seqlens[0] = 0.
  * max_seqlen       host upper bound on every request length (sizes the workspace).
  * block_tables_dev [batch, max_blocks_per_seq] int32, device.  The first ceil(L_b / bs)
@@ -107,8 +109,8 @@ typedef struct dgq_seg_record {
  * Inputs must be finite; requests may be empty (L = 0 writes a record with n_seg = 0).
  * The call launches one cooperative kernel; the whole GPU takes part in it.
  */
-dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, const int32_t *cu_seqlens_dev,
-                        int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                        const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
                         int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
                         int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool,
                         int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,

@@ -44,7 +44,7 @@ def lib() -> ctypes.CDLL:
         P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         L.dgq_status_str.argtypes = [ctypes.c_int]
         L.dgq_status_str.restype = ctypes.c_char_p
-        L.dgq_compress.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
+        L.dgq_compress.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
         L.dgq_compress.restype = ctypes.c_int
         L.dgq_compress_workspace_size.argtypes = [i32, i32, i32]
         L.dgq_compress_workspace_size.restype = sz
@@ -139,7 +139,7 @@ def dgq_compress(k, v, cu_seqlens, max_seqlen, block_size, block_tables, k_pool,
     workspace uint8 (dgq_compress_workspace_size bytes).  All CUDA tensors."""
     B = cu_seqlens.shape[0] - 1
     Hkv = k.shape[1]
-    _check(lib().dgq_compress(_ptr(k), _ptr(v), _ptr(cu_seqlens), B, int(max_seqlen), Hkv, k.shape[2],
+    _check(lib().dgq_compress(_ptr(k), _ptr(v), k.shape[0], _ptr(cu_seqlens), B, int(max_seqlen), Hkv, k.shape[2],
                               int(block_size), _ptr(block_tables), block_tables.shape[1], _ptr(k_pool),
                               _ptr(v_pool), k_pool.shape[0], _ptr(seg_table), _ptr(workspace),
                               _nbytes(workspace), _stream(stream)), "dgq_compress")

@@ -13,7 +13,7 @@
 //    chunks of one pair is a "piece"; pieces are merged per pair by the CTA that finishes
 //    last, in CTA order (fixed, so results are bitwise reproducible on a given GPU).
 //  * Pipeline: one producer warp issues TMA tiled copies (128-byte swizzle) of the uint8 K
-//    and V blocks of each chunk into a 4-stage shared-memory ring (mbarrier complete_tx);
+//    and V blocks of each chunk into a 6-stage shared-memory ring (mbarrier complete_tx);
 //    four consumer warps each take 16 tokens of a stage.
 //  * Math: codes become fp16 (1024 + q) with one byte-permute per two codes, and the GQA
 //    query group multiplies them on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
@@ -35,7 +35,7 @@
 namespace dgq {
 
 constexpr int kChunk = 64;                      // tokens per pipeline stage
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageBytes = kChunk * kD;        // 8 KB per tensor per stage
@@ -88,7 +88,7 @@ __device__ __forceinline__ void mma16816(float *c, uint32_t a0, uint32_t a1, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) { return ld_shared_v4(addr); }
 
 __device__ __forceinline__ uint32_t word(const uint4 &v, int i)
 {
@@ -99,7 +99,29 @@ struct ChunkLoc {
     int32_t b, h, j, nch, L;
 };
 
-__device__ __forceinline__ ChunkLoc locate_chunk(int32_t x, const int32_t *s_cpre, const int32_t *seq_lens, int32_t B,
+// Step a chunk cursor to the next chunk of the flat list (pairs in (request, head) order).
+__device__ __forceinline__ void advance(ChunkLoc &c, const int32_t *s_len, int32_t Hkv)
+{
+    if (++c.j == c.nch) {
+        c.j = 0;
+        if (++c.h == Hkv) {
+            c.h = 0;
+            ++c.b;
+            c.L = s_len[c.b];
+            c.nch = max(1, (c.L + 63) / 64);
+        }
+    }
+}
+
+// 2^x on the MUFU unit (flush-to-zero); arguments here are <= 8 or -inf.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ ChunkLoc locate_chunk(int32_t x, const int32_t *s_cpre, const int32_t *s_len, int32_t B,
                                                  int32_t Hkv)
 {
     int32_t lo = 0, hi = B - 1;
@@ -114,7 +136,7 @@ __device__ __forceinline__ ChunkLoc locate_chunk(int32_t x, const int32_t *s_cpr
     int32_t off = x - s_cpre[lo];
     c.h = off / c.nch;
     c.j = off - c.h * c.nch;
-    c.L = __ldg(seq_lens + lo);
+    c.L = s_len[lo];
     return c;
 }
 
@@ -152,11 +174,11 @@ struct WarpState {
     float o[8][4];
 };
 
-__global__ void __launch_bounds__(kAttnThreads, 3)
+__global__ void __launch_bounds__(kAttnThreads, 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *sK = smem;
     uint8_t *sV = smem + kStages * kStageBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + 2 * kStages * kStageBytes);
@@ -166,6 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
     dgq_seg_record *s_rec = reinterpret_cast<dgq_seg_record *>(s_snew + 8);
     float *s_comb = reinterpret_cast<float *>(s_rec + 1);                               // [4][G][132]
     int32_t *s_cpre = reinterpret_cast<int32_t *>(s_comb + kConsumerWarps * a.G * kPartStride);  // [B+1]
+    int32_t *s_len = s_cpre + (a.B + 1);                                                         // [B]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = a.B, Hkv = a.Hkv, G = a.G;
@@ -186,6 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
             int32_t v = 0;
             if (i < B) {
                 int32_t L = __ldg(a.seq_lens + i);
+                s_len[i] = L;
                 v = Hkv * max(1, (L + kChunk - 1) / kChunk);
             }
             int32_t x = v;
@@ -211,29 +235,51 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
-            uint32_t it = 0;
-            for (int32_t x = cbeg; x < cend; ++x) {
-                ChunkLoc c = locate_chunk(x, s_cpre, a.seq_lens, B, Hkv);
+            // Block ids of the next chunk are loaded one chunk ahead, so the table lookups overlap
+            // the wait for a free stage instead of sitting between the wait and the copies.
+            const int per_chunk = kChunk / a.bs;  // 1, 2 or 4 blocks
+            auto fetch = [&](const ChunkLoc &c, int32_t *dst) {
                 const int32_t nt = min(kChunk, c.L - kChunk * c.j);
-                if (nt <= 0) continue;
-                const int stage = it % kStages;
-                const uint32_t use = it / kStages;
-                if (use > 0 && !mbar_wait_bounded(&empty[stage], (use - 1) & 1)) {
-                    record_error(a.hdr, kErrEmptyWait);
-                    s_flag[0] = 1;
-                    break;
+                const int nblk = nt > 0 ? (nt + a.bs - 1) / a.bs : 0;
+                const int32_t *btrow = a.bt + (int64_t)c.b * a.max_blocks + per_chunk * c.j;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i < nblk) dst[i] = __ldg(btrow + i);
+            };
+            if (cbeg < cend) {
+                ChunkLoc cur = locate_chunk(cbeg, s_cpre, s_len, B, Hkv);
+                int32_t nxt[4] = {0, 0, 0, 0};
+                fetch(cur, nxt);
+                uint32_t it = 0;
+                for (int32_t x = cbeg; x < cend; ++x) {
+                    const ChunkLoc c = cur;
+                    int32_t blk[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+                    if (x + 1 < cend) {
+                        advance(cur, s_len, Hkv);
+                        fetch(cur, nxt);
+                    }
+                    const int32_t nt = min(kChunk, c.L - kChunk * c.j);
+                    if (nt <= 0) continue;
+                    const int stage = it % kStages;
+                    const uint32_t use = it / kStages;
+                    if (use > 0 && !mbar_wait_bounded(&empty[stage], (use - 1) & 1)) {
+                        record_error(a.hdr, kErrEmptyWait);
+                        s_flag[0] = 1;
+                        break;
+                    }
+                    if (s_flag[0]) break;
+                    const int nblk = (nt + a.bs - 1) / a.bs;
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)(nblk * a.bs * kD * 2));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i < nblk) {
+                            const int32_t y = (blk[i] * Hkv + c.h) * a.bs;
+                            tma_load_2d(sK + stage * kStageBytes + i * a.bs * kD, &tmK, 0, y, &full[stage]);
+                            tma_load_2d(sV + stage * kStageBytes + i * a.bs * kD, &tmV, 0, y, &full[stage]);
+                        }
+                    }
+                    ++it;
                 }
-                if (s_flag[0]) break;
-                const int nblk = (nt + a.bs - 1) / a.bs;
-                mbar_arrive_expect_tx(&full[stage], (uint32_t)(nblk * a.bs * kD * 2));
-                const int32_t *btrow = a.bt + (int64_t)c.b * a.max_blocks + (kChunk / a.bs) * c.j;
-                for (int i = 0; i < nblk; ++i) {
-                    const int32_t blk = __ldg(btrow + i);
-                    const int32_t y = (blk * Hkv + c.h) * a.bs;
-                    tma_load_2d(sK + stage * kStageBytes + i * a.bs * kD, &tmK, 0, y, &full[stage]);
-                    tma_load_2d(sV + stage * kStageBytes + i * a.bs * kD, &tmV, 0, y, &full[stage]);
-                }
-                ++it;
             }
         }
         return;
@@ -252,8 +298,11 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
     WarpState st;
     uint32_t it = 0;
 
+    ChunkLoc cur;
+    if (cbeg < cend) cur = locate_chunk(cbeg, s_cpre, s_len, B, Hkv);
     for (int32_t x = cbeg; x < cend; ++x) {
-        const ChunkLoc c = locate_chunk(x, s_cpre, a.seq_lens, B, Hkv);
+        const ChunkLoc c = cur;
+        if (x + 1 < cend) advance(cur, s_len, Hkv);
         const int32_t p = c.b * Hkv + c.h;
         const bool first = (x == cbeg) || (c.j == 0);
         const bool last = (x == cend - 1) || (c.j == c.nch - 1);
@@ -307,8 +356,8 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
             const int32_t t0 = kChunk * c.j + 16 * w;
             const int32_t valid = min(16, c.L - t0);
             if (ok && valid > 0) {
-                const uint8_t *kt = sK + stage * kStageBytes + w * 2048;
-                const uint8_t *vt = sV + stage * kStageBytes + w * 2048;
+                const uint32_t kt = smem_u32(sK) + stage * kStageBytes + w * 2048;
+                const uint32_t vt = smem_u32(sV) + stage * kStageBytes + w * 2048;
                 // ---- segment of this tile
                 const int sg = (t0 >= s_rec->start[1]) + (t0 >= s_rec->start[2]) + (t0 >= s_rec->start[3]) +
                                (t0 >= s_rec->start[4]);
@@ -332,19 +381,33 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
                 const float cv = vflat ? vmin : vmin - 1024.0f * vscale;
 
                 // ---- S^T = Q K^T: two n-tiles of 8 tokens, 8 k-steps of 16 columns
-                float sacc[2][4];
+                // four independent accumulator chains (two n-tiles x even/odd k-steps)
+                float sacc[2][4], sacc2[2][4];
+                uint4 klo[2], khi[2];
 #pragma unroll
                 for (int nt2 = 0; nt2 < 2; ++nt2) {
-                    sacc[nt2][0] = sacc[nt2][1] = sacc[nt2][2] = sacc[nt2][3] = 0.0f;
                     const int row = nt2 * 8 + tr;  // token row this lane supplies (n = r)
-                    const uint8_t *rp = kt + row * kD;
-                    const uint4 lo = lds128(rp + ((cq ^ (row & 7)) << 4));
-                    const uint4 hi = lds128(rp + (((cq + 4) ^ (row & 7)) << 4));
+                    const uint32_t rp = kt + row * kD;
+                    klo[nt2] = lds128(rp + ((cq ^ (row & 7)) << 4));
+                    khi[nt2] = lds128(rp + (((cq + 4) ^ (row & 7)) << 4));
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const uint32_t wd = word(jj < 4 ? lo : hi, jj & 3);
-                        mma16816(sacc[nt2], qa0[jj], 0u, qa2[jj], 0u, prmt(wd, M64, 0x4140), prmt(wd, M64, 0x4342));
+                    for (int e = 0; e < 4; ++e) sacc[nt2][e] = sacc2[nt2][e] = 0.0f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; jj += 2) {
+#pragma unroll
+                    for (int nt2 = 0; nt2 < 2; ++nt2) {
+                        const uint32_t w0 = word(jj < 4 ? klo[nt2] : khi[nt2], jj & 3);
+                        const uint32_t w1 = word(jj < 4 ? klo[nt2] : khi[nt2], (jj + 1) & 3);
+                        mma16816(sacc[nt2], qa0[jj], 0u, qa2[jj], 0u, prmt(w0, M64, 0x4140), prmt(w0, M64, 0x4342));
+                        mma16816(sacc2[nt2], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w1, M64, 0x4140),
+                                 prmt(w1, M64, 0x4342));
                     }
+                }
+#pragma unroll
+                for (int nt2 = 0; nt2 < 2; ++nt2) {
+                    sacc[nt2][0] += sacc2[nt2][0];
+                    sacc[nt2][1] += sacc2[nt2][1];
                 }
                 // lane scores for head r: tokens cq, cq+4 (tile 0) and 8+cq, 12+cq (tile 1)
                 float z[4];
@@ -358,7 +421,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
                 const bool need = gvalid && (mt > st.m + kLazyRescale);
                 float alpha = 1.0f;
                 if (need) {
-                    alpha = (st.m == -INFINITY) ? 0.0f : exp2f(st.m - mt);
+                    alpha = (st.m == -INFINITY) ? 0.0f : ex2(st.m - mt);
                     st.m = mt;
                     st.l *= alpha;
                     st.bsum *= alpha;
@@ -376,7 +439,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
                 }
                 float pr[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pr[e] = gvalid ? exp2f(z[e] - st.m) : 0.0f;
+                for (int e = 0; e < 4; ++e) pr[e] = gvalid ? ex2(z[e] - st.m) : 0.0f;
                 // the tensor cores see p rounded to fp16; the sums use the same rounded weights so
                 // the 1024 offset of the codes cancels exactly against bsum
                 const uint32_t pb0 = f32x2_to_f16x2(pr[0], pr[1]);
@@ -542,28 +605,12 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
 
 // ---- host launcher ---------------------------------------------------------------------------
 
-#include <cudaTypedefs.h>
-
 namespace dgq {
-
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
 
 // 2-D map over a pool [num_blocks * Hkv * bs rows, 128 bytes], box = one (block, head) tile.
 static bool make_pool_map(CUtensorMap *map, const uint8_t *pool, int64_t rows, int32_t bs)
 {
-    auto fn = get_encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kD};
@@ -578,7 +625,7 @@ static bool make_pool_map(CUtensorMap *map, const uint8_t *pool, int64_t rows, i
 size_t attn_smem_bytes(int32_t B, int32_t G)
 {
     return 1024 + 2 * kStages * kStageBytes + 2 * kStages * 8 + 16 + 32 + sizeof(dgq_seg_record) +
-           (size_t)kConsumerWarps * G * kPartStride * 4 + (size_t)(B + 1) * 4;
+           (size_t)kConsumerWarps * G * kPartStride * 4 + (size_t)(2 * B + 1) * 4;
 }
 
 int attn_max_ctas(int nsm) { return nsm * 3; }

@@ -59,8 +59,11 @@ struct CompressArgs {
     int32_t wps;  // windows per super-group
 };
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kCWarps = 8;                          // consumer warps (plus one TMA producer warp)
+constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kCStages = 16;                        // shared-memory ring of window tiles
+constexpr int kTileBytes = kWin * kD * 2;           // 16 tokens x 128 bf16 = 4 KB
+constexpr int kCStageBytes = 2 * kTileBytes;        // K tile + V tile
 
 __device__ __forceinline__ int32_t ngroups(int32_t L)
 {
@@ -277,96 +280,74 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
     __syncwarp();
 }
 
-// ---- statistics of one window (one warp) -----------------------------------------------
+// ---- statistics of one window (one warp, tile in shared memory) --------------------------
+//
+// Lane (half, sub) reads 8 consecutive bf16 of token 2i + half in pass i, so each half-warp
+// covers one 128-element row and the half-warp butterfly reproduces the pairwise order.
 
-__device__ __forceinline__ void window_stats(const CompressArgs &a, int32_t w, const WinLoc &loc,
-                                             const int32_t *s_cu, uint32_t target)
+struct WinStats {
+    float mean, kmn, kmx, vmn, vmx;
+};
+
+__device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32_t cnt)
 {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, sub = lane & 15;
-    const int32_t t0 = loc.wi * kWin;
-    const int32_t cnt = min(kWin, loc.L - t0);
-    const int64_t row0 = ((int64_t)(s_cu[loc.b] + t0) * a.Hkv + loc.h) * kD + sub * 8;
-    const int64_t rstride = (int64_t)a.Hkv * kD;
-
-    uint4 kq[8], vq[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int tt = 2 * i + half;
-        if (tt < cnt) {
-            kq[i] = __ldg(reinterpret_cast<const uint4 *>(a.k + row0 + tt * rstride));
-            vq[i] = __ldg(reinterpret_cast<const uint4 *>(a.v + row0 + tt * rstride));
-        }
-    }
-    // min/max on packed bf16 pairs (exact: bf16 -> fp32 widening preserves order)
     __nv_bfloat162 kmn2 = __float2bfloat162_rn(INFINITY), kmx2 = __float2bfloat162_rn(-INFINITY);
     __nv_bfloat162 vmn2 = kmn2, vmx2 = kmx2;
+    float var[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if ((2 * i + half) < cnt) {
-            const uint32_t *kw = reinterpret_cast<const uint32_t *>(&kq[i]);
-            const uint32_t *vw = reinterpret_cast<const uint32_t *>(&vq[i]);
+        const int tt = 2 * i + half;
+        const bool ok = tt < cnt;
+        const uint4 kq = ld_shared_v4(kt + tt * (kD * 2) + sub * 16);
+        const uint4 vq = ld_shared_v4(vt + tt * (kD * 2) + sub * 16);
+        if (ok) {  // min/max on packed bf16 pairs (exact: widening to fp32 preserves order)
+            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+            const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                __nv_bfloat162 kx = *reinterpret_cast<const __nv_bfloat162 *>(kw + j);
-                __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(vw + j);
+                const __nv_bfloat162 kx = *reinterpret_cast<const __nv_bfloat162 *>(kw + j);
+                const __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(vw + j);
                 kmn2 = __hmin2(kmn2, kx); kmx2 = __hmax2(kmx2, kx);
                 vmn2 = __hmin2(vmn2, vx); vmx2 = __hmax2(vmx2, vx);
             }
         }
-    }
-    float var[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const bool ok = (2 * i + half) < cnt;
         float x[8];
-        unpack8(ok ? kq[i] : make_uint4(0, 0, 0, 0), x);
-        float mean = __fmul_rn(halfwarp_tree(tree8(x)), 0.0078125f);  // exact /128
+        unpack8(kq, x);
+        const float mean = __fmul_rn(halfwarp_tree(tree8(x)), 0.0078125f);  // exact /128
         float e[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            float d = __fsub_rn(x[j], mean);
+            const float d = __fsub_rn(x[j], mean);
             e[j] = __fmul_rn(d, d);
         }
-        float v = __fmul_rn(halfwarp_tree(tree8(e)), 0.0078125f);
+        const float v = __fmul_rn(halfwarp_tree(tree8(e)), 0.0078125f);
         var[i] = ok ? v : 0.0f;
     }
-    float kmn = fminf(__low2float(kmn2), __high2float(kmn2));
-    float kmx = fmaxf(__low2float(kmx2), __high2float(kmx2));
-    float vmn = fminf(__low2float(vmn2), __high2float(vmn2));
-    float vmx = fmaxf(__low2float(vmx2), __high2float(vmx2));
     // window mean: tokens 2i (lower half-warp) and 2i+1 (upper) pair up first
     float s[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i] = __fadd_rn(var[i], __shfl_xor_sync(0xffffffffu, var[i], 16));
-    float sum16 = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
-                            __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
-    float mean_w = __fdiv_rn(sum16, (float)cnt);
-    kmn = warp_min(kmn); kmx = warp_max(kmx);
-    vmn = warp_min(vmn); vmx = warp_max(vmx);
-
-    int last = 0;
-    const int32_t p = loc.b * a.Hkv + loc.h;
-    if (lane == 0) {
-        __stcg(a.win_mean + w, mean_w);
-        __stcg(a.win_mm + w, make_float4(kmn, kmx, vmn, vmx));
-        __threadfence();
-        uint32_t old = atomicAdd(a.pair_count + p, 1u);
-        last = (old == (uint32_t)loc.W - 1u);
-        if (last) __threadfence();
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) segment_pair(a, p, loc.b, loc.h, loc.L, loc.W, w - loc.wi, target);
+    const float sum16 = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
+                                  __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
+    WinStats r;
+    r.mean = __fdiv_rn(sum16, (float)cnt);
+    r.kmn = warp_min(fminf(__low2float(kmn2), __high2float(kmn2)));
+    r.kmx = warp_max(fmaxf(__low2float(kmx2), __high2float(kmx2)));
+    r.vmn = warp_min(fminf(__low2float(vmn2), __high2float(vmn2)));
+    r.vmx = warp_max(fmaxf(__low2float(vmx2), __high2float(vmx2)));
+    return r;
 }
 
-// ---- quantise one window (one warp) ----------------------------------------------------
+// ---- quantisation -----------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t code_bits(float x, float mn, float inv)
 {
     // rint((x - min) * inv) for 0 <= u < 2^22: adding 1.5 * 2^23 rounds u to an integer
     // (round-to-nearest-even) and leaves that integer in the low mantissa bits.  x >= min
     // makes u >= 0, and u <= 255 * (1 + 2^-22) < 255.5, so the low byte is the code.
-    float u = __fmul_rn(__fsub_rn(x, mn), inv);
+    const float u = __fmul_rn(__fsub_rn(x, mn), inv);
     return __float_as_uint(__fadd_rn(u, 12582912.0f));
 }
 
@@ -377,16 +358,23 @@ __device__ __forceinline__ uint2 encode8(const uint4 &q, float mn, float inv)
     uint32_t c[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) c[j] = code_bits(x[j], mn, inv);
-    uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
-    uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+    const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
     return make_uint2(lo, hi);
 }
 
-__device__ __forceinline__ void window_quant(const CompressArgs &a, int32_t w, const WinLoc &loc,
-                                             const int32_t *s_cu, uint32_t target)
+// Quantisation parameters of one pair, read once per run of windows of that pair: lane i < 5
+// holds segment i's (start, k_min, k_inv, v_min, v_inv).
+struct PairCache {
+    int32_t p;
+    int32_t start;
+    float kmn, kinv, vmn, vinv;
+};
+
+// Wait (bounded) for the pair's segmentation; false if the wait timed out.
+__device__ __forceinline__ bool load_pair(const CompressArgs &a, int32_t p, uint32_t target, PairCache &pc)
 {
     const int lane = threadIdx.x & 31;
-    const int32_t p = loc.b * a.Hkv + loc.h;
     int ok = 1;
     if (lane == 0) {
         uint32_t it = 0;
@@ -400,66 +388,101 @@ __device__ __forceinline__ void window_quant(const CompressArgs &a, int32_t w, c
         }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) return;
+    if (!ok) return false;
     (void)ld_acquire_gpu(a.pair_flag + p);  // every lane acquires the published parameters
+    const PairParams *pp = a.params + p;
+    const int i = lane < kMaxSeg ? lane : 0;
+    pc.p = p;
+    pc.start = __ldcg(pp->start + i);
+    pc.kmn = __ldcg(pp->k_min + i);
+    pc.kinv = __ldcg(pp->k_inv + i);
+    pc.vmn = __ldcg(pp->v_min + i);
+    pc.vinv = __ldcg(pp->v_inv + i);
+    return true;
+}
 
+// Codes of one window tile, written straight to its slots in the physical block.
+__device__ __forceinline__ void window_quant(const CompressArgs &a, const WinLoc &loc, uint32_t kt, uint32_t vt,
+                                             const PairCache &pc, int64_t blk)
+{
+    const int lane = threadIdx.x & 31;
     const int half = lane >> 4, sub = lane & 15;
     const int32_t t0 = loc.wi * kWin;
     const int32_t cnt = min(kWin, loc.L - t0);
-    const PairParams *pp = a.params + p;
-    int s = 0;
-#pragma unroll
-    for (int i = 1; i < kMaxSeg; ++i) s += (t0 >= __ldcg(pp->start + i));
-    const float kmn = __ldcg(pp->k_min + s), kinv = __ldcg(pp->k_inv + s);
-    const float vmn = __ldcg(pp->v_min + s), vinv = __ldcg(pp->v_inv + s);
-
-    const int64_t row0 = ((int64_t)(s_cu[loc.b] + t0) * a.Hkv + loc.h) * kD + sub * 8;
-    const int64_t rstride = (int64_t)a.Hkv * kD;
-    const int64_t blk = __ldg(a.bt + (int64_t)loc.b * a.max_blocks + t0 / a.bs);
+    // segment of the window: number of starts 1..4 at or before t0 (lanes 1..4 hold them)
+    const unsigned ballot = __ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pc.start <= t0);
+    const int s = __popc(ballot);
+    const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
+    const float vmn = __shfl_sync(0xffffffffu, pc.vmn, s), vinv = __shfl_sync(0xffffffffu, pc.vinv, s);
     const int64_t dst0 = ((blk * a.Hkv + loc.h) * a.bs + (t0 % a.bs)) * kD + sub * 8;
-
-    uint4 kq[8], vq[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        int tt = 2 * i + half;
+        const int tt = 2 * i + half;
         if (tt < cnt) {
-            kq[i] = __ldcs(reinterpret_cast<const uint4 *>(a.k + row0 + tt * rstride));
-            vq[i] = __ldcs(reinterpret_cast<const uint4 *>(a.v + row0 + tt * rstride));
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int tt = 2 * i + half;
-        if (tt < cnt) {
-            __stcs(reinterpret_cast<uint2 *>(a.kpool + dst0 + tt * kD), encode8(kq[i], kmn, kinv));
-            __stcs(reinterpret_cast<uint2 *>(a.vpool + dst0 + tt * kD), encode8(vq[i], vmn, vinv));
+            const uint4 kq = ld_shared_v4(kt + tt * (kD * 2) + sub * 16);
+            const uint4 vq = ld_shared_v4(vt + tt * (kD * 2) + sub * 16);
+            __stcs(reinterpret_cast<uint2 *>(a.kpool + dst0 + tt * kD), encode8(kq, kmn, kinv));
+            __stcs(reinterpret_cast<uint2 *>(a.vpool + dst0 + tt * kD), encode8(vq, vmn, vinv));
         }
     }
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
+// Per-warp pending arrivals: windows of one pair counted locally and published with one fence.
+struct Pending {
+    int32_t p, cnt, b, h, L, W, wbase;
+};
+
+__device__ __forceinline__ void flush_pending(const CompressArgs &a, Pending &pd, uint32_t target)
 {
-    extern __shared__ int32_t smem[];
-    int32_t *s_cu = smem;              // [B+1]
-    int32_t *s_wpre = smem + a.B + 1;  // [B+1]
+    if (pd.cnt == 0) return;
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();  // this warp's window statistics before the arrival count
+        const uint32_t old = atomicAdd(a.pair_count + pd.p, (uint32_t)pd.cnt);
+        last = (old + (uint32_t)pd.cnt == (uint32_t)pd.W);
+        if (last) __threadfence();
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) segment_pair(a, pd.p, pd.b, pd.h, pd.L, pd.W, pd.wbase, target);
+    pd.cnt = 0;
+    pd.p = -1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    compress_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, CompressArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_smem_1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kCStages * kCStageBytes);
+    uint64_t *empty = full + kCStages;
+    int32_t *s_cu = reinterpret_cast<int32_t *>(empty + kCStages);  // [B+1]
+    int32_t *s_wpre = s_cu + a.B + 1;                                // [B+1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
 
+    if (tid == 0) {
+        for (int s = 0; s < kCStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
     for (int i = tid; i <= B; i += kThreads) s_cu[i] = __ldg(a.cu + i);
     __syncthreads();
     // exclusive scan of Hkv * ceil(L_b / 16) (single warp; B is small)
     if (warp == 0) {
         int32_t carry = 0;
         for (int base = 0; base < B; base += 32) {
-            int i = base + lane;
+            const int i = base + lane;
             int32_t v = 0;
             if (i < B) v = a.Hkv * ((s_cu[i + 1] - s_cu[i] + kWin - 1) / kWin);
             int32_t x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
             if (i < B) s_wpre[i] = carry + x - v;
@@ -483,37 +506,127 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
         }
     }
 
+    // The work list of this CTA, identical for the producer and the consumers: for each
+    // super-group i, the statistics of its share of super-group i, then the quantisation of its
+    // share of the pairs that end in super-group i-1.  Item k uses stage k % kCStages and is
+    // processed by consumer warp k % kCWarps.
     const int32_t wps = a.wps;
     const int32_t nsg = (Wtot + wps - 1) / wps;
-    for (int32_t i = 0; i <= nsg; ++i) {
-        if (i < nsg) {  // statistics of super-group i, this CTA's contiguous share
-            int32_t lo = i * wps, len = min(wps, Wtot - lo);
-            int32_t w0 = lo + (int32_t)(((int64_t)len * cta) / ncta);
-            int32_t w1 = lo + (int32_t)(((int64_t)len * (cta + 1)) / ncta);
-            for (int32_t w = w0 + warp; w < w1; w += kWarps) {
-                WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
-                window_stats(a, w, loc, s_cu, target);
-            }
+    auto ranges = [&](int32_t i, int32_t &s0, int32_t &s1, int32_t &q0, int32_t &q1) {
+        s0 = s1 = q0 = q1 = 0;
+        if (i < nsg) {
+            const int32_t lo = i * wps, len = min(wps, Wtot - lo);
+            s0 = lo + (int32_t)(((int64_t)len * cta) / ncta);
+            s1 = lo + (int32_t)(((int64_t)len * (cta + 1)) / ncta);
         }
-        if (i >= 1) {  // quantise the pairs whose last window lies in super-group i-1
-            // Those pairs form one contiguous run of windows: from the start of the pair
-            // holding the super-group's first window (if that pair ends inside it) to the end
-            // of the pair holding its last window (if that pair ends exactly there; else to
-            // that pair's start).
+        if (i >= 1) {
+            // pairs whose last window lies in super-group i-1: from the start of the pair holding
+            // its first window to the end of the pair holding its last window (or that pair's
+            // start, if it ends later)
             const int32_t A = (i - 1) * wps, Z = min(i * wps, Wtot) - 1;
             int32_t fA, eA, fZ, eZ;
             pair_span(A, s_wpre, s_cu, B, a.Hkv, &fA, &eA);
             pair_span(Z, s_wpre, s_cu, B, a.Hkv, &fZ, &eZ);
-            const int32_t q0 = fA;
-            const int32_t q1 = (eZ - 1 == Z) ? eZ : fZ;
-            int32_t len = q1 - q0;
-            if (len > 0) {
-                int32_t w0 = q0 + (int32_t)(((int64_t)len * cta) / ncta);
-                int32_t w1 = q0 + (int32_t)(((int64_t)len * (cta + 1)) / ncta);
-                for (int32_t w = w0 + warp; w < w1; w += kWarps) {
-                    WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
-                    window_quant(a, w, loc, s_cu, target);
+            const int32_t lo = fA, hi = (eZ - 1 == Z) ? eZ : fZ;
+            if (hi > lo) {
+                q0 = lo + (int32_t)(((int64_t)(hi - lo) * cta) / ncta);
+                q1 = lo + (int32_t)(((int64_t)(hi - lo) * (cta + 1)) / ncta);
+            }
+        }
+    };
+
+    if (warp == kCWarps) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            const uint64_t pol_first = make_policy_evict_first();
+            uint32_t k = 0;
+            bool abort = false;
+            for (int32_t i = 0; i <= nsg && !abort; ++i) {
+                int32_t s0, s1, q0, q1;
+                ranges(i, s0, s1, q0, q1);
+                for (int part = 0; part < 2 && !abort; ++part) {
+                    const int32_t w0 = part ? q0 : s0, w1 = part ? q1 : s1;
+                    for (int32_t w = w0; w < w1; ++w, ++k) {
+                        const int stage = k % kCStages;
+                        const uint32_t use = k / kCStages;
+                        if (use > 0 && !mbar_wait_bounded(&empty[stage], (use - 1) & 1)) {
+                            record_error(a.hdr, kErrEmptyWait);
+                            abort = true;
+                            break;
+                        }
+                        const WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
+                        const int32_t row = s_cu[loc.b] + loc.wi * kWin;
+                        uint8_t *dst = smem + stage * kCStageBytes;
+                        mbar_arrive_expect_tx(&full[stage], kCStageBytes);
+                        // first read: normal priority, so the tile stays in L2 for its second read;
+                        // second read (quantisation) is the last use: evict first
+                        if (part) {
+                            tma_load_3d_hint(dst, &tmK, 0, loc.h, row, &full[stage], pol_first);
+                            tma_load_3d_hint(dst + kTileBytes, &tmV, 0, loc.h, row, &full[stage], pol_first);
+                        } else {
+                            tma_load_3d(dst, &tmK, 0, loc.h, row, &full[stage]);
+                            tma_load_3d(dst + kTileBytes, &tmV, 0, loc.h, row, &full[stage]);
+                        }
+                    }
                 }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- consumers
+        Pending pd;
+        pd.p = -1;
+        pd.cnt = 0;
+        PairCache pc;
+        pc.p = -1;
+        bool pc_ok = false;
+        uint32_t k = 0;
+        for (int32_t i = 0; i <= nsg; ++i) {
+            int32_t s0, s1, q0, q1;
+            ranges(i, s0, s1, q0, q1);
+            for (int part = 0; part < 2; ++part) {
+                const int32_t w0 = part ? q0 : s0, w1 = part ? q1 : s1;
+                for (int32_t w = w0; w < w1; ++w, ++k) {
+                    if ((int)(k % kCWarps) != warp) continue;
+                    const int stage = k % kCStages;
+                    const uint32_t use = k / kCStages;
+                    const WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
+                    int64_t blk = 0;
+                    if (part == 1) {  // block id and pair parameters, before waiting for the tile
+                        blk = __ldg(a.bt + (int64_t)loc.b * a.max_blocks + (loc.wi * kWin) / a.bs);
+                        const int32_t p = loc.b * a.Hkv + loc.h;
+                        if (p != pc.p) pc_ok = load_pair(a, p, target, pc);
+                    }
+                    if (!mbar_wait_bounded(&full[stage], use & 1)) {
+                        record_error(a.hdr, kErrFullWait);
+                        continue;  // no data: skip the window (the call reports the error)
+                    }
+                    const uint32_t kt = smem_u32(smem) + stage * kCStageBytes;
+                    const uint32_t vt = kt + kTileBytes;
+                    if (part == 0) {
+                        const int32_t cnt = min(kWin, loc.L - loc.wi * kWin);
+                        const WinStats st = window_stats(kt, vt, cnt);
+                        const int32_t p = loc.b * a.Hkv + loc.h;
+                        if (lane == 0) {
+                            __stcg(a.win_mean + w, st.mean);
+                            __stcg(a.win_mm + w, make_float4(st.kmn, st.kmx, st.vmn, st.vmx));
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[stage]);
+                        if (p != pd.p) {
+                            flush_pending(a, pd, target);
+                            pd.p = p; pd.b = loc.b; pd.h = loc.h; pd.L = loc.L; pd.W = loc.W;
+                            pd.wbase = w - loc.wi;
+                        }
+                        ++pd.cnt;
+                    } else {
+                        if (pc_ok) window_quant(a, loc, kt, vt, pc, blk);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[stage]);
+                    }
+                }
+                if (part == 0) flush_pending(a, pd, target);  // before any wait on a flag
             }
         }
     }
@@ -521,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        uint32_t old = atomicAdd(&a.hdr->done_ctas, 1u);
+        const uint32_t old = atomicAdd(&a.hdr->done_ctas, 1u);
         if (old == (uint32_t)ncta - 1u) {  // last CTA of the call: advance the epoch
             a.hdr->done_ctas = 0;
             a.hdr->epoch = target;
@@ -532,10 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
 
 }  // namespace dgq
 
-// ---- host launcher (called from dgq_host.cpp after argument checks) ---------------------
+// ---- host launcher (called from dgq_host.cu after argument checks) ---------------------
 
 namespace dgq {
-
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -554,10 +666,32 @@ CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv)
     return l;
 }
 
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
-                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                            uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream)
+size_t compress_smem_bytes(int32_t B)
 {
+    return 1024 + (size_t)kCStages * kCStageBytes + 2 * kCStages * 8 + (size_t)(2 * (B + 1)) * 4;
+}
+
+// 3-D map over a packed [T, Hkv, 128] bf16 tensor; box = 16 tokens of one head (4 KB).
+static bool make_kv_map(CUtensorMap *map, const void *base, int32_t T, int32_t Hkv)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)kWin};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t T,
+                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, bool *map_failed,
+                            cudaStream_t stream)
+{
+    *map_failed = false;
     CompressLayout l = compress_layout(B, max_seqlen, Hkv);
     char *base = static_cast<char *>(ws);
     CompressArgs a;
@@ -580,24 +714,27 @@ cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int
     a.max_blocks = max_blocks;
     a.wps = 4096;  // 4096 windows x 16 tokens x 512 B (K+V bf16) = 32 MB per super-group
 
+    CUtensorMap mk, mv;
+    const int32_t Tmap = T > 0 ? T : 1;
+    if (!make_kv_map(&mk, k, Tmap, Hkv) || !make_kv_map(&mv, v, Tmap, Hkv)) {
+        *map_failed = true;
+        return cudaErrorInvalidValue;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     int nsm = 0;
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    size_t smem = (size_t)(2 * (B + 1)) * sizeof(int32_t);
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    const size_t smem = compress_smem_bytes(B);
+    e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    if (occ > 2) occ = 2;
-    dim3 grid(nsm * occ), block(kThreads);
-    void *args[] = {&a};
+    dim3 grid(nsm), block(kThreads);  // one CTA per SM; every CTA is resident (cooperative launch)
+    void *args[] = {&mk, &mv, &a};
     return cudaLaunchCooperativeKernel((const void *)compress_kernel, grid, block, args, smem, stream);
 }
 

@@ -13,6 +13,22 @@
 
 static_assert(sizeof(dgq_seg_record) == 128, "dgq_seg_record must be 128 bytes");
 
+namespace dgq {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+}  // namespace dgq
+
 namespace {
 
 constexpr int32_t kMaxBatch = 8192;  // per-call limit (the kernels keep per-request prefixes on chip)
@@ -53,15 +69,15 @@ size_t dgq_compress_workspace_size(int32_t batch, int32_t max_seqlen, int32_t nu
     return dgq::compress_layout(batch, max_seqlen, num_kv_heads).total;
 }
 
-dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, const int32_t *cu_seqlens_dev, int32_t batch,
-                        int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_tokens, const int32_t *cu_seqlens_dev,
+                        int32_t batch, int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                         const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
                         uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
                         size_t workspace_bytes, void *cuda_stream)
 {
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
     if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
-        max_blocks_per_seq <= 0)
+        max_blocks_per_seq <= 0 || total_tokens < 0)
         return DGQ_ERR_INVALID_ARG;
     if ((int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size) return DGQ_ERR_INVALID_ARG;
     // flat window index and pool row index are 32-bit on the device
@@ -76,9 +92,11 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, const int32_t *c
     if (!workspace || !aligned16(workspace) ||
         workspace_bytes < dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads))
         return DGQ_ERR_WORKSPACE;
-    cudaError_t e = dgq::launch_compress(k_bf16, v_bf16, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
-                                         block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table, workspace,
-                                         static_cast<cudaStream_t>(cuda_stream));
+    bool map_failed = false;
+    cudaError_t e = dgq::launch_compress(k_bf16, v_bf16, cu_seqlens_dev, batch, total_tokens, max_seqlen, num_kv_heads,
+                                         block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
+                                         workspace, &map_failed, static_cast<cudaStream_t>(cuda_stream));
+    if (map_failed) return DGQ_ERR_INVALID_ARG;
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 

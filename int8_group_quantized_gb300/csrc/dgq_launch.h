@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -13,9 +14,10 @@ struct CompressLayout {
     size_t off_count, off_flag, off_params, off_mean, off_mm, total;
 };
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
-                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                            uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream);
+cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t T,
+                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, bool *map_failed,
+                            cudaStream_t stream);
 
 struct AttnLayout {
     size_t off_count, off_part, total;
@@ -25,5 +27,8 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
                         const dgq_seg_record *table, const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen,
                         int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
                         void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query), or null.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 }  // namespace dgq

@@ -45,10 +45,10 @@ FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: checks f
 
 
 def _compress(L, **kw):
-    a = dict(k=FAKE, v=FAKE, cu=FAKE, batch=2, max_seqlen=300, hkv=2, d=128, bs=16, bt=FAKE,
+    a = dict(k=FAKE, v=FAKE, T=337, cu=FAKE, batch=2, max_seqlen=300, hkv=2, d=128, bs=16, bt=FAKE,
              max_blocks=19, kp=FAKE, vp=FAKE, nb=32, table=FAKE, ws=FAKE, wsb=1 << 30, stream=0)
     a.update(kw)
-    return L.dgq_compress(a["k"], a["v"], a["cu"], a["batch"], a["max_seqlen"], a["hkv"], a["d"], a["bs"],
+    return L.dgq_compress(a["k"], a["v"], a["T"], a["cu"], a["batch"], a["max_seqlen"], a["hkv"], a["d"], a["bs"],
                           a["bt"], a["max_blocks"], a["kp"], a["vp"], a["nb"], a["table"], a["ws"], a["wsb"],
                           a["stream"])
 
@@ -62,6 +62,7 @@ def test_compress_rejects_bad_arguments_before_launch(L):
     assert _compress(L, k=FAKE + 2) == INVALID           # misaligned
     assert _compress(L, batch=0) == INVALID
     assert _compress(L, max_seqlen=305) == INVALID       # > max_blocks * bs
+    assert _compress(L, T=-1) == INVALID
     assert _compress(L, ws=0) == WORKSPACE
     need = L.dgq_compress_workspace_size(2, 300, 2)
     assert need > 0

@@ -7,23 +7,29 @@
 // DeepSeek-V4 KV-cache article), plus the current token's own bf16 key/value.
 //
 // GPU design.
-//  * Work space: every (request, KV head) pair is cut into 64-token chunks; all chunks of
-//    all pairs form one flat list, and each persistent CTA takes an equal contiguous slice
-//    of it (a pair may span several CTAs, a CTA may cover several pairs).  A CTA's run of
-//    chunks of one pair is a "piece"; pieces are merged per pair by the CTA that finishes
-//    last, in CTA order (fixed, so results are bitwise reproducible on a given GPU).
-//  * Pipeline: one producer warp issues TMA tiled copies (128-byte swizzle) of the uint8 K
-//    and V blocks of each chunk into a 6-stage shared-memory ring (mbarrier complete_tx);
-//    four consumer warps each take 16 tokens of a stage.
-//  * Math: codes become fp16 (1024 + q) with one byte-permute per two codes, and the GQA
-//    query group multiplies them on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
-//    S^T = Q . K^T (16 x 8 tokens per mma) and O^T += V^T . P^T.  The affine dequantisation
-//    is folded out of the inner loop: for a tile inside segment s,
+//  * Work: every (request, KV head) pair is cut into 16-token tiles (a tile never crosses a
+//    block, since block sizes are multiples of 16, nor a segment, since segment starts are);
+//    all tiles of all pairs form one flat list and each persistent CTA takes an equal
+//    contiguous slice of it, so mixed lengths and a single long request balance alike.  The
+//    four warps of a CTA take every fourth tile of the slice and combine their softmax states
+//    in shared memory wherever the slice crosses from one pair to the next.  A CTA's part of a
+//    pair is a "piece"; a pair covered by several CTAs is merged by the CTA that finishes it
+//    last (all 128 threads, in CTA order of the pieces: bitwise reproducible on a given GPU),
+//    together with the current token.
+//  * Loads: each lane copies exactly the 128 bytes of codes it will use from a tile (4 x 16 B
+//    of K rows for its MMA B fragment, 4 x 16 B of V rows for its A fragment) with cp.async into
+//    its warp's shared-memory ring, four tiles deep (slot-major, so every access is conflict
+//    free).  Measured on this GPU, the per-copy issue cost of TMA caps single-tile copies of
+//    2 KB blocks at 2-4 TB/s, while per-thread 16-byte copies stream at the HBM rate.  Block ids
+//    come 32 tiles ahead from one coalesced load per warp.
+//  * Math: codes become fp16 (1024 + q) with byte permutes, and the GQA query group multiplies
+//    them on the tensor cores (mma.sync m16n8k16, fp32 accumulate): S^T = Q . K^T and
+//    O^T += V^T . P^T.  The affine dequantisation is folded out of the inner loop: for a tile
+//    inside segment s,
 //      q . x_K = k_scale[s] * (q . (1024 + c)) + (k_min[s] - 1024 k_scale[s]) * sum(q),
 //      sum_t p_t x_V = v_scale[s] * sum_t p_t (1024 + c_t) + (v_min[s] - 1024 v_scale[s]) sum p.
-//    Segment starts are multiples of 16, so a 16-token tile never straddles two segments.
-//  * Online softmax in the log2 domain with lazy rescaling (the running max moves only when
-//    a tile's max exceeds it by more than 8, so p <= 256 stays exact enough in fp16).
+//  * Online softmax in the log2 domain with lazy rescaling (the running max moves only when a
+//    tile's max exceeds it by more than 8, so p <= 256 stays exact enough in fp16).
 #include "dgq_device.cuh"
 #include "dgq.h"
 #include "dgq_launch.h"
@@ -34,19 +40,24 @@
 
 namespace dgq {
 
-constexpr int kChunk = 64;                      // tokens per pipeline stage
-constexpr int kStages = 6;
-constexpr int kConsumerWarps = 4;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStageBytes = kChunk * kD;        // 8 KB per tensor per stage
-constexpr int kPartStride = 132;                // floats per (piece, head) partial: m, l, O[128], pad
+constexpr int kTile = 16;                          // tokens per tile
+constexpr int kWarpsPerCta = 4;
+constexpr int kAttnThreads = kWarpsPerCta * 32;
+constexpr int kMaxCtasPerSm = 3;
+constexpr int kDepth = 4;                          // tiles in flight per warp
+constexpr int kSlotBytes = 32 * 16;                // one 16-byte piece per lane
+constexpr int kTileSmem = 8 * kSlotBytes;          // 4 K pieces + 4 V pieces per lane = 4 KB
+constexpr int kWarpSmem = kDepth * kTileSmem;
+constexpr int kPartStride = 132;                   // floats per (piece, head) partial: m, l, pad, pad, O[128]
 constexpr float kLog2eOverSqrtD = 0.12751743074570180f;  // log2(e) / sqrt(128)
-constexpr float kLazyRescale = 8.0f;            // log2 units
+constexpr float kLazyRescale = 8.0f;               // log2 units
 
 struct AttnArgs {
     const uint16_t *q;
     const uint16_t *knew;
     const uint16_t *vnew;
+    const uint8_t *kpool;
+    const uint8_t *vpool;
     const dgq_seg_record *table;
     const int32_t *bt;
     const int32_t *seq_lens;
@@ -57,8 +68,8 @@ struct AttnArgs {
     int32_t B, Hq, Hkv, G, bs, max_blocks;
 };
 
-// token order inside each 8-column n-tile: column n holds token kTau[n]; it keeps the rows a
-// quarter-warp reads at the same time in different halves of the 128-byte swizzle pattern.
+// Token order inside each 8-column n-tile: column n holds token tau(n).  With it, the K row a
+// lane supplies to S^T and the V rows it supplies to O^T cover the tokens whose scores it holds.
 __device__ __forceinline__ int tau(int n) { return (n >> 1) + ((n & 1) << 2); }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
@@ -81,36 +92,15 @@ __device__ __forceinline__ float f16hi(uint32_t w) { return __high2float(*reinte
 __device__ __forceinline__ void mma16816(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) { return ld_shared_v4(addr); }
-
 __device__ __forceinline__ uint32_t word(const uint4 &v, int i)
 {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
-struct ChunkLoc {
-    int32_t b, h, j, nch, L;
-};
-
-// Step a chunk cursor to the next chunk of the flat list (pairs in (request, head) order).
-__device__ __forceinline__ void advance(ChunkLoc &c, const int32_t *s_len, int32_t Hkv)
-{
-    if (++c.j == c.nch) {
-        c.j = 0;
-        if (++c.h == Hkv) {
-            c.h = 0;
-            ++c.b;
-            c.L = s_len[c.b];
-            c.nch = max(1, (c.L + 63) / 64);
-        }
-    }
 }
 
 // 2^x on the MUFU unit (flush-to-zero); arguments here are <= 8 or -inf.
@@ -121,210 +111,233 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-__device__ __forceinline__ ChunkLoc locate_chunk(int32_t x, const int32_t *s_cpre, const int32_t *s_len, int32_t B,
-                                                 int32_t Hkv)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// ---- the flat tile list ---------------------------------------------------------------------
+
+struct TileLoc {
+    int32_t b, h, j, ntl, L;  // request, head, tile within the pair, tiles in the pair, length
+};
+
+__device__ __forceinline__ int32_t tiles_of(int32_t L) { return max(1, (L + kTile - 1) / kTile); }
+
+__device__ __forceinline__ TileLoc locate_tile(int32_t x, const int32_t *s_tpre, const int32_t *s_len, int32_t B)
 {
     int32_t lo = 0, hi = B - 1;
     while (lo < hi) {
-        int32_t mid = (lo + hi + 1) >> 1;
-        if (s_cpre[mid] <= x) lo = mid;
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (s_tpre[mid] <= x) lo = mid;
         else hi = mid - 1;
     }
-    ChunkLoc c;
+    TileLoc c;
     c.b = lo;
-    c.nch = (s_cpre[lo + 1] - s_cpre[lo]) / Hkv;
-    int32_t off = x - s_cpre[lo];
-    c.h = off / c.nch;
-    c.j = off - c.h * c.nch;
     c.L = s_len[lo];
+    c.ntl = tiles_of(c.L);
+    const int32_t off = x - s_tpre[lo];
+    c.h = off / c.ntl;
+    c.j = off - c.h * c.ntl;
     return c;
 }
 
-// CTA owning flat chunk x when C chunks are split evenly over n CTAs
-__device__ __forceinline__ int32_t owner(int32_t x, int32_t C, int32_t n)
+__device__ __forceinline__ void advance(TileLoc &c, const int32_t *s_len, int32_t Hkv)
 {
-    return (int32_t)((((int64_t)x + 1) * n - 1) / C);
+    if (++c.j == c.ntl) {
+        c.j = 0;
+        if (++c.h == Hkv) {
+            c.h = 0;
+            ++c.b;
+            c.L = s_len[c.b];
+            c.ntl = tiles_of(c.L);
+        }
+    }
 }
 
-// whether CTA c owns at least one chunk (with fewer chunks than CTAs, some own none)
-__device__ __forceinline__ bool owns_chunks(int32_t c, int32_t C, int32_t n)
+// CTA owning flat tile x when T tiles are split evenly over n CTAs
+__device__ __forceinline__ int32_t owner(int32_t x, int32_t T, int32_t n)
 {
-    return ((int64_t)(c + 1) * C) / n > ((int64_t)c * C) / n;
+    return (int32_t)((((int64_t)x + 1) * n - 1) / T);
+}
+
+__device__ __forceinline__ bool owns_tiles(int32_t w, int32_t T, int32_t n)
+{
+    return ((int64_t)(w + 1) * T) / n > ((int64_t)w * T) / n;
 }
 
 // Final softmax merge with the current token: (O + p_new v_new) / (L + p_new), where (M, L, O)
 // are the cached tokens' max, sum and weighted value sum relative to M (log2 domain).
-__device__ __forceinline__ uint16_t finish(float M, float L, float O, float s_new, float v_new)
+__device__ __forceinline__ float finish(float M, float L, float O, float s_new, float v_new)
 {
     const float Mf = fmaxf(M, s_new);
-    const float wo = (M == -INFINITY) ? 0.0f : exp2f(M - Mf);
-    const float wn = exp2f(s_new - Mf);
-    const float o = fmaf(O, wo, wn * v_new) / fmaf(L, wo, wn);
-    __nv_bfloat16 ob = __float2bfloat16_rn(o);
-    return *reinterpret_cast<uint16_t *>(&ob);
+    const float wo = (M == -INFINITY) ? 0.0f : ex2(M - Mf);
+    const float wn = ex2(s_new - Mf);
+    return fmaf(O, wo, wn * v_new) / fmaf(L, wo, wn);
 }
 
-// Per-warp online-softmax state of the current piece.
-struct WarpState {
-    float m;      // running max (log2 domain) of head g = lane/4
-    float l;      // partial sum of p over this lane's tokens
-    float bsum;   // partial sum of (v_min - 1024 sigma) * p
-    float sigma;  // V scale of the current (non-flat) segment: O = sigma * o + bsum
-    int seg;      // current segment (-1 before the first tile)
-    float o[8][4];
-};
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 
-__global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a)
+// q . k_new over 128 dims for one query head (every lane gets the sum), log2 domain
+__device__ __forceinline__ float score_new(const uint16_t *qrow, const uint16_t *krow, int lane)
+{
+    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(qrow) + lane);
+    const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(krow) + lane);
+    float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
+    acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
+    acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
+    acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc * kLog2eOverSqrtD;
+}
+
+// online-softmax pair (max, sum) combine; -inf maxima carry no weight
+__device__ __forceinline__ void ml_combine(float &m, float &l, float m2, float l2)
+{
+    const float M = fmaxf(m, m2);
+    if (M == -INFINITY) return;
+    l = (m == -INFINITY ? 0.0f : l * ex2(m - M)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - M));
+    m = M;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
-    uint8_t *sK = smem;
-    uint8_t *sV = smem + kStages * kStageBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + 2 * kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
-    volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(empty + kStages);  // [0] abort [1] last
-    float *s_snew = reinterpret_cast<float *>(const_cast<int32_t *>(s_flag) + 4);      // [8]
-    dgq_seg_record *s_rec = reinterpret_cast<dgq_seg_record *>(s_snew + 8);
-    float *s_comb = reinterpret_cast<float *>(s_rec + 1);                               // [4][G][132]
-    int32_t *s_cpre = reinterpret_cast<int32_t *>(s_comb + kConsumerWarps * a.G * kPartStride);  // [B+1]
-    int32_t *s_len = s_cpre + (a.B + 1);                                                         // [B]
-
+    float *s_comb = reinterpret_cast<float *>(smem + kWarpsPerCta * kWarpSmem);  // [4][G][132]
+    float *s_red = s_comb + kWarpsPerCta * a.G * kPartStride;                      // [4][8][2] (m, l)
+    float *s_snew = s_red + kWarpsPerCta * 8 * 2;                                   // [8]
+    volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(s_snew + 8);    // [4]
+    int32_t *s_tpre = const_cast<int32_t *>(s_flag) + 4;                            // [B+1]
+    int32_t *s_len = s_tpre + a.B + 1;                                              // [B]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = a.B, Hkv = a.Hkv, G = a.G;
 
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        s_flag[0] = 0;
-        s_flag[1] = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0) {  // exclusive scan of Hkv * max(1, ceil(L_b / 64))
+    for (int i = tid; i < B; i += kAttnThreads) s_len[i] = __ldg(a.seq_lens + i);
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of Hkv * tiles_of(L_b)
         int32_t carry = 0;
         for (int base = 0; base < B; base += 32) {
-            int i = base + lane;
-            int32_t v = 0;
-            if (i < B) {
-                int32_t L = __ldg(a.seq_lens + i);
-                s_len[i] = L;
-                v = Hkv * max(1, (L + kChunk - 1) / kChunk);
-            }
+            const int i = base + lane;
+            const int32_t v = i < B ? Hkv * tiles_of(s_len[i]) : 0;
             int32_t x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            if (i < B) s_cpre[i] = carry + x - v;
+            if (i < B) s_tpre[i] = carry + x - v;
             carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) s_cpre[B] = carry;
+        if (lane == 0) s_tpre[B] = carry;
     }
     __syncthreads();
 
-    const int32_t C = s_cpre[B];
+    const int32_t T = s_tpre[B];
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
-    const int32_t cbeg = (int32_t)(((int64_t)C * cta) / ncta);
-    const int32_t cend = (int32_t)(((int64_t)C * (cta + 1)) / ncta);
+    const int32_t c0 = (int32_t)(((int64_t)T * cta) / ncta);
+    const int32_t c1 = (int32_t)(((int64_t)T * (cta + 1)) / ncta);
+    if (c0 >= c1) return;  // the whole CTA: no barrier follows for it
 
-    // ------------------------------------------------------------------ producer warp
-    if (warp == kConsumerWarps) {
-        if (lane == 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
-            // Block ids of the next chunk are loaded one chunk ahead, so the table lookups overlap
-            // the wait for a free stage instead of sitting between the wait and the copies.
-            const int per_chunk = kChunk / a.bs;  // 1, 2 or 4 blocks
-            auto fetch = [&](const ChunkLoc &c, int32_t *dst) {
-                const int32_t nt = min(kChunk, c.L - kChunk * c.j);
-                const int nblk = nt > 0 ? (nt + a.bs - 1) / a.bs : 0;
-                const int32_t *btrow = a.bt + (int64_t)c.b * a.max_blocks + per_chunk * c.j;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (i < nblk) dst[i] = __ldg(btrow + i);
-            };
-            if (cbeg < cend) {
-                ChunkLoc cur = locate_chunk(cbeg, s_cpre, s_len, B, Hkv);
-                int32_t nxt[4] = {0, 0, 0, 0};
-                fetch(cur, nxt);
-                uint32_t it = 0;
-                for (int32_t x = cbeg; x < cend; ++x) {
-                    const ChunkLoc c = cur;
-                    int32_t blk[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
-                    if (x + 1 < cend) {
-                        advance(cur, s_len, Hkv);
-                        fetch(cur, nxt);
-                    }
-                    const int32_t nt = min(kChunk, c.L - kChunk * c.j);
-                    if (nt <= 0) continue;
-                    const int stage = it % kStages;
-                    const uint32_t use = it / kStages;
-                    if (use > 0 && !mbar_wait_bounded(&empty[stage], (use - 1) & 1)) {
-                        record_error(a.hdr, kErrEmptyWait);
-                        s_flag[0] = 1;
-                        break;
-                    }
-                    if (s_flag[0]) break;
-                    const int nblk = (nt + a.bs - 1) / a.bs;
-                    mbar_arrive_expect_tx(&full[stage], (uint32_t)(nblk * a.bs * kD * 2));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (i < nblk) {
-                            const int32_t y = (blk[i] * Hkv + c.h) * a.bs;
-                            tma_load_2d(sK + stage * kStageBytes + i * a.bs * kD, &tmK, 0, y, &full[stage]);
-                            tma_load_2d(sV + stage * kStageBytes + i * a.bs * kD, &tmV, 0, y, &full[stage]);
-                        }
-                    }
-                    ++it;
-                }
-            }
-        }
-        return;
-    }
-
-    // ------------------------------------------------------------------ consumer warps
-    const int w = warp;                 // 0..3: tokens [16w, 16w+16) of each chunk
     const int r = lane >> 2, cq = lane & 3;
-    const int tr = tau(r);              // 16-byte column (of 8) this lane reads from V rows
-    const bool gvalid = r < G;          // this lane's softmax head
-    const int ctid = tid;               // 0..127
+    const int tr = tau(r);
+    const bool gvalid = r < G;  // this lane's softmax head (rows of S^T)
     const uint32_t M64 = 0x64646464u;
+    const uint32_t ring = smem_u32(smem) + warp * kWarpSmem + lane * 16;
+    const int per_blk = a.bs / kTile;  // tiles per block
+    const uint32_t nthr = kAttnThreads;
+
+    // This warp's tiles: x = xw0 + 4k, k = 0 .. nmine-1, inside the CTA's slice [c0, c1).
+    const int32_t xw0 = c0 + warp;
+    const int32_t nmine = c1 > xw0 ? (c1 - xw0 + kWarpsPerCta - 1) / kWarpsPerCta : 0;
+
+    // ---- block ids, 32 tiles ahead: lane l of a batch holds the block of this warp's tile kbase + l
+    auto fetch_batch = [&](int32_t kbase) -> int32_t {
+        const int32_t k = kbase + lane;
+        int32_t blk = 0;
+        if (k < nmine) {
+            const TileLoc c = locate_tile(xw0 + kWarpsPerCta * k, s_tpre, s_len, B);
+            if (c.L > 0) blk = __ldg(a.bt + (int64_t)c.b * a.max_blocks + c.j / per_blk);
+        }
+        return blk;
+    };
+    int32_t kb = 0;
+    int32_t bq_cur = fetch_batch(0), bq_next = fetch_batch(32);
+
+    // ---- copies of one tile into ring stage `st` (every lane: its 8 pieces); the issue point runs
+    // kDepth tiles ahead of the compute point and always lies in the two fetched batches
+    TileLoc ic;
+    if (nmine > 0) ic = locate_tile(xw0, s_tpre, s_len, B);
+    int32_t kn = 0;  // next of this warp's tiles to issue
+    auto issue = [&](int st) {
+        if (kn - kb >= 32) {
+            kb += 32;
+            bq_cur = bq_next;
+            bq_next = fetch_batch(kb + 32);
+        }
+        const int32_t blk = __shfl_sync(0xffffffffu, bq_cur, (kn - kb) & 31);
+        if (kn < nmine && ic.L > 0) {
+            const int64_t row0 = ((int64_t)blk * Hkv + ic.h) * a.bs + (ic.j % per_blk) * kTile;
+            const uint8_t *kp = a.kpool + row0 * kD;
+            const uint8_t *vp = a.vpool + row0 * kD;
+            const uint32_t dst = ring + st * kTileSmem;
+            cp_async16(dst + 0 * kSlotBytes, kp + tr * kD + cq * 16);
+            cp_async16(dst + 1 * kSlotBytes, kp + tr * kD + (cq + 4) * 16);
+            cp_async16(dst + 2 * kSlotBytes, kp + (8 + tr) * kD + cq * 16);
+            cp_async16(dst + 3 * kSlotBytes, kp + (8 + tr) * kD + (cq + 4) * 16);
+            cp_async16(dst + 4 * kSlotBytes, vp + cq * kD + tr * 16);
+            cp_async16(dst + 5 * kSlotBytes, vp + (cq + 4) * kD + tr * 16);
+            cp_async16(dst + 6 * kSlotBytes, vp + (cq + 8) * kD + tr * 16);
+            cp_async16(dst + 7 * kSlotBytes, vp + (cq + 12) * kD + tr * 16);
+        }
+        cp_async_commit();
+        if (kn < nmine) {
+            if (kn + 1 < nmine)
+                for (int i = 0; i < kWarpsPerCta; ++i) advance(ic, s_len, Hkv);
+            ++kn;
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) issue(k);
 
     uint32_t qa0[8], qa2[8];
-    float qsum = 0.0f;
-    WarpState st;
-    uint32_t it = 0;
+    float o[8][4];
+    int32_t kc = 0;  // next of this warp's tiles to compute
 
-    ChunkLoc cur;
-    if (cbeg < cend) cur = locate_chunk(cbeg, s_cpre, s_len, B, Hkv);
-    for (int32_t x = cbeg; x < cend; ++x) {
-        const ChunkLoc c = cur;
-        if (x + 1 < cend) advance(cur, s_len, Hkv);
-        const int32_t p = c.b * Hkv + c.h;
-        const bool first = (x == cbeg) || (c.j == 0);
-        const bool last = (x == cend - 1) || (c.j == c.nch - 1);
+    // ---- pieces: the CTA walks the pairs its slice touches; all four warps meet at each end
+    TileLoc pc = locate_tile(c0, s_tpre, s_len, B);
+    int32_t ps = c0;
+    while (ps < c1) {
+        const int32_t p = pc.b * Hkv + pc.h;
+        const int32_t fp = s_tpre[pc.b] + pc.h * pc.ntl;  // flat index of the pair's first tile
+        const int32_t pe = min(fp + pc.ntl, c1);            // end of this piece
 
-        if (first) {
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (ctid < 32) reinterpret_cast<uint32_t *>(s_rec)[ctid] = __ldg(reinterpret_cast<const uint32_t *>(a.table + p) + ctid);
-            // Q fragments: head g = r, columns d = 16cq + 64(jj/4) + 4(jj%4) + {0,1 | 2,3}
+        // piece start (per warp): record, Q fragments, state
+        const uint32_t recw = __ldg(reinterpret_cast<const uint32_t *>(a.table + p) + lane);
+        float qsum;
+        {
             float qs = 0.0f;
-            if (gvalid) {
-                const uint16_t *qrow = a.q + ((int64_t)c.b * a.Hq + c.h * G + r) * kD;
+            if (gvalid) {  // Q fragments of head g = r: columns d = 16cq + 64(jj/4) + 4(jj%4) + {0,1 | 2,3}
+                const uint16_t *qrow = a.q + ((int64_t)pc.b * a.Hq + pc.h * G + r) * kD;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(qrow + 16 * cq + 64 * half);
-                    uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-                    uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+                    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        uint32_t h0 = bf16x2_to_f16x2(wv[2 * m]), h1 = bf16x2_to_f16x2(wv[2 * m + 1]);
+                        const uint32_t h0 = bf16x2_to_f16x2(wv[2 * m]), h1 = bf16x2_to_f16x2(wv[2 * m + 1]);
                         qa0[4 * half + m] = h0;
                         qa2[4 * half + m] = h1;
-                        qs += f16lo(h0) + f16hi(h0) + f16lo(h1) + f16hi(h1);
+                        qs += (f16lo(h0) + f16hi(h0)) + (f16lo(h1) + f16hi(h1));
                     }
                 }
             } else {
@@ -334,271 +347,290 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             qs += __shfl_xor_sync(0xffffffffu, qs, 1);
             qs += __shfl_xor_sync(0xffffffffu, qs, 2);
             qsum = qs;
-            st.m = -INFINITY;
-            st.l = 0.0f;
-            st.bsum = 0.0f;
-            st.sigma = 1.0f;
-            st.seg = -1;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.0f;
-            named_bar_sync(1, kConsumerWarps * 32);
         }
+        int seg = -1, vseg = -1;
+        float ak = 0.f, bk = 0.f, cv = 0.f;
+        bool vflat = false;
+        float m_run = -INFINITY, l_run = 0.f, bsum = 0.f, sigma = 1.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
 
-        const int32_t nt = min(kChunk, c.L - kChunk * c.j);
-        if (nt > 0 && !s_flag[0]) {
-            const int stage = it % kStages;
-            const uint32_t use = it / kStages;
-            bool ok = mbar_wait_bounded(&full[stage], use & 1);
-            if (!ok) {
-                record_error(a.hdr, kErrFullWait);
-                s_flag[0] = 1;
-            }
-            const int32_t t0 = kChunk * c.j + 16 * w;
-            const int32_t valid = min(16, c.L - t0);
-            if (ok && valid > 0) {
-                const uint32_t kt = smem_u32(sK) + stage * kStageBytes + w * 2048;
-                const uint32_t vt = smem_u32(sV) + stage * kStageBytes + w * 2048;
-                // ---- segment of this tile
-                const int sg = (t0 >= s_rec->start[1]) + (t0 >= s_rec->start[2]) + (t0 >= s_rec->start[3]) +
-                               (t0 >= s_rec->start[4]);
-                const float kscale = s_rec->k_scale[sg], kmin = s_rec->k_min[sg];
-                const float vscale = s_rec->v_scale[sg], vmin = s_rec->v_min[sg];
-                // A flat V segment (scale 0) decodes to v_min whatever its codes: it only feeds bsum.
-                const bool vflat = !(vscale > 0.0f);
-                if (!vflat && sg != st.seg) {
-                    if (st.seg >= 0) {  // keep sigma * o invariant across the change of scale
-                        const float ratio = st.sigma / vscale;
+        // this warp's tiles of the piece
+        for (; kc < nmine && xw0 + kWarpsPerCta * kc < pe; ++kc) {
+            const int32_t j = xw0 + kWarpsPerCta * kc - fp;  // tile within the pair
+            const int st = kc % kDepth;
+            cp_async_wait<kDepth - 1>();  // this lane's copies of the tile have landed
+            const int32_t tok0 = j * kTile;
+            const int32_t valid = min(kTile, pc.L - tok0);
+            if (valid > 0) {
+                // segment constants (record words: start 2..6, k_min 7.., k_scale 12.., v_min 17.., v_scale 22..)
+                const int sg = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
+                if (sg != seg) {
+                    seg = sg;
+                    const float kmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 7 + sg));
+                    const float kscale = __uint_as_float(__shfl_sync(0xffffffffu, recw, 12 + sg));
+                    const float vmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 17 + sg));
+                    const float vsc = __uint_as_float(__shfl_sync(0xffffffffu, recw, 22 + sg));
+                    // a flat V segment (scale 0) decodes to v_min whatever its codes: it only feeds bsum
+                    vflat = !(vsc > 0.0f);
+                    ak = kscale * kLog2eOverSqrtD;
+                    bk = (kmin - 1024.0f * kscale) * qsum * kLog2eOverSqrtD;
+                    cv = vflat ? vmin : vmin - 1024.0f * vsc;
+                    if (!vflat && sg != vseg) {
+                        if (vseg >= 0) {  // keep sigma * o invariant across the change of V scale
+                            const float ratio = sigma / vsc;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
+                            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) st.o[i][e] *= ratio;
+                                for (int e = 0; e < 4; ++e) o[i][e] *= ratio;
+                        }
+                        sigma = vsc;
+                        vseg = sg;
                     }
-                    st.sigma = vscale;
-                    st.seg = sg;
                 }
-                const float ak = kscale * kLog2eOverSqrtD;
-                const float bk = (kmin - 1024.0f * kscale) * qsum * kLog2eOverSqrtD;
-                const float cv = vflat ? vmin : vmin - 1024.0f * vscale;
 
-                // ---- S^T = Q K^T: two n-tiles of 8 tokens, 8 k-steps of 16 columns
-                // four independent accumulator chains (two n-tiles x even/odd k-steps)
-                float sacc[2][4], sacc2[2][4];
-                uint4 klo[2], khi[2];
+                const uint32_t tile = ring + st * kTileSmem;
+                // S^T = Q K^T: two n-tiles of 8 tokens x 8 k-steps, four accumulator chains
+                const uint4 k0 = ld_shared_v4(tile + 0 * kSlotBytes), k1 = ld_shared_v4(tile + 1 * kSlotBytes);
+                const uint4 k2 = ld_shared_v4(tile + 2 * kSlotBytes), k3 = ld_shared_v4(tile + 3 * kSlotBytes);
+                float sa[2][4], sb[2][4];
 #pragma unroll
-                for (int nt2 = 0; nt2 < 2; ++nt2) {
-                    const int row = nt2 * 8 + tr;  // token row this lane supplies (n = r)
-                    const uint32_t rp = kt + row * kD;
-                    klo[nt2] = lds128(rp + ((cq ^ (row & 7)) << 4));
-                    khi[nt2] = lds128(rp + (((cq + 4) ^ (row & 7)) << 4));
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[nt2][e] = sacc2[nt2][e] = 0.0f;
-                }
+                for (int e = 0; e < 4; ++e) sa[0][e] = sa[1][e] = sb[0][e] = sb[1][e] = 0.0f;
 #pragma unroll
                 for (int jj = 0; jj < 8; jj += 2) {
-#pragma unroll
-                    for (int nt2 = 0; nt2 < 2; ++nt2) {
-                        const uint32_t w0 = word(jj < 4 ? klo[nt2] : khi[nt2], jj & 3);
-                        const uint32_t w1 = word(jj < 4 ? klo[nt2] : khi[nt2], (jj + 1) & 3);
-                        mma16816(sacc[nt2], qa0[jj], 0u, qa2[jj], 0u, prmt(w0, M64, 0x4140), prmt(w0, M64, 0x4342));
-                        mma16816(sacc2[nt2], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w1, M64, 0x4140),
-                                 prmt(w1, M64, 0x4342));
-                    }
+                    const uint4 &lo0 = jj < 4 ? k0 : k1;  // n-tile 0: row tau(r), columns cq | cq + 4
+                    const uint4 &lo1 = jj < 4 ? k2 : k3;  // n-tile 1: row 8 + tau(r)
+                    const uint32_t w00 = word(lo0, jj & 3), w01 = word(lo0, (jj + 1) & 3);
+                    const uint32_t w10 = word(lo1, jj & 3), w11 = word(lo1, (jj + 1) & 3);
+                    mma16816(sa[0], qa0[jj], 0u, qa2[jj], 0u, prmt(w00, M64, 0x4140), prmt(w00, M64, 0x4342));
+                    mma16816(sa[1], qa0[jj], 0u, qa2[jj], 0u, prmt(w10, M64, 0x4140), prmt(w10, M64, 0x4342));
+                    mma16816(sb[0], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w01, M64, 0x4140), prmt(w01, M64, 0x4342));
+                    mma16816(sb[1], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w11, M64, 0x4140), prmt(w11, M64, 0x4342));
                 }
-#pragma unroll
-                for (int nt2 = 0; nt2 < 2; ++nt2) {
-                    sacc[nt2][0] += sacc2[nt2][0];
-                    sacc[nt2][1] += sacc2[nt2][1];
-                }
-                // lane scores for head r: tokens cq, cq+4 (tile 0) and 8+cq, 12+cq (tile 1)
+                // lane scores for head r: tokens cq, cq+4 (n-tile 0) and 8+cq, 12+cq (n-tile 1)
                 float z[4];
-                z[0] = (cq < valid) ? fmaf(ak, sacc[0][0], bk) : -INFINITY;
-                z[1] = (cq + 4 < valid) ? fmaf(ak, sacc[0][1], bk) : -INFINITY;
-                z[2] = (cq + 8 < valid) ? fmaf(ak, sacc[1][0], bk) : -INFINITY;
-                z[3] = (cq + 12 < valid) ? fmaf(ak, sacc[1][1], bk) : -INFINITY;
+                z[0] = (cq < valid) ? fmaf(ak, sa[0][0] + sb[0][0], bk) : -INFINITY;
+                z[1] = (cq + 4 < valid) ? fmaf(ak, sa[0][1] + sb[0][1], bk) : -INFINITY;
+                z[2] = (cq + 8 < valid) ? fmaf(ak, sa[1][0] + sb[1][0], bk) : -INFINITY;
+                z[3] = (cq + 12 < valid) ? fmaf(ak, sa[1][1] + sb[1][1], bk) : -INFINITY;
                 float mt = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-                const bool need = gvalid && (mt > st.m + kLazyRescale);
+                const bool need = gvalid && (mt > m_run + kLazyRescale);
                 float alpha = 1.0f;
                 if (need) {
-                    alpha = (st.m == -INFINITY) ? 0.0f : ex2(st.m - mt);
-                    st.m = mt;
-                    st.l *= alpha;
-                    st.bsum *= alpha;
+                    alpha = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mt);
+                    m_run = mt;
+                    l_run *= alpha;
+                    bsum *= alpha;
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * cq);      // head 2cq
                     const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * cq + 4);  // head 2cq+1
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        st.o[i][0] *= a0;
-                        st.o[i][2] *= a0;
-                        st.o[i][1] *= a1;
-                        st.o[i][3] *= a1;
+                        o[i][0] *= a0;
+                        o[i][2] *= a0;
+                        o[i][1] *= a1;
+                        o[i][3] *= a1;
                     }
                 }
                 float pr[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pr[e] = gvalid ? ex2(z[e] - st.m) : 0.0f;
+                for (int e = 0; e < 4; ++e) pr[e] = gvalid ? ex2(z[e] - m_run) : 0.0f;
                 // the tensor cores see p rounded to fp16; the sums use the same rounded weights so
                 // the 1024 offset of the codes cancels exactly against bsum
                 const uint32_t pb0 = f32x2_to_f16x2(pr[0], pr[1]);
                 const uint32_t pb1 = f32x2_to_f16x2(pr[2], pr[3]);
                 const float psum = (f16lo(pb0) + f16hi(pb0)) + (f16lo(pb1) + f16hi(pb1));
-                st.l += psum;
-                st.bsum = fmaf(cv, psum, st.bsum);
+                l_run += psum;
+                bsum = fmaf(cv, psum, bsum);
 
-                // ---- O^T += V^T P^T: rows (d) 16*tr + 2i (+1), k = tokens cq, cq+4, 8+cq, 12+cq
+                // O^T += V^T P^T: rows (d) 16*tr + 2i (+1), k = tokens cq, cq+4, 8+cq, 12+cq
                 if (!vflat) {
-                const uint4 va = lds128(vt + cq * kD + ((tr ^ cq) << 4));
-                const uint4 vb = lds128(vt + (cq + 4) * kD + ((tr ^ (cq + 4)) << 4));
-                const uint4 vc = lds128(vt + (cq + 8) * kD + ((tr ^ cq) << 4));
-                const uint4 vd = lds128(vt + (cq + 12) * kD + ((tr ^ (cq + 4)) << 4));
+                    const uint4 va = ld_shared_v4(tile + 4 * kSlotBytes), vb = ld_shared_v4(tile + 5 * kSlotBytes);
+                    const uint4 vc = ld_shared_v4(tile + 6 * kSlotBytes), vd = ld_shared_v4(tile + 7 * kSlotBytes);
 #pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    const uint32_t xab01 = prmt(word(va, wi), word(vb, wi), 0x5140);
-                    const uint32_t xab23 = prmt(word(va, wi), word(vb, wi), 0x7362);
-                    const uint32_t xcd01 = prmt(word(vc, wi), word(vd, wi), 0x5140);
-                    const uint32_t xcd23 = prmt(word(vc, wi), word(vd, wi), 0x7362);
-                    mma16816(st.o[2 * wi], prmt(xab01, M64, 0x4140), prmt(xab01, M64, 0x4342),
-                             prmt(xcd01, M64, 0x4140), prmt(xcd01, M64, 0x4342), pb0, pb1);
-                    mma16816(st.o[2 * wi + 1], prmt(xab23, M64, 0x4140), prmt(xab23, M64, 0x4342),
-                             prmt(xcd23, M64, 0x4140), prmt(xcd23, M64, 0x4342), pb0, pb1);
-                }
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint32_t xab01 = prmt(word(va, wi), word(vb, wi), 0x5140);
+                        const uint32_t xab23 = prmt(word(va, wi), word(vb, wi), 0x7362);
+                        const uint32_t xcd01 = prmt(word(vc, wi), word(vd, wi), 0x5140);
+                        const uint32_t xcd23 = prmt(word(vc, wi), word(vd, wi), 0x7362);
+                        mma16816(o[2 * wi], prmt(xab01, M64, 0x4140), prmt(xab01, M64, 0x4342),
+                                 prmt(xcd01, M64, 0x4140), prmt(xcd01, M64, 0x4342), pb0, pb1);
+                        mma16816(o[2 * wi + 1], prmt(xab23, M64, 0x4140), prmt(xab23, M64, 0x4342),
+                                 prmt(xcd23, M64, 0x4140), prmt(xcd23, M64, 0x4342), pb0, pb1);
+                    }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            ++it;
+            issue(st);  // refill this stage kDepth tiles ahead (its reads above are complete)
         }
 
-        if (!last) continue;
-
-        // ================================================================ end of a piece
-        // reduce the per-lane partial sums of head r over its four lanes
-        float l = st.l, bsum = st.bsum;
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+        // ================================================ end of the piece: combine the four warps
         {
-            float *cw = s_comb + w * G * kPartStride;
+            float l = l_run, bs_ = bsum;
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            bs_ += __shfl_xor_sync(0xffffffffu, bs_, 1);
+            bs_ += __shfl_xor_sync(0xffffffffu, bs_, 2);
+            float *cw = s_comb + warp * G * kPartStride;
             if (gvalid && cq == 0) {
-                cw[r * kPartStride + 0] = st.m;
+                cw[r * kPartStride + 0] = m_run;
                 cw[r * kPartStride + 1] = l;
             }
-            const float b0 = __shfl_sync(0xffffffffu, bsum, 8 * cq);
-            const float b1 = __shfl_sync(0xffffffffu, bsum, 8 * cq + 4);
             const int g0 = 2 * cq, g1 = 2 * cq + 1;
+            const float b0 = __shfl_sync(0xffffffffu, bs_, 8 * cq), b1 = __shfl_sync(0xffffffffu, bs_, 8 * cq + 4);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int d = 16 * tr + 2 * i;
-                if (g0 < G) {
-                    cw[g0 * kPartStride + 2 + d] = fmaf(st.sigma, st.o[i][0], b0);
-                    cw[g0 * kPartStride + 3 + d] = fmaf(st.sigma, st.o[i][2], b0);
-                }
-                if (g1 < G) {
-                    cw[g1 * kPartStride + 2 + d] = fmaf(st.sigma, st.o[i][1], b1);
-                    cw[g1 * kPartStride + 3 + d] = fmaf(st.sigma, st.o[i][3], b1);
-                }
+                if (g0 < G)
+                    *reinterpret_cast<float2 *>(cw + g0 * kPartStride + 4 + d) =
+                        make_float2(fmaf(sigma, o[i][0], b0), fmaf(sigma, o[i][2], b0));
+                if (g1 < G)
+                    *reinterpret_cast<float2 *>(cw + g1 * kPartStride + 4 + d) =
+                        make_float2(fmaf(sigma, o[i][1], b1), fmaf(sigma, o[i][3], b1));
+            }
+            // the current token's score s_new = q . k_new (log2 domain), one warp per head
+            const uint16_t *krow = a.knew + ((int64_t)pc.b * Hkv + pc.h) * kD;
+            for (int g = warp; g < G; g += kWarpsPerCta) {
+                const float sn = score_new(a.q + ((int64_t)pc.b * a.Hq + pc.h * G + g) * kD, krow, lane);
+                if (lane == 0) s_snew[g] = sn;
             }
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(1, nthr);
 
-        // the current token's score s_new = q . k_new / sqrt(D) (log2 domain), one warp per head
-        for (int g = w; g < G; g += kConsumerWarps) {
-            const uint16_t *qrow = a.q + ((int64_t)c.b * a.Hq + c.h * G + g) * kD;
-            const uint16_t *krow = a.knew + ((int64_t)c.b * Hkv + c.h) * kD;
-            float acc = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int dd = lane + 32 * i;
-                acc = fmaf(__uint_as_float((uint32_t)__ldg(qrow + dd) << 16),
-                           __uint_as_float((uint32_t)__ldg(krow + dd) << 16), acc);
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) s_snew[g] = acc * kLog2eOverSqrtD;
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-
-        // combine the four warps (thread ctid owns column d = ctid), then either finish the
-        // pair here (it has a single piece) or publish this piece
-        const int d = ctid;
-        const float vn = __uint_as_float((uint32_t)__ldg(a.vnew + ((int64_t)c.b * Hkv + c.h) * kD + d) << 16);
-        uint16_t *orow = a.out + ((int64_t)c.b * a.Hq + c.h * G) * kD + d;
-        const int32_t first_chunk = s_cpre[c.b] + c.h * c.nch;
-        const int32_t cfirst = owner(first_chunk, C, ncta);
-        const int32_t clast = owner(first_chunk + c.nch - 1, C, ncta);
+        const int d = tid;  // thread d owns output column d
+        const float vn = bf16lo_to_f32((uint32_t)__ldg(a.vnew + ((int64_t)pc.b * Hkv + pc.h) * kD + d));
+        uint16_t *orow = a.out + ((int64_t)pc.b * a.Hq + pc.h * G) * kD + d;
+        const int32_t cfirst = owner(fp, T, ncta);
+        const int32_t clast = owner(fp + pc.ntl - 1, T, ncta);
         for (int g = 0; g < G; ++g) {
-            float M = -INFINITY;
+            float M = -INFINITY, L = 0.0f, O = 0.0f;
 #pragma unroll
-            for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, s_comb[(ww * G + g) * kPartStride]);
-            float Ls = 0.0f, Os = 0.0f;
+            for (int ww = 0; ww < kWarpsPerCta; ++ww) M = fmaxf(M, s_comb[(ww * G + g) * kPartStride]);
             if (M != -INFINITY) {
 #pragma unroll
-                for (int ww = 0; ww < kConsumerWarps; ++ww) {
+                for (int ww = 0; ww < kWarpsPerCta; ++ww) {
                     const float *cw = s_comb + (ww * G + g) * kPartStride;
-                    const float mw = cw[0];
-                    if (mw != -INFINITY) {
-                        const float f = exp2f(mw - M);
-                        Ls = fmaf(cw[1], f, Ls);
-                        Os = fmaf(cw[2 + d], f, Os);
+                    if (cw[0] != -INFINITY) {
+                        const float f = ex2(cw[0] - M);
+                        L = fmaf(cw[1], f, L);
+                        O = fmaf(cw[4 + d], f, O);
                     }
                 }
             }
             if (cfirst == clast) {
-                orow[g * kD] = finish(M, Ls, Os, s_snew[g], vn);
-            } else {
+                __nv_bfloat16 ob = __float2bfloat16_rn(finish(M, L, O, s_snew[g], vn));
+                orow[g * kD] = *reinterpret_cast<uint16_t *>(&ob);
+            } else {  // publish this CTA's piece at slot p + cta (unique per piece)
                 float *dst = a.part + ((int64_t)(p + cta) * G + g) * kPartStride;
-                __stcg(dst + 2 + d, Os);
-                if (d == 0) {
-                    __stcg(dst + 0, M);
-                    __stcg(dst + 1, Ls);
-                }
+                __stcg(dst + 4 + d, O);
+                if (d == 0) __stcg(reinterpret_cast<float2 *>(dst), make_float2(M, L));
             }
         }
         if (cfirst != clast) {
-            // the last piece to arrive merges all pieces of the pair in CTA order
             __threadfence();
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (ctid == 0) {
+            named_bar_sync(1, nthr);
+            if (tid == 0) {
                 uint32_t pieces = 0;  // CTAs holding a piece of this pair
-                for (int32_t cc = cfirst; cc <= clast; ++cc) pieces += owns_chunks(cc, C, ncta) ? 1u : 0u;
+                for (int32_t cc = cfirst; cc <= clast; ++cc) pieces += owns_tiles(cc, T, ncta) ? 1u : 0u;
                 const uint32_t old = atomicAdd(a.pair_count + p, 1u);
-                const bool is_last = old + 1u == pieces;
-                if (is_last) {
+                const bool last = old + 1u == pieces;
+                if (last) {
                     __threadfence();
                     a.pair_count[p] = 0;
                 }
-                s_flag[1] = is_last ? 1 : 0;
+                s_flag[0] = last ? 1 : 0;
             }
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (s_flag[1]) {
-                for (int g = 0; g < G; ++g) {
-                    float M = -INFINITY;
-                    for (int32_t cc = cfirst; cc <= clast; ++cc)
-                        if (owns_chunks(cc, C, ncta))
-                            M = fmaxf(M, __ldcg(a.part + ((int64_t)(p + cc) * G + g) * kPartStride));
-                    float Ls = 0.0f, Os = 0.0f;
-                    if (M != -INFINITY) {
-                        for (int32_t cc = cfirst; cc <= clast; ++cc) {
-                            if (!owns_chunks(cc, C, ncta)) continue;
-                            const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
-                            const float mc = __ldcg(src);
-                            if (mc != -INFINITY) {
-                                const float f = exp2f(mc - M);
-                                Ls = fmaf(__ldcg(src + 1), f, Ls);
-                                Os = fmaf(__ldcg(src + 2 + d), f, Os);
-                            }
+            named_bar_sync(1, nthr);
+            if (s_flag[0]) {
+                // merge every piece of the pair, in CTA order of the slots
+                // (1) per-head (max, sum): thread t folds slots cfirst + t, + 128, ...
+                float mg[8], lg[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    mg[g] = -INFINITY;
+                    lg[g] = 0.0f;
+                }
+                for (int32_t cc = cfirst + tid; cc <= clast; cc += kAttnThreads) {
+                    if (!owns_tiles(cc, T, ncta)) continue;
+                    const float *src = a.part + (int64_t)(p + cc) * G * kPartStride;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        if (g < G) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + g * kPartStride));
+                            ml_combine(mg[g], lg[g], ml.x, ml.y);
                         }
                     }
-                    orow[g * kD] = finish(M, Ls, Os, s_snew[g], vn);
+                }
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+#pragma unroll
+                    for (int off = 16; off; off >>= 1) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, mg[g], off);
+                        const float l2 = __shfl_xor_sync(0xffffffffu, lg[g], off);
+                        ml_combine(mg[g], lg[g], m2, l2);
+                    }
+                    if (lane == 0 && g < G) {
+                        s_red[(warp * 8 + g) * 2] = mg[g];
+                        s_red[(warp * 8 + g) * 2 + 1] = lg[g];
+                    }
+                }
+                named_bar_sync(1, nthr);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    if (g < G) {
+                        mg[g] = s_red[g * 2];
+                        lg[g] = s_red[g * 2 + 1];
+#pragma unroll
+                        for (int ww = 1; ww < kWarpsPerCta; ++ww)
+                            ml_combine(mg[g], lg[g], s_red[(ww * 8 + g) * 2], s_red[(ww * 8 + g) * 2 + 1]);
+                    }
+                }
+                // (2) weighted O: warp w folds slots cfirst + w, + 4, ...; lane owns d = 4 lane .. + 3
+                float4 acc[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int32_t cc = cfirst + warp; cc <= clast; cc += kWarpsPerCta) {
+                    if (!owns_tiles(cc, T, ncta)) continue;
+                    const float *src = a.part + (int64_t)(p + cc) * G * kPartStride;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        if (g < G) {
+                            const float mw = __ldcg(src + g * kPartStride);
+                            const float4 ov = __ldcg(reinterpret_cast<const float4 *>(src + g * kPartStride + 4) + lane);
+                            const float f = mw == -INFINITY ? 0.0f : ex2(mw - mg[g]);
+                            acc[g].x = fmaf(ov.x, f, acc[g].x);
+                            acc[g].y = fmaf(ov.y, f, acc[g].y);
+                            acc[g].z = fmaf(ov.z, f, acc[g].z);
+                            acc[g].w = fmaf(ov.w, f, acc[g].w);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    if (g < G)
+                        *reinterpret_cast<float4 *>(s_comb + (warp * G + g) * kPartStride + 4 + 4 * lane) = acc[g];
+                named_bar_sync(1, nthr);
+                for (int g = 0; g < G; ++g) {
+                    float O = 0.0f;
+#pragma unroll
+                    for (int ww = 0; ww < kWarpsPerCta; ++ww) O += s_comb[(ww * G + g) * kPartStride + 4 + d];
+                    __nv_bfloat16 ob = __float2bfloat16_rn(finish(mg[g], lg[g], O, s_snew[g], vn));
+                    orow[g * kD] = *reinterpret_cast<uint16_t *>(&ob);
                 }
             }
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(1, nthr);  // s_comb / s_red / s_snew are free again
+
+        // next pair
+        ps = pe;
+        if (ps < c1) {
+            pc.j = pc.ntl - 1;
+            advance(pc, s_len, Hkv);
+        }
     }
+    cp_async_wait<0>();  // no copy may still target shared memory when the CTA exits
 }
 
 }  // namespace dgq
@@ -607,35 +639,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
 namespace dgq {
 
-// 2-D map over a pool [num_blocks * Hkv * bs rows, 128 bytes], box = one (block, head) tile.
-static bool make_pool_map(CUtensorMap *map, const uint8_t *pool, int64_t rows, int32_t bs)
-{
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kD};
-    cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)bs};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(pool), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 size_t attn_smem_bytes(int32_t B, int32_t G)
 {
-    return 1024 + 2 * kStages * kStageBytes + 2 * kStages * 8 + 16 + 32 + sizeof(dgq_seg_record) +
-           (size_t)kConsumerWarps * G * kPartStride * 4 + (size_t)(2 * B + 1) * 4;
+    return 1024 + (size_t)kWarpsPerCta * kWarpSmem + (size_t)kWarpsPerCta * G * kPartStride * 4 +
+           (kWarpsPerCta * 8 * 2 + 8 + 4) * 4 + (size_t)(2 * B + 1) * 4;
 }
 
-int attn_max_ctas(int nsm) { return nsm * 3; }
-
+int attn_max_ctas(int nsm) { return nsm * kMaxCtasPerSm; }
 
 AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm)
 {
     AttnLayout l;
-    size_t P = (size_t)batch * Hkv;
-    size_t G = (size_t)(Hq / Hkv);
+    const size_t P = (size_t)batch * Hkv;
+    const size_t G = (size_t)(Hq / Hkv);
     size_t off = sizeof(WsHeader);
     l.off_count = off;
     off = (off + P * 4 + 255) & ~size_t(255);
@@ -650,13 +666,8 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
                         int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
                         void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
 {
+    (void)num_blocks;
     *map_failed = false;
-    CUtensorMap mk, mv;
-    const int64_t rows = (int64_t)num_blocks * Hkv * bs;
-    if (!make_pool_map(&mk, kpool, rows, bs) || !make_pool_map(&mv, vpool, rows, bs)) {
-        *map_failed = true;
-        return cudaErrorInvalidValue;
-    }
     const int32_t G = Hq / Hkv;
     AttnLayout l = attn_layout(B, Hq, Hkv, nsm);
     char *base = static_cast<char *>(ws);
@@ -664,6 +675,8 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.q = static_cast<const uint16_t *>(q);
     a.knew = static_cast<const uint16_t *>(knew);
     a.vnew = static_cast<const uint16_t *>(vnew);
+    a.kpool = kpool;
+    a.vpool = vpool;
     a.table = table;
     a.bt = bt;
     a.seq_lens = seq_lens;
@@ -685,13 +698,13 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel, kAttnThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    if (occ > 3) occ = 3;
-    // upper bound on chunks: every request at max_seqlen
-    const int64_t cmax = (int64_t)B * Hkv * (int64_t)((max_seqlen + kChunk - 1) / kChunk > 0 ? (max_seqlen + kChunk - 1) / kChunk : 1);
+    if (occ > kMaxCtasPerSm) occ = kMaxCtasPerSm;
+    // upper bound on tiles (every request at max_seqlen): no more CTAs than tiles
+    const int64_t tiles = (int64_t)B * Hkv * (max_seqlen > 0 ? (max_seqlen + kTile - 1) / kTile : 1);
     int64_t grid = (int64_t)nsm * occ;
-    if (grid > cmax) grid = cmax;
+    if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
-    attn_kernel<<<(unsigned)grid, kAttnThreads, smem, stream>>>(mk, mv, a);
+    attn_kernel<<<(unsigned)grid, kAttnThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -13,13 +13,14 @@
 //    contiguous slice of it, so mixed lengths and a single long request balance alike.  The
 //    four warps of a CTA take every fourth tile of the slice and combine their softmax states
 //    in shared memory wherever the slice crosses from one pair to the next.  A CTA's part of a
-//    pair is a "piece"; a pair covered by several CTAs is merged by the CTA that finishes it
-//    last (all 128 threads, in CTA order of the pieces: bitwise reproducible on a given GPU),
-//    together with the current token.
-//  * Loads: each lane copies exactly the 128 bytes of codes it will use from a tile (4 x 16 B
-//    of K rows for its MMA B fragment, 4 x 16 B of V rows for its A fragment) with cp.async into
-//    its warp's shared-memory ring, four tiles deep (slot-major, so every access is conflict
-//    free).  Measured on this GPU, the per-copy issue cost of TMA caps single-tile copies of
+//    pair is a "piece".  A pair inside one CTA is finished there; the pieces of a pair shared by
+//    several CTAs go to a small combine kernel chained with programmatic dependent launch, which
+//    folds them in a fixed order (bitwise reproducible on a given GPU) with the current token.
+//    The next pieces' record, query rows and current key/value are staged in shared memory by
+//    bulk copies while the current piece streams, so a piece boundary waits on no global load.
+//  * Loads: each warp copies its tiles' K and V rows with cp.async (whole 128-byte rows, four
+//    rows per instruction) into its own shared-memory ring, four tiles deep, with the 16-byte
+//    columns of row i XOR-permuted by i % 8 so the fragment reads hit distinct banks.  Measured on this GPU, the per-copy issue cost of TMA caps single-tile copies of
 //    2 KB blocks at 2-4 TB/s, while per-thread 16-byte copies stream at the HBM rate.  Block ids
 //    come 32 tiles ahead from one coalesced load per warp.
 //  * Math: codes become fp16 (1024 + q) with byte permutes, and the GQA query group multiplies
@@ -45,8 +46,8 @@ constexpr int kWarpsPerCta = 4;
 constexpr int kAttnThreads = kWarpsPerCta * 32;
 constexpr int kMaxCtasPerSm = 3;
 constexpr int kDepth = 4;                          // tiles in flight per warp
-constexpr int kSlotBytes = 32 * 16;                // one 16-byte piece per lane
-constexpr int kTileSmem = 8 * kSlotBytes;          // 4 K pieces + 4 V pieces per lane = 4 KB
+constexpr int kTileBytes = kTile * kD;            // 16 rows of 128 codes = 2 KB
+constexpr int kTileSmem = 2 * kTileBytes;          // K tile + V tile
 constexpr int kWarpSmem = kDepth * kTileSmem;
 constexpr int kPartStride = 132;                   // floats per (piece, head) partial: m, l, pad, pad, O[128]
 constexpr float kLog2eOverSqrtD = 0.12751743074570180f;  // log2(e) / sqrt(128)
@@ -63,7 +64,7 @@ struct AttnArgs {
     const int32_t *seq_lens;
     uint16_t *out;
     WsHeader *hdr;
-    uint32_t *pair_count;
+    int2 *pair_info;  // per pair: first and last CTA holding a piece of it
     float *part;
     int32_t B, Hq, Hkv, G, bs, max_blocks;
 };
@@ -199,28 +200,53 @@ __device__ __forceinline__ float score_new(const uint16_t *qrow, const uint16_t 
     return acc * kLog2eOverSqrtD;
 }
 
-// online-softmax pair (max, sum) combine; -inf maxima carry no weight
-__device__ __forceinline__ void ml_combine(float &m, float &l, float m2, float l2)
+// One pair's slice of this CTA: request b, KV head h, its tiles in the flat list start at fp.
+struct Piece {
+    int32_t b, h, ntl, L, fp;
+};
+
+__device__ __forceinline__ void next_piece(Piece &pz, const int32_t *s_tpre, const int32_t *s_len, int32_t B,
+                                           int32_t Hkv)
 {
-    const float M = fmaxf(m, m2);
-    if (M == -INFINITY) return;
-    l = (m == -INFINITY ? 0.0f : l * ex2(m - M)) + (m2 == -INFINITY ? 0.0f : l2 * ex2(m2 - M));
-    m = M;
+    if (++pz.h == Hkv) {
+        pz.h = 0;
+        if (++pz.b >= B) {
+            pz.fp = INT32_MAX;
+            return;
+        }
+        pz.L = s_len[pz.b];
+        pz.ntl = tiles_of(pz.L);
+    }
+    pz.fp = s_tpre[pz.b] + pz.h * pz.ntl;
 }
+
+// Per-piece data staged in shared memory ahead of use: the segment record, the current token's
+// key and value and the group's query rows.
+constexpr int kPbRec = 0, kPbKnew = 128, kPbVnew = 384, kPbQ = 640;
+constexpr int kPieceBytes = kPbQ + 8 * 256;
+
+// Workspace header words used to hand the split to the combine kernel.
+constexpr int kHdrTiles = 0, kHdrCtas = 1;
 
 __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
-    float *s_comb = reinterpret_cast<float *>(smem + kWarpsPerCta * kWarpSmem);  // [4][G][132]
-    float *s_red = s_comb + kWarpsPerCta * a.G * kPartStride;                      // [4][8][2] (m, l)
-    float *s_snew = s_red + kWarpsPerCta * 8 * 2;                                   // [8]
-    volatile int32_t *s_flag = reinterpret_cast<volatile int32_t *>(s_snew + 8);    // [4]
-    int32_t *s_tpre = const_cast<int32_t *>(s_flag) + 4;                            // [B+1]
-    int32_t *s_len = s_tpre + a.B + 1;                                              // [B]
+    uint8_t *pbuf = smem + kWarpsPerCta * kWarpSmem;                                 // [2][kPieceBytes]
+    uint64_t *pbar = reinterpret_cast<uint64_t *>(pbuf + 2 * kPieceBytes);          // [2]
+    float *s_comb = reinterpret_cast<float *>(pbar + 2);                           // [4][G][132]
+    float *s_snew = s_comb + kWarpsPerCta * a.G * kPartStride;                       // [8]
+    int32_t *s_tpre = reinterpret_cast<int32_t *>(s_snew + 8);                       // [B+1]
+    int32_t *s_len = s_tpre + a.B + 1;                                               // [B]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t B = a.B, Hkv = a.Hkv, G = a.G;
 
+    pdl_launch_dependents();  // the combine kernel may be scheduled while this one runs
+    if (tid == 0) {
+        mbar_init(&pbar[0], 1);
+        mbar_init(&pbar[1], 1);
+        fence_barrier_init();
+    }
     for (int i = tid; i < B; i += kAttnThreads) s_len[i] = __ldg(a.seq_lens + i);
     __syncthreads();
     if (warp == 0) {  // exclusive scan of Hkv * tiles_of(L_b)
@@ -243,6 +269,10 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 
     const int32_t T = s_tpre[B];
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
+    if (cta == 0 && tid == 0) {
+        a.hdr->pad[kHdrTiles] = (uint32_t)T;
+        a.hdr->pad[kHdrCtas] = (uint32_t)ncta;
+    }
     const int32_t c0 = (int32_t)(((int64_t)T * cta) / ncta);
     const int32_t c1 = (int32_t)(((int64_t)T * (cta + 1)) / ncta);
     if (c0 >= c1) return;  // the whole CTA: no barrier follows for it
@@ -251,9 +281,34 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     const int tr = tau(r);
     const bool gvalid = r < G;  // this lane's softmax head (rows of S^T)
     const uint32_t M64 = 0x64646464u;
-    const uint32_t ring = smem_u32(smem) + warp * kWarpSmem + lane * 16;
+    const uint32_t ring = smem_u32(smem) + warp * kWarpSmem;
     const int per_blk = a.bs / kTile;  // tiles per block
     const uint32_t nthr = kAttnThreads;
+
+    // ---- pieces of this CTA's slice, and the staging of their data two pieces ahead
+    Piece cur;
+    {
+        const TileLoc c = locate_tile(c0, s_tpre, s_len, B);
+        cur.b = c.b; cur.h = c.h; cur.ntl = c.ntl; cur.L = c.L;
+        cur.fp = s_tpre[c.b] + c.h * c.ntl;
+    }
+    auto stage_piece = [&](const Piece &pz, int buf) {  // thread 0 only
+        uint8_t *dst = pbuf + buf * kPieceBytes;
+        mbar_arrive_expect_tx(&pbar[buf], (uint32_t)(kPbQ + 256 * G));
+        bulk_load(dst + kPbRec, a.table + (int64_t)pz.b * Hkv + pz.h, 128, &pbar[buf]);
+        bulk_load(dst + kPbKnew, a.knew + ((int64_t)pz.b * Hkv + pz.h) * kD, 256, &pbar[buf]);
+        bulk_load(dst + kPbVnew, a.vnew + ((int64_t)pz.b * Hkv + pz.h) * kD, 256, &pbar[buf]);
+        bulk_load(dst + kPbQ, a.q + ((int64_t)pz.b * a.Hq + pz.h * G) * kD, (uint32_t)(256 * G), &pbar[buf]);
+    };
+    Piece ahead = cur;  // the next piece to stage
+    if (tid == 0) {
+        stage_piece(ahead, 0);
+        next_piece(ahead, s_tpre, s_len, B, Hkv);
+        if (ahead.fp < c1) stage_piece(ahead, 1);
+    } else {
+        next_piece(ahead, s_tpre, s_len, B, Hkv);
+    }
+    next_piece(ahead, s_tpre, s_len, B, Hkv);  // ahead = piece 2
 
     // This warp's tiles: x = xw0 + 4k, k = 0 .. nmine-1, inside the CTA's slice [c0, c1).
     const int32_t xw0 = c0 + warp;
@@ -272,8 +327,8 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     int32_t kb = 0;
     int32_t bq_cur = fetch_batch(0), bq_next = fetch_batch(32);
 
-    // ---- copies of one tile into ring stage `st` (every lane: its 8 pieces); the issue point runs
-    // kDepth tiles ahead of the compute point and always lies in the two fetched batches
+    // ---- copies of one tile into ring stage `st`; the issue point runs kDepth tiles ahead of the
+    // compute point and always lies in the two fetched batches
     TileLoc ic;
     if (nmine > 0) ic = locate_tile(xw0, s_tpre, s_len, B);
     int32_t kn = 0;  // next of this warp's tiles to issue
@@ -288,15 +343,16 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
             const int64_t row0 = ((int64_t)blk * Hkv + ic.h) * a.bs + (ic.j % per_blk) * kTile;
             const uint8_t *kp = a.kpool + row0 * kD;
             const uint8_t *vp = a.vpool + row0 * kD;
+            // whole 128-byte rows: lane l copies 16-byte column l % 8 of rows 4i + l / 8, stored
+            // at column (l % 8) ^ (row % 8) so the fragment reads below hit 8 distinct columns
             const uint32_t dst = ring + st * kTileSmem;
-            cp_async16(dst + 0 * kSlotBytes, kp + tr * kD + cq * 16);
-            cp_async16(dst + 1 * kSlotBytes, kp + tr * kD + (cq + 4) * 16);
-            cp_async16(dst + 2 * kSlotBytes, kp + (8 + tr) * kD + cq * 16);
-            cp_async16(dst + 3 * kSlotBytes, kp + (8 + tr) * kD + (cq + 4) * 16);
-            cp_async16(dst + 4 * kSlotBytes, vp + cq * kD + tr * 16);
-            cp_async16(dst + 5 * kSlotBytes, vp + (cq + 4) * kD + tr * 16);
-            cp_async16(dst + 6 * kSlotBytes, vp + (cq + 8) * kD + tr * 16);
-            cp_async16(dst + 7 * kSlotBytes, vp + (cq + 12) * kD + tr * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = 4 * i + (lane >> 3), col = lane & 7;
+                const uint32_t off = row * kD + ((col ^ (row & 7)) << 4);
+                cp_async16(dst + off, kp + row * kD + col * 16);
+                cp_async16(dst + kTileBytes + off, vp + row * kD + col * 16);
+            }
         }
         cp_async_commit();
         if (kn < nmine) {
@@ -312,25 +368,24 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     float o[8][4];
     int32_t kc = 0;  // next of this warp's tiles to compute
 
-    // ---- pieces: the CTA walks the pairs its slice touches; all four warps meet at each end
-    TileLoc pc = locate_tile(c0, s_tpre, s_len, B);
-    int32_t ps = c0;
-    while (ps < c1) {
-        const int32_t p = pc.b * Hkv + pc.h;
-        const int32_t fp = s_tpre[pc.b] + pc.h * pc.ntl;  // flat index of the pair's first tile
-        const int32_t pe = min(fp + pc.ntl, c1);            // end of this piece
+    for (int32_t n = 0; cur.fp < c1; ++n) {
+        const int buf = n & 1;
+        const int32_t p = cur.b * Hkv + cur.h;
+        const int32_t pe = min(cur.fp + cur.ntl, c1);  // end of this piece
+        const uint8_t *pb = pbuf + buf * kPieceBytes;
+        if (!mbar_wait_bounded(&pbar[buf], (uint32_t)(n >> 1) & 1u)) record_error(a.hdr, kErrFullWait);
 
-        // piece start (per warp): record, Q fragments, state
-        const uint32_t recw = __ldg(reinterpret_cast<const uint32_t *>(a.table + p) + lane);
+        // piece start (per warp): record word, Q fragments of head g = r, state
+        const uint32_t recw = reinterpret_cast<const uint32_t *>(pb + kPbRec)[lane];
         float qsum;
         {
             float qs = 0.0f;
-            if (gvalid) {  // Q fragments of head g = r: columns d = 16cq + 64(jj/4) + 4(jj%4) + {0,1 | 2,3}
-                const uint16_t *qrow = a.q + ((int64_t)pc.b * a.Hq + pc.h * G + r) * kD;
+            if (gvalid) {  // columns d = 16cq + 64(jj/4) + 4(jj%4) + {0,1 | 2,3}
+                const uint32_t qrow = smem_u32(pb + kPbQ) + r * 256;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(qrow + 16 * cq + 64 * half);
-                    const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+                    const uint4 u0 = ld_shared_v4(qrow + 32 * cq + 128 * half);
+                    const uint4 u1 = ld_shared_v4(qrow + 32 * cq + 128 * half + 16);
                     const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
@@ -357,11 +412,12 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 
         // this warp's tiles of the piece
         for (; kc < nmine && xw0 + kWarpsPerCta * kc < pe; ++kc) {
-            const int32_t j = xw0 + kWarpsPerCta * kc - fp;  // tile within the pair
+            const int32_t j = xw0 + kWarpsPerCta * kc - cur.fp;  // tile within the pair
             const int st = kc % kDepth;
-            cp_async_wait<kDepth - 1>();  // this lane's copies of the tile have landed
+            cp_async_wait<kDepth - 1>();  // this lane's copies of the tile have landed ...
+            __syncwarp();                  // ... and, after the warp meets, every lane's
             const int32_t tok0 = j * kTile;
-            const int32_t valid = min(kTile, pc.L - tok0);
+            const int32_t valid = min(kTile, cur.L - tok0);
             if (valid > 0) {
                 // segment constants (record words: start 2..6, k_min 7.., k_scale 12.., v_min 17.., v_scale 22..)
                 const int sg = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
@@ -390,9 +446,11 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                 }
 
                 const uint32_t tile = ring + st * kTileSmem;
-                // S^T = Q K^T: two n-tiles of 8 tokens x 8 k-steps, four accumulator chains
-                const uint4 k0 = ld_shared_v4(tile + 0 * kSlotBytes), k1 = ld_shared_v4(tile + 1 * kSlotBytes);
-                const uint4 k2 = ld_shared_v4(tile + 2 * kSlotBytes), k3 = ld_shared_v4(tile + 3 * kSlotBytes);
+                // S^T = Q K^T: two n-tiles of 8 tokens x 8 k-steps, four accumulator chains;
+                // this lane supplies rows tau(r) and 8 + tau(r), columns cq and cq + 4
+                const uint32_t kr0 = tile + tr * kD, kr1 = tile + (8 + tr) * kD;
+                const uint4 k0 = ld_shared_v4(kr0 + ((cq ^ tr) << 4)), k1 = ld_shared_v4(kr0 + (((cq + 4) ^ tr) << 4));
+                const uint4 k2 = ld_shared_v4(kr1 + ((cq ^ tr) << 4)), k3 = ld_shared_v4(kr1 + (((cq + 4) ^ tr) << 4));
                 float sa[2][4], sb[2][4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sa[0][e] = sa[1][e] = sb[0][e] = sb[1][e] = 0.0f;
@@ -448,8 +506,12 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 
                 // O^T += V^T P^T: rows (d) 16*tr + 2i (+1), k = tokens cq, cq+4, 8+cq, 12+cq
                 if (!vflat) {
-                    const uint4 va = ld_shared_v4(tile + 4 * kSlotBytes), vb = ld_shared_v4(tile + 5 * kSlotBytes);
-                    const uint4 vc = ld_shared_v4(tile + 6 * kSlotBytes), vd = ld_shared_v4(tile + 7 * kSlotBytes);
+                    // rows cq, cq + 4, cq + 8, cq + 12, column tau(r)
+                    const uint32_t vt = tile + kTileBytes;
+                    const uint4 va = ld_shared_v4(vt + cq * kD + ((tr ^ cq) << 4));
+                    const uint4 vb = ld_shared_v4(vt + (cq + 4) * kD + ((tr ^ (cq + 4)) << 4));
+                    const uint4 vc = ld_shared_v4(vt + (cq + 8) * kD + ((tr ^ cq) << 4));
+                    const uint4 vd = ld_shared_v4(vt + (cq + 12) * kD + ((tr ^ (cq + 4)) << 4));
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
                         const uint32_t xab01 = prmt(word(va, wi), word(vb, wi), 0x5140);
@@ -491,19 +553,25 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                         make_float2(fmaf(sigma, o[i][1], b1), fmaf(sigma, o[i][3], b1));
             }
             // the current token's score s_new = q . k_new (log2 domain), one warp per head
-            const uint16_t *krow = a.knew + ((int64_t)pc.b * Hkv + pc.h) * kD;
             for (int g = warp; g < G; g += kWarpsPerCta) {
-                const float sn = score_new(a.q + ((int64_t)pc.b * a.Hq + pc.h * G + g) * kD, krow, lane);
-                if (lane == 0) s_snew[g] = sn;
+                const uint2 qv = reinterpret_cast<const uint2 *>(pb + kPbQ + g * 256)[lane];
+                const uint2 kv = reinterpret_cast<const uint2 *>(pb + kPbKnew)[lane];
+                float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
+                acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
+                acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
+                acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
+#pragma unroll
+                for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (lane == 0) s_snew[g] = acc * kLog2eOverSqrtD;
             }
         }
         named_bar_sync(1, nthr);
 
         const int d = tid;  // thread d owns output column d
-        const float vn = bf16lo_to_f32((uint32_t)__ldg(a.vnew + ((int64_t)pc.b * Hkv + pc.h) * kD + d));
-        uint16_t *orow = a.out + ((int64_t)pc.b * a.Hq + pc.h * G) * kD + d;
-        const int32_t cfirst = owner(fp, T, ncta);
-        const int32_t clast = owner(fp + pc.ntl - 1, T, ncta);
+        const float vn = bf16lo_to_f32((uint32_t)reinterpret_cast<const uint16_t *>(pb + kPbVnew)[d]);
+        uint16_t *orow = a.out + ((int64_t)cur.b * a.Hq + cur.h * G) * kD + d;
+        const int32_t cfirst = owner(cur.fp, T, ncta);
+        const int32_t clast = owner(cur.fp + cur.ntl - 1, T, ncta);
         for (int g = 0; g < G; ++g) {
             float M = -INFINITY, L = 0.0f, O = 0.0f;
 #pragma unroll
@@ -522,115 +590,117 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
             if (cfirst == clast) {
                 __nv_bfloat16 ob = __float2bfloat16_rn(finish(M, L, O, s_snew[g], vn));
                 orow[g * kD] = *reinterpret_cast<uint16_t *>(&ob);
-            } else {  // publish this CTA's piece at slot p + cta (unique per piece)
+            } else {  // this CTA's piece at slot p + cta (unique per piece); merged by the combine kernel
                 float *dst = a.part + ((int64_t)(p + cta) * G + g) * kPartStride;
                 __stcg(dst + 4 + d, O);
                 if (d == 0) __stcg(reinterpret_cast<float2 *>(dst), make_float2(M, L));
             }
         }
-        if (cfirst != clast) {
-            __threadfence();
-            named_bar_sync(1, nthr);
-            if (tid == 0) {
-                uint32_t pieces = 0;  // CTAs holding a piece of this pair
-                for (int32_t cc = cfirst; cc <= clast; ++cc) pieces += owns_tiles(cc, T, ncta) ? 1u : 0u;
-                const uint32_t old = atomicAdd(a.pair_count + p, 1u);
-                const bool last = old + 1u == pieces;
-                if (last) {
-                    __threadfence();
-                    a.pair_count[p] = 0;
-                }
-                s_flag[0] = last ? 1 : 0;
-            }
-            named_bar_sync(1, nthr);
-            if (s_flag[0]) {
-                // merge every piece of the pair, in CTA order of the slots
-                // (1) per-head (max, sum): thread t folds slots cfirst + t, + 128, ...
-                float mg[8], lg[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    mg[g] = -INFINITY;
-                    lg[g] = 0.0f;
-                }
-                for (int32_t cc = cfirst + tid; cc <= clast; cc += kAttnThreads) {
-                    if (!owns_tiles(cc, T, ncta)) continue;
-                    const float *src = a.part + (int64_t)(p + cc) * G * kPartStride;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        if (g < G) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + g * kPartStride));
-                            ml_combine(mg[g], lg[g], ml.x, ml.y);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-#pragma unroll
-                    for (int off = 16; off; off >>= 1) {
-                        const float m2 = __shfl_xor_sync(0xffffffffu, mg[g], off);
-                        const float l2 = __shfl_xor_sync(0xffffffffu, lg[g], off);
-                        ml_combine(mg[g], lg[g], m2, l2);
-                    }
-                    if (lane == 0 && g < G) {
-                        s_red[(warp * 8 + g) * 2] = mg[g];
-                        s_red[(warp * 8 + g) * 2 + 1] = lg[g];
-                    }
-                }
-                named_bar_sync(1, nthr);
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    if (g < G) {
-                        mg[g] = s_red[g * 2];
-                        lg[g] = s_red[g * 2 + 1];
-#pragma unroll
-                        for (int ww = 1; ww < kWarpsPerCta; ++ww)
-                            ml_combine(mg[g], lg[g], s_red[(ww * 8 + g) * 2], s_red[(ww * 8 + g) * 2 + 1]);
-                    }
-                }
-                // (2) weighted O: warp w folds slots cfirst + w, + 4, ...; lane owns d = 4 lane .. + 3
-                float4 acc[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int32_t cc = cfirst + warp; cc <= clast; cc += kWarpsPerCta) {
-                    if (!owns_tiles(cc, T, ncta)) continue;
-                    const float *src = a.part + (int64_t)(p + cc) * G * kPartStride;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        if (g < G) {
-                            const float mw = __ldcg(src + g * kPartStride);
-                            const float4 ov = __ldcg(reinterpret_cast<const float4 *>(src + g * kPartStride + 4) + lane);
-                            const float f = mw == -INFINITY ? 0.0f : ex2(mw - mg[g]);
-                            acc[g].x = fmaf(ov.x, f, acc[g].x);
-                            acc[g].y = fmaf(ov.y, f, acc[g].y);
-                            acc[g].z = fmaf(ov.z, f, acc[g].z);
-                            acc[g].w = fmaf(ov.w, f, acc[g].w);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    if (g < G)
-                        *reinterpret_cast<float4 *>(s_comb + (warp * G + g) * kPartStride + 4 + 4 * lane) = acc[g];
-                named_bar_sync(1, nthr);
-                for (int g = 0; g < G; ++g) {
-                    float O = 0.0f;
-#pragma unroll
-                    for (int ww = 0; ww < kWarpsPerCta; ++ww) O += s_comb[(ww * G + g) * kPartStride + 4 + d];
-                    __nv_bfloat16 ob = __float2bfloat16_rn(finish(mg[g], lg[g], O, s_snew[g], vn));
-                    orow[g * kD] = *reinterpret_cast<uint16_t *>(&ob);
-                }
-            }
-        }
-        named_bar_sync(1, nthr);  // s_comb / s_red / s_snew are free again
-
-        // next pair
-        ps = pe;
-        if (ps < c1) {
-            pc.j = pc.ntl - 1;
-            advance(pc, s_len, Hkv);
-        }
+        if (tid == 0 && cur.fp >= c0) a.pair_info[p] = make_int2(cfirst, clast);  // first piece of the pair
+        named_bar_sync(1, nthr);  // the piece buffer, s_comb and s_snew are free again
+        if (tid == 0 && ahead.fp < c1) stage_piece(ahead, buf);
+        next_piece(ahead, s_tpre, s_len, B, Hkv);
+        next_piece(cur, s_tpre, s_len, B, Hkv);
     }
     cp_async_wait<0>();  // no copy may still target shared memory when the CTA exits
+}
+
+// Merge of the pieces of every pair that several CTAs share: one CTA per (pair, query head),
+// after the main kernel (programmatic dependent launch).  Pieces are folded in CTA order; the
+// current token is added last, as in the single-piece path.  Every load that does not depend on
+// the piece range is issued before the range is read, and all pieces are fetched in one round.
+constexpr int kCombineWarps = 8;
+constexpr int kCombineSlots = 8;  // pieces one warp keeps in flight per round
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(AttnArgs a)
+{
+    const int32_t G = a.G, Hkv = a.Hkv;
+    const int32_t p = blockIdx.x / G, g = blockIdx.x - p * G;
+    const int32_t b = p / Hkv, h = p - b * Hkv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+    __shared__ float4 s_o[kCombineWarps][32];
+    __shared__ float s_sn;
+
+    // independent of the piece range (inputs of this call, not written by the main kernel)
+    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * a.Hq + h * G + g) * kD) + lane);
+    const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(a.knew + ((int64_t)b * Hkv + h) * kD) + lane);
+    const float vn = bf16lo_to_f32((uint32_t)__ldg(a.vnew + ((int64_t)b * Hkv + h) * kD + (tid & (kD - 1))));
+
+    pdl_wait_primary();
+    const int2 info = __ldcg(a.pair_info + p);
+    const int32_t cfirst = info.x, clast = info.y;
+    if (cfirst == clast) return;  // finished inside the main kernel
+    const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
+    const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
+    const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
+
+    // warp w folds slots cfirst + w, + 8, ...: per slot its (m, l) and this lane's 4 columns of O
+    float m_w = -INFINITY, l_w = 0.0f;
+    float4 o_w = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int32_t base = cfirst + warp; base <= clast; base += kCombineWarps * kCombineSlots) {
+        float mm[kCombineSlots], ll[kCombineSlots];
+        float4 oo[kCombineSlots];
+#pragma unroll
+        for (int i = 0; i < kCombineSlots; ++i) {
+            const int32_t cc = base + i * kCombineWarps;
+            mm[i] = -INFINITY;
+            ll[i] = 0.0f;
+            oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
+                const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
+                mm[i] = ml.x;
+                ll[i] = ml.y;
+                oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kCombineSlots; ++i) {  // in slot order: online fold
+            const float M = fmaxf(m_w, mm[i]);
+            if (M == -INFINITY) continue;
+            const float fo = m_w == -INFINITY ? 0.0f : ex2(m_w - M);
+            const float fn = mm[i] == -INFINITY ? 0.0f : ex2(mm[i] - M);
+            l_w = l_w * fo + ll[i] * fn;
+            o_w.x = o_w.x * fo + oo[i].x * fn;
+            o_w.y = o_w.y * fo + oo[i].y * fn;
+            o_w.z = o_w.z * fo + oo[i].z * fn;
+            o_w.w = o_w.w * fo + oo[i].w * fn;
+            m_w = M;
+        }
+    }
+    if (lane == 0) {
+        s_m[warp] = m_w;
+        s_l[warp] = l_w;
+    }
+    s_o[warp][lane] = o_w;
+    if (warp == 0) {  // the current token's score
+        float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
+        acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
+        acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
+        acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) s_sn = acc * kLog2eOverSqrtD;
+    }
+    __syncthreads();
+    if (tid < kD) {  // thread d: fold the warps in order, then the current token
+        const int d = tid;
+        float M = -INFINITY, L = 0.0f, O = 0.0f;
+        for (int w = 0; w < kCombineWarps; ++w) {
+            const float mw = s_m[w];
+            const float Mn = fmaxf(M, mw);
+            if (Mn == -INFINITY) continue;
+            const float fo = M == -INFINITY ? 0.0f : ex2(M - Mn);
+            const float fn = mw == -INFINITY ? 0.0f : ex2(mw - Mn);
+            const float ow = reinterpret_cast<const float *>(&s_o[w][d >> 2])[d & 3];
+            L = L * fo + s_l[w] * fn;
+            O = O * fo + ow * fn;
+            M = Mn;
+        }
+        __nv_bfloat16 ob = __float2bfloat16_rn(finish(M, L, O, s_sn, vn));
+        a.out[((int64_t)b * a.Hq + h * G + g) * kD + d] = *reinterpret_cast<uint16_t *>(&ob);
+    }
 }
 
 }  // namespace dgq
@@ -641,8 +711,8 @@ namespace dgq {
 
 size_t attn_smem_bytes(int32_t B, int32_t G)
 {
-    return 1024 + (size_t)kWarpsPerCta * kWarpSmem + (size_t)kWarpsPerCta * G * kPartStride * 4 +
-           (kWarpsPerCta * 8 * 2 + 8 + 4) * 4 + (size_t)(2 * B + 1) * 4;
+    return 1024 + (size_t)kWarpsPerCta * kWarpSmem + 2 * kPieceBytes + 16 + (size_t)kWarpsPerCta * G * kPartStride * 4 +
+           8 * 4 + (size_t)(2 * B + 1) * 4;
 }
 
 int attn_max_ctas(int nsm) { return nsm * kMaxCtasPerSm; }
@@ -653,8 +723,8 @@ AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm)
     const size_t P = (size_t)batch * Hkv;
     const size_t G = (size_t)(Hq / Hkv);
     size_t off = sizeof(WsHeader);
-    l.off_count = off;
-    off = (off + P * 4 + 255) & ~size_t(255);
+    l.off_count = off;  // per-pair piece range (int2)
+    off = (off + P * 8 + 255) & ~size_t(255);
     l.off_part = off;
     off += (P + (size_t)attn_max_ctas(nsm)) * G * kPartStride * 4;
     l.total = (off + 255) & ~size_t(255);
@@ -682,7 +752,7 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.seq_lens = seq_lens;
     a.out = static_cast<uint16_t *>(out);
     a.hdr = reinterpret_cast<WsHeader *>(base);
-    a.pair_count = reinterpret_cast<uint32_t *>(base + l.off_count);
+    a.pair_info = reinterpret_cast<int2 *>(base + l.off_count);
     a.part = reinterpret_cast<float *>(base + l.off_part);
     a.B = B;
     a.Hq = Hq;
@@ -691,21 +761,46 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.bs = bs;
     a.max_blocks = max_blocks;
 
+    // per-device launch shape, computed once per (device, shared-memory size)
+    static int cached_dev = -1;
+    static size_t cached_smem = 0;
+    static int cached_occ = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     const size_t smem = attn_smem_bytes(B, G);
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel, kAttnThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    if (occ > kMaxCtasPerSm) occ = kMaxCtasPerSm;
+    if (dev != cached_dev || smem != cached_smem) {
+        e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel, kAttnThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        cached_dev = dev;
+        cached_smem = smem;
+        cached_occ = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
+    }
     // upper bound on tiles (every request at max_seqlen): no more CTAs than tiles
     const int64_t tiles = (int64_t)B * Hkv * (max_seqlen > 0 ? (max_seqlen + kTile - 1) / kTile : 1);
-    int64_t grid = (int64_t)nsm * occ;
+    int64_t grid = (int64_t)nsm * cached_occ;
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
     attn_kernel<<<(unsigned)grid, kAttnThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // merge of shared pairs, chained with programmatic dependent launch
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hkv * G));
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace dgq

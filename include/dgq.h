@@ -53,7 +53,8 @@ typedef enum dgq_status {
     DGQ_ERR_WORKSPACE = -3,      /* workspace missing or smaller than the queried size */
     DGQ_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed */
     DGQ_ERR_POOL_EXHAUSTED = -5, /* block pool has fewer free blocks than requested */
-    DGQ_ERR_DEVICE = -6          /* a device-side wait timed out (see dgq_workspace_error) */
+    DGQ_ERR_DEVICE = -6,         /* a device-side wait timed out (see dgq_workspace_error) */
+    DGQ_ERR_SCRATCH_LIMIT = -7   /* the problem needs more scratch than the library's fixed array */
 } dgq_status;
 
 /*
@@ -151,6 +152,41 @@ dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16,
 
 size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                int32_t max_seqlen);
+
+/* ---------------------------------------------------------------------------------------
+ * dgq_paged_decode_attn_noalloc -- the same decode attention for callers that cannot
+ * allocate device memory.  The source articles have no counterpart: this is a deployment
+ * convenience of this library.
+ *
+ * Who needs it: code that must not call cudaMalloc (or any allocator) while it runs -- an
+ * operator inside a serving engine that only receives the buffers it planned ahead, or a
+ * plugin whose host framework forbids new device allocations during a step -- and so has no
+ * workspace to pass.  Here the workspace is a fixed array that lives in the library's own
+ * device memory: DGQ_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, held until
+ * the process exits.  Nothing is allocated by this call.
+ *
+ * Arguments, layouts and results are those of dgq_paged_decode_attn without the workspace.
+ * Limits and behaviour:
+ *   - a problem whose dgq_attn_workspace_size(batch, Hq, Hkv, max_seqlen) exceeds
+ *     DGQ_NOALLOC_SCRATCH_BYTES is rejected with DGQ_ERR_SCRATCH_LIMIT before any launch;
+ *   - the first call on a device looks up the array's device address (with that device
+ *     current) and keeps it; make that first call before any stream capture;
+ *   - every call on a device shares the one array, which keeps the previous call's contents:
+ *     each call clears the array's 256-byte header on the stream before it launches, so calls
+ *     issued in order on one stream are safe, while calls that overlap on the GPU (several
+ *     streams at once) race and give wrong results;
+ *   - a device-side wait that timed out is not reported (there is no workspace to query).
+ */
+#define DGQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+dgq_status dgq_paged_decode_attn_noalloc(const void *q_bf16, const void *k_new_bf16,
+                                         const void *v_new_bf16, const uint8_t *k_pool,
+                                         const uint8_t *v_pool, const dgq_seg_record *seg_table,
+                                         const int32_t *block_tables_dev, const int32_t *seq_lens_dev,
+                                         int32_t max_seqlen, int32_t batch, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                         int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
+                                         void *cuda_stream);
 
 /* Zero-fill a workspace (cudaMemsetAsync on the stream). */
 dgq_status dgq_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream);

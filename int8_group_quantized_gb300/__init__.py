@@ -51,6 +51,9 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                             P, P, sz, P]
         L.dgq_paged_decode_attn.restype = ctypes.c_int
+        L.dgq_paged_decode_attn_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                    i32, P, P]
+        L.dgq_paged_decode_attn_noalloc.restype = ctypes.c_int
         L.dgq_attn_workspace_size.argtypes = [i32, i32, i32, i32]
         L.dgq_attn_workspace_size.restype = sz
         L.dgq_workspace_init.argtypes = [P, sz, P]
@@ -156,6 +159,19 @@ def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tabl
                                        B, Hq, Hkv, D, k_pool.shape[2], block_tables.shape[1], k_pool.shape[0],
                                        _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
            "dgq_paged_decode_attn")
+
+
+def dgq_paged_decode_attn_noalloc(q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens,
+                                  max_seqlen, out, stream=None) -> None:
+    """dgq_paged_decode_attn without a workspace: the scratch is the library's own fixed
+    device array (for callers that cannot allocate).  Same arguments otherwise."""
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    _check(lib().dgq_paged_decode_attn_noalloc(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                               _ptr(seg_table), _ptr(block_tables), _ptr(seq_lens),
+                                               int(max_seqlen), B, Hq, Hkv, D, k_pool.shape[2],
+                                               block_tables.shape[1], k_pool.shape[0], _ptr(out), _stream(stream)),
+           "dgq_paged_decode_attn_noalloc")
 
 
 class BlockPool:

@@ -22,6 +22,7 @@ UNITS = {
     "dgq_compress.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_attn.cu": [],
     "dgq_host.cu": [],
+    "dgq_noalloc.cu": [],
 }
 
 

@@ -59,6 +59,7 @@ const char *dgq_status_str(dgq_status s)
     case DGQ_ERR_CUDA: return "CUDA error";
     case DGQ_ERR_POOL_EXHAUSTED: return "block pool exhausted";
     case DGQ_ERR_DEVICE: return "device-side wait timed out";
+    case DGQ_ERR_SCRATCH_LIMIT: return "problem too large for the fixed no-allocation scratch array";
     }
     return "unknown status";
 }

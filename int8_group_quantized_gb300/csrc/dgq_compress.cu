@@ -7,21 +7,37 @@
 // q = rint((x - min) * (255 / (max - min))).  Codes go to the physical block named by the
 // block table ("PagedAttention implementation", DeepSeek-V4 KV-cache article).
 //
-// GPU design: one persistent cooperative kernel.  The flat space of all 16-token windows
-// of all (request, head) pairs is cut into super-groups of ~32 MB of bf16 K+V.  Every CTA
-// walks the super-groups in order; for super-group i it first computes window statistics
-// (variance mean, K/V min/max) for its share of super-group i, then quantises its share
-// of the pairs that were completed in super-group i-1.  The warp that finishes the last
-// window of a pair segments that pair (no waiting) and publishes a per-pair flag; a
-// quantising warp waits on that flag (bounded).  The second read of K/V therefore trails
-// the first by about two super-groups (~64 MB), so it is served from the 126 MB L2.
-// All windows stay within one block (bs is a multiple of 16) and within one segment
-// (boundaries sit on window edges), so a warp's quantisation of a window needs one block
-// id and one (min, inv) pair per tensor.
+// GPU design: one persistent cooperative kernel, one CTA per SM: 12 worker warps and one
+// sync warp.
+//  * The flat list of all 16-token windows of all (request, head) pairs, in (request, head,
+//    window) order, is cut into chunks of kChunk windows (64 MB of bf16 K+V).  Workers
+//    compute window statistics (variance mean; K and V min/max, also folded into aggregates
+//    of 64 windows with exact order-preserving integer atomics) for their CTA's share of
+//    each chunk.  Quantisation range m holds the pairs whose last window lies in chunk m; it
+//    needs the statistics of chunks 0..m of every CTA: one grid barrier per chunk.
+//  * The barrier is split.  A CTA publishes its progress once its workers have finished a
+//    chunk's statistics (one release store per CTA and chunk, to a word of its own, so CTAs
+//    may run several chunks apart), and only waits for the other CTAs when it is about to
+//    quantise range m.  Meanwhile its workers keep computing statistics of later chunks, up
+//    to kAhead windows past their quantisation position, so that the K/V read for
+//    statistics are mostly still in the 126 MB L2 when they are read again for
+//    quantisation (those second reads carry an evict-first hint).
+//  * Under full HBM load every dependent round trip through L2 costs microseconds, so all
+//    global synchronisation lives in the sync warp: it publishes progress, polls the
+//    progress words of all CTAs, and segments every pair that overlaps its CTA's share of a
+//    range (a pair shared by several CTAs is segmented by each; the result is the same
+//    bits).  Parameters go to a per-CTA slice of the workspace; workers learn of them
+//    through shared-memory flags with CTA-scope release/acquire and never wait on global
+//    memory themselves.
+//  * Each worker streams its windows (every 12th window of its CTA's share) through a
+//    private two-window shared-memory ring filled with cp.async.  Windows never cross a
+//    block (block sizes are multiples of 16) nor a segment (boundaries sit on window
+//    edges), so quantising a window needs one block id and one (min, inv) pair per tensor.
 //
 // Bit-exactness: every fp32 step that feeds a code or a boundary is a single IEEE
 // operation via __fadd_rn / __fsub_rn / __fmul_rn / __fdiv_rn, in the pairwise order the
-// oracle fixes (this file is also compiled with -fmad=false).
+// oracle fixes (this file is also compiled with -fmad=false).  Min and max are exact in any
+// order.
 #include "dgq_device.cuh"
 #include "dgq.h"
 #include "dgq_launch.h"
@@ -32,14 +48,25 @@
 
 namespace dgq {
 
-// Per-(request, head) quantisation parameters published by the segmenting warp.
-struct PairParams {
+// Quantisation parameters of one pair as the sync warp publishes them.
+struct alignas(16) PairParams {
     float k_min[kMaxSeg], k_inv[kMaxSeg], v_min[kMaxSeg], v_inv[kMaxSeg];
     int32_t start[kMaxSeg];
     int32_t n_seg;
     int32_t pad[6];
 };
 static_assert(sizeof(PairParams) == 128, "PairParams is 128 bytes");
+
+constexpr int kAgg = 64;        // windows per min/max aggregate
+constexpr int kWorkers = 12;    // worker warps per CTA (plus one sync warp)
+constexpr int kThreads = (kWorkers + 1) * 32;
+constexpr int kRing = 2;                   // windows in flight per worker
+constexpr int kTileBytes = kWin * kD * 2;  // 16 tokens x 128 bf16 = 4 KB
+constexpr int kWinBytes = 2 * kTileBytes;  // K tile + V tile
+constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
+constexpr int32_t kChunk = 8192;           // windows per chunk: 64 MB of K+V
+constexpr int32_t kAhead = 16384;          // statistics may lead quantisation by this many windows
+constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for
 
 struct CompressArgs {
     const uint16_t *k;
@@ -50,63 +77,69 @@ struct CompressArgs {
     uint8_t *vpool;
     dgq_seg_record *table;
     WsHeader *hdr;
-    uint32_t *pair_count;
-    uint32_t *pair_flag;
-    PairParams *params;
+    PairParams *params;  // [ncta][2][cap]: per-CTA slices, double-buffered by range parity
+    uint32_t *prog;      // [ncta]: chunks whose statistics the CTA has published
     float *win_mean;
     float4 *win_mm;
-    int32_t B, Hkv, bs, max_blocks;
-    int32_t wps;  // windows per super-group
+    uint4 *agg;  // per 64 flat windows: ~enc(k min), enc(k max), ~enc(v min), enc(v max); 0 = empty
+    int32_t B, Hkv, bs, max_blocks, cap;
 };
-
-constexpr int kCWarps = 8;                          // consumer warps (plus one TMA producer warp)
-constexpr int kThreads = (kCWarps + 1) * 32;
-constexpr int kCStages = 16;                        // shared-memory ring of window tiles
-constexpr int kTileBytes = kWin * kD * 2;           // 16 tokens x 128 bf16 = 4 KB
-constexpr int kCStageBytes = 2 * kTileBytes;        // K tile + V tile
 
 __device__ __forceinline__ int32_t ngroups(int32_t L)
 {
     if (L < 2048) return 2;
     if (L < 16384) return 3;
     // floor(log2(L / 1024)) = floor(log2(L)) - 10 for integer L >= 1024
-    int32_t g = (31 - __clz(L)) - 10 + 2;
+    const int32_t g = (31 - __clz(L)) - 10 + 2;
     return g < 5 ? g : 5;
 }
 
 // ---- window decomposition ------------------------------------------------------------------
 
 struct WinLoc {
-    int32_t b, h, wi, W, L;  // request, head, window within the pair, windows in pair, length
+    int32_t b, h, wi, W, L, c0;  // request, head, window in pair, windows in pair, length, cu[b]
 };
 
-// s_wpre[b] = Hkv * (windows of requests 0..b-1); s_cu = cu_seqlens copy.
-__device__ __forceinline__ WinLoc locate(int32_t w, const int32_t *s_wpre, const int32_t *s_cu, int32_t B,
-                                         int32_t Hkv)
+// s_wpre[b] = Hkv * (windows of requests 0..b-1).
+__device__ __forceinline__ WinLoc locate(int32_t w, const int32_t *s_wpre, const int32_t *cu, int32_t B)
 {
     int32_t lo = 0, hi = B - 1;
     while (lo < hi) {
-        int32_t mid = (lo + hi + 1) >> 1;
+        const int32_t mid = (lo + hi + 1) >> 1;
         if (s_wpre[mid] <= w) lo = mid;
         else hi = mid - 1;
     }
     WinLoc r;
     r.b = lo;
-    r.L = s_cu[lo + 1] - s_cu[lo];
+    r.c0 = __ldg(cu + lo);
+    r.L = __ldg(cu + lo + 1) - r.c0;
     r.W = (r.L + kWin - 1) / kWin;
-    int32_t off = w - s_wpre[lo];
+    const int32_t off = w - s_wpre[lo];
     r.h = off / r.W;
     r.wi = off - r.h * r.W;
     return r;
 }
 
-// first window of the pair containing window w, and one past its last window
-__device__ __forceinline__ void pair_span(int32_t w, const int32_t *s_wpre, const int32_t *s_cu, int32_t B,
-                                          int32_t Hkv, int32_t *first, int32_t *end)
+// Move a location n windows forward (the target window must exist); returns how many pair
+// boundaries were crossed.
+__device__ __forceinline__ int32_t step_loc(WinLoc &l, int32_t n, const int32_t *cu, int32_t Hkv)
 {
-    WinLoc l = locate(w, s_wpre, s_cu, B, Hkv);
-    *first = w - l.wi;
-    *end = *first + l.W;
+    int32_t crossed = 0;
+    l.wi += n;
+    while (l.wi >= l.W) {
+        l.wi -= l.W;
+        ++crossed;
+        if (++l.h == Hkv) {
+            l.h = 0;
+            do {  // next non-empty request
+                l.c0 += l.L;
+                ++l.b;
+                l.L = __ldg(cu + l.b + 1) - l.c0;
+            } while (l.L == 0);
+            l.W = (l.L + kWin - 1) / kWin;
+        }
+    }
+    return crossed;
 }
 
 // ---- canonical fp32 sums ---------------------------------------------------------------------
@@ -152,89 +185,134 @@ __device__ __forceinline__ float warp_max(float v)
 
 __device__ __forceinline__ float canon_zero(float x) { return x == 0.0f ? 0.0f : x; }
 
-// ---- segmentation of one pair (one warp, after its last window's statistics) -------------
+// Order-preserving map of fp32 (finite, or infinite) onto uint32, so that an integer max
+// atomic gives the exact fp32 max in any order; every value maps above 0, the empty mark.
+__device__ __forceinline__ uint32_t ord_enc(float x)
+{
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_dec(uint32_t e)
+{
+    return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+}
 
-__device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int32_t b, int32_t h, int32_t L,
-                                          int32_t W, int32_t wbase, uint32_t target)
+// ---- segmentation of one pair (one warp; all of the pair's statistics are visible) ---------
+
+__device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int32_t L, int32_t W, int32_t wbase,
+                                          PairParams *dst, bool write_record)
 {
     const int lane = threadIdx.x & 31;
     const int32_t k = min(ngroups(L), W) - 1;  // boundaries to place (0..4)
 
-    // per-lane top-k of (jump desc, window asc) over this lane's windows
+    // (1) per-lane top-k of (jump desc, window asc); the jump of window w < W-1 is
+    // |m[w+1] - m[w]|.  Lanes read aligned quads of the flat mean array overlapping the pair,
+    // eight quads in flight per lane.
     float cj[4] = {-1.0f, -1.0f, -1.0f, -1.0f};
     int32_t cw[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
     if (k > 0) {
-        for (int32_t w = lane; w + 1 < W; w += 32) {
-            float m0 = __ldcg(a.win_mean + wbase + w);
-            float m1 = __ldcg(a.win_mean + wbase + w + 1);
-            float j = fabsf(__fsub_rn(m1, m0));
-            // insert; windows arrive in increasing order, so equal jumps keep the earlier one
-            if (j > cj[3]) {
-                cj[3] = j; cw[3] = w;
+        const int32_t q0 = wbase >> 2, q1 = (wbase + W - 1) >> 2;
+        const float4 *mq = reinterpret_cast<const float4 *>(a.win_mean);
+        for (int32_t qb = q0 + lane; qb <= q1; qb += 32 * 8) {
+            float4 mv[8];
+            float nx[8];
 #pragma unroll
-                for (int s = 3; s > 0; --s) {
-                    if (cj[s] > cj[s - 1]) {
-                        float tj = cj[s]; cj[s] = cj[s - 1]; cj[s - 1] = tj;
-                        int32_t tw = cw[s]; cw[s] = cw[s - 1]; cw[s - 1] = tw;
+            for (int u = 0; u < 8; ++u) {
+                const int32_t q = qb + 32 * u;
+                mv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                nx[u] = 0.0f;
+                if (q <= q1) {
+                    mv[u] = __ldcg(mq + q);
+                    if (4 * q + 4 < wbase + W) nx[u] = __ldcg(a.win_mean + 4 * q + 4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t q = qb + 32 * u;
+                const float m5[5] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w, nx[u]};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int32_t w = 4 * q + e - wbase;  // window within the pair
+                    if (q > q1 || w < 0 || w + 1 >= W) continue;
+                    const float j = fabsf(__fsub_rn(m5[e + 1], m5[e]));
+                    // a lane meets its windows in increasing order, so an equal jump keeps the
+                    // earlier window ahead of it
+                    if (j > cj[3]) {
+                        cj[3] = j;
+                        cw[3] = w;
+#pragma unroll
+                        for (int s = 3; s > 0; --s) {
+                            if (cj[s] > cj[s - 1]) {
+                                const float tj = cj[s]; cj[s] = cj[s - 1]; cj[s - 1] = tj;
+                                const int32_t tw = cw[s]; cw[s] = cw[s - 1]; cw[s - 1] = tw;
+                            }
+                        }
                     }
                 }
             }
         }
     }
-    // k rounds of warp arg-best; the winning lane advances its list
+    // k rounds of warp arg-best; the winning lane pops its head
     int32_t cut[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};  // first window of segments 1..k
     for (int r = 0; r < k; ++r) {
         const float bj = cj[0];
         const int32_t bw = cw[0];
-        // select (jump desc, window asc)
         float j = bj;
         int32_t wv = bw;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
-            float oj = __shfl_xor_sync(0xffffffffu, j, o);
-            int32_t ow = __shfl_xor_sync(0xffffffffu, wv, o);
+            const float oj = __shfl_xor_sync(0xffffffffu, j, o);
+            const int32_t ow = __shfl_xor_sync(0xffffffffu, wv, o);
             if (oj > j || (oj == j && ow < wv)) {
                 j = oj;
                 wv = ow;
             }
         }
-        if (bw == wv) {  // windows are unique, so exactly one lane matches: pop its head
+        if (bw == wv) {  // a window sits in one lane only, so exactly one lane matches
             cj[0] = cj[1]; cj[1] = cj[2]; cj[2] = cj[3]; cj[3] = -1.0f;
             cw[0] = cw[1]; cw[1] = cw[2]; cw[2] = cw[3]; cw[3] = INT32_MAX;
         }
-        // insertion into the sorted cut list
-        int32_t c = wv + 1;
+        int32_t c = wv + 1;  // insertion into the sorted cut list
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             if (c < cut[s]) {
-                int32_t t = cut[s];
+                const int32_t t = cut[s];
                 cut[s] = c;
                 c = t;
             }
         }
     }
 
-    // per-segment fp32 min/max from the window min/max
+    // (2) per-segment fp32 min/max: whole 64-window aggregates inside the segment, single
+    // windows at its two ragged ends
     float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
-        kmn[s] = INFINITY; kmx[s] = -INFINITY; vmn[s] = INFINITY; vmx[s] = -INFINITY;
-    }
-    for (int32_t w = lane; w < W; w += 32) {
-        float4 mm = __ldcg(a.win_mm + wbase + w);
-        int s = (w >= cut[0]) + (w >= cut[1]) + (w >= cut[2]) + (w >= cut[3]);
-#pragma unroll
-        for (int i = 0; i < kMaxSeg; ++i) {
-            if (s == i) {
-                kmn[i] = fminf(kmn[i], mm.x); kmx[i] = fmaxf(kmx[i], mm.y);
-                vmn[i] = fminf(vmn[i], mm.z); vmx[i] = fmaxf(vmx[i], mm.w);
+        float kn = INFINITY, kx = -INFINITY, vn = INFINITY, vx = -INFINITY;
+        if (s <= k) {
+            const int32_t sw = s == 0 ? 0 : cut[s - 1];
+            const int32_t ew = s < k ? cut[s] : W;
+            const int32_t f0 = wbase + sw, f1 = wbase + ew;             // flat windows [f0, f1)
+            const int32_t a0 = (f0 + kAgg - 1) / kAgg, a1 = f1 / kAgg;  // aggregates [a0, a1) inside
+            const bool whole = a0 < a1;
+            const int32_t e0 = whole ? a0 * kAgg : f1;  // head windows [f0, e0)
+            const int32_t e1 = whole ? a1 * kAgg : f1;  // tail windows [e1, f1)
+            for (int32_t ab = a0 + lane; whole && ab < a1; ab += 32) {
+                const uint4 g = __ldcg(a.agg + ab);
+                kn = fminf(kn, ord_dec(~g.x)); kx = fmaxf(kx, ord_dec(g.y));
+                vn = fminf(vn, ord_dec(~g.z)); vx = fmaxf(vx, ord_dec(g.w));
+            }
+            for (int32_t w = f0 + lane; w < e0; w += 32) {
+                const float4 mm = __ldcg(a.win_mm + w);
+                kn = fminf(kn, mm.x); kx = fmaxf(kx, mm.y); vn = fminf(vn, mm.z); vx = fmaxf(vx, mm.w);
+            }
+            for (int32_t w = e1 + lane; w < f1; w += 32) {
+                const float4 mm = __ldcg(a.win_mm + w);
+                kn = fminf(kn, mm.x); kx = fmaxf(kx, mm.y); vn = fminf(vn, mm.z); vx = fmaxf(vx, mm.w);
             }
         }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxSeg; ++i) {
-        kmn[i] = warp_min(kmn[i]); kmx[i] = warp_max(kmx[i]);
-        vmn[i] = warp_min(vmn[i]); vmx[i] = warp_max(vmx[i]);
+        kmn[s] = warp_min(kn); kmx[s] = warp_max(kx);
+        vmn[s] = warp_min(vn); vmx[s] = warp_max(vx);
     }
 
     if (lane == 0) {
@@ -247,9 +325,9 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
             rec.pad[i] = 0;
             pp.start[i] = rec.start[i];
             if (i < n) {
-                float kn = canon_zero(kmn[i]), kx = canon_zero(kmx[i]);
-                float vn = canon_zero(vmn[i]), vx = canon_zero(vmx[i]);
-                float kr = __fsub_rn(kx, kn), vr = __fsub_rn(vx, vn);
+                const float kn = canon_zero(kmn[i]), kx = canon_zero(kmx[i]);
+                const float vn = canon_zero(vmn[i]), vx = canon_zero(vmx[i]);
+                const float kr = __fsub_rn(kx, kn), vr = __fsub_rn(vx, vn);
                 rec.k_min[i] = kn;
                 rec.v_min[i] = vn;
                 rec.k_scale[i] = kr == 0.0f ? 0.0f : __fdiv_rn(kr, 255.0f);
@@ -268,14 +346,11 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
         pp.n_seg = n;
 #pragma unroll
         for (int i = 0; i < 6; ++i) pp.pad[i] = 0;
-        a.table[p] = rec;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(&pp);
-        uint32_t *dst = reinterpret_cast<uint32_t *>(a.params + p);
+        if (write_record) a.table[p] = rec;
+        const uint4 *src = reinterpret_cast<const uint4 *>(&pp);
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) __stcg(dst + i, src[i]);
-        a.pair_count[p] = 0;  // nobody else touches the counter in this call
-        __threadfence();
-        st_release_gpu(a.pair_flag + p, target);
+        for (int i = 0; i < 8; ++i) __stcg(d + i, src[i]);
     }
     __syncwarp();
 }
@@ -363,45 +438,28 @@ __device__ __forceinline__ uint2 encode8(const uint4 &q, float mn, float inv)
     return make_uint2(lo, hi);
 }
 
-// Quantisation parameters of one pair, read once per run of windows of that pair: lane i < 5
-// holds segment i's (start, k_min, k_inv, v_min, v_inv).
+
+// Quantisation parameters of one pair held by a warp: lane i < 5 holds segment i's
+// (start, k_min, k_inv, v_min, v_inv).
 struct PairCache {
-    int32_t p;
     int32_t start;
     float kmn, kinv, vmn, vinv;
 };
 
-// Wait (bounded) for the pair's segmentation; false if the wait timed out.
-__device__ __forceinline__ bool load_pair(const CompressArgs &a, int32_t p, uint32_t target, PairCache &pc)
+__device__ __forceinline__ PairCache load_params(const PairParams *pp)
 {
     const int lane = threadIdx.x & 31;
-    int ok = 1;
-    if (lane == 0) {
-        uint32_t it = 0;
-        while (ld_acquire_gpu(a.pair_flag + p) != target) {
-            if (++it >= kSpinLimit) {
-                record_error(a.hdr, kErrFlagWait);
-                ok = 0;
-                break;
-            }
-            __nanosleep(64);
-        }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) return false;
-    (void)ld_acquire_gpu(a.pair_flag + p);  // every lane acquires the published parameters
-    const PairParams *pp = a.params + p;
     const int i = lane < kMaxSeg ? lane : 0;
-    pc.p = p;
+    PairCache pc;
     pc.start = __ldcg(pp->start + i);
     pc.kmn = __ldcg(pp->k_min + i);
     pc.kinv = __ldcg(pp->k_inv + i);
     pc.vmn = __ldcg(pp->v_min + i);
     pc.vinv = __ldcg(pp->v_inv + i);
-    return true;
+    return pc;
 }
 
-// Codes of one window tile, written straight to its slots in the physical block.
+// Codes of one window tile, written straight to their slots in the physical block.
 __device__ __forceinline__ void window_quant(const CompressArgs &a, const WinLoc &loc, uint32_t kt, uint32_t vt,
                                              const PairCache &pc, int64_t blk)
 {
@@ -409,7 +467,7 @@ __device__ __forceinline__ void window_quant(const CompressArgs &a, const WinLoc
     const int half = lane >> 4, sub = lane & 15;
     const int32_t t0 = loc.wi * kWin;
     const int32_t cnt = min(kWin, loc.L - t0);
-    // segment of the window: number of starts 1..4 at or before t0 (lanes 1..4 hold them)
+    // segment of the window: how many of starts 1..4 (lanes 1..4) lie at or before t0
     const unsigned ballot = __ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pc.start <= t0);
     const int s = __popc(ballot);
     const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
@@ -429,56 +487,64 @@ __device__ __forceinline__ void window_quant(const CompressArgs &a, const WinLoc
 
 // ---- the kernel ---------------------------------------------------------------------------
 
-// Per-warp pending arrivals: windows of one pair counted locally and published with one fence.
-struct Pending {
-    int32_t p, cnt, b, h, L, W, wbase;
-};
-
-__device__ __forceinline__ void flush_pending(const CompressArgs &a, Pending &pd, uint32_t target)
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src)
 {
-    if (pd.cnt == 0) return;
-    const int lane = threadIdx.x & 31;
-    int last = 0;
-    if (lane == 0) {
-        __threadfence();  // this warp's window statistics before the arrival count
-        const uint32_t old = atomicAdd(a.pair_count + pd.p, (uint32_t)pd.cnt);
-        last = (old + (uint32_t)pd.cnt == (uint32_t)pd.W);
-        if (last) __threadfence();
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) segment_pair(a, pd.p, pd.b, pd.h, pd.L, pd.W, pd.wbase, target);
-    pd.cnt = 0;
-    pd.p = -1;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp16_hint(uint32_t dst, const void *src, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    compress_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, CompressArgs a)
+// A warp's position in one of its two item sequences (statistics of chunk m, or
+// quantisation of range m): window w of the CTA's share [.., end), its location, and (for
+// quantisation) the ordinal of its pair among the pairs of the share.  w < 0: sequence over.
+struct Cursor {
+    int32_t m, w, end, slot;
+    WinLoc loc;
+};
+
+// One window in flight in a worker's ring.
+struct Item {
+    int32_t kind;  // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
+    int32_t w, m, stage;
+    int32_t next_m;  // chunk / range of the worker's next item of the same kind (M if none)
+    WinLoc loc;
+    int64_t blk;
+    PairCache pc;
+};
+
+// shared-memory control words
+struct CtaCtl {
+    int32_t stats_done[kWorkers];  // per worker: first chunk whose statistics are not all done
+    int32_t quant_done[kWorkers];  // per worker: first range whose quantisation is not all done
+    int32_t ready[2];              // range m's parameters are published when ready[m & 1] >= m + 1
+    int32_t abort;
+    int32_t last;
+    int32_t pad[4];
+};
+
+__global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align_smem_1024(smem_raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kCStages * kCStageBytes);
-    uint64_t *empty = full + kCStages;
-    int32_t *s_cu = reinterpret_cast<int32_t *>(empty + kCStages);  // [B+1]
-    int32_t *s_wpre = s_cu + a.B + 1;                                // [B+1]
+    extern __shared__ __align__(16) uint8_t smem[];
+    CtaCtl *ctl = reinterpret_cast<CtaCtl *>(smem + kRingBytes);
+    int32_t *s_wpre = reinterpret_cast<int32_t *>(smem + kRingBytes + sizeof(CtaCtl));  // [B+1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
 
-    if (tid == 0) {
-        for (int s = 0; s < kCStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        fence_barrier_init();
-    }
-    for (int i = tid; i <= B; i += kThreads) s_cu[i] = __ldg(a.cu + i);
-    __syncthreads();
-    // exclusive scan of Hkv * ceil(L_b / 16) (single warp; B is small)
-    if (warp == 0) {
+    if (warp == 0) {  // exclusive scan of Hkv * ceil(L_b / 16)
         int32_t carry = 0;
         for (int base = 0; base < B; base += 32) {
             const int i = base + lane;
             int32_t v = 0;
-            if (i < B) v = a.Hkv * ((s_cu[i + 1] - s_cu[i] + kWin - 1) / kWin);
+            if (i < B) v = a.Hkv * ((__ldg(a.cu + i + 1) - __ldg(a.cu + i) + kWin - 1) / kWin);
             int32_t x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -490,15 +556,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) s_wpre[B] = carry;
     }
+    if (tid >= 32 && tid < 32 + kWorkers) {
+        ctl->stats_done[tid - 32] = 0;
+        ctl->quant_done[tid - 32] = 0;
+    }
+    if (tid == 32) {
+        ctl->ready[0] = ctl->ready[1] = 0;
+        ctl->abort = 0;
+        ctl->last = 0;
+    }
     __syncthreads();
 
     const int32_t Wtot = s_wpre[B];
-    const uint32_t target = *reinterpret_cast<volatile uint32_t *>(&a.hdr->epoch) + 1u;
+    const int32_t M = (Wtot + kChunk - 1) / kChunk;  // chunks (and quantisation ranges)
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
 
     // empty requests: a record with n_seg = 0
     for (int32_t b = cta; b < B; b += ncta) {
-        if (s_cu[b + 1] == s_cu[b]) {
+        if (__ldg(a.cu + b + 1) == __ldg(a.cu + b)) {
             for (int32_t h = tid; h < a.Hkv; h += kThreads) {
                 dgq_seg_record rec = {};
                 a.table[(int64_t)b * a.Hkv + h] = rec;
@@ -506,140 +581,281 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // The work list of this CTA, identical for the producer and the consumers: for each
-    // super-group i, the statistics of its share of super-group i, then the quantisation of its
-    // share of the pairs that end in super-group i-1.  Item k uses stage k % kCStages and is
-    // processed by consumer warp k % kCWarps.
-    const int32_t wps = a.wps;
-    const int32_t nsg = (Wtot + wps - 1) / wps;
-    auto ranges = [&](int32_t i, int32_t &s0, int32_t &s1, int32_t &q0, int32_t &q1) {
-        s0 = s1 = q0 = q1 = 0;
-        if (i < nsg) {
-            const int32_t lo = i * wps, len = min(wps, Wtot - lo);
-            s0 = lo + (int32_t)(((int64_t)len * cta) / ncta);
-            s1 = lo + (int32_t)(((int64_t)len * (cta + 1)) / ncta);
-        }
-        if (i >= 1) {
-            // pairs whose last window lies in super-group i-1: from the start of the pair holding
-            // its first window to the end of the pair holding its last window (or that pair's
-            // start, if it ends later)
-            const int32_t A = (i - 1) * wps, Z = min(i * wps, Wtot) - 1;
-            int32_t fA, eA, fZ, eZ;
-            pair_span(A, s_wpre, s_cu, B, a.Hkv, &fA, &eA);
-            pair_span(Z, s_wpre, s_cu, B, a.Hkv, &fZ, &eZ);
-            const int32_t lo = fA, hi = (eZ - 1 == Z) ? eZ : fZ;
-            if (hi > lo) {
-                q0 = lo + (int32_t)(((int64_t)(hi - lo) * cta) / ncta);
-                q1 = lo + (int32_t)(((int64_t)(hi - lo) * (cta + 1)) / ncta);
-            }
-        }
+    // end of the pairs completed by chunk m (the first window of the pair holding window
+    // min((m+1) kChunk, Wtot), or Wtot)
+    auto qend = [&](int32_t m) -> int32_t {
+        const int32_t E = (int32_t)min((int64_t)(m + 1) * kChunk, (int64_t)Wtot);
+        if (E >= Wtot) return Wtot;
+        return E - locate(E, s_wpre, a.cu, B).wi;
     };
+    auto split = [&](int32_t lo0, int32_t hi0, int32_t &lo, int32_t &hi) {
+        const int64_t n = hi0 - lo0;
+        lo = lo0 + (int32_t)((n * cta) / ncta);
+        hi = lo0 + (int32_t)((n * (cta + 1)) / ncta);
+    };
+    // this CTA's share of chunk m's statistics / of range m's quantisation
+    auto stats_share = [&](int32_t m, int32_t &lo, int32_t &hi) {
+        split(m * kChunk, (int32_t)min((int64_t)(m + 1) * kChunk, (int64_t)Wtot), lo, hi);
+    };
+    auto quant_share = [&](int32_t m, int32_t &lo, int32_t &hi) {
+        split(m == 0 ? 0 : qend(m - 1), qend(m), lo, hi);
+    };
+    auto slice = [&](int32_t m) { return a.params + ((int64_t)cta * 2 + (m & 1)) * a.cap; };
 
-    if (warp == kCWarps) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
-            const uint64_t pol_first = make_policy_evict_first();
-            uint32_t k = 0;
-            bool abort = false;
-            for (int32_t i = 0; i <= nsg && !abort; ++i) {
-                int32_t s0, s1, q0, q1;
-                ranges(i, s0, s1, q0, q1);
-                for (int part = 0; part < 2 && !abort; ++part) {
-                    const int32_t w0 = part ? q0 : s0, w1 = part ? q1 : s1;
-                    for (int32_t w = w0; w < w1; ++w, ++k) {
-                        const int stage = k % kCStages;
-                        const uint32_t use = k / kCStages;
-                        if (use > 0 && !mbar_wait_bounded(&empty[stage], (use - 1) & 1)) {
-                            record_error(a.hdr, kErrEmptyWait);
-                            abort = true;
-                            break;
+    if (warp == kWorkers) {
+        // ================================================================ sync warp
+        int32_t ma = 0, ms = 0;  // chunks published, ranges segmented
+        uint32_t spins = 0;
+        while (ma < M || ms < M) {
+            bool progressed = false;
+            if (ma < M) {  // publish once every worker has finished the statistics of chunk ma
+                int32_t d = INT32_MAX;
+                if (lane == 0)
+                    for (int i = 0; i < kWorkers; ++i) d = min(d, ld_acquire_cta_shared(ctl->stats_done + i));
+                d = __shfl_sync(0xffffffffu, d, 0);
+                if (d > ma) {
+                    ma = d < M ? d : M;
+                    // the workers' window statistics (acquired above) before the progress word
+                    if (lane == 0) st_release_gpu(a.prog + cta, (uint32_t)ma);
+                    progressed = true;
+                }
+            }
+            if (!progressed && ms < ma) {
+                int32_t qlo, qhi;
+                quant_share(ms, qlo, qhi);
+                if (qlo >= qhi) {
+                    if (lane == 0) st_release_cta_shared(ctl->ready + (ms & 1), ms + 1);
+                    ++ms;
+                    progressed = true;
+                } else {
+                    // the slice buffer is free once no worker still quantises range ms-2
+                    int32_t d = INT32_MAX;
+                    if (lane == 0)
+                        for (int i = 0; i < kWorkers; ++i) d = min(d, ld_acquire_cta_shared(ctl->quant_done + i));
+                    d = __shfl_sync(0xffffffffu, d, 0);
+                    // barrier ms: every CTA has published the statistics of chunks 0..ms
+                    uint32_t done = 0;
+                    if (d >= ms - 1) {  // all progress words in one round of relaxed loads
+                        uint32_t pv[kMaxSms / 32];
+#pragma unroll
+                        for (int j = 0; j < kMaxSms / 32; ++j)
+                            pv[j] = lane + 32 * j < ncta ? ld_relaxed_gpu(a.prog + lane + 32 * j) : 0xffffffffu;
+                        done = 0xffffffffu;
+#pragma unroll
+                        for (int j = 0; j < kMaxSms / 32; ++j) done = min(done, pv[j]);
+                        done = __reduce_min_sync(0xffffffffu, done);
+                    }
+                    if (d >= ms - 1 && done >= (uint32_t)(ms + 1)) {
+                        __threadfence();  // with the relaxed loads above: acquire of every CTA's progress
+                        __syncwarp();
+                        // segment the pairs overlapping this CTA's share
+                        PairParams *out = slice(ms);
+                        WinLoc l = locate(qlo, s_wpre, a.cu, B);
+                        int32_t w = qlo, slot = 0;
+                        while (true) {
+                            const int32_t wbase = w - l.wi;
+                            segment_pair(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
+                            ++slot;
+                            w = wbase + l.W;
+                            if (w >= qhi) break;
+                            step_loc(l, l.W - l.wi, a.cu, a.Hkv);
                         }
-                        const WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
-                        const int32_t row = s_cu[loc.b] + loc.wi * kWin;
-                        uint8_t *dst = smem + stage * kCStageBytes;
-                        mbar_arrive_expect_tx(&full[stage], kCStageBytes);
-                        // first read: normal priority, so the tile stays in L2 for its second read;
-                        // second read (quantisation) is the last use: evict first
-                        if (part) {
-                            tma_load_3d_hint(dst, &tmK, 0, loc.h, row, &full[stage], pol_first);
-                            tma_load_3d_hint(dst + kTileBytes, &tmV, 0, loc.h, row, &full[stage], pol_first);
-                        } else {
-                            tma_load_3d(dst, &tmK, 0, loc.h, row, &full[stage]);
-                            tma_load_3d(dst + kTileBytes, &tmV, 0, loc.h, row, &full[stage]);
+                        __syncwarp();
+                        if (lane == 0) {
+                            __threadfence_block();
+                            st_release_cta_shared(ctl->ready + (ms & 1), ms + 1);
                         }
+                        ++ms;
+                        progressed = true;
                     }
                 }
+            }
+            if (progressed) {
+                spins = 0;
+            } else {
+                if (++spins >= kSpinLimit) {
+                    if (lane == 0) {
+                        record_error(a.hdr, kErrBarrierWait);
+                        st_release_cta_shared(&ctl->abort, 1);
+                    }
+                    break;
+                }
+                __nanosleep(128);
             }
         }
     } else {
-        // ---------------------------------------------------------------- consumers
-        Pending pd;
-        pd.p = -1;
-        pd.cnt = 0;
-        PairCache pc;
-        pc.p = -1;
-        bool pc_ok = false;
-        uint32_t k = 0;
-        for (int32_t i = 0; i <= nsg; ++i) {
-            int32_t s0, s1, q0, q1;
-            ranges(i, s0, s1, q0, q1);
-            for (int part = 0; part < 2; ++part) {
-                const int32_t w0 = part ? q0 : s0, w1 = part ? q1 : s1;
-                for (int32_t w = w0; w < w1; ++w, ++k) {
-                    if ((int)(k % kCWarps) != warp) continue;
-                    const int stage = k % kCStages;
-                    const uint32_t use = k / kCStages;
-                    const WinLoc loc = locate(w, s_wpre, s_cu, B, a.Hkv);
-                    int64_t blk = 0;
-                    if (part == 1) {  // block id and pair parameters, before waiting for the tile
-                        blk = __ldg(a.bt + (int64_t)loc.b * a.max_blocks + (loc.wi * kWin) / a.bs);
-                        const int32_t p = loc.b * a.Hkv + loc.h;
-                        if (p != pc.p) pc_ok = load_pair(a, p, target, pc);
-                    }
-                    if (!mbar_wait_bounded(&full[stage], use & 1)) {
-                        record_error(a.hdr, kErrFullWait);
-                        continue;  // no data: skip the window (the call reports the error)
-                    }
-                    const uint32_t kt = smem_u32(smem) + stage * kCStageBytes;
-                    const uint32_t vt = kt + kTileBytes;
-                    if (part == 0) {
-                        const int32_t cnt = min(kWin, loc.L - loc.wi * kWin);
-                        const WinStats st = window_stats(kt, vt, cnt);
-                        const int32_t p = loc.b * a.Hkv + loc.h;
-                        if (lane == 0) {
-                            __stcg(a.win_mean + w, st.mean);
-                            __stcg(a.win_mm + w, make_float4(st.kmn, st.kmx, st.vmn, st.vmx));
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[stage]);
-                        if (p != pd.p) {
-                            flush_pending(a, pd, target);
-                            pd.p = p; pd.b = loc.b; pd.h = loc.h; pd.L = loc.L; pd.W = loc.W;
-                            pd.wbase = w - loc.wi;
-                        }
-                        ++pd.cnt;
+        // ================================================================ worker warps
+        const uint32_t ring = smem_u32(smem) + warp * (kRing * kWinBytes);
+        const uint64_t pol_first = make_policy_evict_first();
+        const int64_t rstride = (int64_t)a.Hkv * kD;  // elements between consecutive tokens of a head
+
+        auto seek = [&](Cursor &c, bool quant) {
+            for (; c.m < M; ++c.m) {
+                int32_t lo, hi;
+                if (quant) quant_share(c.m, lo, hi);
+                else stats_share(c.m, lo, hi);
+                if (lo + warp < hi) {
+                    c.w = lo + warp;
+                    c.end = hi;
+                    if (quant) {
+                        c.loc = locate(lo, s_wpre, a.cu, B);
+                        c.slot = step_loc(c.loc, warp, a.cu, a.Hkv);
                     } else {
-                        if (pc_ok) window_quant(a, loc, kt, vt, pc, blk);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[stage]);
+                        c.loc = locate(c.w, s_wpre, a.cu, B);
+                        c.slot = 0;
+                    }
+                    return;
+                }
+            }
+            c.w = -1;
+        };
+        auto advance = [&](Cursor &c, bool quant) {
+            c.w += kWorkers;
+            if (c.w < c.end) {
+                c.slot += step_loc(c.loc, kWorkers, a.cu, a.Hkv);
+                return;
+            }
+            ++c.m;
+            seek(c, quant);
+        };
+
+        Cursor sc, qc;
+        sc.m = 0;
+        qc.m = 0;
+        seek(sc, false);
+        seek(qc, true);
+        if (lane == 0) {
+            st_release_cta_shared(ctl->stats_done + warp, sc.w >= 0 ? sc.m : M);
+            st_release_cta_shared(ctl->quant_done + warp, qc.w >= 0 ? qc.m : M);
+        }
+
+        int32_t cur_m = -1, cur_slot = -1;  // parameters currently held in `params`
+        PairCache params = {0, 0.0f, 0.0f, 0.0f, 0.0f};
+        int next_stage = 0;
+
+        // Start the copies of the next item; false when nothing may start now.
+        auto try_issue = [&](Item &it) -> bool {
+            const bool aborted = *reinterpret_cast<volatile int32_t *>(&ctl->abort) != 0;
+            if (qc.w >= 0 && (aborted || ld_acquire_cta_shared(ctl->ready + (qc.m & 1)) >= qc.m + 1)) {
+                it.kind = aborted ? 2 : 1;
+                it.w = qc.w;
+                it.m = qc.m;
+                it.loc = qc.loc;
+                it.stage = next_stage;
+                if (!aborted) {
+                    if (qc.m != cur_m || qc.slot != cur_slot) {
+                        params = load_params(slice(qc.m) + qc.slot);
+                        cur_m = qc.m;
+                        cur_slot = qc.slot;
+                    }
+                    it.pc = params;
+                    it.blk = __ldg(a.bt + (int64_t)qc.loc.b * a.max_blocks + (qc.loc.wi * kWin) / a.bs);
+                }
+            } else if (sc.w >= 0 && (qc.w < 0 || sc.m <= qc.m || sc.w < qc.w + kAhead)) {
+                it.kind = 0;
+                it.w = sc.w;
+                it.m = sc.m;
+                it.loc = sc.loc;
+                it.stage = next_stage;
+            } else {
+                return false;
+            }
+            if (it.kind != 2) {
+                const WinLoc &l = it.loc;
+                const int32_t t0 = l.wi * kWin, cnt = min(kWin, l.L - t0);
+                const int64_t row0 = ((int64_t)(l.c0 + t0) * a.Hkv + l.h) * kD;
+                const uint32_t dst = ring + it.stage * kWinBytes;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 2 * i + (lane >> 4), col = lane & 15;
+                    if (row < cnt) {  // rows past the request end are not copied
+                        const uint16_t *ks = a.k + row0 + row * rstride + col * 8;
+                        const uint16_t *vs = a.v + row0 + row * rstride + col * 8;
+                        const uint32_t off = row * (kD * 2) + col * 16;
+                        if (it.kind == 1) {  // second read: last use
+                            cp16_hint(dst + off, ks, pol_first);
+                            cp16_hint(dst + kTileBytes + off, vs, pol_first);
+                        } else {
+                            cp16(dst + off, ks);
+                            cp16(dst + kTileBytes + off, vs);
+                        }
                     }
                 }
-                if (part == 0) flush_pending(a, pd, target);  // before any wait on a flag
             }
+            cp_commit();
+            next_stage ^= 1;
+            if (it.kind == 0) {
+                advance(sc, false);
+                it.next_m = sc.w >= 0 ? sc.m : M;
+            } else {
+                advance(qc, true);
+                it.next_m = qc.w >= 0 ? qc.m : M;
+            }
+            return true;
+        };
+
+        Item f0, f1;
+        int nin = 0;
+        uint32_t spins = 0;
+        while (true) {
+            if (nin == 0 && try_issue(f0)) nin = 1;
+            if (nin == 1 && try_issue(f1)) nin = 2;
+            if (nin == 0) {
+                if (sc.w < 0 && qc.w < 0) break;
+                // blocked on the parameters of range qc.m
+                if (++spins >= kSpinLimit) {
+                    record_error(a.hdr, kErrBarrierWait);
+                    if (lane == 0) st_release_cta_shared(&ctl->abort, 1);
+                    spins = 0;
+                }
+                __nanosleep(64);
+                continue;
+            }
+            spins = 0;
+            if (nin == 2) cp_wait<1>();
+            else cp_wait<0>();
+            __syncwarp();
+            const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
+            if (f0.kind == 0) {
+                const int32_t cnt = min(kWin, f0.loc.L - f0.loc.wi * kWin);
+                const WinStats s = window_stats(kt, vt, cnt);
+                if (lane == 0) {
+                    __stcg(a.win_mean + f0.w, s.mean);
+                    __stcg(a.win_mm + f0.w, make_float4(s.kmn, s.kmx, s.vmn, s.vmx));
+                    uint32_t *g = reinterpret_cast<uint32_t *>(a.agg + f0.w / kAgg);
+                    atomicMax(g + 0, ~ord_enc(s.kmn));
+                    atomicMax(g + 1, ord_enc(s.kmx));
+                    atomicMax(g + 2, ~ord_enc(s.vmn));
+                    atomicMax(g + 3, ord_enc(s.vmx));
+                    if (f0.next_m != f0.m) st_release_cta_shared(ctl->stats_done + warp, f0.next_m);
+                }
+            } else if (f0.kind == 1) {
+                window_quant(a, f0.loc, kt, vt, f0.pc, f0.blk);
+            }
+            __syncwarp();  // the stage's reads are done before it is refilled
+            if (f0.kind != 0 && lane == 0 && f0.next_m != f0.m)
+                st_release_cta_shared(ctl->quant_done + warp, f0.next_m);
+            f0 = f1;
+            --nin;
         }
+        cp_wait<0>();
     }
 
     __syncthreads();
     if (tid == 0) {
         __threadfence();
         const uint32_t old = atomicAdd(&a.hdr->done_ctas, 1u);
-        if (old == (uint32_t)ncta - 1u) {  // last CTA of the call: advance the epoch
-            a.hdr->done_ctas = 0;
-            a.hdr->epoch = target;
-            __threadfence();
-        }
+        ctl->last = (old == (uint32_t)ncta - 1u);  // last CTA of the call
+    }
+    __syncthreads();
+    if (ctl->last) {
+        __threadfence();
+        // clear the min/max aggregates and the progress words for the next call
+        const int32_t nagg = (Wtot + kAgg - 1) / kAgg;
+        for (int32_t i = tid; i < nagg; i += kThreads) a.agg[i] = make_uint4(0, 0, 0, 0);
+        for (int32_t i = tid; i < ncta; i += kThreads) a.prog[i] = 0;
+        if (tid == 0) a.hdr->done_ctas = 0;
+        __threadfence();
     }
 }
 
@@ -651,48 +867,41 @@ namespace dgq {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Pairs that can overlap one CTA's share of a quantisation range: a range holds at most
+// kChunk + (windows of the longest pair) - 1 windows, and a share of n windows overlaps at
+// most n + 1 pairs.
+static int32_t params_cap(int32_t max_seqlen, int nsm)
+{
+    const int64_t wpair = (max_seqlen + kWin - 1) / kWin;
+    return (int32_t)((kChunk + wpair + nsm - 1) / nsm + 2);
+}
+
+// The layout does not depend on the SM count: nsm * params_cap(.., nsm) is at most
+// kChunk + wpair + 3 * nsm pairs for any nsm <= kMaxSms.
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv)
 {
     CompressLayout l;
-    size_t P = (size_t)batch * Hkv;
-    size_t Wmax = P * (size_t)((max_seqlen + kWin - 1) / kWin);
+    const size_t P = (size_t)batch * Hkv;
+    const size_t wpair = (size_t)((max_seqlen + kWin - 1) / kWin);
+    const size_t Wmax = P * wpair;
     size_t off = sizeof(WsHeader);
-    l.off_count = off; off = align256(off + P * 4);
-    l.off_flag = off; off = align256(off + P * 4);
-    l.off_params = off; off = align256(off + P * sizeof(PairParams));
-    l.off_mean = off; off = align256(off + Wmax * 4);
+    l.off_prog = off; off = align256(off + kMaxSms * 4);
+    l.off_params = off; off = align256(off + 2 * (kChunk + wpair + 3 * kMaxSms) * sizeof(PairParams));
+    l.off_mean = off; off = align256(off + (Wmax + 4) * 4);  // +4: quad reads past the end
     l.off_mm = off; off = align256(off + Wmax * 16);
+    l.off_agg = off; off = align256(off + (Wmax / kAgg + 1) * 16);
     l.total = off;
     return l;
 }
 
-size_t compress_smem_bytes(int32_t B)
-{
-    return 1024 + (size_t)kCStages * kCStageBytes + 2 * kCStages * 8 + (size_t)(2 * (B + 1)) * 4;
-}
+static size_t compress_smem_bytes(int32_t B) { return (size_t)kRingBytes + sizeof(CtaCtl) + (size_t)(B + 1) * 4; }
 
-// 3-D map over a packed [T, Hkv, 128] bf16 tensor; box = 16 tokens of one head (4 KB).
-static bool make_kv_map(CUtensorMap *map, const void *base, int32_t T, int32_t Hkv)
+cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
+                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+                            uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm, cudaStream_t stream)
 {
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)kWin};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t T,
-                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, bool *map_failed,
-                            cudaStream_t stream)
-{
-    *map_failed = false;
-    CompressLayout l = compress_layout(B, max_seqlen, Hkv);
+    if (nsm > kMaxSms) return cudaErrorInvalidConfiguration;
+    const CompressLayout l = compress_layout(B, max_seqlen, Hkv);
     char *base = static_cast<char *>(ws);
     CompressArgs a;
     a.k = static_cast<const uint16_t *>(k);
@@ -703,38 +912,36 @@ cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int
     a.vpool = vpool;
     a.table = table;
     a.hdr = reinterpret_cast<WsHeader *>(base);
-    a.pair_count = reinterpret_cast<uint32_t *>(base + l.off_count);
-    a.pair_flag = reinterpret_cast<uint32_t *>(base + l.off_flag);
+    a.prog = reinterpret_cast<uint32_t *>(base + l.off_prog);
     a.params = reinterpret_cast<PairParams *>(base + l.off_params);
     a.win_mean = reinterpret_cast<float *>(base + l.off_mean);
     a.win_mm = reinterpret_cast<float4 *>(base + l.off_mm);
+    a.agg = reinterpret_cast<uint4 *>(base + l.off_agg);
     a.B = B;
     a.Hkv = Hkv;
     a.bs = bs;
     a.max_blocks = max_blocks;
-    a.wps = 4096;  // 4096 windows x 16 tokens x 512 B (K+V bf16) = 32 MB per super-group
+    a.cap = params_cap(max_seqlen, nsm);
 
-    CUtensorMap mk, mv;
-    const int32_t Tmap = T > 0 ? T : 1;
-    if (!make_kv_map(&mk, k, Tmap, Hkv) || !make_kv_map(&mv, v, Tmap, Hkv)) {
-        *map_failed = true;
-        return cudaErrorInvalidValue;
-    }
+    // per-device launch set-up, done once per (device, shared-memory size)
+    static int cached_dev = -1;
+    static size_t cached_smem = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int nsm = 0;
-    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     const size_t smem = compress_smem_bytes(B);
-    e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    dim3 grid(nsm), block(kThreads);  // one CTA per SM; every CTA is resident (cooperative launch)
-    void *args[] = {&mk, &mv, &a};
+    if (dev != cached_dev || smem != cached_smem) {
+        e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        cached_dev = dev;
+        cached_smem = smem;
+    }
+    dim3 grid(nsm), block(kThreads);  // one CTA per SM, all resident (cooperative launch)
+    void *args[] = {&a};
     return cudaLaunchCooperativeKernel((const void *)compress_kernel, grid, block, args, smem, stream);
 }
 

@@ -16,7 +16,7 @@ constexpr int kMaxSeg = 5;  // segments per (request, KV head)
 // Every workspace starts with this 256-byte header.
 struct WsHeader {
     uint32_t error;        // first device-side error code (0 = none)
-    uint32_t epoch;        // call counter (compress)
+    uint32_t reserved;     // zero
     uint32_t done_ctas;    // CTAs finished in the current call (compress)
     uint32_t pad[61];
 };
@@ -25,7 +25,8 @@ static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 // Device-side error codes written to WsHeader::error.
 enum : uint32_t {
     kErrNone = 0,
-    kErrFlagWait = 1,       // compress: a segmentation flag never arrived
+    kErrBarrierWait = 1,    // compress: a chunk barrier never completed, or a worker waited
+                            // too long for its CTA's segmentation
     kErrFullWait = 2,       // decode: a TMA stage never completed
     kErrEmptyWait = 3,      // decode: consumers never released a stage
 };
@@ -44,6 +45,30 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_acquire_cta_shared(const int32_t *p)
+{
+    int32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta_shared(int32_t *p, int32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))),
+                 "r"(v)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)

@@ -11,13 +11,12 @@
 namespace dgq {
 
 struct CompressLayout {
-    size_t off_count, off_flag, off_params, off_mean, off_mm, total;
+    size_t off_prog, off_params, off_mean, off_mm, off_agg, total;
 };
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t T,
-                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, bool *map_failed,
-                            cudaStream_t stream);
+cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
+                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+                            uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm, cudaStream_t stream);
 
 struct AttnLayout {
     size_t off_count, off_part, total;

@@ -605,102 +605,112 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     cp_async_wait<0>();  // no copy may still target shared memory when the CTA exits
 }
 
-// Merge of the pieces of every pair that several CTAs share: one CTA per (pair, query head),
-// after the main kernel (programmatic dependent launch).  Pieces are folded in CTA order; the
-// current token is added last, as in the single-piece path.  Every load that does not depend on
-// the piece range is issued before the range is read, and all pieces are fetched in one round.
-constexpr int kCombineWarps = 8;
-constexpr int kCombineSlots = 8;  // pieces one warp keeps in flight per round
+// Merge of the pieces of every pair that several CTAs share, after the main kernel
+// (programmatic dependent launch).  One item per (pair, query head); a grid of at most 8 CTAs
+// per SM walks the items, so the whole merge is one wave of small CTAs that can already be
+// resident while the main kernel runs.  Pieces are folded in CTA order and the current token
+// is added last, as in the single-piece path; all pieces of an item are fetched in one round.
+constexpr int kCombineWarps = 4;
+constexpr int kCombineSlots = 8;    // pieces one warp keeps in flight per round
+constexpr int kCombineCtasPerSm = 8;
 
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(AttnArgs a)
+__global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine_kernel(AttnArgs a)
 {
     const int32_t G = a.G, Hkv = a.Hkv;
-    const int32_t p = blockIdx.x / G, g = blockIdx.x - p * G;
-    const int32_t b = p / Hkv, h = p - b * Hkv;
+    const int32_t items = a.B * Hkv * G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
     __shared__ float4 s_o[kCombineWarps][32];
     __shared__ float s_sn;
 
-    // independent of the piece range (inputs of this call, not written by the main kernel)
-    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * a.Hq + h * G + g) * kD) + lane);
-    const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(a.knew + ((int64_t)b * Hkv + h) * kD) + lane);
-    const float vn = bf16lo_to_f32((uint32_t)__ldg(a.vnew + ((int64_t)b * Hkv + h) * kD + (tid & (kD - 1))));
+    bool waited = false;
+    for (int32_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int32_t p = item / G, g = item - p * G;
+        const int32_t b = p / Hkv, h = p - b * Hkv;
+        // inputs of this call (not written by the main kernel): loaded before the wait
+        const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * a.Hq + h * G + g) * kD) + lane);
+        const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(a.knew + ((int64_t)b * Hkv + h) * kD) + lane);
+        const float vn = bf16lo_to_f32((uint32_t)__ldg(a.vnew + ((int64_t)b * Hkv + h) * kD + tid));
+        if (!waited) {
+            pdl_wait_primary();
+            waited = true;
+        }
+        const int2 info = __ldcg(a.pair_info + p);
+        const int32_t cfirst = info.x, clast = info.y;
+        if (cfirst == clast) continue;  // finished inside the main kernel
+        const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
+        const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
+        const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
 
-    pdl_wait_primary();
-    const int2 info = __ldcg(a.pair_info + p);
-    const int32_t cfirst = info.x, clast = info.y;
-    if (cfirst == clast) return;  // finished inside the main kernel
-    const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
-    const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
-    const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
-
-    // warp w folds slots cfirst + w, + 8, ...: per slot its (m, l) and this lane's 4 columns of O
-    float m_w = -INFINITY, l_w = 0.0f;
-    float4 o_w = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int32_t base = cfirst + warp; base <= clast; base += kCombineWarps * kCombineSlots) {
-        float mm[kCombineSlots], ll[kCombineSlots];
-        float4 oo[kCombineSlots];
+        // warp w folds slots cfirst + w, + 4, ...: per slot its (m, l) and this lane's 4 columns of O
+        float m_w = -INFINITY, l_w = 0.0f;
+        float4 o_w = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t base = cfirst + warp; base <= clast; base += kCombineWarps * kCombineSlots) {
+            float mm[kCombineSlots], ll[kCombineSlots];
+            float4 oo[kCombineSlots];
 #pragma unroll
-        for (int i = 0; i < kCombineSlots; ++i) {
-            const int32_t cc = base + i * kCombineWarps;
-            mm[i] = -INFINITY;
-            ll[i] = 0.0f;
-            oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
-                const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
-                mm[i] = ml.x;
-                ll[i] = ml.y;
-                oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+            for (int i = 0; i < kCombineSlots; ++i) {
+                const int32_t cc = base + i * kCombineWarps;
+                mm[i] = -INFINITY;
+                ll[i] = 0.0f;
+                oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
+                    const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
+                    mm[i] = ml.x;
+                    ll[i] = ml.y;
+                    oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kCombineSlots; ++i) {  // in slot order: online fold
+                const float M = fmaxf(m_w, mm[i]);
+                if (M == -INFINITY) continue;
+                const float fo = m_w == -INFINITY ? 0.0f : ex2(m_w - M);
+                const float fn = mm[i] == -INFINITY ? 0.0f : ex2(mm[i] - M);
+                l_w = l_w * fo + ll[i] * fn;
+                o_w.x = o_w.x * fo + oo[i].x * fn;
+                o_w.y = o_w.y * fo + oo[i].y * fn;
+                o_w.z = o_w.z * fo + oo[i].z * fn;
+                o_w.w = o_w.w * fo + oo[i].w * fn;
+                m_w = M;
             }
         }
-#pragma unroll
-        for (int i = 0; i < kCombineSlots; ++i) {  // in slot order: online fold
-            const float M = fmaxf(m_w, mm[i]);
-            if (M == -INFINITY) continue;
-            const float fo = m_w == -INFINITY ? 0.0f : ex2(m_w - M);
-            const float fn = mm[i] == -INFINITY ? 0.0f : ex2(mm[i] - M);
-            l_w = l_w * fo + ll[i] * fn;
-            o_w.x = o_w.x * fo + oo[i].x * fn;
-            o_w.y = o_w.y * fo + oo[i].y * fn;
-            o_w.z = o_w.z * fo + oo[i].z * fn;
-            o_w.w = o_w.w * fo + oo[i].w * fn;
-            m_w = M;
+        if (lane == 0) {
+            s_m[warp] = m_w;
+            s_l[warp] = l_w;
         }
-    }
-    if (lane == 0) {
-        s_m[warp] = m_w;
-        s_l[warp] = l_w;
-    }
-    s_o[warp][lane] = o_w;
-    if (warp == 0) {  // the current token's score
-        float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
-        acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
-        acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
-        acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
+        s_o[warp][lane] = o_w;
+        if (warp == 0) {  // the current token's score
+            float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
+            acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
+            acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
+            acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
 #pragma unroll
-        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) s_sn = acc * kLog2eOverSqrtD;
-    }
-    __syncthreads();
-    if (tid < kD) {  // thread d: fold the warps in order, then the current token
-        const int d = tid;
-        float M = -INFINITY, L = 0.0f, O = 0.0f;
-        for (int w = 0; w < kCombineWarps; ++w) {
-            const float mw = s_m[w];
-            const float Mn = fmaxf(M, mw);
-            if (Mn == -INFINITY) continue;
-            const float fo = M == -INFINITY ? 0.0f : ex2(M - Mn);
-            const float fn = mw == -INFINITY ? 0.0f : ex2(mw - Mn);
-            const float ow = reinterpret_cast<const float *>(&s_o[w][d >> 2])[d & 3];
-            L = L * fo + s_l[w] * fn;
-            O = O * fo + ow * fn;
-            M = Mn;
+            for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) s_sn = acc * kLog2eOverSqrtD;
         }
-        __nv_bfloat16 ob = __float2bfloat16_rn(finish(M, L, O, s_sn, vn));
-        a.out[((int64_t)b * a.Hq + h * G + g) * kD + d] = *reinterpret_cast<uint16_t *>(&ob);
+        __syncthreads();
+        {  // thread d: fold the warps in order, then the current token
+            const int d = tid;
+            float M = -INFINITY, L = 0.0f, O = 0.0f;
+            for (int w = 0; w < kCombineWarps; ++w) {
+                const float mw = s_m[w];
+                const float Mn = fmaxf(M, mw);
+                if (Mn == -INFINITY) continue;
+                const float fo = M == -INFINITY ? 0.0f : ex2(M - Mn);
+                const float fn = mw == -INFINITY ? 0.0f : ex2(mw - Mn);
+                const float ow = reinterpret_cast<const float *>(&s_o[w][d >> 2])[d & 3];
+                L = L * fo + s_l[w] * fn;
+                O = O * fo + ow * fn;
+                M = Mn;
+            }
+            __nv_bfloat16 ob = __float2bfloat16_rn(finish(M, L, O, s_sn, vn));
+            a.out[((int64_t)b * a.Hq + h * G + g) * kD + d] = *reinterpret_cast<uint16_t *>(&ob);
+        }
+        __syncthreads();  // shared memory is reused by the next item
     }
+    if (!waited) pdl_wait_primary();
 }
 
 }  // namespace dgq
@@ -791,7 +801,9 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
 
     // merge of shared pairs, chained with programmatic dependent launch
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hkv * G));
+    const int64_t items = (int64_t)B * Hkv * G;
+    const int64_t cgrid = items < (int64_t)nsm * kCombineCtasPerSm ? items : (int64_t)nsm * kCombineCtasPerSm;
+    cfg.gridDim = dim3((unsigned)cgrid);
     cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -7,8 +7,8 @@
 // q = rint((x - min) * (255 / (max - min))).  Codes go to the physical block named by the
 // block table ("PagedAttention implementation", DeepSeek-V4 KV-cache article).
 //
-// GPU design: one persistent cooperative kernel, one CTA per SM: 12 worker warps and one
-// sync warp.
+// GPU design: one persistent cooperative kernel, one CTA per SM: 12 worker warps, an
+// arrival warp and a segmentation warp.
 //  * The flat list of all 16-token windows of all (request, head) pairs, in (request, head,
 //    window) order, is cut into chunks of kChunk windows (64 MB of bf16 K+V).  Workers
 //    compute window statistics (variance mean; K and V min/max, also folded into aggregates
@@ -23,10 +23,10 @@
 //    statistics are mostly still in the 126 MB L2 when they are read again for
 //    quantisation (those second reads carry an evict-first hint).
 //  * Under full HBM load every dependent round trip through L2 costs microseconds, so all
-//    global synchronisation lives in the sync warp: it publishes progress, polls the
-//    progress words of all CTAs, and segments every pair that overlaps its CTA's share of a
-//    range (a pair shared by several CTAs is segmented by each; the result is the same
-//    bits).  Parameters go to a per-CTA slice of the workspace; workers learn of them
+//    global synchronisation lives in two control warps: the arrival warp publishes the CTA's
+//    progress; the segmentation warp polls the progress words of all CTAs and segments every
+//    pair that overlaps its CTA's share of a range (a pair shared by several CTAs is
+//    segmented by each; the result is the same bits).  Parameters go to a per-CTA slice of the workspace; workers learn of them
 //    through shared-memory flags with CTA-scope release/acquire and never wait on global
 //    memory themselves.
 //  * Each worker streams its windows (every 12th window of its CTA's share) through a
@@ -48,7 +48,7 @@
 
 namespace dgq {
 
-// Quantisation parameters of one pair as the sync warp publishes them.
+// Quantisation parameters of one pair as the segmentation warp publishes them.
 struct alignas(16) PairParams {
     float k_min[kMaxSeg], k_inv[kMaxSeg], v_min[kMaxSeg], v_inv[kMaxSeg];
     int32_t start[kMaxSeg];
@@ -58,8 +58,8 @@ struct alignas(16) PairParams {
 static_assert(sizeof(PairParams) == 128, "PairParams is 128 bytes");
 
 constexpr int kAgg = 64;        // windows per min/max aggregate
-constexpr int kWorkers = 12;    // worker warps per CTA (plus one sync warp)
-constexpr int kThreads = (kWorkers + 1) * 32;
+constexpr int kWorkers = 10;    // worker warps per CTA (plus an arrival warp and a segmentation warp)
+constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
 constexpr int kTileBytes = kWin * kD * 2;  // 16 tokens x 128 bf16 = 4 KB
 constexpr int kWinBytes = 2 * kTileBytes;  // K tile + V tile
@@ -142,32 +142,7 @@ __device__ __forceinline__ int32_t step_loc(WinLoc &l, int32_t n, const int32_t 
     return crossed;
 }
 
-// ---- canonical fp32 sums ---------------------------------------------------------------------
-
-// In-lane balanced tree over 8 values, then butterfly over the 16 lanes of a half-warp
-// (xor 1, 2, 4, 8): lane i holds elements [8i, 8i+8) of a 128-element row, so the result
-// is sum(left 64) + sum(right 64) recursively, identical in every lane.
-__device__ __forceinline__ float tree8(const float *x)
-{
-    float a = __fadd_rn(x[0], x[1]), b = __fadd_rn(x[2], x[3]);
-    float c = __fadd_rn(x[4], x[5]), d = __fadd_rn(x[6], x[7]);
-    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
-}
-
-__device__ __forceinline__ float halfwarp_tree(float s)
-{
-#pragma unroll
-    for (int o = 1; o <= 8; o <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
-    return s;
-}
-
-__device__ __forceinline__ void unpack8(const uint4 &q, float *x)
-{
-    x[0] = bf16lo_to_f32(q.x); x[1] = bf16hi_to_f32(q.x);
-    x[2] = bf16lo_to_f32(q.y); x[3] = bf16hi_to_f32(q.y);
-    x[4] = bf16lo_to_f32(q.z); x[5] = bf16hi_to_f32(q.z);
-    x[6] = bf16lo_to_f32(q.w); x[7] = bf16hi_to_f32(q.w);
-}
+// ---- warp reductions ------------------------------------------------------------------------
 
 __device__ __forceinline__ float warp_min(float v)
 {
@@ -206,11 +181,46 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
     const int32_t k = min(ngroups(L), W) - 1;  // boundaries to place (0..4)
 
     // (1) per-lane top-k of (jump desc, window asc); the jump of window w < W-1 is
-    // |m[w+1] - m[w]|.  Lanes read aligned quads of the flat mean array overlapping the pair,
-    // eight quads in flight per lane.
+    // |m[w+1] - m[w]|.  A pair of at most 256 windows is read in one round (lane i holds windows
+    // 8i .. 8i+7 with their means and extremes); a longer one reads aligned quads of the flat
+    // mean array, eight quads in flight per lane, and takes its extremes from aggregates below.
     float cj[4] = {-1.0f, -1.0f, -1.0f, -1.0f};
     int32_t cw[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
-    if (k > 0) {
+    const bool small = W <= 8 * 32;
+    float4 smm[8];  // small pairs: extremes of this lane's windows
+    if (small) {
+        float m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int32_t w = 8 * lane + i;
+            m[i] = 0.0f;
+            smm[i] = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
+            if (w < W) {
+                m[i] = __ldcg(a.win_mean + wbase + w);
+                smm[i] = __ldcg(a.win_mm + wbase + w);
+            }
+        }
+        const float mnext = __shfl_down_sync(0xffffffffu, m[0], 1);  // first mean of the next lane
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int32_t w = 8 * lane + i;
+            if (k == 0 || w + 1 >= W) continue;
+            const float j = fabsf(__fsub_rn(i < 7 ? m[i + 1] : mnext, m[i]));
+            // a lane meets its windows in increasing order, so an equal jump keeps the earlier
+            // window ahead of it
+            if (j > cj[3]) {
+                cj[3] = j;
+                cw[3] = w;
+#pragma unroll
+                for (int s = 3; s > 0; --s) {
+                    if (cj[s] > cj[s - 1]) {
+                        const float tj = cj[s]; cj[s] = cj[s - 1]; cj[s - 1] = tj;
+                        const int32_t tw = cw[s]; cw[s] = cw[s - 1]; cw[s - 1] = tw;
+                    }
+                }
+            }
+        }
+    } else if (k > 0) {
         const int32_t q0 = wbase >> 2, q1 = (wbase + W - 1) >> 2;
         const float4 *mq = reinterpret_cast<const float4 *>(a.win_mean);
         for (int32_t qb = q0 + lane; qb <= q1; qb += 32 * 8) {
@@ -283,36 +293,98 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
         }
     }
 
-    // (2) per-segment fp32 min/max: whole 64-window aggregates inside the segment, single
-    // windows at its two ragged ends
     float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
-        float kn = INFINITY, kx = -INFINITY, vn = INFINITY, vx = -INFINITY;
-        if (s <= k) {
-            const int32_t sw = s == 0 ? 0 : cut[s - 1];
-            const int32_t ew = s < k ? cut[s] : W;
-            const int32_t f0 = wbase + sw, f1 = wbase + ew;             // flat windows [f0, f1)
-            const int32_t a0 = (f0 + kAgg - 1) / kAgg, a1 = f1 / kAgg;  // aggregates [a0, a1) inside
-            const bool whole = a0 < a1;
-            const int32_t e0 = whole ? a0 * kAgg : f1;  // head windows [f0, e0)
-            const int32_t e1 = whole ? a1 * kAgg : f1;  // tail windows [e1, f1)
-            for (int32_t ab = a0 + lane; whole && ab < a1; ab += 32) {
-                const uint4 g = __ldcg(a.agg + ab);
-                kn = fminf(kn, ord_dec(~g.x)); kx = fmaxf(kx, ord_dec(g.y));
-                vn = fminf(vn, ord_dec(~g.z)); vx = fmaxf(vx, ord_dec(g.w));
-            }
-            for (int32_t w = f0 + lane; w < e0; w += 32) {
-                const float4 mm = __ldcg(a.win_mm + w);
-                kn = fminf(kn, mm.x); kx = fmaxf(kx, mm.y); vn = fminf(vn, mm.z); vx = fmaxf(vx, mm.w);
-            }
-            for (int32_t w = e1 + lane; w < f1; w += 32) {
-                const float4 mm = __ldcg(a.win_mm + w);
-                kn = fminf(kn, mm.x); kx = fmaxf(kx, mm.y); vn = fminf(vn, mm.z); vx = fmaxf(vx, mm.w);
+        kmn[s] = INFINITY; kmx[s] = -INFINITY; vmn[s] = INFINITY; vmx[s] = -INFINITY;
+    }
+    if (small) {  // extremes of the windows held in registers
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int32_t w = 8 * lane + i;
+            if (w >= W) continue;
+            const int sg = (w >= cut[0]) + (w >= cut[1]) + (w >= cut[2]) + (w >= cut[3]);
+#pragma unroll
+            for (int s = 0; s < kMaxSeg; ++s) {
+                if (s == sg) {
+                    kmn[s] = fminf(kmn[s], smm[i].x); kmx[s] = fmaxf(kmx[s], smm[i].y);
+                    vmn[s] = fminf(vmn[s], smm[i].z); vmx[s] = fmaxf(vmx[s], smm[i].w);
+                }
             }
         }
-        kmn[s] = warp_min(kn); kmx[s] = warp_max(kx);
-        vmn[s] = warp_min(vn); vmx[s] = warp_max(vx);
+    } else {
+        // (2) per-segment fp32 min/max: whole 64-window aggregates inside the segment, single
+        // windows at its two ragged ends.  The runs of all segments are walked as one list so that
+        // every load of a round is issued before any is used.
+        int32_t rsrc[3 * kMaxSeg], rlen[3 * kMaxSeg], roff[3 * kMaxSeg];
+        int32_t total = 0;
+#pragma unroll
+        for (int s = 0; s < kMaxSeg; ++s) {
+            rsrc[3 * s] = rsrc[3 * s + 1] = rsrc[3 * s + 2] = 0;
+            rlen[3 * s] = rlen[3 * s + 1] = rlen[3 * s + 2] = 0;
+            if (s <= k) {
+                const int32_t sw = s == 0 ? 0 : cut[s - 1];
+                const int32_t ew = s < k ? cut[s] : W;
+                const int32_t f0 = wbase + sw, f1 = wbase + ew;             // flat windows [f0, f1)
+                const int32_t a0 = (f0 + kAgg - 1) / kAgg, a1 = f1 / kAgg;  // aggregates [a0, a1) inside
+                const bool whole = a0 < a1;
+                rsrc[3 * s] = a0;                          // aggregates
+                rlen[3 * s] = whole ? a1 - a0 : 0;
+                rsrc[3 * s + 1] = f0;                      // head windows [f0, e0)
+                rlen[3 * s + 1] = (whole ? a0 * kAgg : f1) - f0;
+                rsrc[3 * s + 2] = whole ? a1 * kAgg : f1;  // tail windows [e1, f1)
+                rlen[3 * s + 2] = whole ? f1 - a1 * kAgg : 0;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 3 * kMaxSeg; ++r) {
+            roff[r] = total;
+            total += rlen[r];
+        }
+        constexpr int kItems = 4;  // loads per lane per round
+        for (int32_t base = 0; base < total; base += 32 * kItems) {
+            uint4 v[kItems];
+            int rr[kItems];
+#pragma unroll
+            for (int u = 0; u < kItems; ++u) {
+                const int32_t idx = base + lane + 32 * u;
+                rr[u] = -1;
+                int32_t src = 0;
+#pragma unroll
+                for (int r = 0; r < 3 * kMaxSeg; ++r) {
+                    if (idx >= roff[r] && idx < roff[r] + rlen[r]) {
+                        rr[u] = r;
+                        src = rsrc[r] + idx - roff[r];
+                    }
+                }
+                if (rr[u] >= 0)
+                    v[u] = (rr[u] % 3 == 0) ? __ldcg(a.agg + src) : __ldcg(reinterpret_cast<const uint4 *>(a.win_mm + src));
+            }
+#pragma unroll
+            for (int u = 0; u < kItems; ++u) {
+                if (rr[u] < 0) continue;
+                float kn, kx, vn, vx;
+                if (rr[u] % 3 == 0) {
+                    kn = ord_dec(~v[u].x); kx = ord_dec(v[u].y); vn = ord_dec(~v[u].z); vx = ord_dec(v[u].w);
+                } else {
+                    kn = __uint_as_float(v[u].x); kx = __uint_as_float(v[u].y);
+                    vn = __uint_as_float(v[u].z); vx = __uint_as_float(v[u].w);
+                }
+                const int sg = rr[u] / 3;
+#pragma unroll
+                for (int s = 0; s < kMaxSeg; ++s) {
+                    if (s == sg) {
+                        kmn[s] = fminf(kmn[s], kn); kmx[s] = fmaxf(kmx[s], kx);
+                        vmn[s] = fminf(vmn[s], vn); vmx[s] = fmaxf(vmx[s], vx);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxSeg; ++s) {
+        kmn[s] = warp_min(kmn[s]); kmx[s] = warp_max(kmx[s]);
+        vmn[s] = warp_min(vmn[s]); vmx[s] = warp_max(vmx[s]);
     }
 
     if (lane == 0) {
@@ -355,89 +427,171 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
     __syncwarp();
 }
 
+// ---- packed fp32 pairs ----------------------------------------------------------------------
+//
+// sm_100-class GPUs execute fp32 add/sub/mul on register pairs (f32x2); each half is an
+// ordinary IEEE operation with round-to-nearest-even.  Measured on this GPU: a packed multiply
+// whose result feeds a packed add is contracted into a fused multiply-add by the assembler,
+// even with explicit rounding, which would change the rounding.  So packed multiplies here only
+// feed conversions, and products that feed sums are scalar __fmul_rn (never contracted).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, uint32_t &lo_bits, uint32_t &hi_bits)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo_bits), "=r"(hi_bits) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bf_lo(uint32_t w) { return w << 16; }          // fp32 bits of the low bf16
+__device__ __forceinline__ uint32_t bf_hi(uint32_t w) { return w & 0xFFFF0000u; }  // and of the high one
+
+// Shared-memory tiles hold row r (one token, 16 chunks of 16 bytes) with chunk c stored at
+// position c ^ (r & 15), so that both the row-per-lane reads below and the chunk-per-lane reads
+// of the quantiser touch 8 distinct 16-byte bank groups per quarter-warp.
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk) { return row * (kD * 2) + ((chunk ^ (row & 15)) * 16); }
+
 // ---- statistics of one window (one warp, tile in shared memory) --------------------------
 //
-// Lane (half, sub) reads 8 consecutive bf16 of token 2i + half in pass i, so each half-warp
-// covers one 128-element row and the half-warp butterfly reproduces the pairwise order.
+// Lane (t, hh) = (lane & 15, lane >> 4) takes elements [64 hh, 64 hh + 64) of token t.  Its
+// 64-element sum is a balanced tree whose two 32-element halves run side by side in the two
+// fp32 lanes of packed registers; one shuffle adds the other half-row.  This is the balanced
+// pairwise order over the 128 elements, identical in both lanes of the token.
 
 struct WinStats {
     float mean, kmn, kmx, vmn, vmx;
 };
 
+// Balanced sum of the 64 values of half-row hh of token t of a K tile: word i holds elements
+// 2i, 2i+1 (bf16).  In each packed register the low half belongs to elements [0, 32), the
+// high half to [32, 64).  With `squares`, the packed pair `centre` is subtracted and the
+// difference squared first.  The words are read again from shared memory for each pass (cheap)
+// instead of being held in registers across both.
+template <bool squares>
+__device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, uint64_t centre, __nv_bfloat162 &mn2,
+                                       __nv_bfloat162 &mx2)
+{
+    // leaf pair i (i < 16) packs elements (2i, 32 + 2i) and (2i+1, 33 + 2i); leaves 4j..4j+3 come
+    // from chunks j and j + 4 of the half-row and are reduced to node j at once.  The first
+    // pass also takes the min/max of the K values (on packed bf16 pairs: exact).
+    uint64_t node[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 qa = ld_shared_v4(kt + tile_off(t, hh * 8 + j));
+        const uint4 qb = ld_shared_v4(kt + tile_off(t, hh * 8 + j + 4));
+        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+        uint64_t l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (!squares) {
+                const __nv_bfloat162 xa = *reinterpret_cast<const __nv_bfloat162 *>(wa + e);
+                const __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162 *>(wb + e);
+                mn2 = __hmin2(mn2, __hmin2(xa, xb));
+                mx2 = __hmax2(mx2, __hmax2(xa, xb));
+            }
+            uint64_t a = f2_pack(bf_lo(wa[e]), bf_lo(wb[e]));
+            uint64_t b = f2_pack(bf_hi(wa[e]), bf_hi(wb[e]));
+            if (squares) {  // (x - mean)^2: packed difference, scalar squares
+                uint32_t a0, a1, b0, b1;
+                f2_unpack(f2_sub(a, centre), a0, a1);
+                f2_unpack(f2_sub(b, centre), b0, b1);
+                const float da0 = __uint_as_float(a0), da1 = __uint_as_float(a1);
+                const float db0 = __uint_as_float(b0), db1 = __uint_as_float(b1);
+                a = f2_pack(__float_as_uint(__fmul_rn(da0, da0)), __float_as_uint(__fmul_rn(da1, da1)));
+                b = f2_pack(__float_as_uint(__fmul_rn(db0, db0)), __float_as_uint(__fmul_rn(db1, db1)));
+            }
+            l[e] = f2_add(a, b);
+        }
+        node[j] = f2_add(f2_add(l[0], l[1]), f2_add(l[2], l[3]));
+    }
+    const uint64_t r = f2_add(f2_add(node[0], node[1]), f2_add(node[2], node[3]));
+    uint32_t lo, hi;
+    f2_unpack(r, lo, hi);
+    return __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
+}
+
 __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32_t cnt)
 {
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, sub = lane & 15;
+    const int t = lane & 15, hh = lane >> 4;
+    const bool ok = t < cnt;  // rows past the request end hold stale data: masked
     __nv_bfloat162 kmn2 = __float2bfloat162_rn(INFINITY), kmx2 = __float2bfloat162_rn(-INFINITY);
     __nv_bfloat162 vmn2 = kmn2, vmx2 = kmx2;
-    float var[8];
+    float s = sum64<false>(kt, t, hh, 0, kmn2, kmx2);
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 16));
+    const float mean = __fmul_rn(s, 0.0078125f);  // exact /128
+    const uint32_t mb = __float_as_uint(mean);
+    float e = sum64<true>(kt, t, hh, f2_pack(mb, mb), kmn2, kmx2);
+    e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 16));
+#pragma unroll 2
+    for (int j = 0; j < 8; ++j) {
+        const uint4 r = ld_shared_v4(vt + tile_off(t, hh * 8 + j));
+        const uint32_t vw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int tt = 2 * i + half;
-        const bool ok = tt < cnt;
-        const uint4 kq = ld_shared_v4(kt + tt * (kD * 2) + sub * 16);
-        const uint4 vq = ld_shared_v4(vt + tt * (kD * 2) + sub * 16);
-        if (ok) {  // min/max on packed bf16 pairs (exact: widening to fp32 preserves order)
-            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-            const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 kx = *reinterpret_cast<const __nv_bfloat162 *>(kw + j);
-                const __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(vw + j);
-                kmn2 = __hmin2(kmn2, kx); kmx2 = __hmax2(kmx2, kx);
-                vmn2 = __hmin2(vmn2, vx); vmx2 = __hmax2(vmx2, vx);
-            }
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(vw + q);
+            vmn2 = __hmin2(vmn2, vx);
+            vmx2 = __hmax2(vmx2, vx);
         }
-        float x[8];
-        unpack8(kq, x);
-        const float mean = __fmul_rn(halfwarp_tree(tree8(x)), 0.0078125f);  // exact /128
-        float e[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float d = __fsub_rn(x[j], mean);
-            e[j] = __fmul_rn(d, d);
-        }
-        const float v = __fmul_rn(halfwarp_tree(tree8(e)), 0.0078125f);
-        var[i] = ok ? v : 0.0f;
     }
-    // window mean: tokens 2i (lower half-warp) and 2i+1 (upper) pair up first
-    float s[8];
+    float var = __fmul_rn(e, 0.0078125f);
+    var = ok ? var : 0.0f;
+    // window mean: balanced tree over the 16 tokens (lanes t and t + 16 hold the same value)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s[i] = __fadd_rn(var[i], __shfl_xor_sync(0xffffffffu, var[i], 16));
-    const float sum16 = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
-                                  __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
-    WinStats r;
-    r.mean = __fdiv_rn(sum16, (float)cnt);
-    r.kmn = warp_min(fminf(__low2float(kmn2), __high2float(kmn2)));
-    r.kmx = warp_max(fmaxf(__low2float(kmx2), __high2float(kmx2)));
-    r.vmn = warp_min(fminf(__low2float(vmn2), __high2float(vmn2)));
-    r.vmx = warp_max(fmaxf(__low2float(vmx2), __high2float(vmx2)));
-    return r;
+    for (int o = 1; o <= 8; o <<= 1) var = __fadd_rn(var, __shfl_xor_sync(0xffffffffu, var, o));
+    WinStats res;
+    res.mean = __fdiv_rn(var, (float)cnt);
+    const float kn = ok ? fminf(__low2float(kmn2), __high2float(kmn2)) : INFINITY;
+    const float kx = ok ? fmaxf(__low2float(kmx2), __high2float(kmx2)) : -INFINITY;
+    const float vn = ok ? fminf(__low2float(vmn2), __high2float(vmn2)) : INFINITY;
+    const float vx = ok ? fmaxf(__low2float(vmx2), __high2float(vmx2)) : -INFINITY;
+    res.kmn = warp_min(kn);
+    res.kmx = warp_max(kx);
+    res.vmn = warp_min(vn);
+    res.vmx = warp_max(vx);
+    return res;
 }
 
 // ---- quantisation -----------------------------------------------------------------------
 
-__device__ __forceinline__ uint32_t code_bits(float x, float mn, float inv)
+// Eight codes from eight bf16 values: rint((x - min) * inv), the difference and the product
+// as packed fp32 pairs (one IEEE rounding each), the rounding to an integer by conversion
+// (round-to-nearest-even; 0 <= u <= 255 * (1 + 2^-22) < 255.5 because x >= min).
+__device__ __forceinline__ uint2 encode8(const uint4 &q, uint64_t mn2, uint64_t inv2)
 {
-    // rint((x - min) * inv) for 0 <= u < 2^22: adding 1.5 * 2^23 rounds u to an integer
-    // (round-to-nearest-even) and leaves that integer in the low mantissa bits.  x >= min
-    // makes u >= 0, and u <= 255 * (1 + 2^-22) < 255.5, so the low byte is the code.
-    const float u = __fmul_rn(__fsub_rn(x, mn), inv);
-    return __float_as_uint(__fadd_rn(u, 12582912.0f));
-}
-
-__device__ __forceinline__ uint2 encode8(const uint4 &q, float mn, float inv)
-{
-    float x[8];
-    unpack8(q, x);
+    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
     uint32_t c[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = code_bits(x[j], mn, inv);
+    for (int e = 0; e < 4; ++e) {
+        uint32_t u0, u1;
+        f2_unpack(f2_mul(f2_sub(f2_pack(bf_lo(wv[e]), bf_hi(wv[e])), mn2), inv2), u0, u1);
+        c[2 * e] = (uint32_t)__float2int_rn(__uint_as_float(u0));
+        c[2 * e + 1] = (uint32_t)__float2int_rn(__uint_as_float(u1));
+    }
     const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
     const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
     return make_uint2(lo, hi);
 }
-
 
 // Quantisation parameters of one pair held by a warp: lane i < 5 holds segment i's
 // (start, k_min, k_inv, v_min, v_inv).
@@ -460,27 +614,29 @@ __device__ __forceinline__ PairCache load_params(const PairParams *pp)
 }
 
 // Codes of one window tile, written straight to their slots in the physical block.
-__device__ __forceinline__ void window_quant(const CompressArgs &a, const WinLoc &loc, uint32_t kt, uint32_t vt,
-                                             const PairCache &pc, int64_t blk)
+__device__ __forceinline__ void window_quant(const CompressArgs &a, int32_t h, int32_t t0, int32_t cnt, int32_t blk,
+                                             uint32_t kt, uint32_t vt, const PairCache &pc)
 {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, sub = lane & 15;
-    const int32_t t0 = loc.wi * kWin;
-    const int32_t cnt = min(kWin, loc.L - t0);
     // segment of the window: how many of starts 1..4 (lanes 1..4) lie at or before t0
     const unsigned ballot = __ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pc.start <= t0);
     const int s = __popc(ballot);
     const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
     const float vmn = __shfl_sync(0xffffffffu, pc.vmn, s), vinv = __shfl_sync(0xffffffffu, pc.vinv, s);
-    const int64_t dst0 = ((blk * a.Hkv + loc.h) * a.bs + (t0 % a.bs)) * kD + sub * 8;
+    const int64_t dst0 = (((int64_t)blk * a.Hkv + h) * a.bs + (t0 % a.bs)) * kD + sub * 8;
+    const uint64_t kmn2 = f2_pack(__float_as_uint(kmn), __float_as_uint(kmn));
+    const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
+    const uint64_t vmn2 = f2_pack(__float_as_uint(vmn), __float_as_uint(vmn));
+    const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int tt = 2 * i + half;
         if (tt < cnt) {
-            const uint4 kq = ld_shared_v4(kt + tt * (kD * 2) + sub * 16);
-            const uint4 vq = ld_shared_v4(vt + tt * (kD * 2) + sub * 16);
-            __stcs(reinterpret_cast<uint2 *>(a.kpool + dst0 + tt * kD), encode8(kq, kmn, kinv));
-            __stcs(reinterpret_cast<uint2 *>(a.vpool + dst0 + tt * kD), encode8(vq, vmn, vinv));
+            const uint4 kq = ld_shared_v4(kt + tile_off(tt, sub));
+            const uint4 vq = ld_shared_v4(vt + tile_off(tt, sub));
+            __stcs(reinterpret_cast<uint2 *>(a.kpool + dst0 + tt * kD), encode8(kq, kmn2, kinv2));
+            __stcs(reinterpret_cast<uint2 *>(a.vpool + dst0 + tt * kD), encode8(vq, vmn2, vinv2));
         }
     }
 }
@@ -513,11 +669,14 @@ struct Cursor {
 
 // One window in flight in a worker's ring.
 struct Item {
-    int32_t kind;  // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
-    int32_t w, m, stage;
+    int32_t kind;    // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
+    int32_t stage, m;
     int32_t next_m;  // chunk / range of the worker's next item of the same kind (M if none)
-    WinLoc loc;
-    int64_t blk;
+    int32_t w;       // flat window index
+    int32_t cnt;     // tokens in the window
+    int32_t t0;      // first token of the window within its pair
+    int32_t h;       // KV head
+    int32_t blk;     // physical block holding the window (quantisation)
     PairCache pc;
 };
 
@@ -602,38 +761,55 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
     };
     auto slice = [&](int32_t m) { return a.params + ((int64_t)cta * 2 + (m & 1)) * a.cap; };
 
+    // bounded wait helper for the control warps: false while waiting may go on; true (after
+    // recording the error and telling the CTA to skip dependent work) once the limit is reached
+    auto give_up = [&](uint32_t &spins) -> bool {
+        if (++spins < kSpinLimit) {
+            __nanosleep(128);
+            return false;
+        }
+        if (lane == 0) {
+            record_error(a.hdr, kErrBarrierWait);
+            st_release_cta_shared(&ctl->abort, 1);
+        }
+        return true;
+    };
+
     if (warp == kWorkers) {
-        // ================================================================ sync warp
-        int32_t ma = 0, ms = 0;  // chunks published, ranges segmented
+        // ================================================================ arrival warp
+        // Publish the CTA's progress as soon as every worker has finished a chunk's statistics.
+        int32_t ma = 0;
         uint32_t spins = 0;
-        while (ma < M || ms < M) {
-            bool progressed = false;
-            if (ma < M) {  // publish once every worker has finished the statistics of chunk ma
-                int32_t d = INT32_MAX;
-                if (lane == 0)
-                    for (int i = 0; i < kWorkers; ++i) d = min(d, ld_acquire_cta_shared(ctl->stats_done + i));
-                d = __shfl_sync(0xffffffffu, d, 0);
-                if (d > ma) {
-                    ma = d < M ? d : M;
-                    // the workers' window statistics (acquired above) before the progress word
-                    if (lane == 0) st_release_gpu(a.prog + cta, (uint32_t)ma);
-                    progressed = true;
-                }
+        while (ma < M) {
+            int32_t d = INT32_MAX;
+            if (lane == 0)
+                for (int i = 0; i < kWorkers; ++i) d = min(d, ld_acquire_cta_shared(ctl->stats_done + i));
+            d = __shfl_sync(0xffffffffu, d, 0);
+            if (d > ma) {
+                ma = d < M ? d : M;
+                // the workers' window statistics (acquired above) before the progress word
+                if (lane == 0) st_release_gpu(a.prog + cta, (uint32_t)ma);
+                spins = 0;
+            } else if (give_up(spins)) {
+                break;
             }
-            if (!progressed && ms < ma) {
-                int32_t qlo, qhi;
-                quant_share(ms, qlo, qhi);
-                if (qlo >= qhi) {
-                    if (lane == 0) st_release_cta_shared(ctl->ready + (ms & 1), ms + 1);
-                    ++ms;
-                    progressed = true;
-                } else {
-                    // the slice buffer is free once no worker still quantises range ms-2
+        }
+    } else if (warp == kWorkers + 1) {
+        // ================================================================ segmentation warp
+        // Per range: wait until every CTA has published chunks 0..m (and no worker still uses
+        // the parameter slice of range m-2), segment the pairs overlapping this CTA's share,
+        // and let the workers quantise the range.
+        for (int32_t ms = 0; ms < M; ++ms) {
+            int32_t qlo, qhi;
+            quant_share(ms, qlo, qhi);
+            if (qlo < qhi) {
+                uint32_t spins = 0;
+                bool ok = true;
+                while (true) {
                     int32_t d = INT32_MAX;
                     if (lane == 0)
                         for (int i = 0; i < kWorkers; ++i) d = min(d, ld_acquire_cta_shared(ctl->quant_done + i));
                     d = __shfl_sync(0xffffffffu, d, 0);
-                    // barrier ms: every CTA has published the statistics of chunks 0..ms
                     uint32_t done = 0;
                     if (d >= ms - 1) {  // all progress words in one round of relaxed loads
                         uint32_t pv[kMaxSms / 32];
@@ -645,42 +821,31 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                         for (int j = 0; j < kMaxSms / 32; ++j) done = min(done, pv[j]);
                         done = __reduce_min_sync(0xffffffffu, done);
                     }
-                    if (d >= ms - 1 && done >= (uint32_t)(ms + 1)) {
-                        __threadfence();  // with the relaxed loads above: acquire of every CTA's progress
-                        __syncwarp();
-                        // segment the pairs overlapping this CTA's share
-                        PairParams *out = slice(ms);
-                        WinLoc l = locate(qlo, s_wpre, a.cu, B);
-                        int32_t w = qlo, slot = 0;
-                        while (true) {
-                            const int32_t wbase = w - l.wi;
-                            segment_pair(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
-                            ++slot;
-                            w = wbase + l.W;
-                            if (w >= qhi) break;
-                            step_loc(l, l.W - l.wi, a.cu, a.Hkv);
-                        }
-                        __syncwarp();
-                        if (lane == 0) {
-                            __threadfence_block();
-                            st_release_cta_shared(ctl->ready + (ms & 1), ms + 1);
-                        }
-                        ++ms;
-                        progressed = true;
+                    if (d >= ms - 1 && done >= (uint32_t)(ms + 1)) break;
+                    if (give_up(spins)) {
+                        ok = false;
+                        break;
                     }
                 }
+                if (!ok) break;
+                __threadfence();  // with the relaxed loads above: acquire of every CTA's progress
+                __syncwarp();
+                PairParams *out = slice(ms);
+                WinLoc l = locate(qlo, s_wpre, a.cu, B);
+                int32_t w = qlo, slot = 0;
+                while (true) {
+                    const int32_t wbase = w - l.wi;
+                    segment_pair(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
+                    ++slot;
+                    w = wbase + l.W;
+                    if (w >= qhi) break;
+                    step_loc(l, l.W - l.wi, a.cu, a.Hkv);
+                }
+                __syncwarp();
             }
-            if (progressed) {
-                spins = 0;
-            } else {
-                if (++spins >= kSpinLimit) {
-                    if (lane == 0) {
-                        record_error(a.hdr, kErrBarrierWait);
-                        st_release_cta_shared(&ctl->abort, 1);
-                    }
-                    break;
-                }
-                __nanosleep(128);
+            if (lane == 0) {
+                __threadfence_block();
+                st_release_cta_shared(ctl->ready + (ms & 1), ms + 1);
             }
         }
     } else {
@@ -738,9 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
             const bool aborted = *reinterpret_cast<volatile int32_t *>(&ctl->abort) != 0;
             if (qc.w >= 0 && (aborted || ld_acquire_cta_shared(ctl->ready + (qc.m & 1)) >= qc.m + 1)) {
                 it.kind = aborted ? 2 : 1;
-                it.w = qc.w;
                 it.m = qc.m;
-                it.loc = qc.loc;
                 it.stage = next_stage;
                 if (!aborted) {
                     if (qc.m != cur_m || qc.slot != cur_slot) {
@@ -750,18 +913,23 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                     }
                     it.pc = params;
                     it.blk = __ldg(a.bt + (int64_t)qc.loc.b * a.max_blocks + (qc.loc.wi * kWin) / a.bs);
+                    it.h = qc.loc.h;
                 }
             } else if (sc.w >= 0 && (qc.w < 0 || sc.m <= qc.m || sc.w < qc.w + kAhead)) {
                 it.kind = 0;
                 it.w = sc.w;
                 it.m = sc.m;
-                it.loc = sc.loc;
                 it.stage = next_stage;
             } else {
                 return false;
             }
+            {
+                const WinLoc &l = it.kind == 0 ? sc.loc : qc.loc;
+                it.t0 = l.wi * kWin;
+                it.cnt = min(kWin, l.L - it.t0);
+            }
             if (it.kind != 2) {
-                const WinLoc &l = it.loc;
+                const WinLoc &l = it.kind == 0 ? sc.loc : qc.loc;
                 const int32_t t0 = l.wi * kWin, cnt = min(kWin, l.L - t0);
                 const int64_t row0 = ((int64_t)(l.c0 + t0) * a.Hkv + l.h) * kD;
                 const uint32_t dst = ring + it.stage * kWinBytes;
@@ -771,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                     if (row < cnt) {  // rows past the request end are not copied
                         const uint16_t *ks = a.k + row0 + row * rstride + col * 8;
                         const uint16_t *vs = a.v + row0 + row * rstride + col * 8;
-                        const uint32_t off = row * (kD * 2) + col * 16;
+                        const uint32_t off = tile_off(row, col);
                         if (it.kind == 1) {  // second read: last use
                             cp16_hint(dst + off, ks, pol_first);
                             cp16_hint(dst + kTileBytes + off, vs, pol_first);
@@ -817,8 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
             __syncwarp();
             const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
             if (f0.kind == 0) {
-                const int32_t cnt = min(kWin, f0.loc.L - f0.loc.wi * kWin);
-                const WinStats s = window_stats(kt, vt, cnt);
+                const WinStats s = window_stats(kt, vt, f0.cnt);
                 if (lane == 0) {
                     __stcg(a.win_mean + f0.w, s.mean);
                     __stcg(a.win_mm + f0.w, make_float4(s.kmn, s.kmx, s.vmn, s.vmx));
@@ -830,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                     if (f0.next_m != f0.m) st_release_cta_shared(ctl->stats_done + warp, f0.next_m);
                 }
             } else if (f0.kind == 1) {
-                window_quant(a, f0.loc, kt, vt, f0.pc, f0.blk);
+                window_quant(a, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
             }
             __syncwarp();  // the stage's reads are done before it is refilled
             if (f0.kind != 0 && lane == 0 && f0.next_m != f0.m)

@@ -20,6 +20,7 @@ COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE
 # The quantiser's fp32 steps are bit-exact IEEE operations: no FMA contraction there.
 UNITS = {
     "dgq_compress.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
+    "dgq_compress_cluster.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_attn.cu": [],
     "dgq_host.cu": [],
     "dgq_noalloc.cu": [],

@@ -41,6 +41,7 @@
 #include "dgq_device.cuh"
 #include "dgq.h"
 #include "dgq_launch.h"
+#include "dgq_window.cuh"
 
 #include <cuda_bf16.h>
 
@@ -48,21 +49,10 @@
 
 namespace dgq {
 
-// Quantisation parameters of one pair as the segmentation warp publishes them.
-struct alignas(16) PairParams {
-    float k_min[kMaxSeg], k_inv[kMaxSeg], v_min[kMaxSeg], v_inv[kMaxSeg];
-    int32_t start[kMaxSeg];
-    int32_t n_seg;
-    int32_t pad[6];
-};
-static_assert(sizeof(PairParams) == 128, "PairParams is 128 bytes");
-
 constexpr int kAgg = 64;        // windows per min/max aggregate
 constexpr int kWorkers = 10;    // worker warps per CTA (plus an arrival warp and a segmentation warp)
 constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
-constexpr int kTileBytes = kWin * kD * 2;  // 16 tokens x 128 bf16 = 4 KB
-constexpr int kWinBytes = 2 * kTileBytes;  // K tile + V tile
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
 constexpr int32_t kChunk = 8192;           // windows per chunk: 64 MB of K+V
 constexpr int32_t kAhead = 16384;          // statistics may lead quantisation by this many windows
@@ -84,15 +74,6 @@ struct CompressArgs {
     uint4 *agg;  // per 64 flat windows: ~enc(k min), enc(k max), ~enc(v min), enc(v max); 0 = empty
     int32_t B, Hkv, bs, max_blocks, cap;
 };
-
-__device__ __forceinline__ int32_t ngroups(int32_t L)
-{
-    if (L < 2048) return 2;
-    if (L < 16384) return 3;
-    // floor(log2(L / 1024)) = floor(log2(L)) - 10 for integer L >= 1024
-    const int32_t g = (31 - __clz(L)) - 10 + 2;
-    return g < 5 ? g : 5;
-}
 
 // ---- window decomposition ------------------------------------------------------------------
 
@@ -141,24 +122,6 @@ __device__ __forceinline__ int32_t step_loc(WinLoc &l, int32_t n, const int32_t 
     }
     return crossed;
 }
-
-// ---- warp reductions ------------------------------------------------------------------------
-
-__device__ __forceinline__ float warp_min(float v)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float canon_zero(float x) { return x == 0.0f ? 0.0f : x; }
 
 // Order-preserving map of fp32 (finite, or infinite) onto uint32, so that an integer max
 // atomic gives the exact fp32 max in any order; every value maps above 0, the empty mark.
@@ -427,237 +390,7 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
     __syncwarp();
 }
 
-// ---- packed fp32 pairs ----------------------------------------------------------------------
-//
-// sm_100-class GPUs execute fp32 add/sub/mul on register pairs (f32x2); each half is an
-// ordinary IEEE operation with round-to-nearest-even.  Measured on this GPU: a packed multiply
-// whose result feeds a packed add is contracted into a fused multiply-add by the assembler,
-// even with explicit rounding, which would change the rounding.  So packed multiplies here only
-// feed conversions, and products that feed sums are scalar __fmul_rn (never contracted).
-__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, uint32_t &lo_bits, uint32_t &hi_bits)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo_bits), "=r"(hi_bits) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t bf_lo(uint32_t w) { return w << 16; }          // fp32 bits of the low bf16
-__device__ __forceinline__ uint32_t bf_hi(uint32_t w) { return w & 0xFFFF0000u; }  // and of the high one
-
-// Shared-memory tiles hold row r (one token, 16 chunks of 16 bytes) with chunk c stored at
-// position c ^ (r & 15), so that both the row-per-lane reads below and the chunk-per-lane reads
-// of the quantiser touch 8 distinct 16-byte bank groups per quarter-warp.
-__device__ __forceinline__ uint32_t tile_off(int row, int chunk) { return row * (kD * 2) + ((chunk ^ (row & 15)) * 16); }
-
-// ---- statistics of one window (one warp, tile in shared memory) --------------------------
-//
-// Lane (t, hh) = (lane & 15, lane >> 4) takes elements [64 hh, 64 hh + 64) of token t.  Its
-// 64-element sum is a balanced tree whose two 32-element halves run side by side in the two
-// fp32 lanes of packed registers; one shuffle adds the other half-row.  This is the balanced
-// pairwise order over the 128 elements, identical in both lanes of the token.
-
-struct WinStats {
-    float mean, kmn, kmx, vmn, vmx;
-};
-
-// Balanced sum of the 64 values of half-row hh of token t of a K tile: word i holds elements
-// 2i, 2i+1 (bf16).  In each packed register the low half belongs to elements [0, 32), the
-// high half to [32, 64).  With `squares`, the packed pair `centre` is subtracted and the
-// difference squared first.  The words are read again from shared memory for each pass (cheap)
-// instead of being held in registers across both.
-template <bool squares>
-__device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, uint64_t centre, __nv_bfloat162 &mn2,
-                                       __nv_bfloat162 &mx2)
-{
-    // leaf pair i (i < 16) packs elements (2i, 32 + 2i) and (2i+1, 33 + 2i); leaves 4j..4j+3 come
-    // from chunks j and j + 4 of the half-row and are reduced to node j at once.  The first
-    // pass also takes the min/max of the K values (on packed bf16 pairs: exact).
-    uint64_t node[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint4 qa = ld_shared_v4(kt + tile_off(t, hh * 8 + j));
-        const uint4 qb = ld_shared_v4(kt + tile_off(t, hh * 8 + j + 4));
-        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-        uint64_t l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (!squares) {
-                const __nv_bfloat162 xa = *reinterpret_cast<const __nv_bfloat162 *>(wa + e);
-                const __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162 *>(wb + e);
-                mn2 = __hmin2(mn2, __hmin2(xa, xb));
-                mx2 = __hmax2(mx2, __hmax2(xa, xb));
-            }
-            uint64_t a = f2_pack(bf_lo(wa[e]), bf_lo(wb[e]));
-            uint64_t b = f2_pack(bf_hi(wa[e]), bf_hi(wb[e]));
-            if (squares) {  // (x - mean)^2: packed difference, scalar squares
-                uint32_t a0, a1, b0, b1;
-                f2_unpack(f2_sub(a, centre), a0, a1);
-                f2_unpack(f2_sub(b, centre), b0, b1);
-                const float da0 = __uint_as_float(a0), da1 = __uint_as_float(a1);
-                const float db0 = __uint_as_float(b0), db1 = __uint_as_float(b1);
-                a = f2_pack(__float_as_uint(__fmul_rn(da0, da0)), __float_as_uint(__fmul_rn(da1, da1)));
-                b = f2_pack(__float_as_uint(__fmul_rn(db0, db0)), __float_as_uint(__fmul_rn(db1, db1)));
-            }
-            l[e] = f2_add(a, b);
-        }
-        node[j] = f2_add(f2_add(l[0], l[1]), f2_add(l[2], l[3]));
-    }
-    const uint64_t r = f2_add(f2_add(node[0], node[1]), f2_add(node[2], node[3]));
-    uint32_t lo, hi;
-    f2_unpack(r, lo, hi);
-    return __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
-}
-
-__device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32_t cnt)
-{
-    const int lane = threadIdx.x & 31;
-    const int t = lane & 15, hh = lane >> 4;
-    const bool ok = t < cnt;  // rows past the request end hold stale data: masked
-    __nv_bfloat162 kmn2 = __float2bfloat162_rn(INFINITY), kmx2 = __float2bfloat162_rn(-INFINITY);
-    __nv_bfloat162 vmn2 = kmn2, vmx2 = kmx2;
-    float s = sum64<false>(kt, t, hh, 0, kmn2, kmx2);
-    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 16));
-    const float mean = __fmul_rn(s, 0.0078125f);  // exact /128
-    const uint32_t mb = __float_as_uint(mean);
-    float e = sum64<true>(kt, t, hh, f2_pack(mb, mb), kmn2, kmx2);
-    e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 16));
-#pragma unroll 2
-    for (int j = 0; j < 8; ++j) {
-        const uint4 r = ld_shared_v4(vt + tile_off(t, hh * 8 + j));
-        const uint32_t vw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162 vx = *reinterpret_cast<const __nv_bfloat162 *>(vw + q);
-            vmn2 = __hmin2(vmn2, vx);
-            vmx2 = __hmax2(vmx2, vx);
-        }
-    }
-    float var = __fmul_rn(e, 0.0078125f);
-    var = ok ? var : 0.0f;
-    // window mean: balanced tree over the 16 tokens (lanes t and t + 16 hold the same value)
-#pragma unroll
-    for (int o = 1; o <= 8; o <<= 1) var = __fadd_rn(var, __shfl_xor_sync(0xffffffffu, var, o));
-    WinStats res;
-    res.mean = __fdiv_rn(var, (float)cnt);
-    const float kn = ok ? fminf(__low2float(kmn2), __high2float(kmn2)) : INFINITY;
-    const float kx = ok ? fmaxf(__low2float(kmx2), __high2float(kmx2)) : -INFINITY;
-    const float vn = ok ? fminf(__low2float(vmn2), __high2float(vmn2)) : INFINITY;
-    const float vx = ok ? fmaxf(__low2float(vmx2), __high2float(vmx2)) : -INFINITY;
-    res.kmn = warp_min(kn);
-    res.kmx = warp_max(kx);
-    res.vmn = warp_min(vn);
-    res.vmx = warp_max(vx);
-    return res;
-}
-
-// ---- quantisation -----------------------------------------------------------------------
-
-// Eight codes from eight bf16 values: rint((x - min) * inv), the difference and the product
-// as packed fp32 pairs (one IEEE rounding each), the rounding to an integer by conversion
-// (round-to-nearest-even; 0 <= u <= 255 * (1 + 2^-22) < 255.5 because x >= min).
-__device__ __forceinline__ uint2 encode8(const uint4 &q, uint64_t mn2, uint64_t inv2)
-{
-    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-    uint32_t c[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        uint32_t u0, u1;
-        f2_unpack(f2_mul(f2_sub(f2_pack(bf_lo(wv[e]), bf_hi(wv[e])), mn2), inv2), u0, u1);
-        c[2 * e] = (uint32_t)__float2int_rn(__uint_as_float(u0));
-        c[2 * e + 1] = (uint32_t)__float2int_rn(__uint_as_float(u1));
-    }
-    const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
-    const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
-    return make_uint2(lo, hi);
-}
-
-// Quantisation parameters of one pair held by a warp: lane i < 5 holds segment i's
-// (start, k_min, k_inv, v_min, v_inv).
-struct PairCache {
-    int32_t start;
-    float kmn, kinv, vmn, vinv;
-};
-
-__device__ __forceinline__ PairCache load_params(const PairParams *pp)
-{
-    const int lane = threadIdx.x & 31;
-    const int i = lane < kMaxSeg ? lane : 0;
-    PairCache pc;
-    pc.start = __ldcg(pp->start + i);
-    pc.kmn = __ldcg(pp->k_min + i);
-    pc.kinv = __ldcg(pp->k_inv + i);
-    pc.vmn = __ldcg(pp->v_min + i);
-    pc.vinv = __ldcg(pp->v_inv + i);
-    return pc;
-}
-
-// Codes of one window tile, written straight to their slots in the physical block.
-__device__ __forceinline__ void window_quant(const CompressArgs &a, int32_t h, int32_t t0, int32_t cnt, int32_t blk,
-                                             uint32_t kt, uint32_t vt, const PairCache &pc)
-{
-    const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, sub = lane & 15;
-    // segment of the window: how many of starts 1..4 (lanes 1..4) lie at or before t0
-    const unsigned ballot = __ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pc.start <= t0);
-    const int s = __popc(ballot);
-    const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
-    const float vmn = __shfl_sync(0xffffffffu, pc.vmn, s), vinv = __shfl_sync(0xffffffffu, pc.vinv, s);
-    const int64_t dst0 = (((int64_t)blk * a.Hkv + h) * a.bs + (t0 % a.bs)) * kD + sub * 8;
-    const uint64_t kmn2 = f2_pack(__float_as_uint(kmn), __float_as_uint(kmn));
-    const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
-    const uint64_t vmn2 = f2_pack(__float_as_uint(vmn), __float_as_uint(vmn));
-    const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int tt = 2 * i + half;
-        if (tt < cnt) {
-            const uint4 kq = ld_shared_v4(kt + tile_off(tt, sub));
-            const uint4 vq = ld_shared_v4(vt + tile_off(tt, sub));
-            __stcs(reinterpret_cast<uint2 *>(a.kpool + dst0 + tt * kD), encode8(kq, kmn2, kinv2));
-            __stcs(reinterpret_cast<uint2 *>(a.vpool + dst0 + tt * kD), encode8(vq, vmn2, vinv2));
-        }
-    }
-}
-
 // ---- the kernel ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void cp16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp16_hint(uint32_t dst, const void *src, uint64_t pol)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // A warp's position in one of its two item sequences (statistics of chunk m, or
 // quantisation of range m): window w of the CTA's share [.., end), its location, and (for
@@ -997,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                     if (f0.next_m != f0.m) st_release_cta_shared(ctl->stats_done + warp, f0.next_m);
                 }
             } else if (f0.kind == 1) {
-                window_quant(a, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
+                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
             }
             __syncwarp();  // the stage's reads are done before it is refilled
             if (f0.kind != 0 && lane == 0 && f0.next_m != f0.m)

@@ -1,0 +1,474 @@
+// dgq_compress_cluster.cu -- DGQ encode of one layer for requests of at most 4096 tokens
+// (sm_103a), on thread-block clusters.
+//
+// Method: as in dgq_compress.cu ("DeepSeek KV-cache dynamic group quantisation (DGQ)" article,
+// sections 2.2, 3.2; paged storage per "PagedAttention implementation", DeepSeek-V4 KV-cache
+// article).  Same arithmetic (dgq_window.cuh), same outputs bit for bit.
+//
+// GPU design.  When every (request, KV head) pair is short (at most 256 windows, 1 MB of bf16
+// K+V), a pair's segmentation needs no grid-wide step: clusters of kCl CTAs take whole pairs
+// round-robin, and the kCl CTAs of a cluster split each pair's windows.
+//  * Workers (per-warp two-window cp.async rings, as in the grid-wide kernel) compute window
+//    statistics into their CTA's shared memory and arrive, with cluster-scope release, on an
+//    mbarrier of the pair's owner CTA (owners rotate through the cluster).
+//  * The owner's segmentation warp reads the pair's statistics from the kCl CTAs through
+//    distributed shared memory in one round, segments the pair, writes the record, stores the
+//    quantiser parameters into every CTA of the cluster and arrives on each CTA's "ready"
+//    mbarrier.  No step goes through L2 or a grid barrier.
+//  * Workers quantise a pair once its parameters are ready, re-reading its K/V (read a few
+//    microseconds earlier, so from L2; the re-read carries an evict-first hint), and meanwhile
+//    compute statistics of at most kSlots - 1 later pairs: a cluster holds at most kSlots pairs
+//    (3 MB) between first read and re-read, the whole GPU about 100 MB.
+//  * Clusters of 4 (not 8): measured on this GPU, only 15 clusters of 8 CTAs fit at once
+//    (120 of 152 SMs), 36 of 4 (144).
+// Every wait is bounded; a timeout records an error in the workspace header and the CTA skips
+// dependent work.
+#include "dgq_device.cuh"
+#include "dgq.h"
+#include "dgq_launch.h"
+#include "dgq_window.cuh"
+
+#include <stdint.h>
+
+namespace dgq {
+
+constexpr int kCl = 4;                                   // CTAs per cluster
+constexpr int kCWorkers = 10;                            // worker warps per CTA (plus a segmentation warp)
+constexpr int kCThreads = (kCWorkers + 1) * 32;
+constexpr int kCRing = 2;                                // windows in flight per worker
+constexpr int kCRingBytes = kCWorkers * kCRing * kWinBytes;
+constexpr int kSlots = 3;                                // pairs a cluster holds at once
+constexpr int kSlotWin = 64;                             // windows of one pair per CTA
+constexpr int32_t kClusterMaxWin = 256;                  // pairs of at most 256 windows (4096 tokens)
+static_assert(kCl * kSlotWin >= kClusterMaxWin, "a CTA holds its share of the longest pair");
+static_assert(kClusterMaxWin == 8 * 32, "segment_small holds 8 windows per lane");
+
+struct ClusterArgs {
+    const uint16_t *k;
+    const uint16_t *v;
+    const int32_t *cu;
+    const int32_t *bt;
+    uint8_t *kpool;
+    uint8_t *vpool;
+    dgq_seg_record *table;
+    WsHeader *hdr;
+    int32_t B, Hkv, bs, max_blocks;
+};
+
+struct ClusterSmem {
+    float mean[kSlots][kSlotWin];
+    float4 mm[kSlots][kSlotWin];
+    PairParams par[kSlots];
+    uint64_t stats_done[kSlots];  // owner side: arrivals of every worker of the cluster
+    uint64_t ready[kSlots];       // parameters of the slot's pair are in par[]
+    int32_t abort;
+    int32_t pad[3];
+};
+
+// ---- cluster helpers (inline PTX) ------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// shared-memory address of the same variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(const void *p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void remote_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// non-blocking test (try_wait may suspend the thread for a while when the phase is open)
+__device__ __forceinline__ bool test_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ float ld_remote_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_remote_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_remote_u4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Quantiser parameters of one pair from this CTA's shared memory: lane i < 5 gets segment i's.
+__device__ __forceinline__ PairCache load_params_smem(const PairParams *pp)
+{
+    const int lane = threadIdx.x & 31;
+    const int i = lane < kMaxSeg ? lane : 0;
+    PairCache pc;
+    pc.start = pp->start[i];
+    pc.kmn = pp->k_min[i];
+    pc.kinv = pp->k_inv[i];
+    pc.vmn = pp->v_min[i];
+    pc.vinv = pp->v_inv[i];
+    return pc;
+}
+
+// Windows [lo, hi) of a pair of W windows held by CTA `r` of the cluster.
+__device__ __forceinline__ void cta_range(int32_t W, int32_t r, int32_t &lo, int32_t &hi)
+{
+    lo = (W * r) / kCl;
+    hi = (W * (r + 1)) / kCl;
+}
+
+// ---- the kernel ---------------------------------------------------------------------------
+
+// A worker's position in the cluster's pair sequence j = 0, 1, ... (pair p = cluster + j *
+// clusters) for one of its two item sequences: window i of its CTA's range [lo, hi).
+struct PairCursor {
+    int32_t j, i, lo, hi;
+    int32_t L, c0, h, b;
+};
+
+struct CItem {
+    int32_t kind;  // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
+    int32_t stage, j, idx, cnt, t0, h, blk;
+    bool last;     // statistics: the worker's last window of pair j
+    PairCache pc;
+};
+
+__global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    ClusterSmem *cs = reinterpret_cast<ClusterSmem *>(smem + kCRingBytes);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t rank = (int32_t)cluster_rank();
+    const int32_t clu = (int32_t)cluster_id(), ncl = (int32_t)cluster_count();
+    const int32_t P = a.B * a.Hkv;
+    const int32_t nj = clu < P ? (P - clu + ncl - 1) / ncl : 0;  // pairs of this cluster
+
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&cs->stats_done[s], kCl * kCWorkers);
+            mbar_init(&cs->ready[s], 1);
+        }
+        cs->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+
+    auto pair_of = [&](int32_t j, PairCursor &c) {
+        const int32_t p = clu + j * ncl;
+        c.b = p / a.Hkv;
+        c.h = p - c.b * a.Hkv;
+        c.c0 = __ldg(a.cu + c.b);
+        c.L = __ldg(a.cu + c.b + 1) - c.c0;
+        cta_range((c.L + kWin - 1) / kWin, rank, c.lo, c.hi);
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int32_t *>(&cs->abort) != 0; };
+
+    if (warp == kCWorkers) {
+        // ================================================================ segmentation warp
+        // Pairs j = rank, rank + kCl, ... are owned by this CTA.
+        for (int32_t q = 0; q * kCl + rank < nj; ++q) {
+            const int32_t j = q * kCl + rank;
+            const int32_t qs = q % kSlots;
+            bool ok = true;
+            for (uint32_t it = 0; !try_wait_cluster(&cs->stats_done[qs], (uint32_t)(q / kSlots) & 1u);) {
+                if (++it >= kSpinLimit || aborted()) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+            }
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(a.hdr, kErrBarrierWait);
+                    st_release_cta_shared(&cs->abort, 1);
+                }
+                break;
+            }
+            PairCursor pc;
+            pair_of(j, pc);
+            const int32_t W = (pc.L + kWin - 1) / kWin;
+            const int32_t p = clu + j * ncl;
+            const int slot = j % kSlots;
+            dgq_seg_record rec = {};
+            PairParams pp = {};
+            if (W > 0) {
+                // the pair's window statistics from the kCl CTAs, lane i holding windows 8i .. 8i+7
+                float m[8];
+                float4 mm[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int32_t w = 8 * lane + i;
+                    m[i] = 0.0f;
+                    mm[i] = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
+                    if (w < W) {
+                        const int32_t r = ((w + 1) * kCl + W - 1) / W - 1;  // CTA holding window w
+                        const int32_t idx = w - (W * r) / kCl;
+                        m[i] = ld_remote_f32(map_rank(&cs->mean[slot][idx], (uint32_t)r));
+                        mm[i] = ld_remote_f4(map_rank(&cs->mm[slot][idx], (uint32_t)r));
+                    }
+                }
+                const int k = min(ngroups(pc.L), W) - 1;
+                int32_t cut[4];
+                float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
+                segment_small(W, k, m, mm, cut, kmn, kmx, vmn, vmx);
+                make_params(pc.L, k, cut, kmn, kmx, vmn, vmx, rec, pp);  // same values in every lane
+            }
+            if (lane == 0) a.table[p] = rec;
+            // parameters into every CTA of the cluster (lane r < kCl serves CTA r), then its ready
+            if (lane < kCl) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(&pp);
+                const uint32_t dst = map_rank(&cs->par[slot], (uint32_t)lane);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_remote_u4(dst + 16 * i, src[i]);
+                remote_arrive(map_rank(&cs->ready[slot], (uint32_t)lane));
+            }
+            __syncwarp();
+        }
+    } else {
+        // ================================================================ worker warps
+        const uint32_t ring = smem_u32(smem) + warp * (kCRing * kWinBytes);
+        const uint64_t pol_first = make_policy_evict_first();
+        const int64_t rstride = (int64_t)a.Hkv * kD;  // elements between consecutive tokens of a head
+
+        // position a cursor on pair j (windows lo + warp, + kCWorkers, ...); i >= hi: none here
+        auto start_pair = [&](PairCursor &c, int32_t j) {
+            c.j = j;
+            if (j < nj) {
+                pair_of(j, c);
+                c.i = c.lo + warp;
+            }
+        };
+        // the arrival a worker owes pair j's owner once its statistics of pair j are done
+        auto arrive_stats = [&](int32_t j) {
+            if (lane == 0) {
+                const int32_t q = j / kCl;
+                remote_arrive(map_rank(&cs->stats_done[q % kSlots], (uint32_t)(j % kCl)));
+            }
+        };
+
+        PairCursor sc, qc;
+        start_pair(sc, 0);
+        start_pair(qc, 0);
+        int32_t pc_j = -1;
+        PairCache params = {0, 0.0f, 0.0f, 0.0f, 0.0f};
+        int next_stage = 0;
+
+        // Start the copies of the next item; false when nothing may start now.
+        auto try_issue = [&](CItem &it) -> bool {
+            // quantisation: pairs whose parameters are ready (pairs with no window here are passed
+            // once ready, so that their statistics slot may be reused)
+            while (qc.j < nj) {
+                const bool ab = aborted();
+                if (!ab && !test_wait_cluster(&cs->ready[qc.j % kSlots], (uint32_t)(qc.j / kSlots) & 1u)) break;
+                if (qc.i >= qc.hi) {
+                    start_pair(qc, qc.j + 1);
+                    continue;
+                }
+                it.kind = ab ? 2 : 1;
+                it.stage = next_stage;
+                it.j = qc.j;
+                it.t0 = qc.i * kWin;
+                it.cnt = min(kWin, qc.L - it.t0);
+                it.h = qc.h;
+                if (!ab) {
+                    if (pc_j != qc.j) {
+                        params = load_params_smem(&cs->par[qc.j % kSlots]);
+                        pc_j = qc.j;
+                    }
+                    it.pc = params;
+                    it.blk = __ldg(a.bt + (int64_t)qc.b * a.max_blocks + it.t0 / a.bs);
+                }
+                goto issue_copy;
+            }
+            // statistics: at most kSlots - 1 pairs past the oldest pair still to quantise
+            while (sc.j < nj && sc.j < qc.j + kSlots) {
+                if (sc.i >= sc.hi) {  // nothing (more) of this pair for this worker
+                    if (sc.i == sc.lo + warp) arrive_stats(sc.j);  // it had no window at all
+                    start_pair(sc, sc.j + 1);
+                    continue;
+                }
+                it.kind = 0;
+                it.stage = next_stage;
+                it.j = sc.j;
+                it.idx = sc.i - sc.lo;
+                it.t0 = sc.i * kWin;
+                it.cnt = min(kWin, sc.L - it.t0);
+                it.last = sc.i + kCWorkers >= sc.hi;
+                goto issue_copy;
+            }
+            return false;
+        issue_copy:
+            if (it.kind != 2) {
+                const PairCursor &c = it.kind == 0 ? sc : qc;
+                const int64_t row0 = ((int64_t)(c.c0 + it.t0) * a.Hkv + c.h) * kD;
+                const uint32_t dst = ring + it.stage * kWinBytes;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 2 * i + (lane >> 4), col = lane & 15;
+                    if (row < it.cnt) {  // rows past the request end are not copied
+                        const uint16_t *ks = a.k + row0 + row * rstride + col * 8;
+                        const uint16_t *vs = a.v + row0 + row * rstride + col * 8;
+                        const uint32_t off = tile_off(row, col);
+                        if (it.kind == 1) {  // second read: last use
+                            cp16_hint(dst + off, ks, pol_first);
+                            cp16_hint(dst + kTileBytes + off, vs, pol_first);
+                        } else {
+                            cp16(dst + off, ks);
+                            cp16(dst + kTileBytes + off, vs);
+                        }
+                    }
+                }
+            }
+            cp_commit();
+            next_stage ^= 1;
+            if (it.kind == 0) sc.i += kCWorkers;
+            else qc.i += kCWorkers;
+            return true;
+        };
+
+        CItem f0, f1;
+        int nin = 0;
+        uint32_t spins = 0;
+        while (true) {
+            if (nin == 0 && try_issue(f0)) nin = 1;
+            if (nin == 1 && try_issue(f1)) nin = 2;
+            if (nin == 0) {
+                if (sc.j >= nj && qc.j >= nj) break;
+                if (++spins >= kSpinLimit) {  // waiting for parameters that never came
+                    if (lane == 0) {
+                        record_error(a.hdr, kErrBarrierWait);
+                        st_release_cta_shared(&cs->abort, 1);
+                    }
+                    spins = 0;
+                }
+                __nanosleep(32);
+                continue;
+            }
+            spins = 0;
+            if (nin == 2) cp_wait<1>();
+            else cp_wait<0>();
+            __syncwarp();
+            const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
+            if (f0.kind == 0) {
+                const WinStats s = window_stats(kt, vt, f0.cnt);
+                if (lane == 0) {
+                    cs->mean[f0.j % kSlots][f0.idx] = s.mean;
+                    cs->mm[f0.j % kSlots][f0.idx] = make_float4(s.kmn, s.kmx, s.vmn, s.vmx);
+                }
+                if (f0.last) arrive_stats(f0.j);  // after this lane's writes (release, cluster scope)
+            } else if (f0.kind == 1) {
+                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
+            }
+            __syncwarp();  // the stage's reads are done before it is refilled
+            f0 = f1;
+            --nin;
+        }
+        cp_wait<0>();
+    }
+    cluster_sync_all();  // no CTA leaves while others may still reach its shared memory
+}
+
+// ---- host launcher -------------------------------------------------------------------------
+
+int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
+
+cudaError_t launch_compress_cluster(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t Hkv,
+                                    int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+                                    uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream)
+{
+    ClusterArgs a;
+    a.k = static_cast<const uint16_t *>(k);
+    a.v = static_cast<const uint16_t *>(v);
+    a.cu = cu;
+    a.bt = bt;
+    a.kpool = kpool;
+    a.vpool = vpool;
+    a.table = table;
+    a.hdr = static_cast<WsHeader *>(ws);
+    a.B = B;
+    a.Hkv = Hkv;
+    a.bs = bs;
+    a.max_blocks = max_blocks;
+
+    const size_t smem = (size_t)kCRingBytes + sizeof(ClusterSmem);
+    static int cached_dev = -1, cached_clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dev != cached_dev) {
+        e = cudaFuncSetAttribute(compress_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(nsm / kCl * kCl));
+        int nclusters = 0;  // clusters that fit on the GPU at once (GPC boundaries)
+        e = cudaOccupancyMaxActiveClusters(&nclusters, compress_cluster_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (nclusters < 1) return cudaErrorInvalidConfiguration;
+        cached_dev = dev;
+        cached_clusters = nclusters;
+    }
+    cfg.gridDim = dim3((unsigned)(cached_clusters * kCl));  // one wave: every cluster resident
+    return cudaLaunchKernelEx(&cfg, compress_cluster_kernel, a);
+}
+
+}  // namespace dgq

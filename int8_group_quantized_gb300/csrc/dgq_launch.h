@@ -18,6 +18,14 @@ cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int
                             int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
                             uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm, cudaStream_t stream);
 
+// Compression of calls whose requests are all at most cluster_compress_max_seqlen() tokens:
+// pairs segmented inside thread-block clusters (no grid-wide step, no workspace beyond the
+// header).
+int32_t cluster_compress_max_seqlen();
+cudaError_t launch_compress_cluster(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t Hkv,
+                                    int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+                                    uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream);
+
 struct AttnLayout {
     size_t off_count, off_part, total;
 };

@@ -45,11 +45,27 @@ def test_untouched_slots_keep_their_bytes():
     assert np.all(kp[~touched] == 0xA5)
 
 
-def test_many_pairs_several_super_groups():
-    # 64 requests x 8 heads x ~1.5K tokens: ~1.5 M windows-worth of work spread over super-groups
+def test_many_short_pairs_cluster_path():
+    # every request <= 4096 tokens: pairs segmented inside thread-block clusters; 512 pairs,
+    # several per cluster and per shared-memory slot
     rng = np.random.default_rng(1)
     lens = rng.integers(1, 3000, 64).tolist()
     run(Case(lens, hq=32, hkv=8, bs=16, seed=11))
+
+
+def test_short_pairs_cluster_path_edges():
+    # the longest pair the cluster path takes (4096 tokens = 256 windows), one-window pairs,
+    # empty requests, a partial last window, block size 64
+    lens = [4096, 1, 0, 16, 17, 4095, 2048, 0, 255, 3333]
+    run(Case(lens, hq=4, hkv=4, bs=64, seed=12))
+
+
+def test_many_pairs_several_chunks_grid_path():
+    # one request above 4096 tokens sends the call through the grid-wide kernel: ~50 K windows
+    # in several 8192-window chunks, pairs crossing chunk and CTA-share edges
+    rng = np.random.default_rng(2)
+    lens = rng.integers(1, 3000, 64).tolist() + [5000]
+    run(Case(lens, hq=32, hkv=8, bs=16, seed=14))
 
 
 def test_repeated_calls_reuse_workspace():

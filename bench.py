@@ -370,11 +370,16 @@ def run_ours(args):
         peak, peak_src = measured_peak()
         dec_launch_us = dec_ms / (K * nl) * 1e3
         comp_launch_us = comp_ms / (K * nl) * 1e3
+        # the library compresses a call whose requests are all at most 4096 tokens with its
+        # cluster kernel, longer ones with the grid-wide kernel
+        comp_name, comp_src = (("compress_cluster_kernel", "dgq_compress_cluster.cu") if max_seqlen <= 4096
+                               else ("compress_kernel", "dgq_compress.cu"))
         kernels = {
             "attn_kernel": {"bytes_per_launch": dec_b, "avg_launch_us": round(dec_launch_us, 2),
-                            "achieved_gbs": round(dec_b / dec_launch_us / 1e3, 1), "src": "dgq_attn.cu"},
-            "compress_kernel": {"bytes_per_launch": comp_b, "avg_launch_us": round(comp_launch_us, 2),
-                                "achieved_gbs": round(comp_b / comp_launch_us / 1e3, 1), "src": "dgq_compress.cu"},
+                            "achieved_gbs": round(dec_b / dec_launch_us / 1e3, 1), "src": "dgq_attn.cu",
+                            "timed_with": "combine_kernel (merge of split pairs)"},
+            comp_name: {"bytes_per_launch": comp_b, "avg_launch_us": round(comp_launch_us, 2),
+                        "achieved_gbs": round(comp_b / comp_launch_us / 1e3, 1), "src": comp_src},
         }
         dom = max(kernels, key=lambda k: kernels[k]["avg_launch_us"])
         ach = kernels[dom]["achieved_gbs"]

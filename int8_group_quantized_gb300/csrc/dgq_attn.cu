@@ -19,10 +19,12 @@
 //    The next pieces' record, query rows and current key/value are staged in shared memory by
 //    bulk copies while the current piece streams, so a piece boundary waits on no global load.
 //  * Loads: each warp copies its tiles' K and V rows with cp.async (whole 128-byte rows, four
-//    rows per instruction) into its own shared-memory ring, four tiles deep, with the 16-byte
-//    columns of row i XOR-permuted by i % 8 so the fragment reads hit distinct banks.  Measured on this GPU, the per-copy issue cost of TMA caps single-tile copies of
-//    2 KB blocks at 2-4 TB/s, while per-thread 16-byte copies stream at the HBM rate.  Block ids
-//    come 32 tiles ahead from one coalesced load per warp.
+//    rows per instruction) into its own shared-memory ring, three tiles deep, with the 16-byte
+//    columns of row i XOR-permuted by i % 8 so the fragment reads hit distinct banks.  Measured
+//    on this GPU: three CTAs per SM at depth 3 stream faster than two at depth 4 to 6; the
+//    per-copy issue cost of TMA caps single-tile copies of 2 KB blocks at 2-4 TB/s, while
+//    per-thread 16-byte copies stream at the HBM rate.  Block ids come 32 tiles ahead from one
+//    coalesced load per warp.
 //  * Math: codes become fp16 (1024 + q) with byte permutes, and the GQA query group multiplies
 //    them on the tensor cores (mma.sync m16n8k16, fp32 accumulate): S^T = Q . K^T and
 //    O^T += V^T . P^T.  The affine dequantisation is folded out of the inner loop: for a tile
@@ -45,7 +47,7 @@ constexpr int kTile = 16;                          // tokens per tile
 constexpr int kWarpsPerCta = 4;
 constexpr int kAttnThreads = kWarpsPerCta * 32;
 constexpr int kMaxCtasPerSm = 3;
-constexpr int kDepth = 4;                          // tiles in flight per warp
+constexpr int kDepth = 3;                          // tiles in flight per warp (3 CTAs of 4 warps fit per SM)
 constexpr int kTileBytes = kTile * kD;            // 16 rows of 128 codes = 2 KB
 constexpr int kTileSmem = 2 * kTileBytes;          // K tile + V tile
 constexpr int kWarpSmem = kDepth * kTileSmem;

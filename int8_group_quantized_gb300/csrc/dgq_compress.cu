@@ -53,6 +53,7 @@ constexpr int kAgg = 64;        // windows per min/max aggregate
 constexpr int kWorkers = 10;    // worker warps per CTA (plus an arrival warp and a segmentation warp)
 constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
+static_assert(kRing == 2 || kRing == 3, "worker loops handle two or three windows in flight");
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
 constexpr int32_t kChunk = 8192;           // windows per chunk: 64 MB of K+V
 constexpr int32_t kAhead = 16384;          // statistics may lead quantisation by this many windows
@@ -684,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                 }
             }
             cp_commit();
-            next_stage ^= 1;
+            if (++next_stage == kRing) next_stage = 0;
             if (it.kind == 0) {
                 advance(sc, false);
                 it.next_m = sc.w >= 0 ? sc.m : M;
@@ -695,12 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
             return true;
         };
 
-        Item f0, f1;
+        Item f0, f1, f2;  // in-flight windows, oldest first (f2 used when kRing == 3)
         int nin = 0;
         uint32_t spins = 0;
         while (true) {
             if (nin == 0 && try_issue(f0)) nin = 1;
             if (nin == 1 && try_issue(f1)) nin = 2;
+            if constexpr (kRing == 3) {
+                if (nin == 2 && try_issue(f2)) nin = 3;
+            }
             if (nin == 0) {
                 if (sc.w < 0 && qc.w < 0) break;
                 // blocked on the parameters of range qc.m
@@ -713,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                 continue;
             }
             spins = 0;
-            if (nin == 2) cp_wait<1>();
+            if (kRing == 3 && nin == 3) cp_wait<2>();
+            else if (nin == 2) cp_wait<1>();
             else cp_wait<0>();
             __syncwarp();
             const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
@@ -736,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
             if (f0.kind != 0 && lane == 0 && f0.next_m != f0.m)
                 st_release_cta_shared(ctl->quant_done + warp, f0.next_m);
             f0 = f1;
+            if constexpr (kRing == 3) f1 = f2;
             --nin;
         }
         cp_wait<0>();

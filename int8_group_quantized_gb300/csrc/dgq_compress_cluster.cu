@@ -36,6 +36,7 @@ constexpr int kCl = 4;                                   // CTAs per cluster
 constexpr int kCWorkers = 10;                            // worker warps per CTA (plus a segmentation warp)
 constexpr int kCThreads = (kCWorkers + 1) * 32;
 constexpr int kCRing = 2;                                // windows in flight per worker
+static_assert(kCRing == 2 || kCRing == 3, "worker loops handle two or three windows in flight");
 constexpr int kCRingBytes = kCWorkers * kCRing * kWinBytes;
 constexpr int kSlots = 3;                                // pairs a cluster holds at once
 constexpr int kSlotWin = 64;                             // windows of one pair per CTA
@@ -367,18 +368,21 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
                 }
             }
             cp_commit();
-            next_stage ^= 1;
+            if (++next_stage == kCRing) next_stage = 0;
             if (it.kind == 0) sc.i += kCWorkers;
             else qc.i += kCWorkers;
             return true;
         };
 
-        CItem f0, f1;
+        CItem f0, f1, f2;  // in-flight windows, oldest first (f2 used when kCRing == 3)
         int nin = 0;
         uint32_t spins = 0;
         while (true) {
             if (nin == 0 && try_issue(f0)) nin = 1;
             if (nin == 1 && try_issue(f1)) nin = 2;
+            if constexpr (kCRing == 3) {
+                if (nin == 2 && try_issue(f2)) nin = 3;
+            }
             if (nin == 0) {
                 if (sc.j >= nj && qc.j >= nj) break;
                 if (++spins >= kSpinLimit) {  // waiting for parameters that never came
@@ -392,7 +396,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
                 continue;
             }
             spins = 0;
-            if (nin == 2) cp_wait<1>();
+            if (kCRing == 3 && nin == 3) cp_wait<2>();
+            else if (nin == 2) cp_wait<1>();
             else cp_wait<0>();
             __syncwarp();
             const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
@@ -408,6 +413,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
             }
             __syncwarp();  // the stage's reads are done before it is refilled
             f0 = f1;
+            if constexpr (kCRing == 3) f1 = f2;
             --nin;
         }
         cp_wait<0>();

@@ -57,8 +57,9 @@ __device__ __forceinline__ float canon_zero(float x) { return x == 0.0f ? 0.0f :
 // sm_100-class GPUs execute fp32 add/sub/mul on register pairs (f32x2); each half is an
 // ordinary IEEE operation with round-to-nearest-even.  Measured on this GPU: a packed multiply
 // whose result feeds a packed add is contracted into a fused multiply-add by the assembler,
-// even with explicit rounding, which would change the rounding.  So packed multiplies here only
-// feed conversions, and products that feed sums are scalar __fmul_rn (never contracted).
+// even with explicit rounding, which would change the rounding.  So a packed product here only
+// feeds scalar __fadd_rn (explicit rounding: not contracted), and products that feed packed
+// sums are scalar __fmul_rn.
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits)
 {
     uint64_t r;
@@ -199,9 +200,13 @@ __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32
 
 // ---- quantisation -----------------------------------------------------------------------
 
-// Eight codes from eight bf16 values: rint((x - min) * inv), the difference and the product
-// as packed fp32 pairs (one IEEE rounding each), the rounding to an integer by conversion
-// (round-to-nearest-even; 0 <= u <= 255 * (1 + 2^-22) < 255.5 because x >= min).
+// Eight codes from eight bf16 values: rint((x - min) * inv).  The difference and the product
+// are packed fp32 pairs (one IEEE rounding each); the rounding to an integer adds 1.5 * 2^23 in
+// scalar fp32 (__fadd_rn: never contracted), which rounds u to an integer (round-to-nearest-even)
+// and leaves it in the low mantissa bits: 0 <= u <= 255 * (1 + 2^-22) < 255.5 because x >= min,
+// so the low byte is the code.  (A packed add after the packed product would be contracted into
+// a fused multiply-add by the assembler, changing the rounding; an integer conversion is exact
+// too but measured 11% slower overall.)
 __device__ __forceinline__ uint2 encode8(const uint4 &q, uint64_t mn2, uint64_t inv2)
 {
     const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
@@ -210,8 +215,8 @@ __device__ __forceinline__ uint2 encode8(const uint4 &q, uint64_t mn2, uint64_t 
     for (int e = 0; e < 4; ++e) {
         uint32_t u0, u1;
         f2_unpack(f2_mul(f2_sub(f2_pack(bf_lo(wv[e]), bf_hi(wv[e])), mn2), inv2), u0, u1);
-        c[2 * e] = (uint32_t)__float2int_rn(__uint_as_float(u0));
-        c[2 * e + 1] = (uint32_t)__float2int_rn(__uint_as_float(u1));
+        c[2 * e] = __float_as_uint(__fadd_rn(__uint_as_float(u0), 12582912.0f));
+        c[2 * e + 1] = __float_as_uint(__fadd_rn(__uint_as_float(u1), 12582912.0f));
     }
     const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
     const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);

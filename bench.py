@@ -193,6 +193,21 @@ class OracleSample:
         return self.dec_b * n, td, self.comp_b * n, tc
 
 
+def max_over_ranks(values, device, world):
+    """The slowest rank's value of each timing (a replica run is as fast as its slowest GPU)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_gbs(bytes_per_step, steps, world, max_ms):
+    """Whole-job GB/s of `world` replicas that each moved `bytes_per_step` per step."""
+    return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -358,15 +373,12 @@ def run_ours(args):
     # ---- parity spot check outside the timed region: one (request, head) of layer 0 vs the oracle
     checked = spot_check(w, lens, cu, bt, layers[0], rank)
 
-    stats = torch.tensor([total_ms, comp_ms, dec_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
-    total_ms, comp_ms, dec_ms, e2e_ms = stats.tolist()
+    total_ms, comp_ms, dec_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, e2e_ms], dev, world)
 
     if rank == 0:
         K = args.steps
-        dec_gbs = world * dec_b_step * K / (dec_ms / 1e3) / 1e9
-        comp_gbs = world * comp_b_step * K / (comp_ms / 1e3) / 1e9
+        dec_gbs = replica_gbs(dec_b_step, K, world, dec_ms)
+        comp_gbs = replica_gbs(comp_b_step, K, world, comp_ms)
         peak, peak_src = measured_peak()
         dec_launch_us = dec_ms / (K * nl) * 1e3
         comp_launch_us = comp_ms / (K * nl) * 1e3

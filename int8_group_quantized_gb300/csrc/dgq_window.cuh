@@ -54,12 +54,12 @@ __device__ __forceinline__ float canon_zero(float x) { return x == 0.0f ? 0.0f :
 
 // ---- packed fp32 pairs ----------------------------------------------------------------------
 //
-// sm_100-class GPUs execute fp32 add/sub/mul on register pairs (f32x2); each half is an
+// sm_100-class GPUs execute fp32 add/sub/mul/fma on register pairs (f32x2); each half is an
 // ordinary IEEE operation with round-to-nearest-even.  Measured on this GPU: a packed multiply
 // whose result feeds a packed add is contracted into a fused multiply-add by the assembler,
-// even with explicit rounding, which would change the rounding.  So a packed product here only
-// feeds scalar __fadd_rn (explicit rounding: not contracted), and products that feed packed
-// sums are scalar __fmul_rn.
+// even with explicit rounding, which would change the rounding.  So products that feed packed
+// sums here are scalar __fmul_rn, and the one packed product (the quantiser's) feeds a packed
+// fused multiply-add by one, which the assembler leaves alone (checked on near-tie inputs).
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits)
 {
     uint64_t r;
@@ -76,20 +76,42 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
 {
     uint64_t r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint32_t bf_lo(uint32_t w) { return w << 16; }          // fp32 bits of the low bf16
-__device__ __forceinline__ uint32_t bf_hi(uint32_t w) { return w & 0xFFFF0000u; }  // and of the high one
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// ---- mixed bf16 / fp32 arithmetic -----------------------------------------------------------
+//
+// sm_100-class GPUs add and subtract a bf16 operand to or from an fp32 one directly: the bf16
+// value is widened exactly and the fp32 result rounded once (round-to-nearest-even), the same
+// IEEE operation as widening first, without the unpacking instruction.
+
+// x - c for the two bf16 of a word (low half to d_lo).
+__device__ __forceinline__ void bf2_sub(uint32_t w, float c, float &d_lo, float &d_hi)
+{
+    asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %2;\nsub.rn.f32.bf16 %0, lo, %3;\nsub.rn.f32.bf16 %1, hi, %3;\n}"
+        : "=f"(d_lo), "=f"(d_hi)
+        : "r"(w), "f"(c));
+}
+// x_lo + x_hi of the two bf16 of a word, in fp32 (one rounding).
+__device__ __forceinline__ float bf2_sum(uint32_t w)
+{
+    float r;
+    asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nadd.rn.f32.bf16 %0, hi, %2;\n}"
+        : "=f"(r)
+        : "r"(w), "f"(__uint_as_float(w << 16)));
+    return r;
+}
 
 // Shared-memory tiles hold row r (one token, 16 chunks of 16 bytes) with chunk c stored at
 // position c ^ (r & 15), so that both the row-per-lane reads below and the chunk-per-lane reads
@@ -109,11 +131,11 @@ struct WinStats {
 
 // Balanced sum of the 64 values of half-row hh of token t of a K tile: word i holds elements
 // 2i, 2i+1 (bf16).  In each packed register the low half belongs to elements [0, 32), the
-// high half to [32, 64).  With `squares`, the packed pair `centre` is subtracted and the
-// difference squared first.  The words are read again from shared memory for each pass (cheap)
+// high half to [32, 64).  With `squares`, `centre` is subtracted and the difference squared
+// first.  The words are read again from shared memory for each pass (cheap)
 // instead of being held in registers across both.
 template <bool squares>
-__device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, uint64_t centre, __nv_bfloat162 &mn2,
+__device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, float centre, __nv_bfloat162 &mn2,
                                        __nv_bfloat162 &mx2)
 {
     // leaf pair i (i < 16) packs elements (2i, 32 + 2i) and (2i+1, 33 + 2i); leaves 4j..4j+3 come
@@ -135,18 +157,15 @@ __device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, uint64_t cent
                 mn2 = __hmin2(mn2, __hmin2(xa, xb));
                 mx2 = __hmax2(mx2, __hmax2(xa, xb));
             }
-            uint64_t a = f2_pack(bf_lo(wa[e]), bf_lo(wb[e]));
-            uint64_t b = f2_pack(bf_hi(wa[e]), bf_hi(wb[e]));
-            if (squares) {  // (x - mean)^2: packed difference, scalar squares
-                uint32_t a0, a1, b0, b1;
-                f2_unpack(f2_sub(a, centre), a0, a1);
-                f2_unpack(f2_sub(b, centre), b0, b1);
-                const float da0 = __uint_as_float(a0), da1 = __uint_as_float(a1);
-                const float db0 = __uint_as_float(b0), db1 = __uint_as_float(b1);
-                a = f2_pack(__float_as_uint(__fmul_rn(da0, da0)), __float_as_uint(__fmul_rn(da1, da1)));
-                b = f2_pack(__float_as_uint(__fmul_rn(db0, db0)), __float_as_uint(__fmul_rn(db1, db1)));
+            if (squares) {  // (x - mean)^2: mixed-precision difference, scalar squares, packed sum
+                float da0, da1, db0, db1;
+                bf2_sub(wa[e], centre, da0, da1);
+                bf2_sub(wb[e], centre, db0, db1);
+                l[e] = f2_add(f2_pack(f2u(__fmul_rn(da0, da0)), f2u(__fmul_rn(db0, db0))),
+                              f2_pack(f2u(__fmul_rn(da1, da1)), f2u(__fmul_rn(db1, db1))));
+            } else {  // x_2i + x_2i+1: the two halves of a word
+                l[e] = f2_pack(f2u(bf2_sum(wa[e])), f2u(bf2_sum(wb[e])));
             }
-            l[e] = f2_add(a, b);
         }
         node[j] = f2_add(f2_add(l[0], l[1]), f2_add(l[2], l[3]));
     }
@@ -166,8 +185,7 @@ __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32
     float s = sum64<false>(kt, t, hh, 0, kmn2, kmx2);
     s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 16));
     const float mean = __fmul_rn(s, 0.0078125f);  // exact /128
-    const uint32_t mb = __float_as_uint(mean);
-    float e = sum64<true>(kt, t, hh, f2_pack(mb, mb), kmn2, kmx2);
+    float e = sum64<true>(kt, t, hh, mean, kmn2, kmx2);
     e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 16));
 #pragma unroll 2
     for (int j = 0; j < 8; ++j) {
@@ -200,23 +218,25 @@ __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32
 
 // ---- quantisation -----------------------------------------------------------------------
 
-// Eight codes from eight bf16 values: rint((x - min) * inv).  The difference and the product
-// are packed fp32 pairs (one IEEE rounding each); the rounding to an integer adds 1.5 * 2^23 in
-// scalar fp32 (__fadd_rn: never contracted), which rounds u to an integer (round-to-nearest-even)
-// and leaves it in the low mantissa bits: 0 <= u <= 255 * (1 + 2^-22) < 255.5 because x >= min,
-// so the low byte is the code.  (A packed add after the packed product would be contracted into
-// a fused multiply-add by the assembler, changing the rounding; an integer conversion is exact
-// too but measured 11% slower overall.)
-__device__ __forceinline__ uint2 encode8(const uint4 &q, uint64_t mn2, uint64_t inv2)
+// Eight codes from eight bf16 values: rint((x - min) * inv).  The difference is the mixed
+// bf16 - fp32 subtraction (one rounding), the product a packed fp32 pair (one rounding each).
+// The rounding to an integer adds 1.5 * 2^23, which rounds u to an integer (round-to-nearest-
+// even) and leaves it in the low mantissa bits: 0 <= u <= 255 * (1 + 2^-22) < 255.5 because
+// x >= min, so the low byte is the code.  The add is written as the packed fused multiply-add
+// u * 1 + 1.5 * 2^23, which is the rounded sum itself: measured on this GPU, a plain packed add
+// whose operand comes from a packed product is contracted with it into one fused multiply-add
+// by the assembler (one rounding instead of two: a different code whenever the rounded product
+// is a tie), and a fused multiply-add by one is not.
+__device__ __forceinline__ uint2 encode8(const uint4 &q, float mn, uint64_t inv2)
 {
     const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+    const uint64_t one2 = f2_pack(0x3F800000u, 0x3F800000u), mag2 = f2_pack(0x4B400000u, 0x4B400000u);
     uint32_t c[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        uint32_t u0, u1;
-        f2_unpack(f2_mul(f2_sub(f2_pack(bf_lo(wv[e]), bf_hi(wv[e])), mn2), inv2), u0, u1);
-        c[2 * e] = __float_as_uint(__fadd_rn(__uint_as_float(u0), 12582912.0f));
-        c[2 * e + 1] = __float_as_uint(__fadd_rn(__uint_as_float(u1), 12582912.0f));
+        float d0, d1;
+        bf2_sub(wv[e], mn, d0, d1);
+        f2_unpack(f2_fma(f2_mul(f2_pack(f2u(d0), f2u(d1)), inv2), one2, mag2), c[2 * e], c[2 * e + 1]);
     }
     const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
     const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
@@ -256,9 +276,7 @@ __device__ __forceinline__ void window_quant(uint8_t *kpool, uint8_t *vpool, int
     const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
     const float vmn = __shfl_sync(0xffffffffu, pc.vmn, s), vinv = __shfl_sync(0xffffffffu, pc.vinv, s);
     const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + (t0 % bs)) * kD + sub * 8;
-    const uint64_t kmn2 = f2_pack(__float_as_uint(kmn), __float_as_uint(kmn));
     const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
-    const uint64_t vmn2 = f2_pack(__float_as_uint(vmn), __float_as_uint(vmn));
     const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -266,8 +284,8 @@ __device__ __forceinline__ void window_quant(uint8_t *kpool, uint8_t *vpool, int
         if (tt < cnt) {
             const uint4 kq = ld_shared_v4(kt + tile_off(tt, sub));
             const uint4 vq = ld_shared_v4(vt + tile_off(tt, sub));
-            __stcs(reinterpret_cast<uint2 *>(kpool + dst0 + tt * kD), encode8(kq, kmn2, kinv2));
-            __stcs(reinterpret_cast<uint2 *>(vpool + dst0 + tt * kD), encode8(vq, vmn2, vinv2));
+            __stcs(reinterpret_cast<uint2 *>(kpool + dst0 + tt * kD), encode8(kq, kmn, kinv2));
+            __stcs(reinterpret_cast<uint2 *>(vpool + dst0 + tt * kD), encode8(vq, vmn, vinv2));
         }
     }
 }

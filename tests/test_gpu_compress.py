@@ -98,3 +98,54 @@ def test_planted_boundaries_on_gpu():
     run(case)
     tab = table_to_numpy(case.d_table)
     assert tab[0, 0]["n_seg"] == 3 and list(tab[0, 0]["start"][:3]) == [0, 1024, 2560]
+
+
+def _tie_segments(n, rng):
+    """n segments (min, max, xs) as bf16 bit patterns, xs in [min, max], chosen so that the fp32
+    product (x - min) * (255 / (max - min)) rounds to exactly k + 0.5 although the exact product
+    is not k + 0.5: there the method's two roundings (product, then to an integer, half to even)
+    and a single fused rounding give different codes whenever k + 0.5 is closer to the odd
+    neighbour."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    lo_pool = bits[finite & (vals > -2.0) & (vals < -0.01)]
+    hi_pool = bits[finite & (vals > 0.01) & (vals < 3.0)]
+    out, flips = [], 0
+    while len(out) < n:
+        ab, bb = rng.choice(lo_pool), rng.choice(hi_pool)
+        a, b = vals[ab], vals[bb]
+        inside = finite & (vals >= a) & (vals <= b)
+        xv = vals[inside]
+        d = (xv - a).astype(np.float32)
+        inv = np.float32(255.0) / np.float32(b - a)
+        p = d.astype(np.float64) * np.float64(inv)       # exact: 24 x 24 bits
+        u = p.astype(np.float32).astype(np.float64)
+        tie = (u - np.floor(u) == 0.5) & (p != u)
+        if tie.sum() >= 2:
+            double = np.rint(u[tie])                      # the method: round the product, then half-even
+            single = np.rint(p[tie])                      # one fused rounding
+            flips += int((double != single).sum())
+            out.append((ab, bb, bits[inside][tie]))
+    return out, flips
+
+
+def test_codes_at_rounding_ties():
+    # every code of these segments sits where rounding the product once instead of twice would
+    # change it: the codes must match the oracle's two IEEE roundings bit for bit
+    lens = [32] * 4
+    case = Case(lens, hq=2, hkv=2, bs=16, seed=21)
+    rng = np.random.default_rng(21)
+    segs, flips = _tie_segments(2 * 2 * len(lens) * 2, rng)  # (K, V) x heads x requests x 2 segments
+    assert flips > 0
+    it = iter(segs)
+    for arr in (case.k, case.v):
+        for b in range(len(lens)):
+            for h in range(2):
+                for s in range(2):  # L = 32: two windows, one cut, segments of 16 tokens
+                    ab, bb, xs = next(it)
+                    vals = np.resize(xs, 16 * 128).astype(np.uint16)
+                    vals[0], vals[1] = ab, bb
+                    r0 = case.cu[b] + 16 * s
+                    arr[r0:r0 + 16, h, :] = vals.reshape(16, 128)
+    run(case)

@@ -215,6 +215,42 @@ def test_round_half_to_even_closed_form():
     assert list(kc[0, :10]) == [0, 255, 0, 2, 2, 4, 4, 254, 254, 100]
 
 
+def test_rounded_product_ties_round_half_to_even():
+    # x where the fp32 product (x - min) * inv is exactly k + 0.5 but the exact product is not:
+    # the method rounds the product first, then half to even, so these codes must differ from
+    # the integer nearest to the exact product (what one fused multiply-add rounding gives) in
+    # every case where k + 0.5 was rounded toward the odd side
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    rng = np.random.default_rng(4)
+    lo_pool = bits[finite & (vals > -2.0) & (vals < -0.01)]
+    hi_pool = bits[finite & (vals > 0.01) & (vals < 3.0)]
+    checked = flipped = 0
+    while flipped < 20:
+        ab, bb = rng.choice(lo_pool), rng.choice(hi_pool)
+        a, b = vals[ab], vals[bb]
+        inside = finite & (vals >= a) & (vals <= b)
+        xv = vals[inside]
+        p = (xv - a).astype(np.float32).astype(np.float64) * np.float64(np.float32(255.0) / np.float32(b - a))
+        u = p.astype(np.float32).astype(np.float64)
+        tie = (u - np.floor(u) == 0.5) & (p != u)
+        if not tie.any():
+            continue
+        row = np.resize(bits[inside][tie], D).astype(np.uint16)
+        row[0], row[1] = ab, bb
+        rec, kc, _ = oracle.compress_pair(np.tile(row, (16, 1)), np.tile(row, (16, 1)))
+        assert rec["n_seg"] == 1 and rec["k_min"][0] == a
+        xs = (row[2:].astype(np.uint32) << 16).view(np.float32)
+        pe = (xs - a).astype(np.float32).astype(np.float64) * np.float64(np.float32(255.0) / np.float32(b - a))
+        ue = pe.astype(np.float32).astype(np.float64)
+        even = 2 * np.round(ue / 2)        # ue = k + 0.5 -> the even one of k, k + 1
+        assert np.all(kc[0, 2:] == even)
+        checked += xs.size
+        flipped += int((even != np.rint(pe)).sum())
+    assert checked > 0
+
+
 def test_flat_segment_codes_zero_and_decode_to_min():
     # 20 tokens = 2 windows -> 2 segments (a zero jump is still a boundary), both flat
     k = np.tile(bf16_bits(np.full(D, -0.375)), (20, 1))

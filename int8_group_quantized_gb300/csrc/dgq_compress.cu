@@ -29,8 +29,8 @@
 //    segmented by each; the result is the same bits).  Parameters go to a per-CTA slice of the workspace; workers learn of them
 //    through shared-memory flags with CTA-scope release/acquire and never wait on global
 //    memory themselves.
-//  * Each worker streams its windows (every 12th window of its CTA's share) through a
-//    private two-window shared-memory ring filled with cp.async.  Windows never cross a
+//  * Each worker streams its windows (every 10th window of its CTA's share) through a
+//    private two-window shared-memory ring, one TMA tile copy per window and tensor.  Windows never cross a
 //    block (block sizes are multiples of 16) nor a segment (boundaries sit on window
 //    edges), so quantising a window needs one block id and one (min, inv) pair per tensor.
 //
@@ -53,15 +53,14 @@ constexpr int kAgg = 64;        // windows per min/max aggregate
 constexpr int kWorkers = 10;    // worker warps per CTA (plus an arrival warp and a segmentation warp)
 constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
-static_assert(kRing == 2 || kRing == 3, "worker loops handle two or three windows in flight");
+static_assert(kRing == 2, "the worker loop alternates two ring slots");
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
 constexpr int32_t kChunk = 8192;           // windows per chunk: 64 MB of K+V
 constexpr int32_t kAhead = 16384;          // statistics may lead quantisation by this many windows
 constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for
 
 struct CompressArgs {
-    const uint16_t *k;
-    const uint16_t *v;
+    TileMaps maps;  // K and V window tiles
     const int32_t *cu;
     const int32_t *bt;
     uint8_t *kpool;
@@ -403,8 +402,9 @@ struct Cursor {
 
 // One window in flight in a worker's ring.
 struct Item {
-    int32_t kind;    // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
-    int32_t stage, m;
+    int32_t kind;    // 0 statistics, 1 quantisation; after an error 2 (quantisation) or 3
+                     // (statistics): nothing to compute
+    int32_t m, slot;
     int32_t next_m;  // chunk / range of the worker's next item of the same kind (M if none)
     int32_t w;       // flat window index
     int32_t cnt;     // tokens in the window
@@ -422,11 +422,13 @@ struct CtaCtl {
     int32_t abort;
     int32_t last;
     int32_t pad[4];
+    uint64_t full[kWorkers][kRing];  // a worker's ring slot holds its window
 };
 
-__global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
+__global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_constant__ CompressArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = align_smem_1024(smem_raw);  // window tiles start on 1024-byte boundaries
     CtaCtl *ctl = reinterpret_cast<CtaCtl *>(smem + kRingBytes);
     int32_t *s_wpre = reinterpret_cast<int32_t *>(smem + kRingBytes + sizeof(CtaCtl));  // [B+1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -457,6 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
         ctl->ready[0] = ctl->ready[1] = 0;
         ctl->abort = 0;
         ctl->last = 0;
+        for (int w = 0; w < kWorkers; ++w)
+            for (int r = 0; r < kRing; ++r) mbar_init(&ctl->full[w][r], 1);
+        fence_barrier_init();
     }
     __syncthreads();
 
@@ -585,8 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
     } else {
         // ================================================================ worker warps
         const uint32_t ring = smem_u32(smem) + warp * (kRing * kWinBytes);
-        const uint64_t pol_first = make_policy_evict_first();
-        const int64_t rstride = (int64_t)a.Hkv * kD;  // elements between consecutive tokens of a head
+        uint64_t *full = ctl->full[warp];
+        const uint64_t pol_stats = make_policy_evict_normal();
+        const uint64_t pol_quant = make_policy_evict_first();  // second read: last use
 
         auto seek = [&](Cursor &c, bool quant) {
             for (; c.m < M; ++c.m) {
@@ -630,15 +636,15 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
 
         int32_t cur_m = -1, cur_slot = -1;  // parameters currently held in `params`
         PairCache params = {0, 0.0f, 0.0f, 0.0f, 0.0f};
-        int next_stage = 0;
 
-        // Start the copies of the next item; false when nothing may start now.
-        auto try_issue = [&](Item &it) -> bool {
+        // Choose the next item and start its copy into ring slot `slot`; false when nothing may
+        // start now.
+        auto try_issue = [&](Item &it, int slot) -> bool {
+            it.slot = slot;
             const bool aborted = *reinterpret_cast<volatile int32_t *>(&ctl->abort) != 0;
             if (qc.w >= 0 && (aborted || ld_acquire_cta_shared(ctl->ready + (qc.m & 1)) >= qc.m + 1)) {
                 it.kind = aborted ? 2 : 1;
                 it.m = qc.m;
-                it.stage = next_stage;
                 if (!aborted) {
                     if (qc.m != cur_m || qc.slot != cur_slot) {
                         params = load_params(slice(qc.m) + qc.slot);
@@ -653,39 +659,17 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
                 it.kind = 0;
                 it.w = sc.w;
                 it.m = sc.m;
-                it.stage = next_stage;
             } else {
                 return false;
             }
-            {
-                const WinLoc &l = it.kind == 0 ? sc.loc : qc.loc;
-                it.t0 = l.wi * kWin;
-                it.cnt = min(kWin, l.L - it.t0);
+            const WinLoc &l = it.kind == 0 ? sc.loc : qc.loc;
+            it.t0 = l.wi * kWin;
+            it.cnt = min(kWin, l.L - it.t0);
+            if (it.kind != 2 && lane == 0) {
+                fence_proxy_async_smem();  // the slot's earlier reads come before the copy
+                load_window(ring + slot * kWinBytes, full + slot, a.maps, l.h, l.c0 + it.t0,
+                            it.kind == 1 ? pol_quant : pol_stats);
             }
-            if (it.kind != 2) {
-                const WinLoc &l = it.kind == 0 ? sc.loc : qc.loc;
-                const int32_t t0 = l.wi * kWin, cnt = min(kWin, l.L - t0);
-                const int64_t row0 = ((int64_t)(l.c0 + t0) * a.Hkv + l.h) * kD;
-                const uint32_t dst = ring + it.stage * kWinBytes;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 2 * i + (lane >> 4), col = lane & 15;
-                    if (row < cnt) {  // rows past the request end are not copied
-                        const uint16_t *ks = a.k + row0 + row * rstride + col * 8;
-                        const uint16_t *vs = a.v + row0 + row * rstride + col * 8;
-                        const uint32_t off = tile_off(row, col);
-                        if (it.kind == 1) {  // second read: last use
-                            cp16_hint(dst + off, ks, pol_first);
-                            cp16_hint(dst + kTileBytes + off, vs, pol_first);
-                        } else {
-                            cp16(dst + off, ks);
-                            cp16(dst + kTileBytes + off, vs);
-                        }
-                    }
-                }
-            }
-            cp_commit();
-            if (++next_stage == kRing) next_stage = 0;
             if (it.kind == 0) {
                 advance(sc, false);
                 it.next_m = sc.w >= 0 ? sc.m : M;
@@ -696,55 +680,70 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(CompressArgs a)
             return true;
         };
 
-        Item f0, f1, f2;  // in-flight windows, oldest first (f2 used when kRing == 3)
-        int nin = 0;
-        uint32_t spins = 0;
-        while (true) {
-            if (nin == 0 && try_issue(f0)) nin = 1;
-            if (nin == 1 && try_issue(f1)) nin = 2;
-            if constexpr (kRing == 3) {
-                if (nin == 2 && try_issue(f2)) nin = 3;
-            }
-            if (nin == 0) {
-                if (sc.w < 0 && qc.w < 0) break;
-                // blocked on the parameters of range qc.m
-                if (++spins >= kSpinLimit) {
+        uint32_t phase = 0;  // bit s: parity of ring slot s's next completion
+        // Wait for the window in ring slot `slot` and compute on it.
+        auto process = [&](Item &it, int slot) {
+            if (it.kind != 2) {
+                if (!mbar_wait_bounded(full + slot, (phase >> slot) & 1u)) {
                     record_error(a.hdr, kErrBarrierWait);
                     if (lane == 0) st_release_cta_shared(&ctl->abort, 1);
-                    spins = 0;
+                    it.kind = it.kind == 0 ? 3 : 2;  // skip the arithmetic, keep the progress
                 }
-                __nanosleep(64);
-                continue;
+                phase ^= 1u << slot;
             }
-            spins = 0;
-            if (kRing == 3 && nin == 3) cp_wait<2>();
-            else if (nin == 2) cp_wait<1>();
-            else cp_wait<0>();
-            __syncwarp();
-            const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
-            if (f0.kind == 0) {
-                const WinStats s = window_stats(kt, vt, f0.cnt);
+            const uint32_t kt = ring + slot * kWinBytes, vt = kt + kTileBytes;
+            if (it.kind == 0) {
+                const WinStats s = window_stats(kt, vt, it.cnt);
                 if (lane == 0) {
-                    __stcg(a.win_mean + f0.w, s.mean);
-                    __stcg(a.win_mm + f0.w, make_float4(s.kmn, s.kmx, s.vmn, s.vmx));
-                    uint32_t *g = reinterpret_cast<uint32_t *>(a.agg + f0.w / kAgg);
+                    __stcg(a.win_mean + it.w, s.mean);
+                    __stcg(a.win_mm + it.w, make_float4(s.kmn, s.kmx, s.vmn, s.vmx));
+                    uint32_t *g = reinterpret_cast<uint32_t *>(a.agg + it.w / kAgg);
                     atomicMax(g + 0, ~ord_enc(s.kmn));
                     atomicMax(g + 1, ord_enc(s.kmx));
                     atomicMax(g + 2, ~ord_enc(s.vmn));
                     atomicMax(g + 3, ord_enc(s.vmx));
-                    if (f0.next_m != f0.m) st_release_cta_shared(ctl->stats_done + warp, f0.next_m);
                 }
-            } else if (f0.kind == 1) {
-                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
+            } else if (it.kind == 1) {
+                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
             }
-            __syncwarp();  // the stage's reads are done before it is refilled
-            if (f0.kind != 0 && lane == 0 && f0.next_m != f0.m)
-                st_release_cta_shared(ctl->quant_done + warp, f0.next_m);
-            f0 = f1;
-            if constexpr (kRing == 3) f1 = f2;
-            --nin;
+            __syncwarp();  // the slot's reads are done before it is refilled
+            if (lane == 0 && it.next_m != it.m) {
+                if (it.kind == 0 || it.kind == 3) st_release_cta_shared(ctl->stats_done + warp, it.next_m);
+                else st_release_cta_shared(ctl->quant_done + warp, it.next_m);
+            }
+        };
+
+        // Windows in flight, oldest first: slots are used in turn, so the slot of the next copy
+        // is always the one the oldest window frees.  One inlined copy of process() (the window
+        // arithmetic is long): two copies measured a third more instruction-fetch stalls.
+        Item f0, f1;
+        int nin = 0, next_slot = 0;
+        uint32_t spins = 0;
+        while (true) {
+            if (nin == 0 && try_issue(f0, next_slot)) {
+                nin = 1;
+                next_slot ^= 1;
+            }
+            if (nin == 1 && try_issue(f1, next_slot)) {
+                nin = 2;
+                next_slot ^= 1;
+            }
+            if (nin > 0) {
+                spins = 0;
+                process(f0, f0.slot);
+                f0 = f1;
+                --nin;
+                continue;
+            }
+            if (sc.w < 0 && qc.w < 0) break;
+            // blocked on the parameters of range qc.m
+            if (++spins >= kSpinLimit) {
+                record_error(a.hdr, kErrBarrierWait);
+                if (lane == 0) st_release_cta_shared(&ctl->abort, 1);
+                spins = 0;
+            }
+            __nanosleep(64);
         }
-        cp_wait<0>();
     }
 
     __syncthreads();
@@ -800,18 +799,22 @@ CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv)
     return l;
 }
 
-static size_t compress_smem_bytes(int32_t B) { return (size_t)kRingBytes + sizeof(CtaCtl) + (size_t)(B + 1) * 4; }
+// + 1024: slack to start the rings on a 1024-byte boundary
+static size_t compress_smem_bytes(int32_t B)
+{
+    return 1024 + (size_t)kRingBytes + sizeof(CtaCtl) + (size_t)(B + 1) * 4;
+}
 
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
-                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                            uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm, cudaStream_t stream)
+cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm,
+                            cudaStream_t stream)
 {
     if (nsm > kMaxSms) return cudaErrorInvalidConfiguration;
     const CompressLayout l = compress_layout(B, max_seqlen, Hkv);
     char *base = static_cast<char *>(ws);
     CompressArgs a;
-    a.k = static_cast<const uint16_t *>(k);
-    a.v = static_cast<const uint16_t *>(v);
+    if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
     a.cu = cu;
     a.bt = bt;
     a.kpool = kpool;

@@ -8,9 +8,9 @@
 // GPU design.  When every (request, KV head) pair is short (at most 256 windows, 1 MB of bf16
 // K+V), a pair's segmentation needs no grid-wide step: clusters of kCl CTAs take whole pairs
 // round-robin, and the kCl CTAs of a cluster split each pair's windows.
-//  * Workers (per-warp two-window cp.async rings, as in the grid-wide kernel) compute window
-//    statistics into their CTA's shared memory and arrive, with cluster-scope release, on an
-//    mbarrier of the pair's owner CTA (owners rotate through the cluster).
+//  * Workers (per-warp two-window rings filled by TMA, as in the grid-wide kernel) compute
+//    window statistics into their CTA's shared memory and arrive, with cluster-scope release,
+//    on an mbarrier of the pair's owner CTA (owners rotate through the cluster).
 //  * The owner's segmentation warp reads the pair's statistics from the kCl CTAs through
 //    distributed shared memory in one round, segments the pair, writes the record, stores the
 //    quantiser parameters into every CTA of the cluster and arrives on each CTA's "ready"
@@ -18,7 +18,10 @@
 //  * Workers quantise a pair once its parameters are ready, re-reading its K/V (read a few
 //    microseconds earlier, so from L2; the re-read carries an evict-first hint), and meanwhile
 //    compute statistics of at most kSlots - 1 later pairs: a cluster holds at most kSlots pairs
-//    (3 MB) between first read and re-read, the whole GPU about 100 MB.
+//    (2 MB) between first read and re-read, the whole GPU about 70 MB.
+//  * Twelve workers and one segmentation warp per CTA (127 registers a thread): measured on
+//    this GPU, 12 workers with 2 pair slots took 104 us per layer of the Llama-3-8B batch-32
+//    workload where 10 workers with 3 slots took 120 us.
 //  * Clusters of 4 (not 8): measured on this GPU, only 15 clusters of 8 CTAs fit at once
 //    (120 of 152 SMs), 36 of 4 (144).
 // Every wait is bounded; a timeout records an error in the workspace header and the CTA skips
@@ -33,20 +36,19 @@
 namespace dgq {
 
 constexpr int kCl = 4;                                   // CTAs per cluster
-constexpr int kCWorkers = 10;                            // worker warps per CTA (plus a segmentation warp)
+constexpr int kCWorkers = 12;                            // worker warps per CTA (plus a segmentation warp)
 constexpr int kCThreads = (kCWorkers + 1) * 32;
 constexpr int kCRing = 2;                                // windows in flight per worker
-static_assert(kCRing == 2 || kCRing == 3, "worker loops handle two or three windows in flight");
+static_assert(kCRing == 2, "the worker loop alternates two ring slots");
 constexpr int kCRingBytes = kCWorkers * kCRing * kWinBytes;
-constexpr int kSlots = 3;                                // pairs a cluster holds at once
+constexpr int kSlots = 2;                                // pairs a cluster holds at once
 constexpr int kSlotWin = 64;                             // windows of one pair per CTA
 constexpr int32_t kClusterMaxWin = 256;                  // pairs of at most 256 windows (4096 tokens)
 static_assert(kCl * kSlotWin >= kClusterMaxWin, "a CTA holds its share of the longest pair");
 static_assert(kClusterMaxWin == 8 * 32, "segment_small holds 8 windows per lane");
 
 struct ClusterArgs {
-    const uint16_t *k;
-    const uint16_t *v;
+    TileMaps maps;  // K and V window tiles
     const int32_t *cu;
     const int32_t *bt;
     uint8_t *kpool;
@@ -62,6 +64,7 @@ struct ClusterSmem {
     PairParams par[kSlots];
     uint64_t stats_done[kSlots];  // owner side: arrivals of every worker of the cluster
     uint64_t ready[kSlots];       // parameters of the slot's pair are in par[]
+    uint64_t full[kCWorkers][kCRing];  // a worker's ring slot holds its window
     int32_t abort;
     int32_t pad[3];
 };
@@ -176,14 +179,15 @@ struct PairCursor {
 
 struct CItem {
     int32_t kind;  // 0 statistics, 1 quantisation, 2 nothing to do (after an error)
-    int32_t stage, j, idx, cnt, t0, h, blk;
+    int32_t j, idx, cnt, t0, h, blk, slot;
     bool last;     // statistics: the worker's last window of pair j
     PairCache pc;
 };
 
-__global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterArgs a)
+__global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __grid_constant__ ClusterArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = align_smem_1024(smem_raw);  // window tiles start on 1024-byte boundaries
     ClusterSmem *cs = reinterpret_cast<ClusterSmem *>(smem + kCRingBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t rank = (int32_t)cluster_rank();
@@ -196,6 +200,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
             mbar_init(&cs->stats_done[s], kCl * kCWorkers);
             mbar_init(&cs->ready[s], 1);
         }
+        for (int w = 0; w < kCWorkers; ++w)
+            for (int r = 0; r < kCRing; ++r) mbar_init(&cs->full[w][r], 1);
         cs->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -275,8 +281,9 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
     } else {
         // ================================================================ worker warps
         const uint32_t ring = smem_u32(smem) + warp * (kCRing * kWinBytes);
-        const uint64_t pol_first = make_policy_evict_first();
-        const int64_t rstride = (int64_t)a.Hkv * kD;  // elements between consecutive tokens of a head
+        uint64_t *full = cs->full[warp];
+        const uint64_t pol_stats = make_policy_evict_normal();
+        const uint64_t pol_quant = make_policy_evict_first();  // second read: last use
 
         // position a cursor on pair j (windows lo + warp, + kCWorkers, ...); i >= hi: none here
         auto start_pair = [&](PairCursor &c, int32_t j) {
@@ -299,10 +306,11 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
         start_pair(qc, 0);
         int32_t pc_j = -1;
         PairCache params = {0, 0.0f, 0.0f, 0.0f, 0.0f};
-        int next_stage = 0;
 
-        // Start the copies of the next item; false when nothing may start now.
-        auto try_issue = [&](CItem &it) -> bool {
+        // Choose the next item and start its copy into ring slot `slot`; false when nothing may
+        // start now.
+        auto try_issue = [&](CItem &it, int slot) -> bool {
+            it.slot = slot;
             // quantisation: pairs whose parameters are ready (pairs with no window here are passed
             // once ready, so that their statistics slot may be reused)
             while (qc.j < nj) {
@@ -313,7 +321,6 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
                     continue;
                 }
                 it.kind = ab ? 2 : 1;
-                it.stage = next_stage;
                 it.j = qc.j;
                 it.t0 = qc.i * kWin;
                 it.cnt = min(kWin, qc.L - it.t0);
@@ -325,8 +332,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
                     }
                     it.pc = params;
                     it.blk = __ldg(a.bt + (int64_t)qc.b * a.max_blocks + it.t0 / a.bs);
+                    if (lane == 0) {
+                        fence_proxy_async_smem();  // the slot's earlier reads come before the copy
+                        load_window(ring + slot * kWinBytes, full + slot, a.maps, qc.h, qc.c0 + it.t0, pol_quant);
+                    }
                 }
-                goto issue_copy;
+                qc.i += kCWorkers;
+                return true;
             }
             // statistics: at most kSlots - 1 pairs past the oldest pair still to quantise
             while (sc.j < nj && sc.j < qc.j + kSlots) {
@@ -336,87 +348,80 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
                     continue;
                 }
                 it.kind = 0;
-                it.stage = next_stage;
                 it.j = sc.j;
                 it.idx = sc.i - sc.lo;
                 it.t0 = sc.i * kWin;
                 it.cnt = min(kWin, sc.L - it.t0);
                 it.last = sc.i + kCWorkers >= sc.hi;
-                goto issue_copy;
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    load_window(ring + slot * kWinBytes, full + slot, a.maps, sc.h, sc.c0 + it.t0, pol_stats);
+                }
+                sc.i += kCWorkers;
+                return true;
             }
             return false;
-        issue_copy:
-            if (it.kind != 2) {
-                const PairCursor &c = it.kind == 0 ? sc : qc;
-                const int64_t row0 = ((int64_t)(c.c0 + it.t0) * a.Hkv + c.h) * kD;
-                const uint32_t dst = ring + it.stage * kWinBytes;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 2 * i + (lane >> 4), col = lane & 15;
-                    if (row < it.cnt) {  // rows past the request end are not copied
-                        const uint16_t *ks = a.k + row0 + row * rstride + col * 8;
-                        const uint16_t *vs = a.v + row0 + row * rstride + col * 8;
-                        const uint32_t off = tile_off(row, col);
-                        if (it.kind == 1) {  // second read: last use
-                            cp16_hint(dst + off, ks, pol_first);
-                            cp16_hint(dst + kTileBytes + off, vs, pol_first);
-                        } else {
-                            cp16(dst + off, ks);
-                            cp16(dst + kTileBytes + off, vs);
-                        }
-                    }
-                }
-            }
-            cp_commit();
-            if (++next_stage == kCRing) next_stage = 0;
-            if (it.kind == 0) sc.i += kCWorkers;
-            else qc.i += kCWorkers;
-            return true;
         };
 
-        CItem f0, f1, f2;  // in-flight windows, oldest first (f2 used when kCRing == 3)
-        int nin = 0;
-        uint32_t spins = 0;
-        while (true) {
-            if (nin == 0 && try_issue(f0)) nin = 1;
-            if (nin == 1 && try_issue(f1)) nin = 2;
-            if constexpr (kCRing == 3) {
-                if (nin == 2 && try_issue(f2)) nin = 3;
-            }
-            if (nin == 0) {
-                if (sc.j >= nj && qc.j >= nj) break;
-                if (++spins >= kSpinLimit) {  // waiting for parameters that never came
+        uint32_t phase = 0;  // bit s: parity of ring slot s's next completion
+        // Wait for the window in ring slot `slot` and compute on it.
+        auto process = [&](CItem &it, int slot) {
+            if (it.kind != 2) {
+                if (!mbar_wait_bounded(full + slot, (phase >> slot) & 1u)) {
                     if (lane == 0) {
                         record_error(a.hdr, kErrBarrierWait);
                         st_release_cta_shared(&cs->abort, 1);
                     }
-                    spins = 0;
+                    it.kind = 2;
                 }
-                __nanosleep(32);
+                phase ^= 1u << slot;
+            }
+            const uint32_t kt = ring + slot * kWinBytes, vt = kt + kTileBytes;
+            if (it.kind == 0) {
+                const WinStats s = window_stats(kt, vt, it.cnt);
+                if (lane == 0) {
+                    cs->mean[it.j % kSlots][it.idx] = s.mean;
+                    cs->mm[it.j % kSlots][it.idx] = make_float4(s.kmn, s.kmx, s.vmn, s.vmx);
+                }
+                if (it.last) arrive_stats(it.j);  // after this lane's writes (release, cluster scope)
+            } else if (it.kind == 1) {
+                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
+            }
+            __syncwarp();  // the slot's reads are done before it is refilled
+        };
+
+        // Windows in flight, oldest first: slots are used in turn, so the slot of the next copy
+        // is always the one the oldest window frees.  One inlined copy of process() (the window
+        // arithmetic is long): two copies measured a third more instruction-fetch stalls.
+        CItem f0, f1;
+        int nin = 0, next_slot = 0;
+        uint32_t spins = 0;
+        while (true) {
+            if (nin == 0 && try_issue(f0, next_slot)) {
+                nin = 1;
+                next_slot ^= 1;
+            }
+            if (nin == 1 && try_issue(f1, next_slot)) {
+                nin = 2;
+                next_slot ^= 1;
+            }
+            if (nin > 0) {
+                spins = 0;
+                process(f0, f0.slot);
+                f0 = f1;
+                --nin;
                 continue;
             }
-            spins = 0;
-            if (kCRing == 3 && nin == 3) cp_wait<2>();
-            else if (nin == 2) cp_wait<1>();
-            else cp_wait<0>();
-            __syncwarp();
-            const uint32_t kt = ring + f0.stage * kWinBytes, vt = kt + kTileBytes;
-            if (f0.kind == 0) {
-                const WinStats s = window_stats(kt, vt, f0.cnt);
+            if (sc.j >= nj && qc.j >= nj) break;
+            if (++spins >= kSpinLimit) {  // waiting for parameters that never came
                 if (lane == 0) {
-                    cs->mean[f0.j % kSlots][f0.idx] = s.mean;
-                    cs->mm[f0.j % kSlots][f0.idx] = make_float4(s.kmn, s.kmx, s.vmn, s.vmx);
+                    record_error(a.hdr, kErrBarrierWait);
+                    st_release_cta_shared(&cs->abort, 1);
                 }
-                if (f0.last) arrive_stats(f0.j);  // after this lane's writes (release, cluster scope)
-            } else if (f0.kind == 1) {
-                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, f0.h, f0.t0, f0.cnt, f0.blk, kt, vt, f0.pc);
+                spins = 0;
             }
-            __syncwarp();  // the stage's reads are done before it is refilled
-            f0 = f1;
-            if constexpr (kCRing == 3) f1 = f2;
-            --nin;
+            __nanosleep(32);
         }
-        cp_wait<0>();
     }
     cluster_sync_all();  // no CTA leaves while others may still reach its shared memory
 }
@@ -425,13 +430,12 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(ClusterA
 
 int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 
-cudaError_t launch_compress_cluster(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t Hkv,
-                                    int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+                                    int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
                                     uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream)
 {
     ClusterArgs a;
-    a.k = static_cast<const uint16_t *>(k);
-    a.v = static_cast<const uint16_t *>(v);
+    if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
     a.cu = cu;
     a.bt = bt;
     a.kpool = kpool;
@@ -443,7 +447,7 @@ cudaError_t launch_compress_cluster(const void *k, const void *v, const int32_t 
     a.bs = bs;
     a.max_blocks = max_blocks;
 
-    const size_t smem = (size_t)kCRingBytes + sizeof(ClusterSmem);
+    const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmem);  // + alignment slack
     static int cached_dev = -1, cached_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

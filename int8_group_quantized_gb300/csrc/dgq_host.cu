@@ -93,18 +93,17 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
     if (!workspace || !aligned16(workspace) ||
         workspace_bytes < dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads))
         return DGQ_ERR_WORKSPACE;
-    (void)total_tokens;  // the rows read are those cu_seqlens names, all below total_tokens
     int nsm = 0;
     if (device_sm_count(&nsm) != 0) return DGQ_ERR_CUDA;
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e =
         max_seqlen <= dgq::cluster_compress_max_seqlen()
-            ? dgq::launch_compress_cluster(k_bf16, v_bf16, cu_seqlens_dev, batch, num_kv_heads, block_size,
-                                           block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
-                                           workspace, stream)
-            : dgq::launch_compress(k_bf16, v_bf16, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
-                                   block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table, workspace,
-                                   nsm, stream);
+            ? dgq::launch_compress_cluster(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, num_kv_heads,
+                                           block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool,
+                                           seg_table, workspace, stream)
+            : dgq::launch_compress(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads,
+                                   block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
+                                   workspace, nsm, stream);
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 

@@ -14,16 +14,17 @@ struct CompressLayout {
     size_t off_prog, off_params, off_mean, off_mm, off_agg, total;
 };
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
-cudaError_t launch_compress(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t max_seqlen,
-                            int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                            uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm, cudaStream_t stream);
+cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+                            int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm,
+                            cudaStream_t stream);
 
 // Compression of calls whose requests are all at most cluster_compress_max_seqlen() tokens:
 // pairs segmented inside thread-block clusters (no grid-wide step, no workspace beyond the
 // header).
 int32_t cluster_compress_max_seqlen();
-cudaError_t launch_compress_cluster(const void *k, const void *v, const int32_t *cu, int32_t B, int32_t Hkv,
-                                    int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
+cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+                                    int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
                                     uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream);
 
 struct AttnLayout {

@@ -6,6 +6,7 @@
 
 #include "dgq_device.cuh"
 #include "dgq.h"
+#include "dgq_launch.h"
 
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -113,17 +114,63 @@ __device__ __forceinline__ float bf2_sum(uint32_t w)
     return r;
 }
 
-// Shared-memory tiles hold row r (one token, 16 chunks of 16 bytes) with chunk c stored at
-// position c ^ (r & 15), so that both the row-per-lane reads below and the chunk-per-lane reads
-// of the quantiser touch 8 distinct 16-byte bank groups per quarter-warp.
-__device__ __forceinline__ uint32_t tile_off(int row, int chunk) { return row * (kD * 2) + ((chunk ^ (row & 15)) * 16); }
+// ---- window tiles ----------------------------------------------------------------------------
+//
+// K and V are [T, Hkv, 128] bf16.  A tensor map views each as 4-D (64 elements, 2 halves, Hkv,
+// T), and one copy brings the tile of a window -- 16 tokens of one head -- into shared memory as
+// 32 rows of 128 bytes (row 2t + half) with the 128-byte swizzle: 16-byte chunk c of row r sits
+// at chunk position c ^ (r & 7) (the tile starts on a 1024-byte boundary).  Rows at or past T
+// are filled with zeros; rows of a partial window past its request's end hold the next
+// request's tokens, and every reader masks them.  With this layout the statistics' row reads
+// (eight lanes on eight consecutive rows) and the quantiser's chunk reads (eight lanes on one
+// row) each touch eight distinct 16-byte bank groups per quarter-warp.
+struct TileMaps {
+    CUtensorMap k, v;
+};
+
+// Byte offset of 16-byte chunk `chunk` (0..15) of token t in a tile.
+__device__ __forceinline__ uint32_t tile_off(int t, int chunk)
+{
+    const int r = 2 * t + (chunk >> 3);
+    return (uint32_t)(r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+// Lane 0's copies of one window: K tile at dst, V tile at dst + kTileBytes, both completing on
+// `bar` (one arrival, kWinBytes of transactions).  `pol`: the copies' L2 eviction policy.
+__device__ __forceinline__ void load_window(uint32_t dst, uint64_t *bar, const TileMaps &m, int32_t h, int32_t tok,
+                                            uint64_t pol)
+{
+    mbar_arrive_expect_tx(bar, kWinBytes);
+    tma_load_4d_hint(dst, &m.k, 0, 0, h, tok, smem_u32(bar), pol);
+    tma_load_4d_hint(dst + kTileBytes, &m.v, 0, 0, h, tok, smem_u32(bar), pol);
+}
+
+// Host: the two tensor maps of a call (K and V of T rows); false if the driver refuses them.
+inline bool encode_tile_maps(const void *k, const void *v, int32_t T, int32_t Hkv, TileMaps *m)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {64, 2, (cuuint64_t)Hkv, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[3] = {128, 256, (cuuint64_t)Hkv * 256};  // bytes, dimensions 1..3
+    const cuuint32_t box[4] = {64, 2, 1, kWin};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const void *src[2] = {k, v};
+    CUtensorMap *dst[2] = {&m->k, &m->v};
+    for (int i = 0; i < 2; ++i) {
+        if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src[i]), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
 
 // ---- statistics of one window (one warp, tile in shared memory) --------------------------
 //
-// Lane (t, hh) = (lane & 15, lane >> 4) takes elements [64 hh, 64 hh + 64) of token t.  Its
-// 64-element sum is a balanced tree whose two 32-element halves run side by side in the two
-// fp32 lanes of packed registers; one shuffle adds the other half-row.  This is the balanced
-// pairwise order over the 128 elements, identical in both lanes of the token.
+// Lane (t, hh) = (lane >> 1, lane & 1) takes elements [64 hh, 64 hh + 64) of token t (tile row
+// 2t + hh).  Its 64-element sum is a balanced tree whose two 32-element halves run side by side
+// in the two fp32 lanes of packed registers; one shuffle adds the other half-row.  This is the
+// balanced pairwise order over the 128 elements, identical in both lanes of the token.
 
 struct WinStats {
     float mean, kmn, kmx, vmn, vmx;
@@ -178,15 +225,15 @@ __device__ __forceinline__ float sum64(uint32_t kt, int t, int hh, float centre,
 __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32_t cnt)
 {
     const int lane = threadIdx.x & 31;
-    const int t = lane & 15, hh = lane >> 4;
-    const bool ok = t < cnt;  // rows past the request end hold stale data: masked
+    const int t = lane >> 1, hh = lane & 1;
+    const bool ok = t < cnt;  // rows past the request end hold other data: masked
     __nv_bfloat162 kmn2 = __float2bfloat162_rn(INFINITY), kmx2 = __float2bfloat162_rn(-INFINITY);
     __nv_bfloat162 vmn2 = kmn2, vmx2 = kmx2;
     float s = sum64<false>(kt, t, hh, 0, kmn2, kmx2);
-    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 16));
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
     const float mean = __fmul_rn(s, 0.0078125f);  // exact /128
     float e = sum64<true>(kt, t, hh, mean, kmn2, kmx2);
-    e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 16));
+    e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 1));
 #pragma unroll 2
     for (int j = 0; j < 8; ++j) {
         const uint4 r = ld_shared_v4(vt + tile_off(t, hh * 8 + j));
@@ -200,9 +247,9 @@ __device__ __forceinline__ WinStats window_stats(uint32_t kt, uint32_t vt, int32
     }
     float var = __fmul_rn(e, 0.0078125f);
     var = ok ? var : 0.0f;
-    // window mean: balanced tree over the 16 tokens (lanes t and t + 16 hold the same value)
+    // window mean: balanced tree over the 16 tokens (lanes 2t and 2t + 1 hold the same value)
 #pragma unroll
-    for (int o = 1; o <= 8; o <<= 1) var = __fadd_rn(var, __shfl_xor_sync(0xffffffffu, var, o));
+    for (int o = 2; o <= 16; o <<= 1) var = __fadd_rn(var, __shfl_xor_sync(0xffffffffu, var, o));
     WinStats res;
     res.mean = __fdiv_rn(var, (float)cnt);
     const float kn = ok ? fminf(__low2float(kmn2), __high2float(kmn2)) : INFINITY;
@@ -288,24 +335,6 @@ __device__ __forceinline__ void window_quant(uint8_t *kpool, uint8_t *vpool, int
             __stcs(reinterpret_cast<uint2 *>(vpool + dst0 + tt * kD), encode8(vq, vmn, vinv2));
         }
     }
-}
-
-// ---- cp.async ------------------------------------------------------------------------------
-
-__device__ __forceinline__ void cp16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp16_hint(uint32_t dst, const void *src, uint64_t pol)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- segment parameters ------------------------------------------------------------------

@@ -207,12 +207,28 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
     }
     cluster_sync_all();  // every CTA's barriers exist before any remote arrive
 
-    auto pair_of = [&](int32_t j, PairCursor &c) {
+    // Request offsets of the cluster's pairs, fetched 32 pairs at a time (lane i: pair jb + i) so
+    // that a warp moving to its next pair does not wait for two dependent global loads.
+    struct PairGeo {
+        int32_t jb, c0, L;
+    };
+    auto geo_fetch = [&](PairGeo &g, int32_t jb) {
+        g.jb = jb;
+        g.c0 = 0;
+        g.L = 0;
+        if (jb + lane < nj) {
+            const int32_t b = (clu + (jb + lane) * ncl) / a.Hkv;
+            g.c0 = __ldg(a.cu + b);
+            g.L = __ldg(a.cu + b + 1) - g.c0;
+        }
+    };
+    auto pair_of = [&](int32_t j, PairCursor &c, PairGeo &g) {
+        if (j - g.jb >= 32) geo_fetch(g, j);  // pairs are visited in increasing order
         const int32_t p = clu + j * ncl;
         c.b = p / a.Hkv;
         c.h = p - c.b * a.Hkv;
-        c.c0 = __ldg(a.cu + c.b);
-        c.L = __ldg(a.cu + c.b + 1) - c.c0;
+        c.c0 = __shfl_sync(0xffffffffu, g.c0, j - g.jb);
+        c.L = __shfl_sync(0xffffffffu, g.L, j - g.jb);
         cta_range((c.L + kWin - 1) / kWin, rank, c.lo, c.hi);
     };
     auto aborted = [&]() { return *reinterpret_cast<volatile int32_t *>(&cs->abort) != 0; };
@@ -220,6 +236,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
     if (warp == kCWorkers) {
         // ================================================================ segmentation warp
         // Pairs j = rank, rank + kCl, ... are owned by this CTA.
+        PairGeo geo;
+        geo_fetch(geo, 0);
         for (int32_t q = 0; q * kCl + rank < nj; ++q) {
             const int32_t j = q * kCl + rank;
             const int32_t qs = q % kSlots;
@@ -239,7 +257,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 break;
             }
             PairCursor pc;
-            pair_of(j, pc);
+            pair_of(j, pc, geo);
             const int32_t W = (pc.L + kWin - 1) / kWin;
             const int32_t p = clu + j * ncl;
             const int slot = j % kSlots;
@@ -286,10 +304,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
         const uint64_t pol_quant = make_policy_evict_first();  // second read: last use
 
         // position a cursor on pair j (windows lo + warp, + kCWorkers, ...); i >= hi: none here
-        auto start_pair = [&](PairCursor &c, int32_t j) {
+        PairGeo sgeo, qgeo;  // one per cursor
+        geo_fetch(sgeo, 0);
+        qgeo = sgeo;
+        auto start_pair = [&](PairCursor &c, PairGeo &g, int32_t j) {
             c.j = j;
             if (j < nj) {
-                pair_of(j, c);
+                pair_of(j, c, g);
                 c.i = c.lo + warp;
             }
         };
@@ -302,8 +323,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
         };
 
         PairCursor sc, qc;
-        start_pair(sc, 0);
-        start_pair(qc, 0);
+        start_pair(sc, sgeo, 0);
+        start_pair(qc, qgeo, 0);
         int32_t pc_j = -1;
         PairCache params = {0, 0.0f, 0.0f, 0.0f, 0.0f};
 
@@ -317,7 +338,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 const bool ab = aborted();
                 if (!ab && !test_wait_cluster(&cs->ready[qc.j % kSlots], (uint32_t)(qc.j / kSlots) & 1u)) break;
                 if (qc.i >= qc.hi) {
-                    start_pair(qc, qc.j + 1);
+                    start_pair(qc, qgeo, qc.j + 1);
                     continue;
                 }
                 it.kind = ab ? 2 : 1;
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
             while (sc.j < nj && sc.j < qc.j + kSlots) {
                 if (sc.i >= sc.hi) {  // nothing (more) of this pair for this worker
                     if (sc.i == sc.lo + warp) arrive_stats(sc.j);  // it had no window at all
-                    start_pair(sc, sc.j + 1);
+                    start_pair(sc, sgeo, sc.j + 1);
                     continue;
                 }
                 it.kind = 0;

@@ -76,8 +76,13 @@ def measured_peak():
 
 
 def src_hash(name):
-    with open(os.path.join(ROOT, "int8_group_quantized_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+    """Hash of a kernel's source file and of every shared device header it may include."""
+    csrc = os.path.join(ROOT, "int8_group_quantized_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in [name] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
 
 
 def ncu_traffic(kernel_src, workload_name):

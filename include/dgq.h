@@ -73,7 +73,9 @@ typedef struct dgq_seg_record {
     float k_scale[DGQ_MAX_SEG]; /* (max - min) / 255, or 0 for a flat segment */
     float v_min[DGQ_MAX_SEG];
     float v_scale[DGQ_MAX_SEG];
-    int32_t pad[DGQ_MAX_SEG];   /* zero */
+    float k_inv_last;           /* 255 / (max - min) of the last segment (0 if flat or n_seg == 0): */
+    float v_inv_last;           /*   the encoder's factor, kept so that dgq_append encodes alike */
+    int32_t pad[3];             /* zero */
 } dgq_seg_record;
 
 /* ---------------------------------------------------------------------------------------

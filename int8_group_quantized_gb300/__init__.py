@@ -109,7 +109,7 @@ def seg_record_dtype():
     dt = np.dtype([("n_seg", "<i4"), ("seq_len", "<i4"), ("start", "<i4", (MAX_SEG,)),
                    ("k_min", "<f4", (MAX_SEG,)), ("k_scale", "<f4", (MAX_SEG,)),
                    ("v_min", "<f4", (MAX_SEG,)), ("v_scale", "<f4", (MAX_SEG,)),
-                   ("pad", "<i4", (MAX_SEG,))])
+                   ("k_inv_last", "<f4"), ("v_inv_last", "<f4"), ("pad", "<i4", (3,))])
     assert dt.itemsize == SEG_RECORD_BYTES
     return dt
 

@@ -357,7 +357,6 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
 #pragma unroll
         for (int i = 0; i < kMaxSeg; ++i) {
             rec.start[i] = i == 0 ? 0 : (i <= k ? kWin * cut[i - 1] : L);
-            rec.pad[i] = 0;
             pp.start[i] = rec.start[i];
             if (i < n) {
                 const float kn = canon_zero(kmn[i]), kx = canon_zero(kmx[i]);
@@ -378,6 +377,15 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
         }
         rec.n_seg = n;
         rec.seq_len = L;
+        rec.k_inv_last = rec.v_inv_last = 0.0f;  // the encoder's factors of segment n - 1 = k
+#pragma unroll
+        for (int i = 0; i < kMaxSeg; ++i) {
+            if (i == k) {
+                rec.k_inv_last = pp.k_inv[i];
+                rec.v_inv_last = pp.v_inv[i];
+            }
+        }
+        rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
         pp.n_seg = n;
 #pragma unroll
         for (int i = 0; i < 6; ++i) pp.pad[i] = 0;

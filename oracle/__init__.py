@@ -32,7 +32,9 @@ SEG_DTYPE = np.dtype(
         ("k_scale", "<f4", (MAX_SEG,)),
         ("v_min", "<f4", (MAX_SEG,)),
         ("v_scale", "<f4", (MAX_SEG,)),
-        ("pad", "<i4", (MAX_SEG,)),
+        ("k_inv_last", "<f4"),
+        ("v_inv_last", "<f4"),
+        ("pad", "<i4", (3,)),
     ]
 )
 assert SEG_DTYPE.itemsize == 128
@@ -79,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_dequant_pair.restype = None
         L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
         L.oracle_paged_decode_attn.restype = None
+        L.oracle_append.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P]
+        L.oracle_append.restype = i32
         L.oracle_compress_bytes_written.argtypes = [i32, i32]
         L.oracle_compress_bytes_written.restype = i64
         _lib = L
@@ -146,6 +150,20 @@ def compress(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_block
     lib().oracle_compress(_p(k), _p(v), _p(cu), B, num_kv_heads, block_size, _p(bt), bt.shape[1],
                           _p(kp), _p(vp), _p(table))
     return kp, vp, table
+
+
+def append(k_new, v_new, block_size, block_tables, k_pool, v_pool, table):
+    """One decode step's token per (request, KV head) into the cache, in place.  k_new, v_new:
+    [B, Hkv, 128] uint16; pools [num_blocks, Hkv, bs, 128] uint8; table [B, Hkv] SEG_DTYPE.
+    Returns the number of pairs skipped for want of a block-table column."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    for a in (k_pool, v_pool, table):
+        assert a.flags["C_CONTIGUOUS"]
+    B, Hkv = k_new.shape[0], k_new.shape[1]
+    return int(lib().oracle_append(_p(k_new), _p(v_new), B, Hkv, int(block_size), _p(bt), bt.shape[1],
+                                   _p(k_pool), _p(v_pool), _p(table)))
 
 
 def dequant_pair(pool, table, block_tables, b, h, L, which_v):

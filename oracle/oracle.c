@@ -34,6 +34,9 @@
  *                  bytes written == 1 B/element + one 128-byte record per (request, head)
  *   attention      numpy fp64 brute force; two-key closed form; uniform average for
  *                  equal keys; invariance under any permutation of physical blocks
+ *   append         a first token alone: its min -> 0, max -> 255; in-range values give
+ *                  the codes compress gives them when the segment keeps its min/max;
+ *                  out-of-range values clamp to 0 / 255; flat segments give 0
  */
 #include <math.h>
 #include <stdint.h>
@@ -53,7 +56,9 @@ typedef struct {
     float k_scale[OR_MAX_SEG];
     float v_min[OR_MAX_SEG];
     float v_scale[OR_MAX_SEG];
-    int32_t pad[OR_MAX_SEG];
+    float k_inv_last;            /* 255/(max-min) of the last segment, K and V (0 when flat) */
+    float v_inv_last;
+    int32_t pad[3];
 } oracle_seg;
 
 static float bf16_to_float(uint16_t h)
@@ -238,6 +243,8 @@ void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stri
         rec->v_min[s] = mn;
         segment_affine(mn, mx, &rec->v_scale[s], &v_inv[s]);
     }
+    rec->k_inv_last = k_inv[n - 1];
+    rec->v_inv_last = v_inv[n - 1];
 
     if (k_codes || v_codes) {
         int32_t s = 0;
@@ -285,6 +292,58 @@ void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seq
             free(vc);
         }
     }
+}
+
+/* Decode-step append for one layer: request b's new key and value (one token per
+ * (request, KV head), bf16 [B, Hkv, 128]) go into the cache at position L = the record's
+ * seq_len.  [DGQ] section 2.2 analyses the cache as each new token is generated, but says
+ * nothing about how a token generated after compression is encoded.  READING: the token
+ * joins the last segment and is encoded with that segment's min and 255/(max-min), the
+ * same two IEEE steps as a6, its codes held to [0, 255] (values outside the segment's
+ * range clamp; the segment's parameters, and so every code already stored, stay as they
+ * are).  The boundaries are not revisited: that needs the bf16 history, which the cache no
+ * longer holds.  A request with no token yet (n_seg == 0) gets a first segment made of the
+ * new token alone (a5 over one token).  The record's seq_len, and every start[] entry past
+ * the last segment, become L + 1.  A pair whose slot L has no block-table column
+ * (L / bs >= max_blocks) is left untouched and counted; the return value is that count. */
+int32_t oracle_append(const uint16_t *k_new, const uint16_t *v_new, int32_t B, int32_t Hkv, int32_t bs,
+                      const int32_t *block_tables, int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool,
+                      oracle_seg *table)
+{
+    int32_t skipped = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        for (int32_t h = 0; h < Hkv; ++h) {
+            oracle_seg *rec = &table[(int64_t)b * Hkv + h];
+            const int32_t L = rec->seq_len;
+            if (L / bs >= max_blocks) {
+                ++skipped;
+                continue;
+            }
+            const uint16_t *kx = k_new + ((int64_t)b * Hkv + h) * OR_D;
+            const uint16_t *vx = v_new + ((int64_t)b * Hkv + h) * OR_D;
+            if (rec->n_seg == 0) {
+                float mn, mx;
+                segment_min_max(kx, OR_D, 0, 1, &mn, &mx);
+                rec->k_min[0] = mn;
+                segment_affine(mn, mx, &rec->k_scale[0], &rec->k_inv_last);
+                segment_min_max(vx, OR_D, 0, 1, &mn, &mx);
+                rec->v_min[0] = mn;
+                segment_affine(mn, mx, &rec->v_scale[0], &rec->v_inv_last);
+                rec->n_seg = 1;
+                rec->start[0] = 0;
+            }
+            const int32_t s = rec->n_seg - 1;
+            const int64_t blk = block_tables[(int64_t)b * max_blocks + L / bs];
+            const int64_t dst = ((blk * Hkv + h) * bs + L % bs) * OR_D;
+            for (int d = 0; d < OR_D; ++d) {
+                k_pool[dst + d] = oracle_encode(bf16_to_float(kx[d]), rec->k_min[s], rec->k_inv_last);
+                v_pool[dst + d] = oracle_encode(bf16_to_float(vx[d]), rec->v_min[s], rec->v_inv_last);
+            }
+            rec->seq_len = L + 1;
+            for (int32_t i = rec->n_seg; i < OR_MAX_SEG; ++i) rec->start[i] = L + 1;
+        }
+    }
+    return skipped;
 }
 
 /* Dequantised value of one code, in fp64: min + q * scale. */

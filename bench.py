@@ -30,6 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "INT8 paged decode-attn HBM GB/s (% of peak); dgq_compress GB/s"
 D = 128
 REC = 128  # bytes per segment record
+APPEND_ROOM = 64  # tokens each request may grow by through dgq_append during a run
+APPEND_PAIR_BYTES = 2 * 2 * D + 2 * REC + 4 + 2 * D  # k_new + v_new, record in/out, table entry, codes
 
 
 def parse_args():
@@ -52,6 +54,21 @@ def workload(cfg):
     lens = configs.seq_lens(w)
     bt, nb = configs.block_tables(w, lens)
     return w, lens, bt, nb, configs.cu_seqlens(lens)
+
+
+def with_append_room(bt, nb, lens, bs, room):
+    """The block table widened so that every request can grow by `room` tokens: fresh blocks
+    (ids from nb upward) in the columns past each request's last block."""
+    import numpy as np
+    need = [(int(L) + room + bs - 1) // bs for L in lens]
+    out = np.zeros((bt.shape[0], max(max(need), bt.shape[1])), dtype=np.int32)
+    out[:, :bt.shape[1]] = bt
+    nxt = nb
+    for b, L in enumerate(lens):
+        for j in range((int(L) + bs - 1) // bs, need[b]):
+            out[b, j] = nxt
+            nxt += 1
+    return out, nxt
 
 
 def algorithmic_bytes(w, lens):
@@ -262,6 +279,7 @@ def run_ours(args):
 
     w, lens, bt, nb, cu = workload(args.config)
     B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
+    bt, nb = with_append_room(bt, nb, lens, bs, APPEND_ROOM)
     if args.layers:
         nl = min(nl, args.layers)
     T = int(cu[-1])
@@ -294,6 +312,7 @@ def run_ours(args):
             out=torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)))
     cws = torch.zeros(dgq.dgq_compress_workspace_size(B, max_seqlen, Hkv), dtype=torch.uint8, device=dev)
     aws = torch.zeros(dgq.dgq_attn_workspace_size(B, Hq, Hkv, max_seqlen), dtype=torch.uint8, device=dev)
+    pws = torch.zeros(dgq.dgq_append_workspace_size(), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     def compress_all():
@@ -305,14 +324,19 @@ def run_ours(args):
             dgq.dgq_paged_decode_attn(L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], d_bt, d_lens,
                                       max_seqlen, L["out"], aws, sp)
 
+    def append_all():  # the step's own token of every layer into its cache
+        for L in layers:
+            dgq.dgq_append(L["kn"], L["vn"], bs, d_bt, L["kp"], L["vp"], L["table"], pws, sp)
+
     for _ in range(args.warmup):
         compress_all()
         decode_all()
+        append_all()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, each = compress all layers + decode all layers
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # ---- timed region: K steps, each = compress all layers + decode all layers + append the
+    # step's token to every layer's cache
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -321,21 +345,31 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for e0, e1, e2 in evs:
+    for e0, e1, e2, e3 in evs:
         e0.record(stream)
         compress_all()
         e1.record(stream)
         decode_all()
         e2.record(stream)
+        append_all()
+        e3.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    comp_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in evs)
-    dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in evs)
-    err = dgq.dgq_workspace_error(cws, sp) or dgq.dgq_workspace_error(aws, sp)
+    comp_ms = sum(e0.elapsed_time(e1) for e0, e1, _, _ in evs)
+    dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2, _ in evs)
+    app_ms = sum(e2.elapsed_time(e3) for _, _, e2, e3 in evs)
+    # parity spot check outside the timed region (layer 0 compressed again: the appends above
+    # have grown its records)
+    dgq.dgq_compress(layers[0]["k"], layers[0]["v"], d_cu, max_seqlen, bs, d_bt, layers[0]["kp"],
+                     layers[0]["vp"], layers[0]["table"], cws, sp)
+    torch.cuda.synchronize()
+    checked = spot_check(w, lens, cu, bt, layers[0], rank)
+    err = (dgq.dgq_workspace_error(cws, sp) or dgq.dgq_workspace_error(aws, sp)
+           or dgq.dgq_workspace_error(pws, sp))
 
     dec_b, comp_b = algorithmic_bytes(w, lens)
     dec_b_step, comp_b_step = dec_b * nl, comp_b * nl
@@ -361,6 +395,7 @@ def run_ours(args):
         decode_all()
         for i, L in enumerate(layers):
             h_out[i].copy_(L["out"], non_blocking=True)
+        append_all()
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
@@ -375,10 +410,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
 
-    # ---- parity spot check outside the timed region: one (request, head) of layer 0 vs the oracle
-    checked = spot_check(w, lens, cu, bt, layers[0], rank)
 
-    total_ms, comp_ms, dec_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, e2e_ms], dev, world)
+    total_ms, comp_ms, dec_ms, app_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, app_ms, e2e_ms], dev,
+                                                              world)
 
     if rank == 0:
         K = args.steps
@@ -387,6 +421,8 @@ def run_ours(args):
         peak, peak_src = measured_peak()
         dec_launch_us = dec_ms / (K * nl) * 1e3
         comp_launch_us = comp_ms / (K * nl) * 1e3
+        app_launch_us = app_ms / (K * nl) * 1e3
+        app_b = B * Hkv * APPEND_PAIR_BYTES
         # the library compresses a call whose requests are all at most 4096 tokens with its
         # cluster kernel, longer ones with the grid-wide kernel
         comp_name, comp_src = (("compress_cluster_kernel", "dgq_compress_cluster.cu") if max_seqlen <= 4096
@@ -397,6 +433,9 @@ def run_ours(args):
                             "timed_with": "combine_kernel (merge of split pairs)"},
             comp_name: {"bytes_per_launch": comp_b, "avg_launch_us": round(comp_launch_us, 2),
                         "achieved_gbs": round(comp_b / comp_launch_us / 1e3, 1), "src": comp_src},
+            "append_kernel": {"bytes_per_launch": app_b, "avg_launch_us": round(app_launch_us, 2),
+                              "achieved_gbs": round(app_b / app_launch_us / 1e3, 1), "src": "dgq_append.cu",
+                              "bound": "launch latency (one warp per (request, head) pair)"},
         }
         dom = max(kernels, key=lambda k: kernels[k]["avg_launch_us"])
         ach = kernels[dom]["achieved_gbs"]
@@ -420,8 +459,8 @@ def run_ours(args):
             "e2e": {"value": round(world * dec_b_step / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "what": "decode step via the C ABI: host->device copy of q/k_new/v_new, 32-layer decode, "
-                            "device->host copy of the outputs"},
-            "gpu_launches": 2 * nl * K,
+                            "device->host copy of the outputs, the step's token appended to every layer's cache"},
+            "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
             "device_error": err,
             "parity_spot_check": checked,

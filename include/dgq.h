@@ -190,6 +190,41 @@ dgq_status dgq_paged_decode_attn_noalloc(const void *q_bf16, const void *k_new_b
                                          int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
                                          void *cuda_stream);
 
+/* ---------------------------------------------------------------------------------------
+ * dgq_append -- one decode step's key and value of every (request b, KV head h) written into
+ * the INT8 paged cache at position L = seg_table[b][h].seq_len.
+ *
+ * [DGQ] section 2.2 analyses the cache as each new token is generated but does not say how a
+ * token that arrives after compression is encoded.  Reading taken here: the token joins the
+ * last segment s = n_seg - 1 and each value x is encoded as q = min(max(rint((x - min[s]) *
+ * inv), 0), 255) with inv = k_inv_last / v_inv_last of the record (the compress quantiser's
+ * two IEEE steps; values outside the segment's range clamp, and the segment's min and scale,
+ * hence every code already stored, stay as they are).  Boundaries are not revisited (that
+ * needs the bf16 history); a caller that keeps it can re-run dgq_compress, e.g. when L
+ * crosses an n_groups threshold (2048, 16384).  A record with n_seg == 0 gets a first
+ * segment made of the new token alone (its min/max over the 128 values, as in compress).
+ * The record's seq_len and its start entries past the last segment become L + 1.
+ *
+ * k_new_bf16, v_new_bf16  [batch, Hkv, 128] bf16, device.
+ * block_tables_dev        [batch, max_blocks_per_seq] int32, device: column L / bs of row b
+ *                         names the block that receives token L.  The caller adds a block
+ *                         (e.g. from dgq_pool_alloc) when L is a multiple of block_size.
+ * k_pool, v_pool          [num_blocks, Hkv, block_size, 128] uint8, device: slot L of every
+ *                         pair is written, nothing else.
+ * seg_table               [batch, Hkv] records, device, read and updated in place.
+ * workspace               >= dgq_append_workspace_size() bytes, zero-filled before first use.
+ *                         A pair whose slot has no column (L / bs >= max_blocks_per_seq) is
+ *                         left untouched and flagged there (dgq_workspace_error).
+ * The launch is programmatic-dependent: it may start while the previous kernel on the stream
+ * finishes and waits for it before reading any record.
+ */
+dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                      int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                      dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+size_t dgq_append_workspace_size(void);
+
 /* Zero-fill a workspace (cudaMemsetAsync on the stream). */
 dgq_status dgq_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream);
 

@@ -18,7 +18,8 @@ MAX_SEG = 5
 SEG_RECORD_BYTES = 128
 
 __all__ = [
-    "DGQError", "lib", "dgq_compress", "dgq_compress_workspace_size", "dgq_paged_decode_attn",
+    "DGQError", "lib", "dgq_compress", "dgq_compress_workspace_size", "dgq_append", "dgq_append_workspace_size",
+    "dgq_paged_decode_attn",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -54,6 +55,10 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                     i32, P, P]
         L.dgq_paged_decode_attn_noalloc.restype = ctypes.c_int
+        L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
+        L.dgq_append.restype = ctypes.c_int
+        L.dgq_append_workspace_size.argtypes = []
+        L.dgq_append_workspace_size.restype = sz
         L.dgq_attn_workspace_size.argtypes = [i32, i32, i32, i32]
         L.dgq_attn_workspace_size.restype = sz
         L.dgq_workspace_init.argtypes = [P, sz, P]
@@ -146,6 +151,20 @@ def dgq_compress(k, v, cu_seqlens, max_seqlen, block_size, block_tables, k_pool,
                               int(block_size), _ptr(block_tables), block_tables.shape[1], _ptr(k_pool),
                               _ptr(v_pool), k_pool.shape[0], _ptr(seg_table), _ptr(workspace),
                               _nbytes(workspace), _stream(stream)), "dgq_compress")
+
+
+def dgq_append_workspace_size() -> int:
+    return int(lib().dgq_append_workspace_size())
+
+
+def dgq_append(k_new, v_new, block_size, block_tables, k_pool, v_pool, seg_table, workspace, stream=None) -> None:
+    """k_new, v_new bf16 [B, Hkv, 128]; block_tables int32 [B, max_blocks]; pools uint8
+    [num_blocks, Hkv, bs, 128] and seg_table uint8 [B, Hkv, 128] updated in place; workspace
+    uint8 (dgq_append_workspace_size bytes).  All CUDA tensors."""
+    B, Hkv, D = k_new.shape
+    _check(lib().dgq_append(_ptr(k_new), _ptr(v_new), B, Hkv, D, int(block_size), _ptr(block_tables),
+                            block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table),
+                            _ptr(workspace), _nbytes(workspace), _stream(stream)), "dgq_append")
 
 
 def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens, max_seqlen,

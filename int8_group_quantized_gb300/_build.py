@@ -21,6 +21,7 @@ COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE
 UNITS = {
     "dgq_compress.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_compress_cluster.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
+    "dgq_append.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_attn.cu": [],
     "dgq_host.cu": [],
     "dgq_noalloc.cu": [],

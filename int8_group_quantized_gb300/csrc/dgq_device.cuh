@@ -29,6 +29,7 @@ enum : uint32_t {
                             // too long for its CTA's segmentation
     kErrFullWait = 2,       // decode: a TMA stage never completed
     kErrEmptyWait = 3,      // decode: consumers never released a stage
+    kErrNoBlock = 4,        // append: a pair's next slot has no block-table column
 };
 
 // Upper bound on spin iterations of any wait (each iteration sleeps or polls ~tens of ns;

@@ -107,6 +107,30 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 
+size_t dgq_append_workspace_size(void) { return 256; }  // the workspace header alone
+
+dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                      int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                      dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || batch > kMaxBatch || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX) return DGQ_ERR_UNSUPPORTED;
+    if (!k_new_bf16 || !v_new_bf16 || !block_tables_dev || !k_pool || !v_pool || !seg_table)
+        return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new_bf16) || !aligned16(v_new_bf16) || !aligned16(block_tables_dev) || !aligned16(k_pool) ||
+        !aligned16(v_pool) || !aligned16(seg_table))
+        return DGQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < dgq_append_workspace_size())
+        return DGQ_ERR_WORKSPACE;
+    const cudaError_t e = dgq::launch_append(k_new_bf16, v_new_bf16, batch, num_kv_heads, block_size,
+                                             block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
+                                             workspace, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
 size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seqlen)
 {
     (void)max_seqlen;

@@ -36,6 +36,10 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
                         int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
                         void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
 
+cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
+                          const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
+                          dgq_seg_record *table, void *ws, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query), or null.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

@@ -89,6 +89,26 @@ def test_attn_rejects_bad_arguments_before_launch(L):
     assert _attn(L, batch=-1) == INVALID
 
 
+def _append(L, **kw):
+    a = dict(kn=FAKE, vn=FAKE, batch=2, hkv=2, d=128, bs=16, bt=FAKE, max_blocks=19, kp=FAKE, vp=FAKE, nb=32,
+             table=FAKE, ws=FAKE, wsb=256, stream=0)
+    a.update(kw)
+    return L.dgq_append(a["kn"], a["vn"], a["batch"], a["hkv"], a["d"], a["bs"], a["bt"], a["max_blocks"], a["kp"],
+                        a["vp"], a["nb"], a["table"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_append_rejects_bad_arguments_before_launch(L):
+    assert L.dgq_append_workspace_size() == 256
+    assert _append(L, d=64) == UNSUPPORTED
+    assert _append(L, bs=24) == UNSUPPORTED
+    assert _append(L, kn=0) == INVALID
+    assert _append(L, table=FAKE + 4) == INVALID         # misaligned
+    assert _append(L, batch=0) == INVALID
+    assert _append(L, max_blocks=0) == INVALID
+    assert _append(L, ws=0) == WORKSPACE
+    assert _append(L, wsb=255) == WORKSPACE
+
+
 def test_workspace_size_is_monotone(L):
     a = L.dgq_compress_workspace_size(4, 1000, 8)
     b = L.dgq_compress_workspace_size(4, 2000, 8)

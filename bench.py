@@ -2,7 +2,8 @@
 """Benchmark of the DGQ INT8 paged KV-cache hot path on GB300.
 
 One step = dgq_compress of every layer's K/V (bf16 -> uint8 codes in paged blocks plus
-segment records) followed by dgq_paged_decode_attn over every layer's INT8 cache, for one
+segment records), dgq_paged_decode_attn over every layer's INT8 cache, then dgq_append of the
+step's own key and value into every layer's cache, for one
 synthetic workload (default: the Llama-3-8B-shaped decode batch, 32 layers, 32 requests of
 2048 tokens, Hq 32 / Hkv 8, block size 16).  Inputs are generated on the GPU by the seeded
 generator before timing and stay resident in HBM; each layer has its own buffers, so one

@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
     __syncthreads();
 
     const int32_t Wtot = s_wpre[B];
+    if (blockIdx.x == 0 && tid == 0) a.hdr->path = kPathGrid;
     const int32_t M = (Wtot + kChunk - 1) / kChunk;  // chunks (and quantisation ranges)
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
 

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+    if (blockIdx.x == 0 && tid == 0) a.hdr->path = kPathClusterWhole;
 
     // Request offsets of the cluster's pairs, fetched 32 pairs at a time (lane i: pair jb + i) so
     // that a warp moving to its next pair does not wait for two dependent global loads.

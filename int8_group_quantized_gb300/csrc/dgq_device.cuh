@@ -16,7 +16,7 @@ constexpr int kMaxSeg = 5;  // segments per (request, KV head)
 // Every workspace starts with this 256-byte header.
 struct WsHeader {
     uint32_t error;        // first device-side error code (0 = none)
-    uint32_t reserved;     // zero
+    uint32_t path;         // compress: which kernel path the last call took (kPath*), for tests
     uint32_t done_ctas;    // CTAs finished in the current call (compress)
     uint32_t pad[61];
 };
@@ -31,6 +31,9 @@ enum : uint32_t {
     kErrEmptyWait = 3,      // decode: consumers never released a stage
     kErrNoBlock = 4,        // append: a pair's next slot has no block-table column
 };
+
+// WsHeader::path values
+enum : uint32_t { kPathGrid = 1, kPathClusterWhole = 2 };
 
 // Upper bound on spin iterations of any wait (each iteration sleeps or polls ~tens of ns;
 // ~2^26 iterations is seconds, far beyond any legitimate wait).

@@ -149,3 +149,21 @@ def test_codes_at_rounding_ties():
                     r0 = case.cu[b] + 16 * s
                     arr[r0:r0 + 16, h, :] = vals.reshape(16, 128)
     run(case)
+
+
+PATH_GRID, PATH_CLUSTER = 1, 2
+
+
+def compress_path(case):
+    """Which compress kernel the case's last call ran (word 1 of the workspace header)."""
+    return int(case.d_cws[4:8].cpu().numpy().view(np.uint32)[0])
+
+
+def test_paths_taken():
+    # requests of at most 4096 tokens go to the cluster kernel, longer ones to the grid-wide one
+    short = Case([37, 300, 4096], hq=4, hkv=2, bs=16, seed=35)
+    run(short)
+    assert compress_path(short) == PATH_CLUSTER
+    lng = Case([37, 4097], hq=4, hkv=2, bs=16, seed=36)
+    run(lng)
+    assert compress_path(lng) == PATH_GRID

@@ -7,10 +7,10 @@
 // q = rint((x - min) * (255 / (max - min))).  Codes go to the physical block named by the
 // block table ("PagedAttention implementation", DeepSeek-V4 KV-cache article).
 //
-// GPU design: one persistent cooperative kernel, one CTA per SM: 12 worker warps, an
+// GPU design: one persistent cooperative kernel, one CTA per SM: 10 worker warps, an
 // arrival warp and a segmentation warp.
 //  * The flat list of all 16-token windows of all (request, head) pairs, in (request, head,
-//    window) order, is cut into chunks of kChunk windows (64 MB of bf16 K+V).  Workers
+//    window) order, is cut into chunks of kChunk windows (256 MB of bf16 K+V).  Workers
 //    compute window statistics (variance mean; K and V min/max, also folded into aggregates
 //    of 64 windows with exact order-preserving integer atomics) for their CTA's share of
 //    each chunk.  Quantisation range m holds the pairs whose last window lies in chunk m; it
@@ -19,9 +19,12 @@
 //    chunk's statistics (one release store per CTA and chunk, to a word of its own, so CTAs
 //    may run several chunks apart), and only waits for the other CTAs when it is about to
 //    quantise range m.  Meanwhile its workers keep computing statistics of later chunks, up
-//    to kAhead windows past their quantisation position, so that the K/V read for
-//    statistics are mostly still in the 126 MB L2 when they are read again for
-//    quantisation (those second reads carry an evict-first hint).
+//    to kAhead windows (three chunks) past their quantisation position, so that they keep
+//    streaming while a range is segmented.  Measured on this GPU (one 131072-token request;
+//    64 requests of 128-32768 tokens): 64 MB chunks with a 128 MB lead took 340 / 790 us per
+//    layer, 256 MB chunks with a 768 MB lead 232 / 664 us.  Most second reads then come from
+//    DRAM rather than L2 (they carry an evict-first hint); fewer segmentation stalls matter
+//    more here than L2 reuse.
 //  * Under full HBM load every dependent round trip through L2 costs microseconds, so all
 //    global synchronisation lives in two control warps: the arrival warp publishes the CTA's
 //    progress; the segmentation warp polls the progress words of all CTAs and segments every
@@ -55,8 +58,8 @@ constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
 static_assert(kRing == 2, "the worker loop alternates two ring slots");
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
-constexpr int32_t kChunk = 8192;           // windows per chunk: 64 MB of K+V
-constexpr int32_t kAhead = 16384;          // statistics may lead quantisation by this many windows
+constexpr int32_t kChunk = 32768;          // windows per chunk: 256 MB of K+V
+constexpr int32_t kAhead = 98304;          // statistics may lead quantisation by this many windows
 constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for
 
 struct CompressArgs {

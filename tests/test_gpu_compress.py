@@ -68,6 +68,13 @@ def test_many_pairs_several_chunks_grid_path():
     run(Case(lens, hq=32, hkv=8, bs=16, seed=14))
 
 
+def test_grid_path_many_chunks():
+    # 160 K windows: five 32768-window chunks, pairs of 1250 windows crossing chunk edges
+    case = Case([20000] * 16, hq=8, hkv=8, bs=64, seed=15)
+    run(case)
+    assert compress_path(case) == PATH_GRID
+
+
 def test_repeated_calls_reuse_workspace():
     import torch
     import int8_group_quantized_gb300 as dgq

@@ -71,12 +71,18 @@ def lib() -> ctypes.CDLL:
         L.oracle_window_means.restype = None
         L.oracle_boundaries.argtypes = [P, i32, i32, P]
         L.oracle_boundaries.restype = i32
+        L.oracle_boundaries_ex.argtypes = [P, i32, i32, i32, ctypes.c_float, P]
+        L.oracle_boundaries_ex.restype = i32
         L.oracle_encode.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         L.oracle_encode.restype = ctypes.c_uint8
         L.oracle_compress_pair.argtypes = [P, P, i64, i32, P, P, P]
         L.oracle_compress_pair.restype = None
         L.oracle_compress.argtypes = [P, P, P, i32, i32, i32, P, i32, P, P, P]
         L.oracle_compress.restype = None
+        L.oracle_compress_pair_ex.argtypes = [P, P, i64, i32, i32, ctypes.c_float, P, P, P]
+        L.oracle_compress_pair_ex.restype = None
+        L.oracle_compress_ex.argtypes = [P, P, P, i32, i32, i32, P, i32, i32, ctypes.c_float, P, P, P]
+        L.oracle_compress_ex.restype = None
         L.oracle_dequant_pair.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_int, P]
         L.oracle_dequant_pair.restype = None
         L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
@@ -112,10 +118,10 @@ def window_means(var: np.ndarray) -> np.ndarray:
     return out
 
 
-def boundaries(means: np.ndarray, L: int) -> list[int]:
+def boundaries(means: np.ndarray, L: int, max_groups: int = MAX_SEG, min_var: float = 0.0) -> list[int]:
     means = np.ascontiguousarray(means, dtype=np.float32)
     start = np.zeros(MAX_SEG, dtype=np.int32)
-    n = lib().oracle_boundaries(_p(means), means.shape[0], int(L), _p(start))
+    n = lib().oracle_boundaries_ex(_p(means), means.shape[0], int(L), int(max_groups), float(min_var), _p(start))
     return [int(x) for x in start[:n]]
 
 
@@ -123,7 +129,7 @@ def encode(x: float, mn: float, inv: float) -> int:
     return int(lib().oracle_encode(float(x), float(mn), float(inv)))
 
 
-def compress_pair(k: np.ndarray, v: np.ndarray):
+def compress_pair(k: np.ndarray, v: np.ndarray, max_groups: int = MAX_SEG, min_var: float = 0.0):
     """k, v: [L, 128] bf16 bit patterns (uint16).  Returns (record, k_codes, v_codes)."""
     k = np.ascontiguousarray(k, dtype=np.uint16)
     v = np.ascontiguousarray(v, dtype=np.uint16)
@@ -131,11 +137,12 @@ def compress_pair(k: np.ndarray, v: np.ndarray):
     rec = np.zeros(1, dtype=SEG_DTYPE)
     kc = np.zeros((max(L, 1), D), dtype=np.uint8)
     vc = np.zeros((max(L, 1), D), dtype=np.uint8)
-    lib().oracle_compress_pair(_p(k), _p(v), D, L, _p(rec), _p(kc), _p(vc))
+    lib().oracle_compress_pair_ex(_p(k), _p(v), D, L, int(max_groups), float(min_var), _p(rec), _p(kc), _p(vc))
     return rec[0], kc[:L], vc[:L]
 
 
-def compress(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_blocks, fill=0):
+def compress(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_blocks, fill=0, max_groups=MAX_SEG,
+             min_var=0.0):
     """One layer.  k, v: [T, Hkv, 128] uint16; block_tables [B, max_blocks] int32.
     Returns (k_pool, v_pool, table) with pools [num_blocks, Hkv, bs, 128] uint8 (slots
     the call does not write keep `fill`) and table [B, Hkv] SEG_DTYPE."""
@@ -147,8 +154,8 @@ def compress(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_block
     kp = np.full((num_blocks, num_kv_heads, block_size, D), fill, dtype=np.uint8)
     vp = np.full((num_blocks, num_kv_heads, block_size, D), fill, dtype=np.uint8)
     table = np.zeros((B, num_kv_heads), dtype=SEG_DTYPE)
-    lib().oracle_compress(_p(k), _p(v), _p(cu), B, num_kv_heads, block_size, _p(bt), bt.shape[1],
-                          _p(kp), _p(vp), _p(table))
+    lib().oracle_compress_ex(_p(k), _p(v), _p(cu), B, num_kv_heads, block_size, _p(bt), bt.shape[1],
+                             int(max_groups), float(min_var), _p(kp), _p(vp), _p(table))
     return kp, vp, table
 
 

@@ -34,6 +34,10 @@
  *                  bytes written == 1 B/element + one 128-byte record per (request, head)
  *   attention      numpy fp64 brute force; two-key closed form; uniform average for
  *                  equal keys; invariance under any permutation of physical blocks
+ *   settings       max_groups = 1 gives one segment; a cap gives the top jumps of the uncapped
+ *                  rule; a floor above every window mean gives one segment; planted quiet /
+ *                  loud regions give boundaries only at loud transitions; brute force over
+ *                  the candidate subsets on tiny inputs
  *   append         a first token alone: its min -> 0, max -> 255; in-range values give
  *                  the codes compress gives them when the segment keeps its min/max;
  *                  out-of-range values clamp to 0 / 255; flat segments give 0
@@ -131,9 +135,19 @@ void oracle_window_means(const float *var, int32_t L, float *means)
  * jumps are taken (ties to the earlier window); a boundary after window w starts a
  * segment at token 16(w+1); the count is capped by the W-1 available jumps; zero jumps
  * are still used when fewer nonzero ones exist.  Returns n_seg, writes n_seg starts. */
-int32_t oracle_boundaries(const float *means, int32_t W, int32_t L, int32_t *start)
+/* Group-selection settings, [DGQ] section 5.3 (tuning switches of its vLLM integration):
+ * max_groups caps the number of segments (the article's VLLM_DGQ_MAX_GROUPS; 5 leaves the
+ * length rule alone) and min_var is a variance floor (its VLLM_DGQ_MIN_VAR: "tokens whose
+ * variance is below the threshold go into the same group").  READING of the floor: a window
+ * whose mean variance is below min_var is quiet, and no boundary is placed between two quiet
+ * windows (a jump between a quiet and a louder window is still a candidate); when fewer
+ * candidates than boundaries exist, the pair gets fewer segments.  min_var = 0 changes
+ * nothing (window means are >= 0). */
+int32_t oracle_boundaries_ex(const float *means, int32_t W, int32_t L, int32_t max_groups, float min_var,
+                             int32_t *start)
 {
     int32_t k = oracle_ngroups(L);
+    if (k > max_groups) k = max_groups;
     if (k > W) k = W;
     k -= 1;
     int32_t chosen[OR_MAX_SEG];
@@ -145,11 +159,16 @@ int32_t oracle_boundaries(const float *means, int32_t W, int32_t L, int32_t *sta
             for (int32_t c = 0; c < s; ++c)
                 if (chosen[c] == w) taken = 1;
             if (taken) continue;
+            if (!(means[w] >= min_var || means[w + 1] >= min_var)) continue; /* both quiet */
             float jump = fabsf(means[w + 1] - means[w]);
             if (best < 0 || jump > best_jump) { /* strict: earlier window wins ties */
                 best = w;
                 best_jump = jump;
             }
+        }
+        if (best < 0) { /* no candidate left */
+            k = s;
+            break;
         }
         chosen[s] = best;
     }
@@ -165,6 +184,11 @@ int32_t oracle_boundaries(const float *means, int32_t W, int32_t L, int32_t *sta
         start[j + 1] = v;
     }
     return k + 1;
+}
+
+int32_t oracle_boundaries(const float *means, int32_t W, int32_t L, int32_t *start)
+{
+    return oracle_boundaries_ex(means, W, L, OR_MAX_SEG, 0.0f, start);
 }
 
 /* a5. fp32 min and max over all tokens x D of one segment, [DGQ] §2.2 ("each segment
@@ -212,8 +236,9 @@ uint8_t oracle_encode(float x, float mn, float inv)
 
 /* Compress one (request, KV head): L rows of K and V (bf16, rows `row_stride` elements
  * apart).  Fills the record and, when non-null, the unpaged codes [L, 128]. */
-void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stride, int32_t L,
-                          oracle_seg *rec, uint8_t *k_codes, uint8_t *v_codes)
+void oracle_compress_pair_ex(const uint16_t *k, const uint16_t *v, int64_t row_stride, int32_t L,
+                             int32_t max_groups, float min_var, oracle_seg *rec, uint8_t *k_codes,
+                             uint8_t *v_codes)
 {
     memset(rec, 0, sizeof *rec);
     rec->seq_len = L;
@@ -230,7 +255,7 @@ void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stri
     /* READING: one segmentation per (request, KV head), derived from K and shared by K
      * and V (the article derives the segments from K, and its storage formula counts a
      * single marker bit per layer x head x token), with separate min/scale for K and V. */
-    int32_t n = oracle_boundaries(means, W, L, rec->start);
+    int32_t n = oracle_boundaries_ex(means, W, L, max_groups, min_var, rec->start);
     rec->n_seg = n;
 
     for (int32_t s = 0; s < n; ++s) {
@@ -270,9 +295,16 @@ void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stri
  * "PagedAttention implementation" (logical block -> physical block).  Slots past the
  * sequence end in its last block are left untouched.  Pools are [num_blocks, Hkv, bs, 128]
  * uint8, the record table [B, Hkv]. */
-void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
-                     int32_t B, int32_t Hkv, int32_t bs, const int32_t *block_tables,
-                     int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool, oracle_seg *table)
+void oracle_compress_pair(const uint16_t *k, const uint16_t *v, int64_t row_stride, int32_t L,
+                          oracle_seg *rec, uint8_t *k_codes, uint8_t *v_codes)
+{
+    oracle_compress_pair_ex(k, v, row_stride, L, OR_MAX_SEG, 0.0f, rec, k_codes, v_codes);
+}
+
+void oracle_compress_ex(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                        int32_t B, int32_t Hkv, int32_t bs, const int32_t *block_tables,
+                        int32_t max_blocks, int32_t max_groups, float min_var, uint8_t *k_pool,
+                        uint8_t *v_pool, oracle_seg *table)
 {
     for (int32_t b = 0; b < B; ++b) {
         int32_t L = cu_seqlens[b + 1] - cu_seqlens[b];
@@ -281,7 +313,8 @@ void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seq
             uint8_t *kc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
             uint8_t *vc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
             oracle_seg *rec = &table[(int64_t)b * Hkv + h];
-            oracle_compress_pair(k + row0, v + row0, (int64_t)Hkv * OR_D, L, rec, kc, vc);
+            oracle_compress_pair_ex(k + row0, v + row0, (int64_t)Hkv * OR_D, L, max_groups, min_var, rec, kc,
+                                    vc);
             for (int32_t t = 0; t < L; ++t) {
                 int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
                 int64_t dst = ((blk * Hkv + h) * bs + t % bs) * OR_D;
@@ -292,6 +325,14 @@ void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seq
             free(vc);
         }
     }
+}
+
+void oracle_compress(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                     int32_t B, int32_t Hkv, int32_t bs, const int32_t *block_tables,
+                     int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool, oracle_seg *table)
+{
+    oracle_compress_ex(k, v, cu_seqlens, B, Hkv, bs, block_tables, max_blocks, OR_MAX_SEG, 0.0f, k_pool, v_pool,
+                       table);
 }
 
 /* Decode-step append for one layer: request b's new key and value (one token per

@@ -121,6 +121,31 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
 
 size_t dgq_compress_workspace_size(int32_t batch, int32_t max_seqlen, int32_t num_kv_heads);
 
+/*
+ * Group-selection settings, [DGQ] section 5.3 (tuning switches of the article's vLLM
+ * integration: a maximum group count, and a variance threshold below which tokens share a
+ * group).
+ *   max_groups  1..5: at most this many segments per (request, KV head): n_groups becomes
+ *               min(n_groups(L), max_groups).  5 leaves the length rule alone.
+ *   min_var     >= 0, finite: a window whose mean variance is below min_var is quiet, and no
+ *               boundary is placed between two quiet windows (a jump between a quiet and a
+ *               louder window is still a candidate); with fewer candidates than boundaries the
+ *               pair gets fewer segments.  0 changes nothing (window means are >= 0).
+ */
+typedef struct dgq_compress_options {
+    int32_t max_groups;
+    float min_var;
+} dgq_compress_options;
+
+/* dgq_compress with explicit settings; options == NULL is { 5, 0.0f }, i.e. dgq_compress.
+ * Settings outside the ranges above: DGQ_ERR_INVALID_ARG. */
+dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                           const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                           int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool,
+                           int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                           size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream);
+
 /* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
  * paged cache plus the step's own (unquantised) key and value.

@@ -47,6 +47,9 @@ def lib() -> ctypes.CDLL:
         L.dgq_status_str.restype = ctypes.c_char_p
         L.dgq_compress.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
         L.dgq_compress.restype = ctypes.c_int
+        L.dgq_compress_ex.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz,
+                                      ctypes.POINTER(CompressOptions), P]
+        L.dgq_compress_ex.restype = ctypes.c_int
         L.dgq_compress_workspace_size.argtypes = [i32, i32, i32]
         L.dgq_compress_workspace_size.restype = sz
         L.dgq_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -140,17 +143,27 @@ def dgq_workspace_error(workspace, stream=None) -> int:
     return int(code.value)
 
 
+class CompressOptions(ctypes.Structure):
+    """dgq_compress_options: group-selection settings (segment cap 1..5, variance floor >= 0)."""
+    _fields_ = [("max_groups", ctypes.c_int32), ("min_var", ctypes.c_float)]
+
+
 def dgq_compress(k, v, cu_seqlens, max_seqlen, block_size, block_tables, k_pool, v_pool, seg_table,
-                 workspace, stream=None) -> None:
+                 workspace, stream=None, max_groups=MAX_SEG, min_var=0.0) -> None:
     """k, v: bf16 [T, Hkv, 128]; cu_seqlens int32 [B+1]; block_tables int32 [B, max_blocks];
     k_pool, v_pool uint8 [num_blocks, Hkv, bs, 128]; seg_table uint8 [B, Hkv, 128] (records);
-    workspace uint8 (dgq_compress_workspace_size bytes).  All CUDA tensors."""
+    workspace uint8 (dgq_compress_workspace_size bytes).  All CUDA tensors.  max_groups /
+    min_var: group-selection settings (dgq_compress_ex); the defaults are the plain method."""
     B = cu_seqlens.shape[0] - 1
     Hkv = k.shape[1]
-    _check(lib().dgq_compress(_ptr(k), _ptr(v), k.shape[0], _ptr(cu_seqlens), B, int(max_seqlen), Hkv, k.shape[2],
-                              int(block_size), _ptr(block_tables), block_tables.shape[1], _ptr(k_pool),
-                              _ptr(v_pool), k_pool.shape[0], _ptr(seg_table), _ptr(workspace),
-                              _nbytes(workspace), _stream(stream)), "dgq_compress")
+    args = (_ptr(k), _ptr(v), k.shape[0], _ptr(cu_seqlens), B, int(max_seqlen), Hkv, k.shape[2], int(block_size),
+            _ptr(block_tables), block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table),
+            _ptr(workspace), _nbytes(workspace))
+    if max_groups == MAX_SEG and min_var == 0.0:
+        _check(lib().dgq_compress(*args, _stream(stream)), "dgq_compress")
+    else:
+        opts = CompressOptions(int(max_groups), float(min_var))
+        _check(lib().dgq_compress_ex(*args, ctypes.byref(opts), _stream(stream)), "dgq_compress_ex")
 
 
 def dgq_append_workspace_size() -> int:

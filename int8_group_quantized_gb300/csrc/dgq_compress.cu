@@ -76,6 +76,8 @@ struct CompressArgs {
     float4 *win_mm;
     uint4 *agg;  // per 64 flat windows: ~enc(k min), enc(k max), ~enc(v min), enc(v max); 0 = empty
     int32_t B, Hkv, bs, max_blocks, cap;
+    int32_t max_groups;  // group-selection settings
+    float min_var;
 };
 
 // ---- window decomposition ------------------------------------------------------------------
@@ -140,11 +142,14 @@ __device__ __forceinline__ float ord_dec(uint32_t e)
 
 // ---- segmentation of one pair (one warp; all of the pair's statistics are visible) ---------
 
+// kFloor: the variance floor is set (a.min_var > 0); without it every jump is a candidate and
+// the test is compiled out of the candidate loops, which are on the critical path of long pairs.
+template <bool kFloor>
 __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int32_t L, int32_t W, int32_t wbase,
                                           PairParams *dst, bool write_record)
 {
     const int lane = threadIdx.x & 31;
-    const int32_t k = min(ngroups(L), W) - 1;  // boundaries to place (0..4)
+    int32_t k = min(min(ngroups(L), a.max_groups), W) - 1;  // boundaries to place (0..4)
 
     // (1) per-lane top-k of (jump desc, window asc); the jump of window w < W-1 is
     // |m[w+1] - m[w]|.  A pair of at most 256 windows is read in one round (lane i holds windows
@@ -171,7 +176,9 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
         for (int i = 0; i < 8; ++i) {
             const int32_t w = 8 * lane + i;
             if (k == 0 || w + 1 >= W) continue;
-            const float j = fabsf(__fsub_rn(i < 7 ? m[i + 1] : mnext, m[i]));
+            const float mn1 = i < 7 ? m[i + 1] : mnext;
+            if (kFloor && !(m[i] >= a.min_var || mn1 >= a.min_var)) continue;  // two quiet windows stay together
+            const float j = fabsf(__fsub_rn(mn1, m[i]));
             // a lane meets its windows in increasing order, so an equal jump keeps the earlier
             // window ahead of it
             if (j > cj[3]) {
@@ -210,6 +217,7 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
                 for (int e = 0; e < 4; ++e) {
                     const int32_t w = 4 * q + e - wbase;  // window within the pair
                     if (q > q1 || w < 0 || w + 1 >= W) continue;
+                    if (kFloor && !(m5[e] >= a.min_var || m5[e + 1] >= a.min_var)) continue;  // two quiet windows
                     const float j = fabsf(__fsub_rn(m5[e + 1], m5[e]));
                     // a lane meets its windows in increasing order, so an equal jump keeps the
                     // earlier window ahead of it
@@ -243,6 +251,10 @@ __device__ __noinline__ void segment_pair(const CompressArgs &a, int32_t p, int3
                 j = oj;
                 wv = ow;
             }
+        }
+        if (j < 0.0f) {  // no candidate left (same in every lane)
+            k = r;
+            break;
         }
         if (bw == wv) {  // a window sits in one lane only, so exactly one lane matches
             cj[0] = cj[1]; cj[1] = cj[2]; cj[2] = cj[3]; cj[3] = -1.0f;
@@ -586,7 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
                 int32_t w = qlo, slot = 0;
                 while (true) {
                     const int32_t wbase = w - l.wi;
-                    segment_pair(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
+                    if (a.min_var > 0.0f)
+                        segment_pair<true>(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
+                    else
+                        segment_pair<false>(a, l.b * a.Hkv + l.h, l.L, l.W, wbase, out + slot, wbase >= qlo);
                     ++slot;
                     w = wbase + l.W;
                     if (w >= qhi) break;
@@ -819,8 +834,8 @@ static size_t compress_smem_bytes(int32_t B)
 
 cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm,
-                            cudaStream_t stream)
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
+                            int nsm, cudaStream_t stream)
 {
     if (nsm > kMaxSms) return cudaErrorInvalidConfiguration;
     const CompressLayout l = compress_layout(B, max_seqlen, Hkv);
@@ -843,6 +858,8 @@ cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32
     a.bs = bs;
     a.max_blocks = max_blocks;
     a.cap = params_cap(max_seqlen, nsm);
+    a.max_groups = gs.max_groups;
+    a.min_var = gs.min_var;
 
     // per-device launch set-up, done once per (device, shared-memory size)
     static int cached_dev = -1;

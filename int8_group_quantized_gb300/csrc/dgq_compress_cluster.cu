@@ -56,6 +56,8 @@ struct ClusterArgs {
     dgq_seg_record *table;
     WsHeader *hdr;
     int32_t B, Hkv, bs, max_blocks;
+    int32_t max_groups;  // group-selection settings
+    float min_var;
 };
 
 struct ClusterSmem {
@@ -280,10 +282,10 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                         mm[i] = ld_remote_f4(map_rank(&cs->mm[slot][idx], (uint32_t)r));
                     }
                 }
-                const int k = min(ngroups(pc.L), W) - 1;
+                int k = min(min(ngroups(pc.L), a.max_groups), W) - 1;
                 int32_t cut[4];
                 float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
-                segment_small(W, k, m, mm, cut, kmn, kmx, vmn, vmx);
+                k = segment_small(W, k, a.min_var, m, mm, cut, kmn, kmx, vmn, vmx);
                 make_params(pc.L, k, cut, kmn, kmx, vmn, vmx, rec, pp);  // same values in every lane
             }
             if (lane == 0) a.table[p] = rec;
@@ -454,7 +456,8 @@ int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 
 cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                                     int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                                    uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream)
+                                    uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
+                                    cudaStream_t stream)
 {
     ClusterArgs a;
     if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
@@ -468,6 +471,8 @@ cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, con
     a.Hkv = Hkv;
     a.bs = bs;
     a.max_blocks = max_blocks;
+    a.max_groups = gs.max_groups;
+    a.min_var = gs.min_var;
 
     const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmem);  // + alignment slack
     static int cached_dev = -1, cached_clusters = 0;

@@ -76,6 +76,26 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
                         uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
                         size_t workspace_bytes, void *cuda_stream)
 {
+    return dgq_compress_ex(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, head_dim,
+                           block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table,
+                           workspace, workspace_bytes, nullptr, cuda_stream);
+}
+
+dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                           const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                           int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                           dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes,
+                           const dgq_compress_options *options, void *cuda_stream)
+{
+    dgq::GroupSettings gs = {DGQ_MAX_SEG, 0.0f};
+    if (options) {
+        if (options->max_groups < 1 || options->max_groups > DGQ_MAX_SEG || !(options->min_var >= 0.0f) ||
+            !(options->min_var <= 3.4e38f))
+            return DGQ_ERR_INVALID_ARG;
+        gs.max_groups = options->max_groups;
+        gs.min_var = options->min_var;
+    }
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
     if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || total_tokens < 0)
@@ -100,10 +120,10 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
         max_seqlen <= dgq::cluster_compress_max_seqlen()
             ? dgq::launch_compress_cluster(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, num_kv_heads,
                                            block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool,
-                                           seg_table, workspace, stream)
+                                           seg_table, workspace, gs, stream)
             : dgq::launch_compress(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads,
                                    block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
-                                   workspace, nsm, stream);
+                                   workspace, gs, nsm, stream);
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 

@@ -10,14 +10,20 @@
 
 namespace dgq {
 
+// Group-selection settings passed to both compress kernels (see dgq_compress_options).
+struct GroupSettings {
+    int32_t max_groups;
+    float min_var;
+};
+
 struct CompressLayout {
     size_t off_prog, off_params, off_mean, off_mm, off_agg, total;
 };
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
 cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, int nsm,
-                            cudaStream_t stream);
+                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
+                            int nsm, cudaStream_t stream);
 
 // Compression of calls whose requests are all at most cluster_compress_max_seqlen() tokens:
 // pairs segmented inside thread-block clusters (no grid-wide step, no workspace beyond the
@@ -25,7 +31,8 @@ cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32
 int32_t cluster_compress_max_seqlen();
 cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                                     int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                                    uint8_t *vpool, dgq_seg_record *table, void *ws, cudaStream_t stream);
+                                    uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
+                                    cudaStream_t stream);
 
 struct AttnLayout {
     size_t off_count, off_part, total;

@@ -385,10 +385,12 @@ __device__ __forceinline__ void make_params(int32_t L, int k, const int32_t (&cu
 
 // Segmentation of a pair of at most 256 windows held by one warp, lane i owning windows
 // 8i .. 8i+7 (means m[], extremes mm[] as K min, K max, V min, V max; unused slots hold the
-// identities).  Returns the segment starts and the per-segment extremes, identical in every lane.
-__device__ __forceinline__ void segment_small(int32_t W, int k, const float (&m)[8], const float4 (&mm)[8],
-                                              int32_t (&cut)[4], float (&kmn)[kMaxSeg], float (&kmx)[kMaxSeg],
-                                              float (&vmn)[kMaxSeg], float (&vmx)[kMaxSeg])
+// identities).  At most k boundaries; a jump between two windows whose means are both below
+// min_var is no candidate.  Returns the number of boundaries placed and fills the segment
+// starts and the per-segment extremes, identical in every lane.
+__device__ __forceinline__ int segment_small(int32_t W, int k, float min_var, const float (&m)[8],
+                                             const float4 (&mm)[8], int32_t (&cut)[4], float (&kmn)[kMaxSeg],
+                                             float (&kmx)[kMaxSeg], float (&vmn)[kMaxSeg], float (&vmx)[kMaxSeg])
 {
     const int lane = threadIdx.x & 31;
     // per-lane top-k of (jump desc, window asc); the jump of window w < W-1 is |m[w+1] - m[w]|
@@ -399,7 +401,9 @@ __device__ __forceinline__ void segment_small(int32_t W, int k, const float (&m)
     for (int i = 0; i < 8; ++i) {
         const int32_t w = 8 * lane + i;
         if (k == 0 || w + 1 >= W) continue;
-        const float j = fabsf(__fsub_rn(i < 7 ? m[i + 1] : mnext, m[i]));
+        const float mn1 = i < 7 ? m[i + 1] : mnext;
+        if (!(m[i] >= min_var || mn1 >= min_var)) continue;  // two quiet windows stay together
+        const float j = fabsf(__fsub_rn(mn1, m[i]));
         // a lane meets its windows in increasing order: an equal jump keeps the earlier window first
         if (j > cj[3]) {
             cj[3] = j;
@@ -429,6 +433,10 @@ __device__ __forceinline__ void segment_small(int32_t W, int k, const float (&m)
                 j = oj;
                 wv = ow;
             }
+        }
+        if (j < 0.0f) {  // no candidate left (same in every lane)
+            k = r;
+            break;
         }
         if (bw == wv) {  // a window sits in one lane only
             cj[0] = cj[1]; cj[1] = cj[2]; cj[2] = cj[3]; cj[3] = -1.0f;
@@ -466,6 +474,7 @@ __device__ __forceinline__ void segment_small(int32_t W, int k, const float (&m)
         kmn[s] = warp_min(kmn[s]); kmx[s] = warp_max(kmx[s]);
         vmn[s] = warp_min(vmn[s]); vmx[s] = warp_max(vmx[s]);
     }
+    return k;
 }
 
 }  // namespace dgq

@@ -44,14 +44,15 @@ class Case:
         self.max_seqlen = int(max(1, self.lens.max()))
 
     # ---- oracle -------------------------------------------------------------------------
-    def oracle_compress(self):
-        return oracle.compress(self.k, self.v, self.cu, self.hkv, self.bs, self.bt, self.num_blocks)
+    def oracle_compress(self, max_groups=oracle.MAX_SEG, min_var=0.0):
+        return oracle.compress(self.k, self.v, self.cu, self.hkv, self.bs, self.bt, self.num_blocks,
+                               max_groups=max_groups, min_var=min_var)
 
     def oracle_attn(self, kp, vp, table):
         return oracle.paged_decode_attn(self.q, self.knew, self.vnew, kp, vp, table, self.bt, self.lens)
 
     # ---- CUDA path ---------------------------------------------------------------------------
-    def gpu_compress(self, fill=0):
+    def gpu_compress(self, fill=0, max_groups=oracle.MAX_SEG, min_var=0.0):
         import torch
         import int8_group_quantized_gb300 as dgq
         dev = torch.device("cuda:0")
@@ -70,7 +71,7 @@ class Case:
         wsz = dgq.dgq_compress_workspace_size(self.B, self.max_seqlen, self.hkv)
         self.d_cws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
         dgq.dgq_compress(self.d_k, self.d_v, self.d_cu, self.max_seqlen, self.bs, self.d_bt, self.d_kp,
-                         self.d_vp, self.d_table, self.d_cws)
+                         self.d_vp, self.d_table, self.d_cws, max_groups=max_groups, min_var=min_var)
         torch.cuda.synchronize()
         assert dgq.dgq_workspace_error(self.d_cws) == 0
 

@@ -69,6 +69,19 @@ def test_compress_rejects_bad_arguments_before_launch(L):
     assert _compress(L, wsb=need - 1) == WORKSPACE
 
 
+def test_compress_ex_rejects_bad_settings(L):
+    import ctypes
+    from int8_group_quantized_gb300 import CompressOptions
+    L.dgq_compress_ex.restype = ctypes.c_int
+
+    def call(mg, mv):
+        o = CompressOptions(mg, mv)
+        return L.dgq_compress_ex(FAKE, FAKE, 300, FAKE, 2, 300, 2, 128, 16, FAKE, 19, FAKE, FAKE, 64, FAKE, FAKE,
+                                 1 << 30, ctypes.byref(o), None)
+    for mg, mv in ((0, 0.0), (6, 0.0), (-1, 0.0), (3, -0.5), (3, float("nan")), (3, float("inf"))):
+        assert call(mg, mv) == INVALID, (mg, mv)
+
+
 def _attn(L, **kw):
     a = dict(q=FAKE, kn=FAKE, vn=FAKE, kp=FAKE, vp=FAKE, table=FAKE, bt=FAKE, lens=FAKE, max_seqlen=300,
              batch=2, hq=4, hkv=2, d=128, bs=16, max_blocks=19, nb=32, out=FAKE, ws=FAKE, wsb=1 << 30, stream=0)

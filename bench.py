@@ -369,6 +369,9 @@ def run_ours(args):
                      layers[0]["vp"], layers[0]["table"], cws, sp)
     torch.cuda.synchronize()
     checked = spot_check(w, lens, cu, bt, layers[0], rank)
+    # segment counts of layer 0's (request, head) pairs, as the article's per-layer debug output
+    n_seg = layers[0]["table"][:, :, 0:4].contiguous().view(torch.int32).cpu().numpy().ravel()
+    seg_hist = {int(k): int(c) for k, c in zip(*np.unique(n_seg, return_counts=True))}
     err = (dgq.dgq_workspace_error(cws, sp) or dgq.dgq_workspace_error(aws, sp)
            or dgq.dgq_workspace_error(pws, sp))
 
@@ -461,6 +464,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "what": "decode step via the C ABI: host->device copy of q/k_new/v_new, 32-layer decode, "
                             "device->host copy of the outputs, the step's token appended to every layer's cache"},
+            "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
             "device_error": err,

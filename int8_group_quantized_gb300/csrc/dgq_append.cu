@@ -36,7 +36,7 @@ struct AppendArgs {
     uint8_t *vpool;
     uint32_t *table;     // records as words
     WsHeader *hdr;
-    int32_t pairs, Hkv, bs, max_blocks;
+    int32_t pairs, Hkv, bs, max_blocks, num_blocks;
 };
 
 __device__ __forceinline__ float bf_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_kernel(AppendA
         return;
     }
     const int32_t blk = __ldg(a.bt + (int64_t)b * a.max_blocks + L / a.bs);
+    if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged, untouched
+        if (lane == 0) record_error(a.hdr, kErrBadBlock);
+        return;
+    }
     const uint2 kw = __ldg(a.k_new + (int64_t)pair * 32 + lane);
     const uint2 vw = __ldg(a.v_new + (int64_t)pair * 32 + lane);
     const float kx[4] = {bf_lo_f(kw.x), bf_hi_f(kw.x), bf_lo_f(kw.y), bf_hi_f(kw.y)};
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_kernel(AppendA
 }
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
-                          const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
+                          const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
                           dgq_seg_record *table, void *ws, cudaStream_t stream)
 {
     AppendArgs a;
@@ -155,6 +159,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32
     a.Hkv = Hkv;
     a.bs = bs;
     a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -68,7 +68,7 @@ struct AttnArgs {
     WsHeader *hdr;
     int2 *pair_info;  // per pair: first and last CTA holding a piece of it
     float *part;
-    int32_t B, Hq, Hkv, G, bs, max_blocks;
+    int32_t B, Hq, Hkv, G, bs, max_blocks, num_blocks;
 };
 
 // Token order inside each 8-column n-tile: column n holds token tau(n).  With it, the K row a
@@ -249,7 +249,14 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         mbar_init(&pbar[1], 1);
         fence_barrier_init();
     }
-    for (int i = tid; i < B; i += kAttnThreads) s_len[i] = __ldg(a.seq_lens + i);
+    for (int i = tid; i < B; i += kAttnThreads) {
+        int32_t L = __ldg(a.seq_lens + i);
+        if (L < 0 || L > a.max_blocks * a.bs) {  // beyond the block table's row: flagged, clamped
+            record_error(a.hdr, kErrBadLength);
+            L = L < 0 ? 0 : a.max_blocks * a.bs;
+        }
+        s_len[i] = L;
+    }
     __syncthreads();
     if (warp == 0) {  // exclusive scan of Hkv * tiles_of(L_b)
         int32_t carry = 0;
@@ -323,6 +330,10 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         if (k < nmine) {
             const TileLoc c = locate_tile(xw0 + kWarpsPerCta * k, s_tpre, s_len, B);
             if (c.L > 0) blk = __ldg(a.bt + (int64_t)c.b * a.max_blocks + c.j / per_blk);
+            if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged,
+                record_error(a.hdr, kErrBadBlock);          // and block 0 read instead
+                blk = 0;
+            }
         }
         return blk;
     };
@@ -748,7 +759,6 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
                         int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
                         void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
 {
-    (void)num_blocks;
     *map_failed = false;
     const int32_t G = Hq / Hkv;
     AttnLayout l = attn_layout(B, Hq, Hkv, nsm);
@@ -772,6 +782,7 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.G = G;
     a.bs = bs;
     a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
 
     // per-device launch shape, computed once per (device, shared-memory size)
     static int cached_dev = -1;

@@ -76,6 +76,7 @@ struct CompressArgs {
     float4 *win_mm;
     uint4 *agg;  // per 64 flat windows: ~enc(k min), enc(k max), ~enc(v min), enc(v max); 0 = empty
     int32_t B, Hkv, bs, max_blocks, cap;
+    int32_t max_seqlen, num_blocks;  // for the device-side checks of lengths and block ids
     int32_t max_groups;  // group-selection settings
     float min_var;
 };
@@ -459,10 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
 
     if (warp == 0) {  // exclusive scan of Hkv * ceil(L_b / 16)
         int32_t carry = 0;
+        bool bad = false;  // a length outside [0, max_seqlen]: the workspace was sized for less
         for (int base = 0; base < B; base += 32) {
             const int i = base + lane;
             int32_t v = 0;
-            if (i < B) v = a.Hkv * ((__ldg(a.cu + i + 1) - __ldg(a.cu + i) + kWin - 1) / kWin);
+            if (i < B) {
+                const int32_t L = __ldg(a.cu + i + 1) - __ldg(a.cu + i);
+                bad |= L < 0 || L > a.max_seqlen;
+                v = a.Hkv * ((max(0, min(L, a.max_seqlen)) + kWin - 1) / kWin);
+            }
             int32_t x = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -473,6 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
             carry += __shfl_sync(0xffffffffu, x, 31);
         }
         if (lane == 0) s_wpre[B] = carry;
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            ctl->last = bad ? 1 : 0;  // read after the barrier below, reset before any other use
+            if (bad) record_error(a.hdr, kErrBadLength);
+        }
     }
     if (tid >= 32 && tid < 32 + kWorkers) {
         ctl->stats_done[tid - 32] = 0;
@@ -481,13 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
     if (tid == 32) {
         ctl->ready[0] = ctl->ready[1] = 0;
         ctl->abort = 0;
-        ctl->last = 0;
         for (int w = 0; w < kWorkers; ++w)
             for (int r = 0; r < kRing; ++r) mbar_init(&ctl->full[w][r], 1);
         fence_barrier_init();
     }
     __syncthreads();
 
+    // every CTA read the same lengths: all leave here together, before any grid-wide step
+    if (ctl->last) return;
+    __syncthreads();  // the check above is read by every thread before the word is reused
+    if (tid == 0) ctl->last = 0;
     const int32_t Wtot = s_wpre[B];
     if (blockIdx.x == 0 && tid == 0) a.hdr->path = kPathGrid;
     const int32_t M = (Wtot + kChunk - 1) / kChunk;  // chunks (and quantisation ranges)
@@ -731,7 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
                     atomicMax(g + 3, ord_enc(s.vmx));
                 }
             } else if (it.kind == 1) {
-                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
+                if ((uint32_t)it.blk < (uint32_t)a.num_blocks)
+                    window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
+                else if (lane == 0)  // not a block of the pools: flagged, nothing written
+                    record_error(a.hdr, kErrBadBlock);
             }
             __syncwarp();  // the slot's reads are done before it is refilled
             if (lane == 0 && it.next_m != it.m) {
@@ -834,8 +851,8 @@ static size_t compress_smem_bytes(int32_t B)
 
 cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
-                            int nsm, cudaStream_t stream)
+                            uint8_t *kpool, uint8_t *vpool, int32_t num_blocks, dgq_seg_record *table, void *ws,
+                            GroupSettings gs, int nsm, cudaStream_t stream)
 {
     if (nsm > kMaxSms) return cudaErrorInvalidConfiguration;
     const CompressLayout l = compress_layout(B, max_seqlen, Hkv);
@@ -858,6 +875,8 @@ cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32
     a.bs = bs;
     a.max_blocks = max_blocks;
     a.cap = params_cap(max_seqlen, nsm);
+    a.max_seqlen = max_seqlen;
+    a.num_blocks = num_blocks;
     a.max_groups = gs.max_groups;
     a.min_var = gs.min_var;
 

@@ -58,6 +58,7 @@ struct ClusterArgs {
     int32_t B, Hkv, bs, max_blocks;
     int32_t max_groups;  // group-selection settings
     float min_var;
+    int32_t max_seqlen, num_blocks;  // for the device-side checks of lengths and block ids
 };
 
 struct ClusterSmem {
@@ -232,6 +233,10 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
         c.h = p - c.b * a.Hkv;
         c.c0 = __shfl_sync(0xffffffffu, g.c0, j - g.jb);
         c.L = __shfl_sync(0xffffffffu, g.L, j - g.jb);
+        if (c.L < 0 || c.L > a.max_seqlen) {  // longer than the call's sizes allow: flagged, skipped
+            if (lane == 0) record_error(a.hdr, kErrBadLength);
+            c.L = 0;
+        }
         cta_range((c.L + kWin - 1) / kWin, rank, c.lo, c.hi);
     };
     auto aborted = [&]() { return *reinterpret_cast<volatile int32_t *>(&cs->abort) != 0; };
@@ -409,7 +414,10 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 }
                 if (it.last) arrive_stats(it.j);  // after this lane's writes (release, cluster scope)
             } else if (it.kind == 1) {
-                window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
+                if ((uint32_t)it.blk < (uint32_t)a.num_blocks)
+                    window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
+                else if (lane == 0)  // not a block of the pools: flagged, nothing written
+                    record_error(a.hdr, kErrBadBlock);
             }
             __syncwarp();  // the slot's reads are done before it is refilled
         };
@@ -455,9 +463,9 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
 int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 
 cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
-                                    int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                                    uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
-                                    cudaStream_t stream)
+                                    int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt,
+                                    int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
+                                    dgq_seg_record *table, void *ws, GroupSettings gs, cudaStream_t stream)
 {
     ClusterArgs a;
     if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
@@ -473,6 +481,8 @@ cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, con
     a.max_blocks = max_blocks;
     a.max_groups = gs.max_groups;
     a.min_var = gs.min_var;
+    a.max_seqlen = max_seqlen;
+    a.num_blocks = num_blocks;
 
     const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmem);  // + alignment slack
     static int cached_dev = -1, cached_clusters = 0;

@@ -30,6 +30,8 @@ enum : uint32_t {
     kErrFullWait = 2,       // decode: a TMA stage never completed
     kErrEmptyWait = 3,      // decode: consumers never released a stage
     kErrNoBlock = 4,        // append: a pair's next slot has no block-table column
+    kErrBadBlock = 5,       // a block-table entry outside [0, num_blocks): its window/tile skipped
+    kErrBadLength = 6,      // a request length outside what the call's sizes allow: clamped or skipped
 };
 
 // WsHeader::path values

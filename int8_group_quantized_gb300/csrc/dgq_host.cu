@@ -118,12 +118,12 @@ dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e =
         max_seqlen <= dgq::cluster_compress_max_seqlen()
-            ? dgq::launch_compress_cluster(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, num_kv_heads,
-                                           block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool,
-                                           seg_table, workspace, gs, stream)
+            ? dgq::launch_compress_cluster(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen,
+                                           num_kv_heads, block_size, block_tables_dev, max_blocks_per_seq, k_pool,
+                                           v_pool, num_blocks, seg_table, workspace, gs, stream)
             : dgq::launch_compress(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads,
-                                   block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
-                                   workspace, gs, nsm, stream);
+                                   block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
+                                   seg_table, workspace, gs, nsm, stream);
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 
@@ -146,8 +146,8 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
     if (!workspace || !aligned16(workspace) || workspace_bytes < dgq_append_workspace_size())
         return DGQ_ERR_WORKSPACE;
     const cudaError_t e = dgq::launch_append(k_new_bf16, v_new_bf16, batch, num_kv_heads, block_size,
-                                             block_tables_dev, max_blocks_per_seq, k_pool, v_pool, seg_table,
-                                             workspace, static_cast<cudaStream_t>(cuda_stream));
+                                             block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
+                                             seg_table, workspace, static_cast<cudaStream_t>(cuda_stream));
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 

@@ -22,17 +22,17 @@ struct CompressLayout {
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
 cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
-                            uint8_t *kpool, uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
-                            int nsm, cudaStream_t stream);
+                            uint8_t *kpool, uint8_t *vpool, int32_t num_blocks, dgq_seg_record *table, void *ws,
+                            GroupSettings gs, int nsm, cudaStream_t stream);
 
 // Compression of calls whose requests are all at most cluster_compress_max_seqlen() tokens:
 // pairs segmented inside thread-block clusters (no grid-wide step, no workspace beyond the
 // header).
 int32_t cluster_compress_max_seqlen();
 cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
-                                    int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks, uint8_t *kpool,
-                                    uint8_t *vpool, dgq_seg_record *table, void *ws, GroupSettings gs,
-                                    cudaStream_t stream);
+                                    int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt,
+                                    int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
+                                    dgq_seg_record *table, void *ws, GroupSettings gs, cudaStream_t stream);
 
 struct AttnLayout {
     size_t off_count, off_part, total;
@@ -44,7 +44,7 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
                         void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
-                          const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
+                          const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
                           dgq_seg_record *table, void *ws, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query), or null.

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_paged_decode_attn.restype = None
         L.oracle_append.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P]
         L.oracle_append.restype = i32
+        L.oracle_decode_attn_unquantised.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P]
+        L.oracle_decode_attn_unquantised.restype = None
         L.oracle_compress_bytes_written.argtypes = [i32, i32]
         L.oracle_compress_bytes_written.restype = i64
         _lib = L
@@ -199,6 +201,25 @@ def paged_decode_attn(q, k_new, v_new, k_pool, v_pool, table, block_tables, seq_
     out = np.zeros((B, Hq, D), dtype=np.float64)
     lib().oracle_paged_decode_attn(_p(q), _p(kn), _p(vn), _p(kp), _p(vp), _p(table), _p(bt),
                                    _p(sl), B, Hq, Hkv, bs, bt.shape[1], _p(out))
+    return out
+
+
+def decode_attn_unquantised(q, k_new, v_new, k, v, cu_seqlens, seq_lens):
+    """fp64 decode attention over the original bf16 K/V (packed [T, Hkv, 128] uint16, request b
+    on rows cu_seqlens[b] ..), for the fidelity of the compressed cache."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kn = np.ascontiguousarray(k_new, dtype=np.uint16)
+    vn = np.ascontiguousarray(v_new, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq = q.shape[0], q.shape[1]
+    Hkv = kn.shape[1]
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lib().oracle_decode_attn_unquantised(_p(q), _p(kn), _p(vn), _p(k if k.size else np.zeros(1, np.uint16)),
+                                         _p(v if v.size else np.zeros(1, np.uint16)), _p(cu), _p(sl), B, Hq, Hkv,
+                                         _p(out))
     return out
 
 

@@ -38,6 +38,8 @@
  *                  rule; a floor above every window mean gives one segment; planted quiet /
  *                  loud regions give boundaries only at loud transitions; brute force over
  *                  the candidate subsets on tiny inputs
+ *   unquantised    attention over the raw bf16 rows equals the paged attention over a
+ *                  cache whose values are all exactly representable; numpy fp64 brute force
  *   append         a first token alone: its min -> 0, max -> 255; in-range values give
  *                  the codes compress gives them when the segment keeps its min/max;
  *                  out-of-range values clamp to 0 / 255; flat segments give 0
@@ -477,6 +479,51 @@ void oracle_paged_decode_attn(const uint16_t *q, const uint16_t *k_new, const ui
             {
                 const uint16_t *vn = v_new + ((int64_t)b * Hkv + h) * OR_D;
                 for (int d = 0; d < OR_D; ++d) o[d] += s[L] * (double)bf16_to_float(vn[d]);
+            }
+            double *dst = out + ((int64_t)b * Hq + hq) * OR_D;
+            for (int d = 0; d < OR_D; ++d) dst[d] = o[d] / l;
+        }
+        free(s);
+    }
+}
+
+/* Fidelity context: the same decode-step attention (a8-a10 in fp64) over the original,
+ * unquantised bf16 keys and values, packed [T, Hkv, 128] with request b on rows
+ * cu_seqlens[b] .. cu_seqlens[b] + seq_lens[b] - 1.  Comparing it with the attention over the
+ * compressed cache shows the error the INT8 encoding itself introduces. */
+void oracle_decode_attn_unquantised(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                                    const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                                    const int32_t *seq_lens, int32_t B, int32_t Hq, int32_t Hkv, double *out)
+{
+    const int32_t G = Hq / Hkv;
+    const double inv_sqrt_d = 1.0 / sqrt((double)OR_D);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t L = seq_lens[b];
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        for (int32_t hq = 0; hq < Hq; ++hq) {
+            const int32_t h = hq / G;
+            const uint16_t *qv = q + ((int64_t)b * Hq + hq) * OR_D;
+            for (int32_t t = 0; t <= L; ++t) {
+                const uint16_t *kr = t < L ? k + (((int64_t)cu_seqlens[b] + t) * Hkv + h) * OR_D
+                                           : k_new + ((int64_t)b * Hkv + h) * OR_D;
+                double acc = 0.0;
+                for (int d = 0; d < OR_D; ++d) acc += (double)bf16_to_float(qv[d]) * (double)bf16_to_float(kr[d]);
+                s[t] = acc * inv_sqrt_d;
+            }
+            double m = s[0];
+            for (int32_t t = 1; t <= L; ++t)
+                if (s[t] > m) m = s[t];
+            double l = 0.0;
+            for (int32_t t = 0; t <= L; ++t) {
+                s[t] = exp(s[t] - m);
+                l += s[t];
+            }
+            double o[OR_D];
+            for (int d = 0; d < OR_D; ++d) o[d] = 0.0;
+            for (int32_t t = 0; t <= L; ++t) {
+                const uint16_t *vr = t < L ? v + (((int64_t)cu_seqlens[b] + t) * Hkv + h) * OR_D
+                                           : v_new + ((int64_t)b * Hkv + h) * OR_D;
+                for (int d = 0; d < OR_D; ++d) o[d] += s[t] * (double)bf16_to_float(vr[d]);
             }
             double *dst = out + ((int64_t)b * Hq + hq) * OR_D;
             for (int d = 0; d < OR_D; ++d) dst[d] = o[d] / l;

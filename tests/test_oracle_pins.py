@@ -427,3 +427,49 @@ def test_gqa_equals_mha_with_duplicated_kv_heads():
                                        np.ascontiguousarray(vp[:, idx]),
                                        np.ascontiguousarray(table[:, idx]), bt, lens)
     assert np.array_equal(out, out_mha)
+
+
+# --- fidelity context: attention over the unquantised bf16 K/V ------------------------------
+
+def test_unquantised_attention_matches_numpy_brute_force():
+    rng = np.random.default_rng(21)
+    lens = np.array([3, 0, 9], dtype=np.int32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    B, Hq, Hkv = 3, 4, 2
+    k = bf16_bits(rng.standard_normal((cu[-1], Hkv, D)).astype(np.float32))
+    v = bf16_bits(rng.standard_normal((cu[-1], Hkv, D)).astype(np.float32))
+    q = bf16_bits(rng.standard_normal((B, Hq, D)).astype(np.float32))
+    kn = bf16_bits(rng.standard_normal((B, Hkv, D)).astype(np.float32))
+    vn = bf16_bits(rng.standard_normal((B, Hkv, D)).astype(np.float32))
+    got = oracle.decode_attn_unquantised(q, kn, vn, k, v, cu, lens)
+    f = lambda a: bf16_float(a).astype(np.float64)
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // (Hq // Hkv)
+            keys = np.concatenate([f(k[cu[b]:cu[b + 1], h]), f(kn[b, h])[None]])
+            vals = np.concatenate([f(v[cu[b]:cu[b + 1], h]), f(vn[b, h])[None]])
+            s = keys @ f(q[b, hq]) / math.sqrt(D)
+            p = np.exp(s - s.max())
+            want = (p[:, None] * vals).sum(0) / p.sum()
+            assert np.allclose(got[b, hq], want, rtol=1e-12, atol=1e-12)
+
+
+def test_unquantised_attention_equals_cache_attention_when_codes_are_exact():
+    # every value on the grid q / 16 with 0 and 255 / 16 in each segment: scale = 1/16 and
+    # inv = 16 exactly, so every code decodes to its value and the two attentions coincide
+    rng = np.random.default_rng(22)
+    L, Hkv, Hq, bs = 40, 1, 2, 16
+    grid = rng.integers(0, 256, (L, Hkv, D)).astype(np.float32) / 16
+    grid[:, :, 0], grid[:, :, 1] = 0.0, 255 / 16
+    k = bf16_bits(grid)
+    v = bf16_bits(grid[::-1].copy())
+    cu = np.array([0, L], dtype=np.int32)
+    bt = np.array([[2, 0, 1]], dtype=np.int32)
+    kp, vp, table = oracle.compress(k, v, cu, Hkv, bs, bt, 3)
+    assert np.all(table["k_scale"][0, 0][:table["n_seg"][0, 0]] == np.float32(1 / 16))
+    q = bf16_bits(rng.standard_normal((1, Hq, D)).astype(np.float32) * 0.2)
+    kn = bf16_bits(rng.standard_normal((1, Hkv, D)).astype(np.float32))
+    lens = np.array([L], dtype=np.int32)
+    cache = oracle.paged_decode_attn(q, kn, kn, kp, vp, table, bt, lens)
+    raw = oracle.decode_attn_unquantised(q, kn, kn, k, v, cu, lens)
+    assert np.array_equal(cache, raw)

@@ -415,6 +415,8 @@ def run_ours(args):
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
 
 
+    fidelity = fidelity_check(w, lens, layers[0], rank)
+
     total_ms, comp_ms, dec_ms, app_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, app_ms, e2e_ms], dev,
                                                               world)
 
@@ -465,6 +467,7 @@ def run_ours(args):
                     "what": "decode step via the C ABI: host->device copy of q/k_new/v_new, 32-layer decode, "
                             "device->host copy of the outputs, the step's token appended to every layer's cache"},
             "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
+            "fidelity": fidelity,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
             "device_error": err,
@@ -501,6 +504,49 @@ def spot_check(w, lens, cu, bt, layer0, rank):
     gk = kp[bt[0, t // w.block_size], 0, t % w.block_size]
     grec = layer0["table"][0, 0].cpu().numpy().tobytes()
     return bool(np.array_equal(gk, kc) and grec == rec.tobytes())
+
+
+def fidelity_check(w, lens, layer0, rank):
+    """Request 0 of layer 0, all query heads: the GPU's decode output against fp64 attention over
+    the unquantised bf16 K/V (the encoding's error, reported as context) and against the oracle's
+    fp64 attention over its own compressed cache (the kernel's error)."""
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    import synth
+    L = int(lens[0])
+    k = np.zeros((L, w.hkv, D), dtype=np.uint16)
+    v = np.zeros((L, w.hkv, D), dtype=np.uint16)
+    for h in range(w.hkv):
+        n, st, sg = synth.spans(w.seed, 0, 0, h, L, w.rule)
+        k[:, h] = synth.fill_pair(w.seed, synth.STREAM_K, 0, 0, h, L, n, st, sg)
+        v[:, h] = synth.fill_pair(w.seed, synth.STREAM_V, 0, 0, h, L, n, st, sg)
+    q = layer0["q"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    kn = layer0["kn"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    vn = layer0["vn"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    got = layer0["out"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    got = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    cu = np.array([0, L], dtype=np.int32)
+    lens1 = np.array([L], dtype=np.int32)
+    raw = oracle.decode_attn_unquantised(q, kn, vn, k, v, cu, lens1)
+    nb = (L + w.block_size - 1) // w.block_size
+    bt = np.arange(nb, dtype=np.int32)[None]
+    kp, vp, table = oracle.compress(k, v, cu, w.hkv, w.block_size, bt, nb)
+    cache = oracle.paged_decode_attn(q, kn, vn, kp, vp, table, bt, lens1)
+
+    def err(a, b):
+        d = np.abs(a - b)
+        return {"max_abs": float(f"{d.max():.3e}"), "mean_abs": float(f"{d.mean():.3e}")}
+    return {"gpu_vs_unquantised": err(got, raw), "dgq_fp64_vs_unquantised": err(cache, raw),
+            "gpu_vs_oracle": err(got, cache),
+            "sample": f"request 0 ({L} tokens), all {w.hq} query heads, layer 0; unquantised = fp64 "
+                      "attention over the original bf16 K/V"}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
 
 
 def main():

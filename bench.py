@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged-input", action="store_true",
+                    help="compress from a bf16 paged cache (dgq_compress_paged) instead of packed rows")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (profiling captures; 0 = all of the workload's layers)")
     return ap.parse_args()
@@ -311,6 +313,16 @@ def run_ours(args):
             vp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
             table=torch.zeros((B, Hkv, REC), dtype=torch.uint8, device=dev),
             out=torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)))
+    if args.paged_input:  # the same tokens in a bf16 paged cache laid out like the INT8 pools
+        tok_blk = torch.from_numpy(np.concatenate(
+            [bt[b, np.arange(int(L)) // bs] for b, L in enumerate(lens)]).astype(np.int64)).to(dev)
+        tok_slot = torch.from_numpy(np.concatenate(
+            [np.arange(int(L)) % bs for L in lens]).astype(np.int64)).to(dev)
+        for L in layers:
+            for name in ("k", "v"):
+                src = torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+                src[tok_blk, :, tok_slot, :] = L[name]
+                L[name + "_src"] = src
     cws = torch.zeros(dgq.dgq_compress_workspace_size(B, max_seqlen, Hkv), dtype=torch.uint8, device=dev)
     aws = torch.zeros(dgq.dgq_attn_workspace_size(B, Hq, Hkv, max_seqlen), dtype=torch.uint8, device=dev)
     pws = torch.zeros(dgq.dgq_append_workspace_size(), dtype=torch.uint8, device=dev)
@@ -318,7 +330,11 @@ def run_ours(args):
 
     def compress_all():
         for L in layers:
-            dgq.dgq_compress(L["k"], L["v"], d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"], cws, sp)
+            if args.paged_input:
+                dgq.dgq_compress_paged(L["k_src"], L["v_src"], d_bt, d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"],
+                                       L["table"], cws, sp)
+            else:
+                dgq.dgq_compress(L["k"], L["v"], d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"], cws, sp)
 
     def decode_all():
         for L in layers:
@@ -454,6 +470,7 @@ def run_ours(args):
             "config": {"workload": w.name, "layers": nl, "batch": B, "q_heads": Hq, "kv_heads": Hkv,
                        "head_dim": D, "block_size": bs, "seq_len": int(max_seqlen) if len(set(lens.tolist())) == 1
                        else f"{int(lens.min())}..{int(lens.max())}", "parallelism": f"replicas x{world}",
+                       "compress_source": "bf16 paged cache" if args.paged_input else "packed bf16 rows",
                        "l2": "inputs larger than L2 (each layer has its own buffers; one step reads "
                              f"{(dec_b_step + comp_b_step) / 1e9:.1f} GB)"},
             "decode_frac_of_peak": round(dec_gbs / world / peak, 4),

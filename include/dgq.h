@@ -147,6 +147,30 @@ dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total
                            size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dgq_compress_paged -- dgq_compress reading K and V straight from a bf16 paged cache (the
+ * layout a serving engine keeps them in after prefill, [PAGED] "PagedAttention implementation"),
+ * so they need not be gathered into packed rows first: one read of the bf16 cache per pass and
+ * no extra copy.  Same computation and outputs as dgq_compress_ex on the gathered rows.
+ *
+ * k_src_bf16, v_src_bf16  [num_src_blocks, Hkv, block_size, 128] bf16, device: token t of
+ *                         request b, head h is row src[src_block_tables[b][t / bs]][h][t % bs].
+ * src_block_tables_dev    [batch, max_src_blocks_per_seq] int32, device; max_seqlen <=
+ *                         max_src_blocks_per_seq * block_size.  An entry outside
+ *                         [0, num_src_blocks) is flagged in the workspace (block 0 read instead).
+ * cu_seqlens_dev          [batch+1] int32, device: lengths only (L_b = cu[b+1] - cu[b]); no
+ *                         packed rows are read.
+ * The destination (block_size, block tables, pools, records), workspace and options are those
+ * of dgq_compress_ex; source and destination use the same block_size.
+ */
+dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                              const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                              const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                              uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                              size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream);
+
+/* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
  * paged cache plus the step's own (unquantised) key and value.
  *

@@ -18,7 +18,8 @@ MAX_SEG = 5
 SEG_RECORD_BYTES = 128
 
 __all__ = [
-    "DGQError", "lib", "dgq_compress", "dgq_compress_workspace_size", "dgq_append", "dgq_append_workspace_size",
+    "DGQError", "lib", "dgq_compress", "dgq_compress_paged", "dgq_compress_workspace_size", "dgq_append",
+    "dgq_append_workspace_size",
     "dgq_paged_decode_attn",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
@@ -50,6 +51,9 @@ def lib() -> ctypes.CDLL:
         L.dgq_compress_ex.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz,
                                       ctypes.POINTER(CompressOptions), P]
         L.dgq_compress_ex.restype = ctypes.c_int
+        L.dgq_compress_paged.argtypes = [P, P, i32, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz,
+                                         ctypes.POINTER(CompressOptions), P]
+        L.dgq_compress_paged.restype = ctypes.c_int
         L.dgq_compress_workspace_size.argtypes = [i32, i32, i32]
         L.dgq_compress_workspace_size.restype = sz
         L.dgq_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -178,6 +182,20 @@ def dgq_append(k_new, v_new, block_size, block_tables, k_pool, v_pool, seg_table
     _check(lib().dgq_append(_ptr(k_new), _ptr(v_new), B, Hkv, D, int(block_size), _ptr(block_tables),
                             block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table),
                             _ptr(workspace), _nbytes(workspace), _stream(stream)), "dgq_append")
+
+
+def dgq_compress_paged(k_src, v_src, src_block_tables, cu_seqlens, max_seqlen, block_size, block_tables, k_pool,
+                       v_pool, seg_table, workspace, stream=None, max_groups=MAX_SEG, min_var=0.0) -> None:
+    """k_src, v_src: bf16 paged cache [num_src_blocks, Hkv, bs, 128]; src_block_tables int32
+    [B, max_src_blocks]; cu_seqlens int32 [B+1] (lengths only); the rest as dgq_compress."""
+    B = cu_seqlens.shape[0] - 1
+    Hkv = k_src.shape[1]
+    opts = CompressOptions(int(max_groups), float(min_var))
+    _check(lib().dgq_compress_paged(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(src_block_tables),
+                                    src_block_tables.shape[1], _ptr(cu_seqlens), B, int(max_seqlen), Hkv,
+                                    k_src.shape[3], int(block_size), _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table), _ptr(workspace),
+                                    _nbytes(workspace), ctypes.byref(opts), _stream(stream)), "dgq_compress_paged")
 
 
 def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens, max_seqlen,

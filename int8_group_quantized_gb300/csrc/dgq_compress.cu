@@ -63,7 +63,7 @@ constexpr int32_t kAhead = 98304;          // statistics may lead quantisation b
 constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for
 
 struct CompressArgs {
-    TileMaps maps;  // K and V window tiles
+    TileSource src;  // where the K and V window tiles come from
     const int32_t *cu;
     const int32_t *bt;
     uint8_t *kpool;
@@ -708,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
             it.cnt = min(kWin, l.L - it.t0);
             if (it.kind != 2 && lane == 0) {
                 fence_proxy_async_smem();  // the slot's earlier reads come before the copy
-                load_window(ring + slot * kWinBytes, full + slot, a.maps, l.h, l.c0 + it.t0,
-                            it.kind == 1 ? pol_quant : pol_stats);
+                load_window(ring + slot * kWinBytes, full + slot, a.src, l.b, l.h, l.c0, it.t0,
+                            it.kind == 1 ? pol_quant : pol_stats, a.hdr);
             }
             if (it.kind == 0) {
                 advance(sc, false);
@@ -849,7 +849,7 @@ static size_t compress_smem_bytes(int32_t B)
     return 1024 + (size_t)kRingBytes + sizeof(CtaCtl) + (size_t)(B + 1) * 4;
 }
 
-cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+cudaError_t launch_compress(const SourceDesc &src, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
                             uint8_t *kpool, uint8_t *vpool, int32_t num_blocks, dgq_seg_record *table, void *ws,
                             GroupSettings gs, int nsm, cudaStream_t stream)
@@ -858,7 +858,7 @@ cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32
     const CompressLayout l = compress_layout(B, max_seqlen, Hkv);
     char *base = static_cast<char *>(ws);
     CompressArgs a;
-    if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
+    if (!encode_tile_source(src, Hkv, bs, &a.src)) return cudaErrorInvalidValue;
     a.cu = cu;
     a.bt = bt;
     a.kpool = kpool;

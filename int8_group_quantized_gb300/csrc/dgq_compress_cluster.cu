@@ -48,7 +48,7 @@ static_assert(kCl * kSlotWin >= kClusterMaxWin, "a CTA holds its share of the lo
 static_assert(kClusterMaxWin == 8 * 32, "segment_small holds 8 windows per lane");
 
 struct ClusterArgs {
-    TileMaps maps;  // K and V window tiles
+    TileSource src;  // where the K and V window tiles come from
     const int32_t *cu;
     const int32_t *bt;
     uint8_t *kpool;
@@ -363,7 +363,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                     it.blk = __ldg(a.bt + (int64_t)qc.b * a.max_blocks + it.t0 / a.bs);
                     if (lane == 0) {
                         fence_proxy_async_smem();  // the slot's earlier reads come before the copy
-                        load_window(ring + slot * kWinBytes, full + slot, a.maps, qc.h, qc.c0 + it.t0, pol_quant);
+                        load_window(ring + slot * kWinBytes, full + slot, a.src, qc.b, qc.h, qc.c0, it.t0,
+                                    pol_quant, a.hdr);
                     }
                 }
                 qc.i += kCWorkers;
@@ -384,7 +385,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 it.last = sc.i + kCWorkers >= sc.hi;
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    load_window(ring + slot * kWinBytes, full + slot, a.maps, sc.h, sc.c0 + it.t0, pol_stats);
+                    load_window(ring + slot * kWinBytes, full + slot, a.src, sc.b, sc.h, sc.c0, it.t0, pol_stats,
+                                a.hdr);
                 }
                 sc.i += kCWorkers;
                 return true;
@@ -462,13 +464,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
 
 int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 
-cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+cudaError_t launch_compress_cluster(const SourceDesc &src, const int32_t *cu, int32_t B,
                                     int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt,
                                     int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
                                     dgq_seg_record *table, void *ws, GroupSettings gs, cudaStream_t stream)
 {
     ClusterArgs a;
-    if (!encode_tile_maps(k, v, T, Hkv, &a.maps)) return cudaErrorInvalidValue;
+    if (!encode_tile_source(src, Hkv, bs, &a.src)) return cudaErrorInvalidValue;
     a.cu = cu;
     a.bt = bt;
     a.kpool = kpool;

@@ -198,6 +198,17 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 5-D tile copy to a 32-bit shared address, with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, int32_t c4, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Orders this thread's earlier shared-memory accesses before later async-proxy (TMA) ones.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {

@@ -81,12 +81,14 @@ dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_to
                            workspace, workspace_bytes, nullptr, cuda_stream);
 }
 
-dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
-                           const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
-                           int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
-                           int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
-                           dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes,
-                           const dgq_compress_options *options, void *cuda_stream)
+namespace {
+
+// Checks and launch shared by the packed and the paged-source entry points.
+dgq_status compress_impl(const dgq::SourceDesc &src, const int32_t *cu_seqlens_dev, int32_t batch,
+                         int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                         uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                         size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream)
 {
     dgq::GroupSettings gs = {DGQ_MAX_SEG, 0.0f};
     if (options) {
@@ -98,16 +100,21 @@ dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total
     }
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
     if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
-        max_blocks_per_seq <= 0 || total_tokens < 0)
+        max_blocks_per_seq <= 0)
         return DGQ_ERR_INVALID_ARG;
     if ((int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size) return DGQ_ERR_INVALID_ARG;
+    if (src.bt == nullptr && src.T < 0) return DGQ_ERR_INVALID_ARG;
+    if (src.bt != nullptr &&
+        (src.num_blocks <= 0 || src.max_blocks <= 0 || (int64_t)max_seqlen > (int64_t)src.max_blocks * block_size ||
+         !aligned16(src.bt)))
+        return DGQ_ERR_INVALID_ARG;
     // flat window index and pool row index are 32-bit on the device
     const int64_t windows = (int64_t)batch * num_kv_heads * ((max_seqlen + DGQ_WINDOW - 1) / DGQ_WINDOW);
     if (windows >= INT32_MAX || (int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX)
         return DGQ_ERR_UNSUPPORTED;
-    if (!k_bf16 || !v_bf16 || !cu_seqlens_dev || !block_tables_dev || !k_pool || !v_pool || !seg_table)
+    if (!src.k || !src.v || !cu_seqlens_dev || !block_tables_dev || !k_pool || !v_pool || !seg_table)
         return DGQ_ERR_INVALID_ARG;
-    if (!aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(k_pool) || !aligned16(v_pool) ||
+    if (!aligned16(src.k) || !aligned16(src.v) || !aligned16(k_pool) || !aligned16(v_pool) ||
         !aligned16(seg_table) || !aligned16(cu_seqlens_dev) || !aligned16(block_tables_dev))
         return DGQ_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) ||
@@ -118,13 +125,44 @@ dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e =
         max_seqlen <= dgq::cluster_compress_max_seqlen()
-            ? dgq::launch_compress_cluster(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen,
-                                           num_kv_heads, block_size, block_tables_dev, max_blocks_per_seq, k_pool,
-                                           v_pool, num_blocks, seg_table, workspace, gs, stream)
-            : dgq::launch_compress(k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads,
-                                   block_size, block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
-                                   seg_table, workspace, gs, nsm, stream);
+            ? dgq::launch_compress_cluster(src, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
+                                           block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
+                                           seg_table, workspace, gs, stream)
+            : dgq::launch_compress(src, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
+                                   block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table,
+                                   workspace, gs, nsm, stream);
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+}  // namespace
+
+dgq_status dgq_compress_ex(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                           const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                           int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                           dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes,
+                           const dgq_compress_options *options, void *cuda_stream)
+{
+    const dgq::SourceDesc src = {k_bf16, v_bf16, total_tokens, nullptr, 0, 0};
+    return compress_impl(src, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, head_dim, block_size,
+                         block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, workspace,
+                         workspace_bytes, options, cuda_stream);
+}
+
+dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                              const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                              const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                              uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table, void *workspace,
+                              size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream)
+{
+    if (!src_block_tables_dev) return DGQ_ERR_INVALID_ARG;
+    const dgq::SourceDesc src = {k_src_bf16, v_src_bf16, 0, src_block_tables_dev, max_src_blocks_per_seq,
+                                 num_src_blocks};
+    return compress_impl(src, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, head_dim, block_size,
+                         block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, workspace,
+                         workspace_bytes, options, cuda_stream);
 }
 
 size_t dgq_append_workspace_size(void) { return 256; }  // the workspace header alone

@@ -16,11 +16,20 @@ struct GroupSettings {
     float min_var;
 };
 
+// Where compress reads K and V: packed rows [T, Hkv, 128] (bt == null) or a bf16 paged cache
+// [num_blocks, Hkv, bs, 128] with its [B, max_blocks] block table.
+struct SourceDesc {
+    const void *k, *v;
+    int32_t T;
+    const int32_t *bt;
+    int32_t max_blocks, num_blocks;
+};
+
 struct CompressLayout {
     size_t off_prog, off_params, off_mean, off_mm, off_agg, total;
 };
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv);
-cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+cudaError_t launch_compress(const SourceDesc &src, const int32_t *cu, int32_t B,
                             int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
                             uint8_t *kpool, uint8_t *vpool, int32_t num_blocks, dgq_seg_record *table, void *ws,
                             GroupSettings gs, int nsm, cudaStream_t stream);
@@ -29,7 +38,7 @@ cudaError_t launch_compress(const void *k, const void *v, int32_t T, const int32
 // pairs segmented inside thread-block clusters (no grid-wide step, no workspace beyond the
 // header).
 int32_t cluster_compress_max_seqlen();
-cudaError_t launch_compress_cluster(const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+cudaError_t launch_compress_cluster(const SourceDesc &src, const int32_t *cu, int32_t B,
                                     int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt,
                                     int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
                                     dgq_seg_record *table, void *ws, GroupSettings gs, cudaStream_t stream);

@@ -116,16 +116,21 @@ __device__ __forceinline__ float bf2_sum(uint32_t w)
 
 // ---- window tiles ----------------------------------------------------------------------------
 //
-// K and V are [T, Hkv, 128] bf16.  A tensor map views each as 4-D (64 elements, 2 halves, Hkv,
-// T), and one copy brings the tile of a window -- 16 tokens of one head -- into shared memory as
-// 32 rows of 128 bytes (row 2t + half) with the 128-byte swizzle: 16-byte chunk c of row r sits
-// at chunk position c ^ (r & 7) (the tile starts on a 1024-byte boundary).  Rows at or past T
-// are filled with zeros; rows of a partial window past its request's end hold the next
-// request's tokens, and every reader masks them.  With this layout the statistics' row reads
-// (eight lanes on eight consecutive rows) and the quantiser's chunk reads (eight lanes on one
-// row) each touch eight distinct 16-byte bank groups per quarter-warp.
-struct TileMaps {
+// K and V come either as packed rows [T, Hkv, 128] bf16 -- a tensor map views each as 4-D (64
+// elements, 2 halves, Hkv, T) -- or from a bf16 paged cache [blocks, Hkv, bs, 128] addressed
+// through a block table -- then a 5-D map (64, 2, bs, Hkv, blocks) and the window's block.
+// One copy per tensor brings the tile of a window -- 16 tokens of one head -- into shared memory
+// as 32 rows of 128 bytes (row 2t + half) with the 128-byte swizzle: 16-byte chunk c of row r sits
+// at chunk position c ^ (r & 7) (the tile starts on a 1024-byte boundary).  Packed rows at or
+// past T are filled with zeros; rows of a partial window past its request's end hold other
+// tokens (the next request's, or the rest of the block), and every reader masks them.  With this
+// layout the statistics' row reads (eight lanes on eight consecutive rows) and the quantiser's
+// chunk reads (eight lanes on one row) each touch eight distinct 16-byte bank groups per
+// quarter-warp.
+struct TileSource {
     CUtensorMap k, v;
+    const int32_t *bt;  // paged source: [B, max_blocks] block table; null for packed rows
+    int32_t max_blocks, num_blocks, bs;
 };
 
 // Byte offset of 16-byte chunk `chunk` (0..15) of token t in a tile.
@@ -135,32 +140,61 @@ __device__ __forceinline__ uint32_t tile_off(int t, int chunk)
     return (uint32_t)(r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
 }
 
-// Lane 0's copies of one window: K tile at dst, V tile at dst + kTileBytes, both completing on
-// `bar` (one arrival, kWinBytes of transactions).  `pol`: the copies' L2 eviction policy.
-__device__ __forceinline__ void load_window(uint32_t dst, uint64_t *bar, const TileMaps &m, int32_t h, int32_t tok,
-                                            uint64_t pol)
+// Lane 0's copies of the window of tokens t0 .. t0+15 of request b (rows from c0 when packed),
+// head h: K tile at dst, V tile at dst + kTileBytes, both completing on `bar` (one arrival,
+// kWinBytes of transactions).  `pol`: the copies' L2 eviction policy.  A paged source's block id
+// outside the cache is flagged in `hdr` and block 0 read instead (the copies always complete).
+// (Fetching the source block one window ahead measured no faster: the copy is not waiting on it.)
+__device__ __forceinline__ void load_window(uint32_t dst, uint64_t *bar, const TileSource &s, int32_t b, int32_t h,
+                                            int32_t c0, int32_t t0, uint64_t pol, WsHeader *hdr)
 {
-    mbar_arrive_expect_tx(bar, kWinBytes);
-    tma_load_4d_hint(dst, &m.k, 0, 0, h, tok, smem_u32(bar), pol);
-    tma_load_4d_hint(dst + kTileBytes, &m.v, 0, 0, h, tok, smem_u32(bar), pol);
+    if (s.bt == nullptr) {
+        mbar_arrive_expect_tx(bar, kWinBytes);
+        tma_load_4d_hint(dst, &s.k, 0, 0, h, c0 + t0, smem_u32(bar), pol);
+        tma_load_4d_hint(dst + kTileBytes, &s.v, 0, 0, h, c0 + t0, smem_u32(bar), pol);
+    } else {
+        int32_t blk = __ldg(s.bt + (int64_t)b * s.max_blocks + t0 / s.bs);
+        if ((uint32_t)blk >= (uint32_t)s.num_blocks) {
+            record_error(hdr, kErrBadBlock);
+            blk = 0;
+        }
+        mbar_arrive_expect_tx(bar, kWinBytes);
+        tma_load_5d_hint(dst, &s.k, 0, 0, t0 % s.bs, h, blk, smem_u32(bar), pol);
+        tma_load_5d_hint(dst + kTileBytes, &s.v, 0, 0, t0 % s.bs, h, blk, smem_u32(bar), pol);
+    }
 }
 
-// Host: the two tensor maps of a call (K and V of T rows); false if the driver refuses them.
-inline bool encode_tile_maps(const void *k, const void *v, int32_t T, int32_t Hkv, TileMaps *m)
+// Host: the tensor maps of a call's source; false if the driver refuses them.
+inline bool encode_tile_source(const SourceDesc &d, int32_t Hkv, int32_t bs, TileSource *s)
 {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[4] = {64, 2, (cuuint64_t)Hkv, (cuuint64_t)(T > 0 ? T : 1)};
-    const cuuint64_t strides[3] = {128, 256, (cuuint64_t)Hkv * 256};  // bytes, dimensions 1..3
-    const cuuint32_t box[4] = {64, 2, 1, kWin};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const void *src[2] = {k, v};
-    CUtensorMap *dst[2] = {&m->k, &m->v};
+    s->bt = d.bt;
+    s->max_blocks = d.max_blocks;
+    s->num_blocks = d.num_blocks;
+    s->bs = bs;
+    const void *src[2] = {d.k, d.v};
+    CUtensorMap *dst[2] = {&s->k, &s->v};
     for (int i = 0; i < 2; ++i) {
-        if (enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src[i]), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return false;
+        CUresult r;
+        if (d.bt == nullptr) {
+            const cuuint64_t dims[4] = {64, 2, (cuuint64_t)Hkv, (cuuint64_t)(d.T > 0 ? d.T : 1)};
+            const cuuint64_t strides[3] = {128, 256, (cuuint64_t)Hkv * 256};  // bytes, dimensions 1..3
+            const cuuint32_t box[4] = {64, 2, 1, kWin};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            r = enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(src[i]), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            const cuuint64_t dims[5] = {64, 2, (cuuint64_t)bs, (cuuint64_t)Hkv, (cuuint64_t)d.num_blocks};
+            const cuuint64_t strides[4] = {128, 256, (cuuint64_t)bs * 256, (cuuint64_t)Hkv * bs * 256};
+            const cuuint32_t box[5] = {64, 2, kWin, 1, 1};
+            const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+            r = enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(src[i]), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return false;
     }
     return true;
 }

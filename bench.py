@@ -555,8 +555,13 @@ def fidelity_check(w, lens, layer0, rank):
     def err(a, b):
         d = np.abs(a - b)
         return {"max_abs": float(f"{d.max():.3e}"), "mean_abs": float(f"{d.mean():.3e}")}
+    comparison = {}  # the same attention with K/V through other 8-bit quantisers, fp64
+    for scheme in oracle.COMPARISON_QUANTISERS:
+        kd = np.stack([oracle.dequant_comparison(k[:, h], scheme) for h in range(w.hkv)], axis=1)
+        vd = np.stack([oracle.dequant_comparison(v[:, h], scheme) for h in range(w.hkv)], axis=1)
+        comparison[scheme] = err(oracle.decode_attn_dense(q[0], kn[0], vn[0], kd, vd), raw[0])
     return {"gpu_vs_unquantised": err(got, raw), "dgq_fp64_vs_unquantised": err(cache, raw),
-            "gpu_vs_oracle": err(got, cache),
+            "gpu_vs_oracle": err(got, cache), "others_fp64_vs_unquantised": comparison,
             "sample": f"request 0 ({L} tokens), all {w.hq} query heads, layer 0; unquantised = fp64 "
                       "attention over the original bf16 K/V"}
 

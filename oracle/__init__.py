@@ -91,6 +91,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_append.restype = i32
         L.oracle_decode_attn_unquantised.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P]
         L.oracle_decode_attn_unquantised.restype = None
+        for name in ("oracle_dequant_fixed64", "oracle_dequant_sym_int8", "oracle_dequant_fp8_e4m3"):
+            getattr(L, name).argtypes = [P, i64, i32, P]
+            getattr(L, name).restype = None
+        L.oracle_decode_attn_dense.argtypes = [P, P, P, P, P, i32, i32, i32, P]
+        L.oracle_decode_attn_dense.restype = None
         L.oracle_compress_bytes_written.argtypes = [i32, i32]
         L.oracle_compress_bytes_written.restype = i64
         _lib = L
@@ -220,6 +225,36 @@ def decode_attn_unquantised(q, k_new, v_new, k, v, cu_seqlens, seq_lens):
     lib().oracle_decode_attn_unquantised(_p(q), _p(kn), _p(vn), _p(k if k.size else np.zeros(1, np.uint16)),
                                          _p(v if v.size else np.zeros(1, np.uint16)), _p(cu), _p(sl), B, Hq, Hkv,
                                          _p(out))
+    return out
+
+
+COMPARISON_QUANTISERS = ("fixed64", "sym_int8", "fp8_e4m3")
+
+
+def dequant_comparison(x, scheme: str) -> np.ndarray:
+    """x: [L, 128] bf16 bits of one (request, head) pair -> fp64 values after a comparison
+    quantiser (fixed64 / sym_int8 / fp8_e4m3) and its dequantisation."""
+    assert scheme in COMPARISON_QUANTISERS
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    L = x.shape[0]
+    out = np.zeros((max(L, 1), D), dtype=np.float64)
+    getattr(lib(), "oracle_dequant_" + scheme)(_p(x), D, L, _p(out))
+    return out[:L]
+
+
+def decode_attn_dense(q, k_new, v_new, kd, vd):
+    """fp64 decode attention of one request: q [Hq, 128], k_new/v_new [Hkv, 128] bf16 bits,
+    kd/vd [L, Hkv, 128] fp64 (dequantised keys and values)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kn = np.ascontiguousarray(k_new, dtype=np.uint16)
+    vn = np.ascontiguousarray(v_new, dtype=np.uint16)
+    kd = np.ascontiguousarray(kd, dtype=np.float64)
+    vd = np.ascontiguousarray(vd, dtype=np.float64)
+    Hq, Hkv = q.shape[0], kn.shape[0]
+    L = kd.shape[0]
+    out = np.zeros((Hq, D), dtype=np.float64)
+    lib().oracle_decode_attn_dense(_p(q), _p(kn), _p(vn), _p(kd if kd.size else np.zeros(1)),
+                                   _p(vd if vd.size else np.zeros(1)), L, Hq, Hkv, _p(out))
     return out
 
 

@@ -38,6 +38,9 @@
  *                  rule; a floor above every window mean gives one segment; planted quiet /
  *                  loud regions give boundaries only at loud transitions; brute force over
  *                  the candidate subsets on tiny inputs
+ *   comparisons    fixed-64 groups: two-valued groups round-trip exactly, error <= scale/2;
+ *                  symmetric INT8: values on the k * max/127 grid round-trip exactly; E4M3: the
+ *                  format's own numbers round-trip, ties go to the even mantissa, 448 caps
  *   unquantised    attention over the raw bf16 rows equals the paged attention over a
  *                  cache whose values are all exactly representable; numpy fp64 brute force
  *   append         a first token alone: its min -> 0, max -> 255; in-range values give
@@ -530,6 +533,120 @@ void oracle_decode_attn_unquantised(const uint16_t *q, const uint16_t *k_new, co
         }
         free(s);
     }
+}
+
+/* ---- comparison quantisers (fidelity context) --------------------------------------------
+ * Each returns the dequantised fp64 values of one (request, head) pair [L, 128] (rows
+ * `row_stride` elements apart in x), so that attention over them can be compared with DGQ's.
+ *   fixed 64-dim groups ([DGQ] section 2.2: "traditional group quantisation cuts the cache into
+ *     fixed blocks of e.g. 64 dimensions, each with its own min/max, INT8"): per token and per
+ *     64-element half, the DGQ affine code (a5-a6 over that group) and its dequantisation;
+ *   symmetric INT8 ("DeepSeek-V4" article, FP8+FP16 section: scale = max|k| / 127, k / scale
+ *     held to [-128, 127]): READING: per (request, head) tensor, round-half-even to an integer
+ *     (the printed snippet omits the rounding), dequantised as q * scale;
+ *   FP8 E4M3 ([DGQ] section 2.3 table): each value rounded half-even to the nearest E4M3 number
+ *     (3 mantissa bits, exponent bias 7, largest 448, subnormal step 2^-9), saturating. */
+void oracle_dequant_fixed64(const uint16_t *x, int64_t row_stride, int32_t L, double *out)
+{
+    for (int32_t t = 0; t < L; ++t)
+        for (int g = 0; g < 2; ++g) {
+            float mn = INFINITY, mx = -INFINITY;
+            for (int d = 64 * g; d < 64 * g + 64; ++d) {
+                float v = bf16_to_float(x[(int64_t)t * row_stride + d]);
+                if (v < mn) mn = v;
+                if (v > mx) mx = v;
+            }
+            if (mn == 0.0f) mn = 0.0f;
+            if (mx == 0.0f) mx = 0.0f;
+            float scale, inv;
+            segment_affine(mn, mx, &scale, &inv);
+            for (int d = 64 * g; d < 64 * g + 64; ++d) {
+                uint8_t q = oracle_encode(bf16_to_float(x[(int64_t)t * row_stride + d]), mn, inv);
+                out[(int64_t)t * OR_D + d] = dequant(q, mn, scale);
+            }
+        }
+}
+
+void oracle_dequant_sym_int8(const uint16_t *x, int64_t row_stride, int32_t L, double *out)
+{
+    float amax = 0.0f;
+    for (int32_t t = 0; t < L; ++t)
+        for (int d = 0; d < OR_D; ++d) {
+            float v = fabsf(bf16_to_float(x[(int64_t)t * row_stride + d]));
+            if (v > amax) amax = v;
+        }
+    const float scale = amax / 127.0f;
+    for (int32_t t = 0; t < L; ++t)
+        for (int d = 0; d < OR_D; ++d) {
+            float v = bf16_to_float(x[(int64_t)t * row_stride + d]);
+            float q = scale > 0.0f ? rintf(v / scale) : 0.0f;
+            if (q < -128.0f) q = -128.0f;
+            if (q > 127.0f) q = 127.0f;
+            out[(int64_t)t * OR_D + d] = (double)q * (double)scale;
+        }
+}
+
+static double round_e4m3(double v)
+{
+    const double a = fabs(v);
+    if (a == 0.0) return 0.0;
+    int e;
+    frexp(a, &e);                       /* a = m * 2^e, 0.5 <= m < 1: leading bit at 2^(e-1) */
+    int lead = e - 1;
+    if (lead < -6) lead = -6;           /* subnormals share the step of the smallest normal */
+    const double quantum = ldexp(1.0, lead - 3);
+    double r = nearbyint(a / quantum) * quantum;  /* half-even (default rounding mode) */
+    if (r > 448.0) r = 448.0;           /* saturate to the largest finite E4M3 value */
+    return v < 0.0 ? -r : r;
+}
+
+void oracle_dequant_fp8_e4m3(const uint16_t *x, int64_t row_stride, int32_t L, double *out)
+{
+    for (int32_t t = 0; t < L; ++t)
+        for (int d = 0; d < OR_D; ++d)
+            out[(int64_t)t * OR_D + d] = round_e4m3((double)bf16_to_float(x[(int64_t)t * row_stride + d]));
+}
+
+/* Decode attention (a9-a10 in fp64) of one request over dense fp64 keys/values [L, Hkv, 128]
+ * plus the current token's bf16 key/value: the comparison quantisers' counterpart of
+ * oracle_paged_decode_attn. */
+void oracle_decode_attn_dense(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new, const double *kd,
+                              const double *vd, int32_t L, int32_t Hq, int32_t Hkv, double *out)
+{
+    const int32_t G = Hq / Hkv;
+    const double inv_sqrt_d = 1.0 / sqrt((double)OR_D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    for (int32_t hq = 0; hq < Hq; ++hq) {
+        const int32_t h = hq / G;
+        const uint16_t *qv = q + (int64_t)hq * OR_D;
+        for (int32_t t = 0; t <= L; ++t) {
+            double acc = 0.0;
+            for (int d = 0; d < OR_D; ++d) {
+                const double kv = t < L ? kd[((int64_t)t * Hkv + h) * OR_D + d]
+                                        : (double)bf16_to_float(k_new[(int64_t)h * OR_D + d]);
+                acc += (double)bf16_to_float(qv[d]) * kv;
+            }
+            s[t] = acc * inv_sqrt_d;
+        }
+        double m = s[0];
+        for (int32_t t = 1; t <= L; ++t)
+            if (s[t] > m) m = s[t];
+        double l = 0.0;
+        for (int32_t t = 0; t <= L; ++t) {
+            s[t] = exp(s[t] - m);
+            l += s[t];
+        }
+        for (int d = 0; d < OR_D; ++d) {
+            double o = 0.0;
+            for (int32_t t = 0; t <= L; ++t) {
+                const double vv = t < L ? vd[((int64_t)t * Hkv + h) * OR_D + d]
+                                        : (double)bf16_to_float(v_new[(int64_t)h * OR_D + d]);
+                o += s[t] * vv;
+            }
+            out[(int64_t)hq * OR_D + d] = o / l;
+        }
+    }
+    free(s);
 }
 
 /* Algorithmic bytes one compress call writes for a request of L tokens and Hkv heads:

@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-formats", action="store_true",
+                    help="skip the comparison encodings (fixed64, sym_int8, fp8_e4m3) after the timed steps")
     ap.add_argument("--paged-input", action="store_true",
                     help="compress from a bf16 paged cache (dgq_compress_paged) instead of packed rows")
     ap.add_argument("--layers", type=int, default=0,
@@ -431,7 +433,12 @@ def run_ours(args):
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
 
 
-    fidelity = fidelity_check(w, lens, layers[0], rank)
+    ref0 = request0_reference(w, lens, layers[0]) if rank == 0 else None
+    fidelity = fidelity_check(w, layers[0], ref0) if rank == 0 else None
+    formats = None
+    if not args.no_formats:
+        formats = time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0,
+                               max(3, min(args.steps, 10)))
 
     total_ms, comp_ms, dec_ms, app_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, app_ms, e2e_ms], dev,
                                                               world)
@@ -485,6 +492,7 @@ def run_ours(args):
                             "device->host copy of the outputs, the step's token appended to every layer's cache"},
             "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
             "fidelity": fidelity,
+            "formats": formats,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
             "device_error": err,
@@ -523,12 +531,9 @@ def spot_check(w, lens, cu, bt, layer0, rank):
     return bool(np.array_equal(gk, kc) and grec == rec.tobytes())
 
 
-def fidelity_check(w, lens, layer0, rank):
-    """Request 0 of layer 0, all query heads: the GPU's decode output against fp64 attention over
-    the unquantised bf16 K/V (the encoding's error, reported as context) and against the oracle's
-    fp64 attention over its own compressed cache (the kernel's error)."""
-    if rank != 0:
-        return None
+def request0_reference(w, lens, layer0):
+    """Request 0 of layer 0: its bf16 K/V (regenerated on the host), the step's q / k_new / v_new,
+    and fp64 attention of all its query heads over the unquantised K/V."""
     import numpy as np
     import oracle
     import synth
@@ -542,19 +547,40 @@ def fidelity_check(w, lens, layer0, rank):
     q = layer0["q"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
     kn = layer0["kn"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
     vn = layer0["vn"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
-    got = layer0["out"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
-    got = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     cu = np.array([0, L], dtype=np.int32)
     lens1 = np.array([L], dtype=np.int32)
     raw = oracle.decode_attn_unquantised(q, kn, vn, k, v, cu, lens1)
+    return dict(L=L, k=k, v=v, q=q, kn=kn, vn=vn, raw=raw)
+
+
+def out0(layer0):
+    """fp64 values of request 0's decode output (bf16) on layer 0."""
+    import numpy as np
+    got = layer0["out"][:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    return (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def err_stats(a, b):
+    import numpy as np
+    d = np.abs(a - b)
+    return {"max_abs": float(f"{d.max():.3e}"), "mean_abs": float(f"{d.mean():.3e}")}
+
+
+def fidelity_check(w, layer0, ref):
+    """Request 0 of layer 0, all query heads: the GPU's decode output against fp64 attention over
+    the unquantised bf16 K/V (the encoding's error, reported as context) and against the oracle's
+    fp64 attention over its own compressed cache (the kernel's error)."""
+    import numpy as np
+    import oracle
+    L, k, v, q, kn, vn, raw = (ref[x] for x in ("L", "k", "v", "q", "kn", "vn", "raw"))
+    got = out0(layer0)
+    cu = np.array([0, L], dtype=np.int32)
+    lens1 = np.array([L], dtype=np.int32)
     nb = (L + w.block_size - 1) // w.block_size
     bt = np.arange(nb, dtype=np.int32)[None]
     kp, vp, table = oracle.compress(k, v, cu, w.hkv, w.block_size, bt, nb)
     cache = oracle.paged_decode_attn(q, kn, vn, kp, vp, table, bt, lens1)
-
-    def err(a, b):
-        d = np.abs(a - b)
-        return {"max_abs": float(f"{d.max():.3e}"), "mean_abs": float(f"{d.mean():.3e}")}
+    err = err_stats
     comparison = {}  # the same attention with K/V through other 8-bit quantisers, fp64
     for scheme in oracle.COMPARISON_QUANTISERS:
         kd = np.stack([oracle.dequant_comparison(k[:, h], scheme) for h in range(w.hkv)], axis=1)
@@ -564,6 +590,67 @@ def fidelity_check(w, lens, layer0, rank):
             "gpu_vs_oracle": err(got, cache), "others_fp64_vs_unquantised": comparison,
             "sample": f"request 0 ({L} tokens), all {w.hq} query heads, layer 0; unquantised = fp64 "
                       "attention over the original bf16 K/V"}
+
+
+def time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0, reps):
+    """The comparison encodings on the same workload, outside the timed steps: every layer's bf16
+    K/V encoded into its own pools (overwriting the DGQ cache), then the same decode over all
+    layers; CUDA-event time per layer over `reps` passes, decode GB/s over the bytes each format
+    reads (codes, plus the per-token parameters of fixed64), and, on rank 0, the GPU output of
+    request 0 against fp64 attention over the unquantised K/V."""
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    dev = layers[0]["k"].device
+    B, Hkv, bs = w.batch, w.hkv, w.block_size
+    nb = layers[0]["kp"].shape[0]
+    ews = torch.zeros(dgq.dgq_encode_format_workspace_size(B, Hkv), dtype=torch.uint8, device=dev)
+    par_bytes = 2 * 16 * Hkv * int(sum(int(L) for L in lens))  # fixed64: (min, scale) x 2 halves x K, V per token
+    res = {}
+    for fmt in ("fixed64", "sym_int8", "fp8_e4m3"):
+        pars = [(torch.empty((nb, Hkv, bs, 4), dtype=torch.float32, device=dev),
+                 torch.empty((nb, Hkv, bs, 4), dtype=torch.float32, device=dev)) if fmt == "fixed64"
+                else (None, None) for _ in layers]
+
+        def enc_all():
+            for L, (kpar, vpar) in zip(layers, pars):
+                dgq.dgq_encode_format(fmt, L["k"], L["v"], d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"],
+                                      ews, kpar, vpar, sp)
+
+        def dec_all():
+            for L, (kpar, vpar) in zip(layers, pars):
+                dgq.dgq_paged_decode_attn_format(fmt, L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], d_bt,
+                                                 d_lens, max_seqlen, L["out"], aws, kpar, vpar, sp)
+        for _ in range(2):
+            enc_all()
+            dec_all()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        enc_ms = dec_ms = 0.0
+        for _ in range(reps):
+            ev[0].record()
+            enc_all()
+            ev[1].record()
+            dec_all()
+            ev[2].record()
+            torch.cuda.synchronize()
+            enc_ms += ev[0].elapsed_time(ev[1])
+            dec_ms += ev[1].elapsed_time(ev[2])
+        err = dgq.dgq_workspace_error(ews, sp) or dgq.dgq_workspace_error(aws, sp)
+        n = reps * len(layers)
+        dec_us, enc_us = dec_ms / n * 1e3, enc_ms / n * 1e3
+        rd = dec_b + (par_bytes if fmt == "fixed64" else 0)
+        entry = {"encode_us_per_layer": round(enc_us, 2), "decode_us_per_layer": round(dec_us, 2),
+                 "decode_bytes_per_layer": rd, "decode_gbs": round(rd / dec_us / 1e3, 1), "device_error": err}
+        if ref0 is not None:
+            import numpy as np
+            import oracle
+            got = out0(layers[0])
+            kd = np.stack([oracle.dequant_comparison(ref0["k"][:, h], fmt) for h in range(Hkv)], axis=1)
+            vd = np.stack([oracle.dequant_comparison(ref0["v"][:, h], fmt) for h in range(Hkv)], axis=1)
+            want = oracle.decode_attn_dense(ref0["q"][0], ref0["kn"][0], ref0["vn"][0], kd, vd)
+            entry["gpu_vs_unquantised"] = err_stats(got, ref0["raw"])
+            entry["gpu_vs_oracle"] = err_stats(got[0], want)
+        res[fmt] = entry
+    return res
 
 
 def torch_int16():

@@ -274,6 +274,84 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
 
 size_t dgq_append_workspace_size(void);
 
+/* ---------------------------------------------------------------------------------------
+ * Comparison encodings: the same paged cache layout and the same decode kernel, with the
+ * K/V codes produced by one of the quantisers DGQ is measured against, so that accuracy and
+ * decode speed can be set side by side on one workload.  Sources:
+ *   [DGQ] section 2.2: the traditional alternative cuts each vector into fixed groups of 64
+ *         dimensions, each with its own min/max INT8 parameters;
+ *   [DGQ] section 2.3: the FP8 (E4M3) comparison row of its format table;
+ *   [PAGED] "FP8+FP16 scheme: technical details" section: symmetric INT8 with scale =
+ *         max|k| / 127 and k / scale held to [-128, 127].
+ *
+ * DGQ_FORMAT_DGQ       the records and codes of dgq_compress (dgq_encode_format rejects it).
+ * DGQ_FORMAT_FIXED64   per token and per 64-value half of each K and V row: min/max over the
+ *                      64 values, scale = (max - min) / 255, codes rint((x - min) * (255 /
+ *                      (max - min))) -- the DGQ quantiser (two IEEE steps, -0 min/max stored as
+ *                      +0, 0 codes and scale for a flat group) on a fixed group.  The parameters
+ *                      go to a side array [num_blocks, Hkv, block_size, 4] fp32 per tensor:
+ *                      (min of values 0..63, its scale, min of values 64..127, its scale) in
+ *                      the slot of the token's codes (16 B per token and head: 12.5% more bytes
+ *                      than the codes).
+ * DGQ_FORMAT_SYM_INT8  per (request, KV head) and tensor: s = amax / 127 (IEEE division; amax =
+ *                      largest |x| over the pair), q = rint(x / s) (IEEE division, half-even)
+ *                      held to [-128, 127], 0 when s == 0.  READING: the printed snippet has no
+ *                      rounding step; round-half-even is taken.  Stored as the byte q + 128,
+ *                      with a one-segment record (min = -128 s, scale = s), so the DGQ decode
+ *                      path reads it unchanged.
+ * DGQ_FORMAT_FP8_E4M3  every value rounded (half-even) to the nearest E4M3 number (bias 7,
+ *                      3 mantissa bits, largest finite 448, subnormal step 2^-9), saturating to
+ *                      +-448; stored as the E4M3 byte.
+ * For FIXED64 and FP8_E4M3 the record of each pair holds n_seg = 1, seq_len = L and the identity
+ * parameters (min 0, scale 1): the codes carry their own scale.  dgq_append supports only DGQ.
+ */
+typedef enum dgq_format {
+    DGQ_FORMAT_DGQ = 0,
+    DGQ_FORMAT_FIXED64 = 1,
+    DGQ_FORMAT_SYM_INT8 = 2,
+    DGQ_FORMAT_FP8_E4M3 = 3
+} dgq_format;
+
+/*
+ * dgq_encode_format -- one layer's K/V of a batch of requests encoded into the paged cache in
+ * a comparison format.  Arguments as for dgq_compress (packed rows, cu_seqlens, block tables,
+ * pools, records), plus:
+ * format            DGQ_FORMAT_FIXED64, DGQ_FORMAT_SYM_INT8 or DGQ_FORMAT_FP8_E4M3 (anything
+ *                   else: DGQ_ERR_INVALID_ARG).
+ * k_group_params, v_group_params  FIXED64 only: [num_blocks, Hkv, block_size, 4] fp32, device,
+ *                   written for the slots of tokens 0..L_b-1; ignored (may be NULL) otherwise.
+ * workspace         >= dgq_encode_format_workspace_size(batch, num_kv_heads) bytes, zero-filled
+ *                   before first use (SYM_INT8 keeps its per-pair maxima there).
+ * A block-table entry outside [0, num_blocks) is flagged in the workspace and its slots are
+ * skipped.  Two or three launches, no cooperative launch.
+ */
+dgq_status dgq_encode_format(int32_t format, const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                             const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                             uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table,
+                             float *k_group_params, float *v_group_params, void *workspace,
+                             size_t workspace_bytes, void *cuda_stream);
+
+size_t dgq_encode_format_workspace_size(int32_t batch, int32_t num_kv_heads);
+
+/*
+ * dgq_paged_decode_attn_format -- dgq_paged_decode_attn over a cache written in `format`
+ * (DGQ_FORMAT_DGQ and DGQ_FORMAT_SYM_INT8 are decoded through the records; FP8_E4M3 codes are
+ * E4M3 values; FIXED64 codes are decoded with their per-token, per-half parameters, read from
+ * k_group_params / v_group_params, which must be non-NULL for it).  Same kernel, tiling,
+ * workspace and results layout as dgq_paged_decode_attn.
+ */
+dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, const void *k_new_bf16,
+                                        const void *v_new_bf16, const uint8_t *k_pool, const uint8_t *v_pool,
+                                        const dgq_seg_record *seg_table, const float *k_group_params,
+                                        const float *v_group_params, const int32_t *block_tables_dev,
+                                        const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                        void *out_bf16, void *workspace, size_t workspace_bytes,
+                                        void *cuda_stream);
+
 /* Zero-fill a workspace (cudaMemsetAsync on the stream). */
 dgq_status dgq_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream);
 

@@ -17,10 +17,18 @@ HEAD_DIM = 128
 MAX_SEG = 5
 SEG_RECORD_BYTES = 128
 
+# dgq_format: the method's own encoding and the comparison encodings on the same cache layout
+FORMAT_DGQ = 0
+FORMAT_FIXED64 = 1
+FORMAT_SYM_INT8 = 2
+FORMAT_FP8_E4M3 = 3
+FORMATS = {"dgq": FORMAT_DGQ, "fixed64": FORMAT_FIXED64, "sym_int8": FORMAT_SYM_INT8, "fp8_e4m3": FORMAT_FP8_E4M3}
+
 __all__ = [
     "DGQError", "lib", "dgq_compress", "dgq_compress_paged", "dgq_compress_workspace_size", "dgq_append",
     "dgq_append_workspace_size",
-    "dgq_paged_decode_attn",
+    "dgq_paged_decode_attn", "dgq_encode_format", "dgq_encode_format_workspace_size",
+    "dgq_paged_decode_attn_format", "FORMATS",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -62,6 +70,14 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                     i32, P, P]
         L.dgq_paged_decode_attn_noalloc.restype = ctypes.c_int
+        L.dgq_encode_format.argtypes = [i32, P, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P, P,
+                                        sz, P]
+        L.dgq_encode_format.restype = ctypes.c_int
+        L.dgq_encode_format_workspace_size.argtypes = [i32, i32]
+        L.dgq_encode_format_workspace_size.restype = sz
+        L.dgq_paged_decode_attn_format.argtypes = [i32, P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                                   i32, i32, P, P, sz, P]
+        L.dgq_paged_decode_attn_format.restype = ctypes.c_int
         L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
         L.dgq_append.restype = ctypes.c_int
         L.dgq_append_workspace_size.argtypes = []
@@ -209,6 +225,41 @@ def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tabl
                                        B, Hq, Hkv, D, k_pool.shape[2], block_tables.shape[1], k_pool.shape[0],
                                        _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
            "dgq_paged_decode_attn")
+
+
+def _format_id(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def dgq_encode_format_workspace_size(batch: int, num_kv_heads: int) -> int:
+    return int(lib().dgq_encode_format_workspace_size(batch, num_kv_heads))
+
+
+def dgq_encode_format(fmt, k, v, cu_seqlens, max_seqlen, block_size, block_tables, k_pool, v_pool, seg_table,
+                      workspace, k_params=None, v_params=None, stream=None) -> None:
+    """A comparison encoding ("fixed64", "sym_int8", "fp8_e4m3") of bf16 [T, Hkv, 128] rows into
+    the paged cache; k_params / v_params fp32 [num_blocks, Hkv, bs, 4] for "fixed64" (else
+    None); the other arguments as dgq_compress (workspace: dgq_encode_format_workspace_size)."""
+    B = cu_seqlens.shape[0] - 1
+    Hkv = k.shape[1]
+    _check(lib().dgq_encode_format(_format_id(fmt), _ptr(k), _ptr(v), k.shape[0], _ptr(cu_seqlens), B,
+                                   int(max_seqlen), Hkv, k.shape[2], int(block_size), _ptr(block_tables),
+                                   block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                   _ptr(seg_table), _ptr(k_params), _ptr(v_params), _ptr(workspace),
+                                   _nbytes(workspace), _stream(stream)), "dgq_encode_format")
+
+
+def dgq_paged_decode_attn_format(fmt, q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens,
+                                 max_seqlen, out, workspace, k_params=None, v_params=None, stream=None) -> None:
+    """dgq_paged_decode_attn over a cache written in format `fmt` (a FORMATS key or id)."""
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    _check(lib().dgq_paged_decode_attn_format(_format_id(fmt), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                              _ptr(v_pool), _ptr(seg_table), _ptr(k_params), _ptr(v_params),
+                                              _ptr(block_tables), _ptr(seq_lens), int(max_seqlen), B, Hq, Hkv, D,
+                                              k_pool.shape[2], block_tables.shape[1], k_pool.shape[0], _ptr(out),
+                                              _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dgq_paged_decode_attn_format")
 
 
 def dgq_paged_decode_attn_noalloc(q, k_new, v_new, k_pool, v_pool, seg_table, block_tables, seq_lens,

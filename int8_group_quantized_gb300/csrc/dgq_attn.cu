@@ -33,12 +33,19 @@
 //      sum_t p_t x_V = v_scale[s] * sum_t p_t (1024 + c_t) + (v_min[s] - 1024 v_scale[s]) sum p.
 //  * Online softmax in the log2 domain with lazy rescaling (the running max moves only when a
 //    tile's max exceeds it by more than 8, so p <= 256 stays exact enough in fp16).
+//  * The comparison encodings run through the same kernel, instantiated per code format: the
+//    symmetric INT8 cache is a one-segment affine cache (the path above); FP8 E4M3 codes are
+//    converted to fp16 exactly (E4M3 values are fp16 values); fixed 64-value groups are
+//    dequantised to fp16 in registers, code * scale + min per (token, half row), from per-token
+//    parameters copied into the ring beside each tile.  Both of the latter feed the tensor
+//    cores the decoded values themselves, so their per-tile fold is the identity.
 #include "dgq_device.cuh"
 #include "dgq.h"
 #include "dgq_launch.h"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace dgq {
@@ -50,7 +57,14 @@ constexpr int kMaxCtasPerSm = 3;
 constexpr int kDepth = 3;                          // tiles in flight per warp (3 CTAs of 4 warps fit per SM)
 constexpr int kTileBytes = kTile * kD;            // 16 rows of 128 codes = 2 KB
 constexpr int kTileSmem = 2 * kTileBytes;          // K tile + V tile
-constexpr int kWarpSmem = kDepth * kTileSmem;
+constexpr int kParBytes = kTile * 16;              // fixed groups: a tile's (min0, scale0, min1, scale1) per token
+
+// Code formats of the decode kernel's instances.
+enum : int { kDecAffine = 0, kDecFp8 = 1, kDecFixed = 2 };
+
+// Bytes of one ring stage: the K and V tiles, and for fixed groups their K and V parameters.
+template <int Fmt>
+__host__ __device__ constexpr int stage_bytes() { return kTileSmem + (Fmt == kDecFixed ? 2 * kParBytes : 0); }
 constexpr int kPartStride = 132;                   // floats per (piece, head) partial: m, l, pad, pad, O[128]
 constexpr float kLog2eOverSqrtD = 0.12751743074570180f;  // log2(e) / sqrt(128)
 constexpr float kLazyRescale = 8.0f;               // log2 units
@@ -62,6 +76,8 @@ struct AttnArgs {
     const uint8_t *kpool;
     const uint8_t *vpool;
     const dgq_seg_record *table;
+    const float4 *kpar;  // fixed groups: per-slot (min0, scale0, min1, scale1) of K and of V
+    const float4 *vpar;
     const int32_t *bt;
     const int32_t *seq_lens;
     uint16_t *out;
@@ -104,6 +120,45 @@ __device__ __forceinline__ void mma16816(float *c, uint32_t a0, uint32_t a1, uin
 __device__ __forceinline__ uint32_t word(const uint4 &v, int i)
 {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Two codes as the fp16 pair the tensor cores take, from bytes 0-1 (Hi = false) or 2-3 of w:
+// 1024 + code for the affine formats (the offset is folded out per tile); the E4M3 values
+// themselves; for fixed groups code * scale + min (per-lane scale and min pairs sc2, mn2; the
+// code is recovered exactly as (1024 + code) - 1024, then one rounded fp16 multiply-add).
+template <int Fmt, bool Hi>
+__device__ __forceinline__ uint32_t codes2(uint32_t w, uint32_t sc2, uint32_t mn2)
+{
+    if constexpr (Fmt == kDecFp8) {
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(Hi ? (w >> 16) : (w & 0xFFFFu)),
+                                                         __NV_E4M3);
+        return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    } else {
+        const uint32_t x = prmt(w, 0x64646464u, Hi ? 0x4342 : 0x4140);
+        if constexpr (Fmt == kDecFixed) {
+            const __half2 c = __hsub2(*reinterpret_cast<const __half2 *>(&x), __half2(__half_raw{0x6400}, __half_raw{0x6400}));
+            const __half2 y = __hfma2(c, *reinterpret_cast<const __half2 *>(&sc2), *reinterpret_cast<const __half2 *>(&mn2));
+            return *reinterpret_cast<const uint32_t *>(&y);
+        } else {
+            (void)sc2;
+            (void)mn2;
+            return x;
+        }
+    }
+}
+
+// 8-byte shared-memory load by 32-bit shared address (volatile: stays after the copy wait)
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // 2^x on the MUFU unit (flush-to-zero); arguments here are <= 8 or -inf.
@@ -230,8 +285,11 @@ constexpr int kPieceBytes = kPbQ + 8 * 256;
 // Workspace header words used to hand the split to the combine kernel.
 constexpr int kHdrTiles = 0, kHdrCtas = 1;
 
+template <int Fmt>
 __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnArgs a)
 {
+    constexpr int kStage = stage_bytes<Fmt>();
+    constexpr int kWarpSmem = kDepth * kStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *pbuf = smem + kWarpsPerCta * kWarpSmem;                                 // [2][kPieceBytes]
@@ -289,7 +347,6 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     const int r = lane >> 2, cq = lane & 3;
     const int tr = tau(r);
     const bool gvalid = r < G;  // this lane's softmax head (rows of S^T)
-    const uint32_t M64 = 0x64646464u;
     const uint32_t ring = smem_u32(smem) + warp * kWarpSmem;
     const int per_blk = a.bs / kTile;  // tiles per block
     const uint32_t nthr = kAttnThreads;
@@ -358,13 +415,17 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
             const uint8_t *vp = a.vpool + row0 * kD;
             // whole 128-byte rows: lane l copies 16-byte column l % 8 of rows 4i + l / 8, stored
             // at column (l % 8) ^ (row % 8) so the fragment reads below hit 8 distinct columns
-            const uint32_t dst = ring + st * kTileSmem;
+            const uint32_t dst = ring + st * kStage;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int row = 4 * i + (lane >> 3), col = lane & 7;
                 const uint32_t off = row * kD + ((col ^ (row & 7)) << 4);
                 cp_async16(dst + off, kp + row * kD + col * 16);
                 cp_async16(dst + kTileBytes + off, vp + row * kD + col * 16);
+            }
+            if constexpr (Fmt == kDecFixed) {  // lanes 0-15: K parameters of token lane; 16-31: V
+                const float4 *src = (lane < 16 ? a.kpar : a.vpar) + row0 + (lane & 15);
+                cp_async16(dst + kTileSmem + lane * 16, src);
             }
         }
         cp_async_commit();
@@ -433,8 +494,16 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
             const int32_t valid = min(kTile, cur.L - tok0);
             if (valid > 0) {
                 // segment constants (record words: start 2..6, k_min 7.., k_scale 12.., v_min 17.., v_scale 22..)
-                const int sg = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
-                if (sg != seg) {
+                const int sg = Fmt != kDecAffine
+                                   ? 0
+                                   : __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
+                if (Fmt != kDecAffine && sg != seg) {  // decoded values reach the tensor cores: identity fold
+                    seg = sg;
+                    vflat = false;
+                    ak = kLog2eOverSqrtD;
+                    bk = 0.0f;
+                    cv = 0.0f;
+                } else if (sg != seg) {
                     seg = sg;
                     const float kmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 7 + sg));
                     const float kscale = __uint_as_float(__shfl_sync(0xffffffffu, recw, 12 + sg));
@@ -458,7 +527,29 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                     }
                 }
 
-                const uint32_t tile = ring + st * kTileSmem;
+                const uint32_t tile = ring + st * kStage;
+                // fixed groups: this lane's K rows tau(r), 8 + tau(r) (columns cq < 4: values 0-63;
+                // cq + 4: 64-127) and V rows cq, cq + 4, cq + 8, cq + 12 (column tau(r): half tau(r) / 4)
+                uint32_t ksc[2][2] = {{0u, 0u}, {0u, 0u}}, kmn[2][2] = {{0u, 0u}, {0u, 0u}};
+                uint32_t vsc_ab = 0u, vmn_ab = 0u, vsc_cd = 0u, vmn_cd = 0u;
+                if constexpr (Fmt == kDecFixed) {
+                    const uint32_t kpb = tile + kTileSmem, vpb = kpb + kParBytes;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) {
+                        const uint4 pw = ld_shared_v4(kpb + (8 * n + tr) * 16);
+                        kmn[n][0] = half2_bits(__uint_as_float(pw.x), __uint_as_float(pw.x));
+                        ksc[n][0] = half2_bits(__uint_as_float(pw.y), __uint_as_float(pw.y));
+                        kmn[n][1] = half2_bits(__uint_as_float(pw.z), __uint_as_float(pw.z));
+                        ksc[n][1] = half2_bits(__uint_as_float(pw.w), __uint_as_float(pw.w));
+                    }
+                    const uint32_t hv = (uint32_t)(tr >> 2) * 8;
+                    const uint2 pa = ld_shared_v2(vpb + cq * 16 + hv), pb_ = ld_shared_v2(vpb + (cq + 4) * 16 + hv);
+                    const uint2 pc = ld_shared_v2(vpb + (cq + 8) * 16 + hv), pd = ld_shared_v2(vpb + (cq + 12) * 16 + hv);
+                    vmn_ab = half2_bits(__uint_as_float(pa.x), __uint_as_float(pb_.x));
+                    vsc_ab = half2_bits(__uint_as_float(pa.y), __uint_as_float(pb_.y));
+                    vmn_cd = half2_bits(__uint_as_float(pc.x), __uint_as_float(pd.x));
+                    vsc_cd = half2_bits(__uint_as_float(pc.y), __uint_as_float(pd.y));
+                }
                 // S^T = Q K^T: two n-tiles of 8 tokens x 8 k-steps, four accumulator chains;
                 // this lane supplies rows tau(r) and 8 + tau(r), columns cq and cq + 4
                 const uint32_t kr0 = tile + tr * kD, kr1 = tile + (8 + tr) * kD;
@@ -471,12 +562,16 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                 for (int jj = 0; jj < 8; jj += 2) {
                     const uint4 &lo0 = jj < 4 ? k0 : k1;  // n-tile 0: row tau(r), columns cq | cq + 4
                     const uint4 &lo1 = jj < 4 ? k2 : k3;  // n-tile 1: row 8 + tau(r)
+                    const int hf = jj < 4 ? 0 : 1;        // which 64-value half these columns are in
                     const uint32_t w00 = word(lo0, jj & 3), w01 = word(lo0, (jj + 1) & 3);
                     const uint32_t w10 = word(lo1, jj & 3), w11 = word(lo1, (jj + 1) & 3);
-                    mma16816(sa[0], qa0[jj], 0u, qa2[jj], 0u, prmt(w00, M64, 0x4140), prmt(w00, M64, 0x4342));
-                    mma16816(sa[1], qa0[jj], 0u, qa2[jj], 0u, prmt(w10, M64, 0x4140), prmt(w10, M64, 0x4342));
-                    mma16816(sb[0], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w01, M64, 0x4140), prmt(w01, M64, 0x4342));
-                    mma16816(sb[1], qa0[jj + 1], 0u, qa2[jj + 1], 0u, prmt(w11, M64, 0x4140), prmt(w11, M64, 0x4342));
+                    const uint32_t s0 = ksc[0][hf], m0 = kmn[0][hf], s1 = ksc[1][hf], m1 = kmn[1][hf];
+                    mma16816(sa[0], qa0[jj], 0u, qa2[jj], 0u, codes2<Fmt, false>(w00, s0, m0), codes2<Fmt, true>(w00, s0, m0));
+                    mma16816(sa[1], qa0[jj], 0u, qa2[jj], 0u, codes2<Fmt, false>(w10, s1, m1), codes2<Fmt, true>(w10, s1, m1));
+                    mma16816(sb[0], qa0[jj + 1], 0u, qa2[jj + 1], 0u, codes2<Fmt, false>(w01, s0, m0),
+                             codes2<Fmt, true>(w01, s0, m0));
+                    mma16816(sb[1], qa0[jj + 1], 0u, qa2[jj + 1], 0u, codes2<Fmt, false>(w11, s1, m1),
+                             codes2<Fmt, true>(w11, s1, m1));
                 }
                 // lane scores for head r: tokens cq, cq+4 (n-tile 0) and 8+cq, 12+cq (n-tile 1)
                 float z[4];
@@ -520,7 +615,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                 // O^T += V^T P^T: rows (d) 16*tr + 2i (+1), k = tokens cq, cq+4, 8+cq, 12+cq
                 if (!vflat) {
                     // rows cq, cq + 4, cq + 8, cq + 12, column tau(r)
-                    const uint32_t vt = tile + kTileBytes;
+                    const uint32_t vt = tile + kTileBytes;  // rows cq + 4i, column tau(r)
                     const uint4 va = ld_shared_v4(vt + cq * kD + ((tr ^ cq) << 4));
                     const uint4 vb = ld_shared_v4(vt + (cq + 4) * kD + ((tr ^ (cq + 4)) << 4));
                     const uint4 vc = ld_shared_v4(vt + (cq + 8) * kD + ((tr ^ cq) << 4));
@@ -531,10 +626,12 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                         const uint32_t xab23 = prmt(word(va, wi), word(vb, wi), 0x7362);
                         const uint32_t xcd01 = prmt(word(vc, wi), word(vd, wi), 0x5140);
                         const uint32_t xcd23 = prmt(word(vc, wi), word(vd, wi), 0x7362);
-                        mma16816(o[2 * wi], prmt(xab01, M64, 0x4140), prmt(xab01, M64, 0x4342),
-                                 prmt(xcd01, M64, 0x4140), prmt(xcd01, M64, 0x4342), pb0, pb1);
-                        mma16816(o[2 * wi + 1], prmt(xab23, M64, 0x4140), prmt(xab23, M64, 0x4342),
-                                 prmt(xcd23, M64, 0x4140), prmt(xcd23, M64, 0x4342), pb0, pb1);
+                        mma16816(o[2 * wi], codes2<Fmt, false>(xab01, vsc_ab, vmn_ab),
+                                 codes2<Fmt, true>(xab01, vsc_ab, vmn_ab), codes2<Fmt, false>(xcd01, vsc_cd, vmn_cd),
+                                 codes2<Fmt, true>(xcd01, vsc_cd, vmn_cd), pb0, pb1);
+                        mma16816(o[2 * wi + 1], codes2<Fmt, false>(xab23, vsc_ab, vmn_ab),
+                                 codes2<Fmt, true>(xab23, vsc_ab, vmn_ab), codes2<Fmt, false>(xcd23, vsc_cd, vmn_cd),
+                                 codes2<Fmt, true>(xcd23, vsc_cd, vmn_cd), pb0, pb1);
                     }
                 }
             }
@@ -732,9 +829,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
 
 namespace dgq {
 
-size_t attn_smem_bytes(int32_t B, int32_t G)
+size_t attn_smem_bytes(int dec, int32_t B, int32_t G)
 {
-    return 1024 + (size_t)kWarpsPerCta * kWarpSmem + 2 * kPieceBytes + 16 + (size_t)kWarpsPerCta * G * kPartStride * 4 +
+    const int stage = dec == kDecFixed ? stage_bytes<kDecFixed>() : stage_bytes<kDecAffine>();
+    return 1024 + (size_t)kWarpsPerCta * kDepth * stage + 2 * kPieceBytes + 16 + (size_t)kWarpsPerCta * G * kPartStride * 4 +
            8 * 4 + (size_t)(2 * B + 1) * 4;
 }
 
@@ -754,10 +852,11 @@ AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm)
     return l;
 }
 
-cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const uint8_t *kpool, const uint8_t *vpool,
-                        const dgq_seg_record *table, const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen,
-                        int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
-                        void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
+cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const void *vnew, const uint8_t *kpool,
+                        const uint8_t *vpool, const dgq_seg_record *table, const float *kpar, const float *vpar,
+                        const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen, int32_t B, int32_t Hq,
+                        int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks, void *out, void *ws, int nsm,
+                        bool *map_failed, cudaStream_t stream)
 {
     *map_failed = false;
     const int32_t G = Hq / Hkv;
@@ -770,6 +869,8 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.kpool = kpool;
     a.vpool = vpool;
     a.table = table;
+    a.kpar = reinterpret_cast<const float4 *>(kpar);
+    a.vpar = reinterpret_cast<const float4 *>(vpar);
     a.bt = bt;
     a.seq_lens = seq_lens;
     a.out = static_cast<uint16_t *>(out);
@@ -784,31 +885,36 @@ cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const
     a.max_blocks = max_blocks;
     a.num_blocks = num_blocks;
 
-    // per-device launch shape, computed once per (device, shared-memory size)
-    static int cached_dev = -1;
-    static size_t cached_smem = 0;
-    static int cached_occ = 0;
+    // the kernel instance for the code format (the symmetric INT8 cache is an affine one)
+    const int dec = format == DGQ_FORMAT_FP8_E4M3 ? kDecFp8 : (format == DGQ_FORMAT_FIXED64 ? kDecFixed : kDecAffine);
+    void (*kern)(AttnArgs) = dec == kDecFp8 ? attn_kernel<kDecFp8>
+                                            : (dec == kDecFixed ? attn_kernel<kDecFixed> : attn_kernel<kDecAffine>);
+
+    // per-device launch shape, computed once per (instance, device, shared-memory size)
+    static int cached_dev[3] = {-1, -1, -1};
+    static size_t cached_smem[3] = {0, 0, 0};
+    static int cached_occ[3] = {0, 0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const size_t smem = attn_smem_bytes(B, G);
-    if (dev != cached_dev || smem != cached_smem) {
-        e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = attn_smem_bytes(dec, B, G);
+    if (dev != cached_dev[dec] || smem != cached_smem[dec]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel, kAttnThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAttnThreads, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) return cudaErrorInvalidConfiguration;
-        cached_dev = dev;
-        cached_smem = smem;
-        cached_occ = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
+        cached_dev[dec] = dev;
+        cached_smem[dec] = smem;
+        cached_occ[dec] = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
     }
     // upper bound on tiles (every request at max_seqlen): no more CTAs than tiles
     const int64_t tiles = (int64_t)B * Hkv * (max_seqlen > 0 ? (max_seqlen + kTile - 1) / kTile : 1);
-    int64_t grid = (int64_t)nsm * cached_occ;
+    int64_t grid = (int64_t)nsm * cached_occ[dec];
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
-    attn_kernel<<<(unsigned)grid, kAttnThreads, smem, stream>>>(a);
+    kern<<<(unsigned)grid, kAttnThreads, smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -205,6 +205,27 @@ dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16, con
                                  int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
                                  void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
+    return dgq_paged_decode_attn_format(DGQ_FORMAT_DGQ, q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table,
+                                        nullptr, nullptr, block_tables_dev, seq_lens_dev, max_seqlen, batch,
+                                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                        num_blocks, out_bf16, workspace, workspace_bytes, cuda_stream);
+}
+
+dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, const void *k_new_bf16,
+                                        const void *v_new_bf16, const uint8_t *k_pool, const uint8_t *v_pool,
+                                        const dgq_seg_record *seg_table, const float *k_group_params,
+                                        const float *v_group_params, const int32_t *block_tables_dev,
+                                        const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                        void *out_bf16, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (format != DGQ_FORMAT_DGQ && format != DGQ_FORMAT_FIXED64 && format != DGQ_FORMAT_SYM_INT8 &&
+        format != DGQ_FORMAT_FP8_E4M3)
+        return DGQ_ERR_INVALID_ARG;
+    if (format == DGQ_FORMAT_FIXED64 && (!k_group_params || !v_group_params || !aligned16(k_group_params) ||
+                                         !aligned16(v_group_params)))
+        return DGQ_ERR_INVALID_ARG;
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
     if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -229,11 +250,52 @@ dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16, con
         workspace_bytes < dgq::attn_layout(batch, num_q_heads, num_kv_heads, nsm).total)
         return DGQ_ERR_WORKSPACE;
     bool map_failed = false;
-    cudaError_t e = dgq::launch_attn(q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table, block_tables_dev,
-                                     seq_lens_dev, max_seqlen, batch, num_q_heads, num_kv_heads, block_size,
-                                     max_blocks_per_seq, num_blocks, out_bf16, workspace, nsm, &map_failed,
-                                     static_cast<cudaStream_t>(cuda_stream));
+    cudaError_t e = dgq::launch_attn(format, q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table,
+                                     k_group_params, v_group_params, block_tables_dev, seq_lens_dev, max_seqlen,
+                                     batch, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq, num_blocks,
+                                     out_bf16, workspace, nsm, &map_failed, static_cast<cudaStream_t>(cuda_stream));
     if (map_failed) return DGQ_ERR_INVALID_ARG;
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+size_t dgq_encode_format_workspace_size(int32_t batch, int32_t num_kv_heads)
+{
+    if (batch <= 0 || num_kv_heads <= 0) return 0;
+    return dgq::format_workspace_bytes(batch, num_kv_heads);
+}
+
+dgq_status dgq_encode_format(int32_t format, const void *k_bf16, const void *v_bf16, int32_t total_tokens,
+                             const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                             int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                             dgq_seg_record *seg_table, float *k_group_params, float *v_group_params,
+                             void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (format != DGQ_FORMAT_FIXED64 && format != DGQ_FORMAT_SYM_INT8 && format != DGQ_FORMAT_FP8_E4M3)
+        return DGQ_ERR_INVALID_ARG;
+    if (format == DGQ_FORMAT_FIXED64 && (!k_group_params || !v_group_params || !aligned16(k_group_params) ||
+                                         !aligned16(v_group_params)))
+        return DGQ_ERR_INVALID_ARG;
+    if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || total_tokens < 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    if ((int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size) return DGQ_ERR_INVALID_ARG;
+    // grid: one CTA column per (request, head) pair, one row per 256 tokens
+    if ((int64_t)batch * num_kv_heads >= INT32_MAX || (max_seqlen + 255) / 256 > 65535 ||
+        (int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX)
+        return DGQ_ERR_UNSUPPORTED;
+    if (!k_bf16 || !v_bf16 || !cu_seqlens_dev || !block_tables_dev || !k_pool || !v_pool || !seg_table)
+        return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(seg_table) || !aligned16(cu_seqlens_dev) || !aligned16(block_tables_dev))
+        return DGQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < dgq::format_workspace_bytes(batch, num_kv_heads))
+        return DGQ_ERR_WORKSPACE;
+    const cudaError_t e = dgq::launch_format_encode(
+        format, k_bf16, v_bf16, total_tokens, cu_seqlens_dev, batch, max_seqlen, num_kv_heads, block_size,
+        block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks, k_group_params, v_group_params, seg_table,
+        workspace, static_cast<cudaStream_t>(cuda_stream));
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 

@@ -47,10 +47,20 @@ struct AttnLayout {
     size_t off_count, off_part, total;
 };
 AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm);
-cudaError_t launch_attn(const void *q, const void *knew, const void *vnew, const uint8_t *kpool, const uint8_t *vpool,
-                        const dgq_seg_record *table, const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen,
-                        int32_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks,
-                        void *out, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+// format: a dgq_format (DGQ and SYM_INT8 decode through the records; kpar / vpar are read for
+// FIXED64 only).
+cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const void *vnew, const uint8_t *kpool,
+                        const uint8_t *vpool, const dgq_seg_record *table, const float *kpar, const float *vpar,
+                        const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen, int32_t B, int32_t Hq,
+                        int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks, void *out, void *ws, int nsm,
+                        bool *map_failed, cudaStream_t stream);
+
+// Comparison encodings (FIXED64, SYM_INT8, FP8_E4M3) of packed rows into the paged cache.
+size_t format_workspace_bytes(int32_t B, int32_t Hkv);
+cudaError_t launch_format_encode(int32_t format, const void *k, const void *v, int32_t T, const int32_t *cu, int32_t B,
+                                 int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt, int32_t max_blocks,
+                                 uint8_t *kpool, uint8_t *vpool, int32_t num_blocks, float *kpar, float *vpar,
+                                 dgq_seg_record *table, void *ws, cudaStream_t stream);
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
                           const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,

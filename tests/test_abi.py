@@ -122,6 +122,44 @@ def test_append_rejects_bad_arguments_before_launch(L):
     assert _append(L, wsb=255) == WORKSPACE
 
 
+def _encode(L, **kw):
+    a = dict(fmt=1, k=FAKE, v=FAKE, T=337, cu=FAKE, batch=2, max_seqlen=300, hkv=2, d=128, bs=16, bt=FAKE,
+             max_blocks=19, kp=FAKE, vp=FAKE, nb=32, table=FAKE, kpar=FAKE, vpar=FAKE, ws=FAKE, wsb=1 << 20, stream=0)
+    a.update(kw)
+    return L.dgq_encode_format(a["fmt"], a["k"], a["v"], a["T"], a["cu"], a["batch"], a["max_seqlen"], a["hkv"],
+                               a["d"], a["bs"], a["bt"], a["max_blocks"], a["kp"], a["vp"], a["nb"], a["table"],
+                               a["kpar"], a["vpar"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_encode_format_rejects_bad_arguments_before_launch(L):
+    for fmt in (0, 4, -1):                               # DGQ itself is dgq_compress; unknown ids
+        assert _encode(L, fmt=fmt) == INVALID, fmt
+    assert _encode(L, kpar=0) == INVALID                 # fixed groups need their parameter arrays
+    assert _encode(L, vpar=FAKE + 4) == INVALID
+    assert _encode(L, d=64) == UNSUPPORTED
+    assert _encode(L, bs=8) == UNSUPPORTED
+    assert _encode(L, k=0) == INVALID
+    assert _encode(L, T=-1) == INVALID
+    assert _encode(L, max_seqlen=305) == INVALID         # > max_blocks * bs
+    assert _encode(L, ws=0) == WORKSPACE
+    need = L.dgq_encode_format_workspace_size(2, 2)
+    assert need >= 256 + 2 * 2 * 8
+    assert _encode(L, wsb=need - 1) == WORKSPACE
+    assert L.dgq_encode_format_workspace_size(0, 2) == 0
+
+
+def test_attn_format_rejects_bad_arguments_before_launch(L):
+    def call(fmt, kpar=FAKE, vpar=FAKE, d=128):
+        return L.dgq_paged_decode_attn_format(fmt, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, kpar, vpar, FAKE, FAKE, 300,
+                                              2, 4, 2, d, 16, 19, 32, FAKE, FAKE, 1 << 30, 0)
+    assert call(5) == INVALID
+    assert call(-1) == INVALID
+    assert call(1, kpar=0) == INVALID                    # fixed groups need their parameter arrays
+    assert call(1, vpar=FAKE + 8) == INVALID
+    for fmt in (0, 1, 2, 3):
+        assert call(fmt, d=64) == UNSUPPORTED, fmt
+
+
 def test_workspace_size_is_monotone(L):
     a = L.dgq_compress_workspace_size(4, 1000, 8)
     b = L.dgq_compress_workspace_size(4, 2000, 8)

@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the two-phase (chunked prefill) compression timing after the timed steps")
     ap.add_argument("--no-formats", action="store_true",
                     help="skip the comparison encodings (fixed64, sym_int8, fp8_e4m3) after the timed steps")
     ap.add_argument("--paged-input", action="store_true",
@@ -435,6 +437,9 @@ def run_ours(args):
 
     ref0 = request0_reference(w, lens, layers[0]) if rank == 0 else None
     fidelity = fidelity_check(w, layers[0], ref0) if rank == 0 else None
+    prefill = None
+    if not args.no_prefill:
+        prefill = time_prefill(w, lens, cu, bt, layers, d_bt, d_lens, max_seqlen, sp, comp_b, max(2, min(args.steps, 5)))
     formats = None
     if not args.no_formats:
         formats = time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0,
@@ -492,6 +497,7 @@ def run_ours(args):
                             "device->host copy of the outputs, the step's token appended to every layer's cache"},
             "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
             "fidelity": fidelity,
+            "prefill_two_phase": prefill,
             "formats": formats,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
@@ -590,6 +596,84 @@ def fidelity_check(w, layer0, ref):
             "gpu_vs_oracle": err(got, cache), "others_fp64_vs_unquantised": comparison,
             "sample": f"request 0 ({L} tokens), all {w.hq} query heads, layer 0; unquantised = fp64 "
                       "attention over the original bf16 K/V"}
+
+
+def time_prefill(w, lens, cu, bt, layers, d_bt, d_lens, max_seqlen, sp, comp_b, reps, max_layers=8):
+    """Compression in two phases as chunked prefill would run it, outside the timed steps.  Per
+    layer (up to `max_layers`), chunk by chunk: the chunk's bf16 K/V are written into a bf16 paged
+    cache (standing in for the prefill kernels; not timed), then dgq_prefill_chunk_stats on that
+    chunk (timed: the chunk is in L2, as right after prefill wrote it); at the end
+    dgq_prefill_finish (timed).  Against it, dgq_compress_paged on the same complete cache.  The
+    chunk covers about 32 MB of K+V (at most 8192 tokens per request)."""
+    import numpy as np
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    dev = layers[0]["k"].device
+    B, Hkv, bs = w.batch, w.hkv, w.block_size
+    nb = layers[0]["kp"].shape[0]
+    C = int(min(8192, max(16, (32 << 20) // (B * Hkv * 512)))) // 16 * 16
+    nchunks = (int(lens.max()) + C - 1) // C
+    chunks = []
+    for c in range(nchunks):  # packed rows, blocks and slots of chunk c's tokens
+        rows, blks, slots = [], [], []
+        for b, L in enumerate(lens):
+            t = np.arange(min(c * C, int(L)), min((c + 1) * C, int(L)))
+            rows.append(int(cu[b]) + t)
+            blks.append(bt[b, t // bs])
+            slots.append(t % bs)
+        beg = np.minimum(c * C, lens).astype(np.int32)
+        end = np.minimum((c + 1) * C, lens).astype(np.int32)
+        chunks.append(tuple(torch.from_numpy(np.concatenate(x).astype(np.int64)).to(dev) for x in (rows, blks, slots))
+                      + (torch.from_numpy(beg).to(dev), torch.from_numpy(end).to(dev)))
+    use = layers[:max_layers]
+    ks = torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vs = torch.zeros_like(ks)
+    W = (max_seqlen + 15) // 16
+    stats = torch.zeros((B, Hkv, W, 8), dtype=torch.float32, device=dev)
+    ws = torch.zeros(dgq.dgq_prefill_workspace_size(B, Hkv), dtype=torch.uint8, device=dev)
+    cws = torch.zeros(dgq.dgq_compress_workspace_size(B, max_seqlen, Hkv), dtype=torch.uint8, device=dev)
+    t_stats = t_fin = t_one = 0.0
+    same = True
+    for r in range(reps + 1):  # the first pass warms up
+        for L in use:
+            evs = []  # no synchronisation between chunks: each statistics launch queues behind the
+            for rows, blks, slots, beg, end in chunks:  # chunk's write, so its events time the kernel
+                ks[blks, :, slots, :] = L["k"][rows]  # the prefill's write of this chunk
+                vs[blks, :, slots, :] = L["v"][rows]
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                dgq.dgq_prefill_chunk_stats(ks, vs, d_bt, beg, end, max_seqlen, stats, ws, sp)
+                e1.record()
+                evs.append((e0, e1))
+            e2, e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e2.record()
+            dgq.dgq_prefill_finish(ks, vs, d_bt, d_lens, max_seqlen, stats, d_bt, L["kp"], L["vp"], L["table"], ws, sp)
+            e3.record()
+            torch.cuda.synchronize()
+            s_ms = sum(a.elapsed_time(b) for a, b in evs)
+            tab = L["table"].clone() if r == reps and L is use[0] else None
+            e3b = torch.cuda.Event(enable_timing=True)
+            e3b.record()
+            dgq.dgq_compress_paged(ks, vs, d_bt, torch.from_numpy(cu).to(dev), max_seqlen, bs, d_bt, L["kp"],
+                                   L["vp"], L["table"], cws, sp)
+            e4.record()
+            torch.cuda.synchronize()
+            if tab is not None:
+                same = bool(torch.equal(tab, L["table"]))
+            if r > 0:
+                t_stats += s_ms
+                t_fin += e2.elapsed_time(e3)
+                t_one += e3b.elapsed_time(e4)
+    n = reps * len(use)
+    err = dgq.dgq_workspace_error(ws, sp) or dgq.dgq_workspace_error(cws, sp)
+    st_us, fin_us, one_us = t_stats / n * 1e3, t_fin / n * 1e3, t_one / n * 1e3
+    return {"chunk_tokens": C, "chunks": nchunks, "layers_timed": len(use),
+            "stats_us_per_layer": round(st_us, 2), "finish_us_per_layer": round(fin_us, 2),
+            "total_us_per_layer": round(st_us + fin_us, 2), "gbs": round(comp_b / (st_us + fin_us) / 1e3, 1),
+            "one_shot_paged_us_per_layer": round(one_us, 2), "one_shot_gbs": round(comp_b / one_us / 1e3, 1),
+            "records_identical_to_one_shot": same, "device_error": err,
+            "what": "statistics per prefill chunk right after the chunk is written (L2-hot), then one "
+                    "finishing pass; bytes as for compress (2 B read + 1 B written per K/V value)"}
 
 
 def time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0, reps):

@@ -171,6 +171,50 @@ dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, in
                               size_t workspace_bytes, const dgq_compress_options *options, void *cuda_stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Compression in two phases, for chunked prefill.  dgq_compress_paged reads the bf16 cache
+ * twice from HBM (statistics, then codes).  When prefill writes a long request chunk by chunk,
+ * the statistics of each chunk can be taken right after the chunk is written, while it is
+ * still in L2; the finishing call then reads the cache from HBM once, for the codes.  Results
+ * are identical to dgq_compress_paged on the complete cache (a window's statistics depend on
+ * its 16 tokens only; segmentation and codes need the whole request, so they wait for the end).
+ * [DGQ] section 3.2 (compression inside the inference pipeline); [PAGED] chunked prefill into
+ * the paged cache.
+ *
+ * window_stats     [batch, Hkv, max_windows, 8] fp32, device, caller-owned: per 16-token window
+ *                  (mean variance, K min, K max, V min, V max, 3 zeros); max_windows >=
+ *                  ceil(max_seqlen / 16).  Written by dgq_prefill_chunk_stats, read by
+ *                  dgq_prefill_finish.
+ * workspace        >= dgq_prefill_workspace_size(batch, Hkv) bytes, zero-filled before first use.
+ * The bf16 source (k_src, v_src, src block tables) is as for dgq_compress_paged.
+ */
+size_t dgq_prefill_workspace_size(int32_t batch, int32_t num_kv_heads);
+
+/* Statistics of the windows of tokens [chunk_begin[b], chunk_end[b]) of every request b (device
+ * arrays [batch] int32).  chunk_begin[b] is a multiple of 16; chunk_end[b] is a multiple of 16
+ * unless the chunk is the request's last one (its partial last window is averaged over its own
+ * tokens, as in dgq_compress); an empty range (begin == end) skips the request.  A range that is
+ * not window-aligned or ends past max_seqlen is flagged in the workspace and skipped. */
+dgq_status dgq_prefill_chunk_stats(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                                   const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                                   const int32_t *chunk_begin_dev, const int32_t *chunk_end_dev, int32_t batch,
+                                   int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   float *window_stats, int32_t max_windows, void *workspace, size_t workspace_bytes,
+                                   void *cuda_stream);
+
+/* Segmentation of every (request, head) from window_stats (every window of tokens
+ * [0, seq_lens[b]) must have been written by earlier dgq_prefill_chunk_stats calls), then the
+ * codes of all tokens from the bf16 cache into the INT8 pools and the records, as
+ * dgq_compress_paged with the same options would write them.  Two launches. */
+dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                              const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                              const int32_t *seq_lens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, const float *window_stats, int32_t max_windows,
+                              const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                              uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table,
+                              const dgq_compress_options *options, void *workspace, size_t workspace_bytes,
+                              void *cuda_stream);
+
+/* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
  * paged cache plus the step's own (unquantised) key and value.
  *

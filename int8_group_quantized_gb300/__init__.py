@@ -28,7 +28,8 @@ __all__ = [
     "DGQError", "lib", "dgq_compress", "dgq_compress_paged", "dgq_compress_workspace_size", "dgq_append",
     "dgq_append_workspace_size",
     "dgq_paged_decode_attn", "dgq_encode_format", "dgq_encode_format_workspace_size",
-    "dgq_paged_decode_attn_format", "FORMATS",
+    "dgq_paged_decode_attn_format", "FORMATS", "dgq_prefill_workspace_size", "dgq_prefill_chunk_stats",
+    "dgq_prefill_finish",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -78,6 +79,13 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn_format.argtypes = [i32, P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                    i32, i32, P, P, sz, P]
         L.dgq_paged_decode_attn_format.restype = ctypes.c_int
+        L.dgq_prefill_workspace_size.argtypes = [i32, i32]
+        L.dgq_prefill_workspace_size.restype = sz
+        L.dgq_prefill_chunk_stats.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, P, i32, P, sz, P]
+        L.dgq_prefill_chunk_stats.restype = ctypes.c_int
+        L.dgq_prefill_finish.argtypes = [P, P, i32, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, i32, P,
+                                         P, P, sz, P]
+        L.dgq_prefill_finish.restype = ctypes.c_int
         L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
         L.dgq_append.restype = ctypes.c_int
         L.dgq_append_workspace_size.argtypes = []
@@ -225,6 +233,39 @@ def dgq_paged_decode_attn(q, k_new, v_new, k_pool, v_pool, seg_table, block_tabl
                                        B, Hq, Hkv, D, k_pool.shape[2], block_tables.shape[1], k_pool.shape[0],
                                        _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
            "dgq_paged_decode_attn")
+
+
+def dgq_prefill_workspace_size(batch: int, num_kv_heads: int) -> int:
+    return int(lib().dgq_prefill_workspace_size(batch, num_kv_heads))
+
+
+def dgq_prefill_chunk_stats(k_src, v_src, src_block_tables, chunk_begin, chunk_end, max_seqlen, window_stats,
+                            workspace, stream=None) -> None:
+    """Window statistics of tokens [chunk_begin[b], chunk_end[b]) of each request (int32 CUDA
+    tensors [B]) from the bf16 paged cache k_src / v_src [num_src_blocks, Hkv, bs, 128] into
+    window_stats fp32 [B, Hkv, max_windows, 8]; workspace: dgq_prefill_workspace_size bytes."""
+    B = chunk_begin.shape[0]
+    _, Hkv, bs, D = k_src.shape
+    _check(lib().dgq_prefill_chunk_stats(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(src_block_tables),
+                                         src_block_tables.shape[1], _ptr(chunk_begin), _ptr(chunk_end), B,
+                                         int(max_seqlen), Hkv, D, bs, _ptr(window_stats), window_stats.shape[2],
+                                         _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dgq_prefill_chunk_stats")
+
+
+def dgq_prefill_finish(k_src, v_src, src_block_tables, seq_lens, max_seqlen, window_stats, block_tables, k_pool,
+                       v_pool, seg_table, workspace, stream=None, max_groups=MAX_SEG, min_var=0.0) -> None:
+    """Segmentation from window_stats and codes of every token [0, seq_lens[b]) into the INT8
+    pools / records (as dgq_compress_paged with the same settings would write them)."""
+    B = seq_lens.shape[0]
+    _, Hkv, bs, D = k_src.shape
+    opts = CompressOptions(int(max_groups), float(min_var))
+    _check(lib().dgq_prefill_finish(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(src_block_tables),
+                                    src_block_tables.shape[1], _ptr(seq_lens), B, int(max_seqlen), Hkv, D, bs,
+                                    _ptr(window_stats), window_stats.shape[2], _ptr(block_tables),
+                                    block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                    _ptr(seg_table), ctypes.byref(opts), _ptr(workspace), _nbytes(workspace),
+                                    _stream(stream)), "dgq_prefill_finish")
 
 
 def _format_id(fmt) -> int:

@@ -23,6 +23,7 @@ UNITS = {
     "dgq_compress_cluster.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_append.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_formats.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
+    "dgq_prefill.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true"],
     "dgq_attn.cu": [],
     "dgq_host.cu": [],
     "dgq_noalloc.cu": [],

@@ -258,6 +258,106 @@ dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, cons
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
 
+size_t dgq_prefill_workspace_size(int32_t batch, int32_t num_kv_heads)
+{
+    if (batch <= 0 || num_kv_heads <= 0) return 0;
+    return dgq::prefill_workspace_bytes(batch, num_kv_heads);
+}
+
+namespace {
+
+// Checks shared by the two prefill calls (source, sizes, statistics array, workspace).
+dgq_status prefill_checks(const void *k_src, const void *v_src, int32_t num_src_blocks, const int32_t *src_bt,
+                          int32_t max_src_blocks, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, const void *stats, int32_t max_windows,
+                          const void *workspace, size_t workspace_bytes)
+{
+    if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || batch > kMaxBatch || max_seqlen < 0 || num_kv_heads <= 0 || num_src_blocks <= 0 ||
+        max_src_blocks <= 0)
+        return DGQ_ERR_INVALID_ARG;
+    if ((int64_t)max_seqlen > (int64_t)max_src_blocks * block_size) return DGQ_ERR_INVALID_ARG;
+    if (max_windows < (max_seqlen + DGQ_WINDOW - 1) / DGQ_WINDOW || max_windows <= 0) return DGQ_ERR_INVALID_ARG;
+    const int64_t windows = (int64_t)batch * num_kv_heads * max_windows;
+    if (windows >= INT32_MAX || (int64_t)num_src_blocks * num_kv_heads * block_size >= INT32_MAX)
+        return DGQ_ERR_UNSUPPORTED;
+    if (!k_src || !v_src || !src_bt || !stats) return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(src_bt) || !aligned16(stats))
+        return DGQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < dgq::prefill_workspace_bytes(batch, num_kv_heads))
+        return DGQ_ERR_WORKSPACE;
+    return DGQ_OK;
+}
+
+}  // namespace
+
+dgq_status dgq_prefill_chunk_stats(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                                   const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                                   const int32_t *chunk_begin_dev, const int32_t *chunk_end_dev, int32_t batch,
+                                   int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   float *window_stats, int32_t max_windows, void *workspace, size_t workspace_bytes,
+                                   void *cuda_stream)
+{
+    dgq_status st = prefill_checks(k_src_bf16, v_src_bf16, num_src_blocks, src_block_tables_dev,
+                                   max_src_blocks_per_seq, batch, max_seqlen, num_kv_heads, head_dim, block_size,
+                                   window_stats, max_windows, workspace, workspace_bytes);
+    if (st != DGQ_OK) return st;
+    if (!chunk_begin_dev || !chunk_end_dev || !aligned16(chunk_begin_dev) || !aligned16(chunk_end_dev))
+        return DGQ_ERR_INVALID_ARG;
+    int nsm = 0;
+    if (device_sm_count(&nsm) != 0) return DGQ_ERR_CUDA;
+    const dgq::SourceDesc src = {k_src_bf16, v_src_bf16, 0, src_block_tables_dev, max_src_blocks_per_seq,
+                                 num_src_blocks};
+    bool map_failed = false;
+    const cudaError_t e = dgq::launch_prefill_stats(src, chunk_begin_dev, chunk_end_dev, batch, max_seqlen,
+                                                    num_kv_heads, block_size, window_stats, max_windows, workspace,
+                                                    nsm, &map_failed, static_cast<cudaStream_t>(cuda_stream));
+    if (map_failed) return DGQ_ERR_INVALID_ARG;
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
+dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                              const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                              const int32_t *seq_lens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, const float *window_stats, int32_t max_windows,
+                              const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
+                              uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table,
+                              const dgq_compress_options *options, void *workspace, size_t workspace_bytes,
+                              void *cuda_stream)
+{
+    dgq::GroupSettings gs = {DGQ_MAX_SEG, 0.0f};
+    if (options) {
+        if (options->max_groups < 1 || options->max_groups > DGQ_MAX_SEG || !(options->min_var >= 0.0f) ||
+            !(options->min_var <= 3.4e38f))
+            return DGQ_ERR_INVALID_ARG;
+        gs.max_groups = options->max_groups;
+        gs.min_var = options->min_var;
+    }
+    dgq_status st = prefill_checks(k_src_bf16, v_src_bf16, num_src_blocks, src_block_tables_dev,
+                                   max_src_blocks_per_seq, batch, max_seqlen, num_kv_heads, head_dim, block_size,
+                                   window_stats, max_windows, workspace, workspace_bytes);
+    if (st != DGQ_OK) return st;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+        (int64_t)max_seqlen > (int64_t)max_blocks_per_seq * block_size ||
+        (int64_t)num_blocks * num_kv_heads * block_size >= INT32_MAX)
+        return DGQ_ERR_INVALID_ARG;
+    if (!seq_lens_dev || !block_tables_dev || !k_pool || !v_pool || !seg_table) return DGQ_ERR_INVALID_ARG;
+    if (!aligned16(seq_lens_dev) || !aligned16(block_tables_dev) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(seg_table))
+        return DGQ_ERR_INVALID_ARG;
+    int nsm = 0;
+    if (device_sm_count(&nsm) != 0) return DGQ_ERR_CUDA;
+    const dgq::SourceDesc src = {k_src_bf16, v_src_bf16, 0, src_block_tables_dev, max_src_blocks_per_seq,
+                                 num_src_blocks};
+    bool map_failed = false;
+    const cudaError_t e = dgq::launch_prefill_finish(
+        src, seq_lens_dev, batch, max_seqlen, num_kv_heads, block_size, window_stats, max_windows, block_tables_dev,
+        max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, gs, workspace, nsm, &map_failed,
+        static_cast<cudaStream_t>(cuda_stream));
+    if (map_failed) return DGQ_ERR_INVALID_ARG;
+    return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
+}
+
 size_t dgq_encode_format_workspace_size(int32_t batch, int32_t num_kv_heads)
 {
     if (batch <= 0 || num_kv_heads <= 0) return 0;

@@ -1,0 +1,429 @@
+// dgq_prefill.cu -- DGQ compression in two phases for chunked prefill (sm_103a): the window
+// statistics of each prefill chunk are taken as soon as the chunk's bf16 K/V are in the paged
+// cache (while they are still in L2), and one finishing call segments every (request, head) from
+// the accumulated statistics and writes the codes in a single pass over the bf16 cache.
+//
+// Method ("DeepSeek KV-cache dynamic group quantisation (DGQ)" article, sections 2.2 and 3.2):
+// the same per-token variance, 16-token window means, n_groups-1 largest jumps, per-segment
+// min/max and codes as dgq_compress -- a window's statistics depend only on its own 16 tokens,
+// so computing them chunk by chunk changes nothing.  The paged bf16 source follows the
+// "PagedAttention implementation" section of the DeepSeek-V4 KV-cache article; the point of the
+// split is that K/V do not travel from HBM twice (the DeepSeek-V4 article's chunked-prefill
+// remark; DGQ section 3.2 on keeping compression inside the inference pipeline).
+//
+// GPU design.
+//  * Statistics and codes: sixteen warps per SM stream the windows of the call (a flat list over
+//    (request, head, window)) through one shared-memory slot each, one TMA tile copy per tensor
+//    and window (the 5-D paged tile map of dgq_window.cuh), and run the shared window arithmetic
+//    (window_stats / window_quant) on them.  Measured on this GPU: 16 warps with one window in
+//    flight each beat 8 or 12 warps with two (the statistics of an L2-resident chunk are bound
+//    by the latency of the window arithmetic, not by bandwidth).
+//  * Segmentation: one CTA of eight warps per (request, head): every thread keeps the top four
+//    jumps (descending, earlier window first) of its strided share of the windows, each warp
+//    reduces its lanes' lists to its own top k, warp 0 merges the eight lists, and the CTA
+//    reduces the per-segment extremes; the record and the quantiser parameters follow from
+//    make_params.  Compiled with -fmad=false.
+#include "dgq_device.cuh"
+#include "dgq.h"
+#include "dgq_launch.h"
+#include "dgq_window.cuh"
+
+#include <stdint.h>
+
+namespace dgq {
+
+constexpr int kPfWarps = 16;                      // worker warps per CTA (statistics and codes)
+constexpr int kPfSlots = 1;                       // windows in flight per warp
+constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kPfRingBytes = kPfWarps * kPfSlots * kWinBytes;
+constexpr int kSegThreads = 256;                  // segmentation CTA (one per pair)
+constexpr int32_t kMaxPrefillBatch = 8192;       // the library's per-call batch limit
+constexpr int kStatFloats = 8;                    // per window: mean, k min, k max, v min, v max, 0, 0, 0
+
+struct PrefillArgs {
+    TileSource src;
+    const int32_t *begin;  // statistics: first token of each request's chunk (a multiple of 16)
+    const int32_t *end;    // statistics: one past its last token; codes: the request's length
+    const int32_t *bt;     // codes: destination block table
+    uint8_t *kpool, *vpool;
+    float *stats;          // [B, Hkv, max_windows, 8]
+    dgq_seg_record *table;
+    PairParams *params;    // [B * Hkv] quantiser parameters (workspace)
+    WsHeader *hdr;
+    int32_t B, Hkv, bs, max_windows, max_blocks, num_blocks, max_seqlen;
+    int32_t max_groups;
+    float min_var;
+};
+
+// Windows of request b in this call: [w0, w1).  Statistics: the chunk's windows; codes: all of
+// the request's.  A range that the call's sizes cannot hold is flagged and dropped.
+__device__ __forceinline__ void pf_range(const PrefillArgs &a, bool quant, int32_t b, int32_t &w0, int32_t &w1)
+{
+    const int32_t t0 = quant ? 0 : __ldg(a.begin + b), t1 = __ldg(a.end + b);
+    w0 = w1 = 0;
+    if (t0 < 0 || t1 < t0 || t1 > a.max_seqlen || (t0 & (kWin - 1)) != 0) {
+        if (t1 != t0) record_error(a.hdr, kErrBadLength);
+        return;
+    }
+    w0 = t0 / kWin;
+    w1 = (t1 + kWin - 1) / kWin;
+}
+
+// Statistics (quant == false) or codes (quant == true) of every window of the call.
+template <bool quant>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_window_kernel(const __grid_constant__ PrefillArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_smem_1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kPfRingBytes);  // [kPfWarps][kPfSlots]
+    int32_t *s_pre = reinterpret_cast<int32_t *>(full + kPfSlots * kPfWarps);  // [B + 1] window prefix
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t B = a.B, Hkv = a.Hkv;
+
+    if (tid < kPfSlots * kPfWarps) mbar_init(&full[tid], 1);
+    if (tid == 0) fence_barrier_init();
+    if (warp == 0) {  // exclusive scan of Hkv * (windows of request b)
+        int32_t carry = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int i = base + lane;
+            int32_t v = 0;
+            if (i < B) {
+                int32_t w0, w1;
+                pf_range(a, quant, i, w0, w1);
+                v = Hkv * (w1 - w0);
+            }
+            int32_t x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (i < B) s_pre[i] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) s_pre[B] = carry;
+    }
+    __syncthreads();
+    const int32_t total = s_pre[B];
+    const int32_t nwarps = gridDim.x * kPfWarps;
+    const uint32_t ring = smem_u32(smem) + warp * kPfSlots * kWinBytes;
+    uint64_t *bars = full + kPfSlots * warp;
+    const uint64_t pol = quant ? make_policy_evict_first() : make_policy_evict_normal();
+
+    struct Loc {
+        int32_t b, h, w, t1;
+    };
+    auto locate = [&](int32_t x) -> Loc {
+        int32_t lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (s_pre[mid] <= x) lo = mid;
+            else hi = mid - 1;
+        }
+        int32_t w0, w1;
+        pf_range(a, quant, lo, w0, w1);
+        const int32_t off = x - s_pre[lo], n = w1 - w0;
+        Loc l;
+        l.b = lo;
+        l.h = off / n;
+        l.w = w0 + (off - l.h * n);
+        l.t1 = __ldg(a.end + lo);
+        return l;
+    };
+    auto issue = [&](int32_t x, int slot) {
+        if (x < total && lane == 0) {
+            const Loc l = locate(x);
+            fence_proxy_async_smem();  // the slot's earlier reads come before the copy
+            load_window(ring + slot * kWinBytes, bars + slot, a.src, l.b, l.h, 0, l.w * kWin, pol, a.hdr);
+        }
+    };
+
+    const int32_t nw = nwarps;
+    int32_t x = blockIdx.x * kPfWarps + warp;
+#pragma unroll
+    for (int k = 0; k < kPfSlots; ++k) issue(x + k * nw, k);
+    uint32_t phase = 0;  // bit s: parity of ring slot s's next completion
+    int slot = 0;
+    bool failed = false;
+    for (; x < total; x += nw, slot = slot + 1 == kPfSlots ? 0 : slot + 1) {
+        const Loc l = locate(x);
+        if (!mbar_wait_bounded(bars + slot, (phase >> slot) & 1u)) {  // the copy never completed
+            if (lane == 0) record_error(a.hdr, kErrBarrierWait);
+            failed = true;
+            break;
+        }
+        phase ^= 1u << slot;
+        const uint32_t kt = ring + slot * kWinBytes, vt = kt + kTileBytes;
+        const int32_t t0 = l.w * kWin, cnt = min(kWin, l.t1 - t0);
+        const int64_t pair = (int64_t)l.b * Hkv + l.h;
+        if (!quant) {
+            const WinStats s = window_stats(kt, vt, cnt);
+            if (lane == 0) {
+                float4 *dst = reinterpret_cast<float4 *>(a.stats + (pair * a.max_windows + l.w) * kStatFloats);
+                __stcg(dst, make_float4(s.mean, s.kmn, s.kmx, s.vmn));
+                __stcg(dst + 1, make_float4(s.vmx, 0.0f, 0.0f, 0.0f));
+            }
+        } else {
+            const PairCache pc = load_params(a.params + pair);
+            int32_t blk = -1;
+            if (t0 / a.bs < a.max_blocks) blk = __ldg(a.bt + (int64_t)l.b * a.max_blocks + t0 / a.bs);
+            if ((uint32_t)blk < (uint32_t)a.num_blocks)
+                window_quant(a.kpool, a.vpool, Hkv, a.bs, l.h, t0, cnt, blk, kt, vt, pc);
+            else if (lane == 0)  // not a block of the pools: flagged, nothing written
+                record_error(a.hdr, kErrBadBlock);
+        }
+        __syncwarp();  // the slot's reads are done before it is refilled
+        issue(x + kPfSlots * nw, slot);
+    }
+    // A normal exit leaves no copy in flight (windows past the end are never issued).  After a
+    // timed-out wait, wait again (bounded) for this slot's copy and those of the next windows, so
+    // that no copy still targets shared memory when the CTA exits.
+    if (failed) {
+        for (int k = 0; k < kPfSlots; ++k) {
+            const int sl = (slot + k) % kPfSlots;
+            if (x + k * nw < total) mbar_wait_bounded(bars + sl, (phase >> sl) & 1u);
+        }
+    }
+}
+
+// Segmentation of pair blockIdx.x from its window statistics: record and quantiser parameters.
+__global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __grid_constant__ PrefillArgs a)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t pair = blockIdx.x, b = pair / a.Hkv;
+    int32_t L = __ldg(a.end + b);
+    if (L < 0 || L > a.max_seqlen) {
+        if (tid == 0) record_error(a.hdr, kErrBadLength);
+        L = 0;
+    }
+    const int32_t W = (L + kWin - 1) / kWin;
+    int k = L == 0 ? -1 : min(min(ngroups(L), a.max_groups), W) - 1;  // boundaries to place
+    const float *st = a.stats + (int64_t)pair * a.max_windows * kStatFloats;
+    __shared__ float s_cj[kSegThreads / 32][4];
+    __shared__ int32_t s_cw[kSegThreads / 32][4];
+    __shared__ int32_t s_cut[4];
+    __shared__ int s_k;
+    __shared__ float s_mm[kSegThreads / 32][4][kMaxSeg];
+
+    // (1) per-thread top four of (jump desc, window asc) over windows tid, tid + 256, ...
+    float cj[4] = {-1.0f, -1.0f, -1.0f, -1.0f};
+    int32_t cw[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
+    if (k > 0) {
+        for (int32_t w = tid; w + 1 < W; w += kSegThreads) {
+            const float m0 = __ldcg(st + (int64_t)w * kStatFloats), m1 = __ldcg(st + (int64_t)(w + 1) * kStatFloats);
+            if (!(m0 >= a.min_var || m1 >= a.min_var)) continue;  // two quiet windows stay together
+            const float j = fabsf(__fsub_rn(m1, m0));
+            if (j > cj[3]) {  // windows arrive in increasing order: an equal jump keeps the earlier
+                cj[3] = j;
+                cw[3] = w;
+#pragma unroll
+                for (int s = 3; s > 0; --s) {
+                    if (cj[s] > cj[s - 1]) {
+                        const float tj = cj[s]; cj[s] = cj[s - 1]; cj[s - 1] = tj;
+                        const int32_t tw = cw[s]; cw[s] = cw[s - 1]; cw[s - 1] = tw;
+                    }
+                }
+            }
+        }
+    }
+    // (2) each warp: its top k by k rounds of arg-best over the lanes' list heads
+    for (int r = 0; r < 4; ++r) {
+        float j = cj[0];
+        int32_t wv = cw[0];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float oj = __shfl_xor_sync(0xffffffffu, j, o);
+            const int32_t ow = __shfl_xor_sync(0xffffffffu, wv, o);
+            if (oj > j || (oj == j && ow < wv)) {
+                j = oj;
+                wv = ow;
+            }
+        }
+        if (lane == 0) {
+            s_cj[warp][r] = j;
+            s_cw[warp][r] = wv;
+        }
+        if (cw[0] == wv && j >= 0.0f) {  // the winner pops its head (a window sits in one thread)
+            cj[0] = cj[1]; cj[1] = cj[2]; cj[2] = cj[3]; cj[3] = -1.0f;
+            cw[0] = cw[1]; cw[1] = cw[2]; cw[2] = cw[3]; cw[3] = INT32_MAX;
+        }
+    }
+    __syncthreads();
+    // (3) warp 0 merges the warps' lists (one candidate per lane) into the k boundaries
+    if (warp == 0) {
+        float mj = s_cj[lane >> 2][lane & 3];
+        int32_t mw = s_cw[lane >> 2][lane & 3];
+        int32_t cut[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
+        int kk = k < 0 ? 0 : k;
+        for (int r = 0; r < kk; ++r) {
+            float j = mj;
+            int32_t wv = mw;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float oj = __shfl_xor_sync(0xffffffffu, j, o);
+                const int32_t ow = __shfl_xor_sync(0xffffffffu, wv, o);
+                if (oj > j || (oj == j && ow < wv)) {
+                    j = oj;
+                    wv = ow;
+                }
+            }
+            if (j < 0.0f) {  // no candidate left
+                kk = r;
+                break;
+            }
+            if (mw == wv) {
+                mj = -1.0f;
+                mw = INT32_MAX;
+            }
+            int32_t c = wv + 1;  // insertion into the sorted list of starts (in windows)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                if (c < cut[s]) {
+                    const int32_t t = cut[s];
+                    cut[s] = c;
+                    c = t;
+                }
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) s_cut[s] = cut[s];
+            s_k = k < 0 ? -1 : kk;
+        }
+    }
+    __syncthreads();
+    k = s_k;
+    int32_t cut[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) cut[s] = s_cut[s];
+
+    // (4) per-segment extremes (exact in any order)
+    float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
+#pragma unroll
+    for (int s = 0; s < kMaxSeg; ++s) {
+        kmn[s] = INFINITY; kmx[s] = -INFINITY; vmn[s] = INFINITY; vmx[s] = -INFINITY;
+    }
+    for (int32_t w = tid; w < W; w += kSegThreads) {
+        const float4 e = __ldcg(reinterpret_cast<const float4 *>(st + (int64_t)w * kStatFloats));
+        const float vx = __ldcg(st + (int64_t)w * kStatFloats + 4);
+        const int sg = (w >= cut[0]) + (w >= cut[1]) + (w >= cut[2]) + (w >= cut[3]);
+#pragma unroll
+        for (int s = 0; s < kMaxSeg; ++s) {
+            if (s == sg) {
+                kmn[s] = fminf(kmn[s], e.y); kmx[s] = fmaxf(kmx[s], e.z);
+                vmn[s] = fminf(vmn[s], e.w); vmx[s] = fmaxf(vmx[s], vx);
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxSeg; ++s) {
+        kmn[s] = warp_min(kmn[s]); kmx[s] = warp_max(kmx[s]);
+        vmn[s] = warp_min(vmn[s]); vmx[s] = warp_max(vmx[s]);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kMaxSeg; ++s) {
+            s_mm[warp][0][s] = kmn[s]; s_mm[warp][1][s] = kmx[s];
+            s_mm[warp][2][s] = vmn[s]; s_mm[warp][3][s] = vmx[s];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < kMaxSeg; ++s) {
+            for (int w = 1; w < kSegThreads / 32; ++w) {
+                kmn[s] = fminf(kmn[s], s_mm[w][0][s]); kmx[s] = fmaxf(kmx[s], s_mm[w][1][s]);
+                vmn[s] = fminf(vmn[s], s_mm[w][2][s]); vmx[s] = fmaxf(vmx[s], s_mm[w][3][s]);
+            }
+        }
+        dgq_seg_record rec = {};
+        PairParams pp = {};
+        if (k >= 0) make_params(L, k, cut, kmn, kmx, vmn, vmx, rec, pp);
+        a.table[pair] = rec;
+        a.params[pair] = pp;
+    }
+}
+
+size_t prefill_workspace_bytes(int32_t B, int32_t Hkv)
+{
+    return sizeof(WsHeader) + (size_t)B * Hkv * sizeof(PairParams);
+}
+
+static size_t prefill_smem(int32_t B) { return 1024 + kPfRingBytes + 8 * kPfSlots * kPfWarps + 4 * ((size_t)B + 1); }
+
+template <bool quant>
+static cudaError_t launch_windows(const PrefillArgs &a, int nsm, cudaStream_t stream)
+{
+    // the shared-memory limit is raised once per device, to what the largest batch needs
+    static int ready_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != ready_dev) {
+        e = cudaFuncSetAttribute(prefill_window_kernel<quant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)prefill_smem(kMaxPrefillBatch));
+        if (e != cudaSuccess) return e;
+        ready_dev = dev;
+    }
+    prefill_window_kernel<quant><<<nsm, kPfThreads, prefill_smem(a.B), stream>>>(a);
+    return cudaGetLastError();
+}
+
+static bool prefill_args(const SourceDesc &src, int32_t B, int32_t max_seqlen, int32_t Hkv, int32_t bs,
+                         float *stats, int32_t max_windows, void *ws, PrefillArgs &a)
+{
+    if (!encode_tile_source(src, Hkv, bs, &a.src)) return false;
+    a.begin = a.end = a.bt = nullptr;
+    a.kpool = a.vpool = nullptr;
+    a.stats = stats;
+    a.table = nullptr;
+    a.hdr = static_cast<WsHeader *>(ws);
+    a.params = reinterpret_cast<PairParams *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
+    a.B = B;
+    a.Hkv = Hkv;
+    a.bs = bs;
+    a.max_windows = max_windows;
+    a.max_blocks = a.num_blocks = 0;
+    a.max_seqlen = max_seqlen;
+    a.max_groups = kMaxSeg;
+    a.min_var = 0.0f;
+    return true;
+}
+
+cudaError_t launch_prefill_stats(const SourceDesc &src, const int32_t *begin, const int32_t *end, int32_t B,
+                                 int32_t max_seqlen, int32_t Hkv, int32_t bs, float *stats, int32_t max_windows,
+                                 void *ws, int nsm, bool *map_failed, cudaStream_t stream)
+{
+    PrefillArgs a;
+    *map_failed = !prefill_args(src, B, max_seqlen, Hkv, bs, stats, max_windows, ws, a);
+    if (*map_failed) return cudaErrorInvalidValue;
+    a.begin = begin;
+    a.end = end;
+    return launch_windows<false>(a, nsm, stream);
+}
+
+cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens, int32_t B, int32_t max_seqlen,
+                                  int32_t Hkv, int32_t bs, const float *stats, int32_t max_windows,
+                                  const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
+                                  int32_t num_blocks, dgq_seg_record *table, GroupSettings gs, void *ws, int nsm,
+                                  bool *map_failed, cudaStream_t stream)
+{
+    PrefillArgs a;
+    *map_failed = !prefill_args(src, B, max_seqlen, Hkv, bs, const_cast<float *>(stats), max_windows, ws, a);
+    if (*map_failed) return cudaErrorInvalidValue;
+    a.end = seq_lens;
+    a.bt = bt;
+    a.max_blocks = max_blocks;
+    a.kpool = kpool;
+    a.vpool = vpool;
+    a.num_blocks = num_blocks;
+    a.table = table;
+    a.max_groups = gs.max_groups;
+    a.min_var = gs.min_var;
+    prefill_segment_kernel<<<(unsigned)(B * Hkv), kSegThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_windows<true>(a, nsm, stream);
+}
+
+}  // namespace dgq

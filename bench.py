@@ -604,14 +604,14 @@ def time_prefill(w, lens, cu, bt, layers, d_bt, d_lens, max_seqlen, sp, comp_b, 
     cache (standing in for the prefill kernels; not timed), then dgq_prefill_chunk_stats on that
     chunk (timed: the chunk is in L2, as right after prefill wrote it); at the end
     dgq_prefill_finish (timed).  Against it, dgq_compress_paged on the same complete cache.  The
-    chunk covers about 32 MB of K+V (at most 8192 tokens per request)."""
+    chunk covers about 64 MB of K+V (at most 16384 tokens per request)."""
     import numpy as np
     import torch
     import int8_group_quantized_gb300 as dgq
     dev = layers[0]["k"].device
     B, Hkv, bs = w.batch, w.hkv, w.block_size
     nb = layers[0]["kp"].shape[0]
-    C = int(min(8192, max(16, (32 << 20) // (B * Hkv * 512)))) // 16 * 16
+    C = int(min(16384, max(16, (64 << 20) // (B * Hkv * 512)))) // 16 * 16
     nchunks = (int(lens.max()) + C - 1) // C
     chunks = []
     for c in range(nchunks):  # packed rows, blocks and slots of chunk c's tokens

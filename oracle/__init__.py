@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_compress_pair_ex.restype = None
         L.oracle_compress_ex.argtypes = [P, P, P, i32, i32, i32, P, i32, i32, ctypes.c_float, P, P, P]
         L.oracle_compress_ex.restype = None
+        L.oracle_compress_split.argtypes = [P, P, P, i32, i32, i32, P, i32, i32, ctypes.c_float, P, P, P, P]
+        L.oracle_compress_split.restype = None
         L.oracle_dequant_pair.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_int, P]
         L.oracle_dequant_pair.restype = None
         L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
@@ -164,6 +166,25 @@ def compress(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_block
     lib().oracle_compress_ex(_p(k), _p(v), _p(cu), B, num_kv_heads, block_size, _p(bt), bt.shape[1],
                              int(max_groups), float(min_var), _p(kp), _p(vp), _p(table))
     return kp, vp, table
+
+
+def compress_split(k, v, cu_seqlens, num_kv_heads, block_size, block_tables, num_blocks, fill=0,
+                   max_groups=MAX_SEG, min_var=0.0):
+    """One layer with independent V segmentation (V segmented by the same rule on V's own
+    variance).  Returns (k_pool, v_pool, k_table, v_table): k_table holds K's segments and K
+    parameters, v_table V's segments and V parameters (the other tensor's fields 0)."""
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    B = cu.shape[0] - 1
+    kp = np.full((num_blocks, num_kv_heads, block_size, D), fill, dtype=np.uint8)
+    vp = np.full((num_blocks, num_kv_heads, block_size, D), fill, dtype=np.uint8)
+    kt = np.zeros((B, num_kv_heads), dtype=SEG_DTYPE)
+    vt = np.zeros((B, num_kv_heads), dtype=SEG_DTYPE)
+    lib().oracle_compress_split(_p(k), _p(v), _p(cu), B, num_kv_heads, block_size, _p(bt), bt.shape[1],
+                                int(max_groups), float(min_var), _p(kp), _p(vp), _p(kt), _p(vt))
+    return kp, vp, kt, vt
 
 
 def append(k_new, v_new, block_size, block_tables, k_pool, v_pool, table):

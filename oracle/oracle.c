@@ -294,6 +294,101 @@ void oracle_compress_pair_ex(const uint16_t *k, const uint16_t *v, int64_t row_s
     free(means);
 }
 
+/* Independent V segmentation (a group-selection variant; the article derives its segments from
+ * K only, [DGQ] section 2.2).  READING: V is segmented by the same rule applied to V's own
+ * per-token variance (a2-a4 on V), and each tensor is encoded with its own segments (a5-a6).
+ * One tensor x of one (request, KV head): its starts, per-segment min / scale / inverse and codes
+ * (unpaged [L, 128], when non-null).  Returns the number of segments (0 when L == 0). */
+static int32_t encode_own_segments(const uint16_t *x, int64_t row_stride, int32_t L, int32_t max_groups,
+                                   float min_var, int32_t *start, float *mn, float *scale, float *inv,
+                                   uint8_t *codes)
+{
+    for (int i = 0; i < OR_MAX_SEG; ++i) {
+        start[i] = L;
+        mn[i] = scale[i] = inv[i] = 0.0f;
+    }
+    if (L <= 0) return 0;
+    int32_t W = (L + OR_WIN - 1) / OR_WIN;
+    float *var = (float *)malloc(sizeof(float) * (size_t)L);
+    float *means = (float *)malloc(sizeof(float) * (size_t)W);
+    for (int32_t t = 0; t < L; ++t) var[t] = oracle_token_variance(x + (int64_t)t * row_stride);
+    oracle_window_means(var, L, means);
+    int32_t n = oracle_boundaries_ex(means, W, L, max_groups, min_var, start);
+    for (int32_t s = 0; s < n; ++s) {
+        int32_t t0 = start[s], t1 = s + 1 < n ? start[s + 1] : L;
+        float mx;
+        segment_min_max(x, row_stride, t0, t1, &mn[s], &mx);
+        segment_affine(mn[s], mx, &scale[s], &inv[s]);
+    }
+    if (codes) {
+        int32_t s = 0;
+        for (int32_t t = 0; t < L; ++t) {
+            while (s + 1 < n && start[s + 1] <= t) ++s;
+            for (int d = 0; d < OR_D; ++d)
+                codes[(int64_t)t * OR_D + d] = oracle_encode(bf16_to_float(x[(int64_t)t * row_stride + d]), mn[s],
+                                                             inv[s]);
+        }
+    }
+    free(var);
+    free(means);
+    return n;
+}
+
+/* One (request, KV head) with independent segmentations: k_rec holds K's segments (start,
+ * k_min, k_scale, k_inv_last; V fields 0), v_rec V's (start, v_min, v_scale, v_inv_last; K fields
+ * 0); both carry n_seg of their own tensor and seq_len = L. */
+void oracle_compress_pair_split(const uint16_t *k, const uint16_t *v, int64_t row_stride, int32_t L,
+                                int32_t max_groups, float min_var, oracle_seg *k_rec, oracle_seg *v_rec,
+                                uint8_t *k_codes, uint8_t *v_codes)
+{
+    float inv[OR_MAX_SEG], sc[OR_MAX_SEG], mn[OR_MAX_SEG];
+    memset(k_rec, 0, sizeof *k_rec);
+    memset(v_rec, 0, sizeof *v_rec);
+    k_rec->seq_len = v_rec->seq_len = L;
+    int32_t n = encode_own_segments(k, row_stride, L, max_groups, min_var, k_rec->start, mn, sc, inv, k_codes);
+    k_rec->n_seg = n;
+    for (int i = 0; i < OR_MAX_SEG; ++i) {
+        k_rec->k_min[i] = mn[i];
+        k_rec->k_scale[i] = sc[i];
+    }
+    k_rec->k_inv_last = n > 0 ? inv[n - 1] : 0.0f;
+    n = encode_own_segments(v, row_stride, L, max_groups, min_var, v_rec->start, mn, sc, inv, v_codes);
+    v_rec->n_seg = n;
+    for (int i = 0; i < OR_MAX_SEG; ++i) {
+        v_rec->v_min[i] = mn[i];
+        v_rec->v_scale[i] = sc[i];
+    }
+    v_rec->v_inv_last = n > 0 ? inv[n - 1] : 0.0f;
+    if (L <= 0) {  /* as the shared path: an empty pair's starts are all 0 */
+        for (int i = 0; i < OR_MAX_SEG; ++i) k_rec->start[i] = v_rec->start[i] = 0;
+    }
+}
+
+/* One layer with independent segmentations (pools as oracle_compress_ex; two record tables). */
+void oracle_compress_split(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens, int32_t B, int32_t Hkv,
+                           int32_t bs, const int32_t *block_tables, int32_t max_blocks, int32_t max_groups,
+                           float min_var, uint8_t *k_pool, uint8_t *v_pool, oracle_seg *k_table, oracle_seg *v_table)
+{
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t L = cu_seqlens[b + 1] - cu_seqlens[b];
+        for (int32_t h = 0; h < Hkv; ++h) {
+            const int64_t row0 = ((int64_t)cu_seqlens[b] * Hkv + h) * OR_D;
+            uint8_t *kc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
+            uint8_t *vc = (uint8_t *)malloc((size_t)(L > 0 ? L : 1) * OR_D);
+            oracle_compress_pair_split(k + row0, v + row0, (int64_t)Hkv * OR_D, L, max_groups, min_var,
+                                       &k_table[(int64_t)b * Hkv + h], &v_table[(int64_t)b * Hkv + h], kc, vc);
+            for (int32_t t = 0; t < L; ++t) {
+                int64_t blk = block_tables[(int64_t)b * max_blocks + t / bs];
+                int64_t dst = ((blk * Hkv + h) * bs + t % bs) * OR_D;
+                memcpy(k_pool + dst, kc + (int64_t)t * OR_D, OR_D);
+                memcpy(v_pool + dst, vc + (int64_t)t * OR_D, OR_D);
+            }
+            free(kc);
+            free(vc);
+        }
+    }
+}
+
 /* a2-a7 for one layer of a batch.  K and V are packed variable-length [T, Hkv, 128]
  * with request b on rows cu_seqlens[b] .. cu_seqlens[b+1]).  Token t of request b, head h
  * is stored at pool[block_tables[b][t / bs]][h][t % bs][0..128), [PAGED]

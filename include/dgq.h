@@ -181,38 +181,50 @@ dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, in
  * the paged cache.
  *
  * window_stats     [batch, Hkv, max_windows, 8] fp32, device, caller-owned: per 16-token window
- *                  (mean variance, K min, K max, V min, V max, 3 zeros); max_windows >=
- *                  ceil(max_seqlen / 16).  Written by dgq_prefill_chunk_stats, read by
- *                  dgq_prefill_finish.
+ *                  (K mean variance, K min, K max, V min, V max, V mean variance (0 unless
+ *                  DGQ_PREFILL_V_VARIANCE), 2 zeros); max_windows >= ceil(max_seqlen / 16).
+ *                  Written by dgq_prefill_chunk_stats, read by dgq_prefill_finish.
+ *
+ * Independent V segmentation (a group-selection variant; the method itself derives one
+ * segmentation from K, [DGQ] section 2.2): V is segmented by the same rule applied to V's own
+ * variance and encoded with its own segments.  Statistics taken with DGQ_PREFILL_V_VARIANCE and
+ * a non-NULL v_seg_table in dgq_prefill_finish select it: seg_table then receives K's records
+ * (V fields 0) and v_seg_table V's (start, n_seg, v_min, v_scale, v_inv_last; K fields 0); decode
+ * with dgq_paged_decode_attn_split.  dgq_append does not support it.
  * workspace        >= dgq_prefill_workspace_size(batch, Hkv) bytes, zero-filled before first use.
  * The bf16 source (k_src, v_src, src block tables) is as for dgq_compress_paged.
  */
 size_t dgq_prefill_workspace_size(int32_t batch, int32_t num_kv_heads);
 
+#define DGQ_PREFILL_V_VARIANCE 1 /* dgq_prefill_chunk_stats flag: also V's mean variance per window */
+
 /* Statistics of the windows of tokens [chunk_begin[b], chunk_end[b]) of every request b (device
  * arrays [batch] int32).  chunk_begin[b] is a multiple of 16; chunk_end[b] is a multiple of 16
  * unless the chunk is the request's last one (its partial last window is averaged over its own
  * tokens, as in dgq_compress); an empty range (begin == end) skips the request.  A range that is
- * not window-aligned or ends past max_seqlen is flagged in the workspace and skipped. */
+ * not window-aligned or ends past max_seqlen is flagged in the workspace and skipped.  flags: 0 or
+ * DGQ_PREFILL_V_VARIANCE (other bits: DGQ_ERR_INVALID_ARG). */
 dgq_status dgq_prefill_chunk_stats(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
                                    const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
                                    const int32_t *chunk_begin_dev, const int32_t *chunk_end_dev, int32_t batch,
                                    int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                   float *window_stats, int32_t max_windows, void *workspace, size_t workspace_bytes,
-                                   void *cuda_stream);
+                                   float *window_stats, int32_t max_windows, int32_t flags, void *workspace,
+                                   size_t workspace_bytes, void *cuda_stream);
 
 /* Segmentation of every (request, head) from window_stats (every window of tokens
  * [0, seq_lens[b]) must have been written by earlier dgq_prefill_chunk_stats calls), then the
  * codes of all tokens from the bf16 cache into the INT8 pools and the records, as
- * dgq_compress_paged with the same options would write them.  Two launches. */
+ * dgq_compress_paged with the same options would write them.  v_seg_table: NULL for the method's
+ * shared segmentation, else [batch, Hkv] records for independent V segmentation (above).  Two
+ * launches. */
 dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
                               const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
                               const int32_t *seq_lens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,
                               int32_t head_dim, int32_t block_size, const float *window_stats, int32_t max_windows,
                               const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
                               uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table,
-                              const dgq_compress_options *options, void *workspace, size_t workspace_bytes,
-                              void *cuda_stream);
+                              dgq_seg_record *v_seg_table, const dgq_compress_options *options, void *workspace,
+                              size_t workspace_bytes, void *cuda_stream);
 
 /* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
@@ -247,6 +259,17 @@ dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16,
 
 size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                int32_t max_seqlen);
+
+/* dgq_paged_decode_attn over a cache with independent V segmentation (dgq_prefill_finish with a
+ * v_seg_table): keys are dequantised with k_seg_table's segments and K parameters, values with
+ * v_seg_table's segments and V parameters.  Same arguments otherwise. */
+dgq_status dgq_paged_decode_attn_split(const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                                       const uint8_t *k_pool, const uint8_t *v_pool, const dgq_seg_record *k_seg_table,
+                                       const dgq_seg_record *v_seg_table, const int32_t *block_tables_dev,
+                                       const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
+                                       void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn_noalloc -- the same decode attention for callers that cannot

@@ -29,7 +29,7 @@ __all__ = [
     "dgq_append_workspace_size",
     "dgq_paged_decode_attn", "dgq_encode_format", "dgq_encode_format_workspace_size",
     "dgq_paged_decode_attn_format", "FORMATS", "dgq_prefill_workspace_size", "dgq_prefill_chunk_stats",
-    "dgq_prefill_finish",
+    "dgq_prefill_finish", "dgq_paged_decode_attn_split",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -81,10 +81,14 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn_format.restype = ctypes.c_int
         L.dgq_prefill_workspace_size.argtypes = [i32, i32]
         L.dgq_prefill_workspace_size.restype = sz
-        L.dgq_prefill_chunk_stats.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, P, i32, P, sz, P]
+        L.dgq_prefill_chunk_stats.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, P, i32, i32, P, sz,
+                                              P]
         L.dgq_prefill_chunk_stats.restype = ctypes.c_int
         L.dgq_prefill_finish.argtypes = [P, P, i32, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, i32, P,
-                                         P, P, sz, P]
+                                         P, P, P, sz, P]
+        L.dgq_paged_decode_attn_split.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                  i32, P, P, sz, P]
+        L.dgq_paged_decode_attn_split.restype = ctypes.c_int
         L.dgq_prefill_finish.restype = ctypes.c_int
         L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
         L.dgq_append.restype = ctypes.c_int
@@ -239,24 +243,31 @@ def dgq_prefill_workspace_size(batch: int, num_kv_heads: int) -> int:
     return int(lib().dgq_prefill_workspace_size(batch, num_kv_heads))
 
 
+PREFILL_V_VARIANCE = 1
+
+
 def dgq_prefill_chunk_stats(k_src, v_src, src_block_tables, chunk_begin, chunk_end, max_seqlen, window_stats,
-                            workspace, stream=None) -> None:
+                            workspace, stream=None, v_variance=False) -> None:
     """Window statistics of tokens [chunk_begin[b], chunk_end[b]) of each request (int32 CUDA
     tensors [B]) from the bf16 paged cache k_src / v_src [num_src_blocks, Hkv, bs, 128] into
-    window_stats fp32 [B, Hkv, max_windows, 8]; workspace: dgq_prefill_workspace_size bytes."""
+    window_stats fp32 [B, Hkv, max_windows, 8]; workspace: dgq_prefill_workspace_size bytes.
+    v_variance: also V's mean variance (for independent V segmentation)."""
     B = chunk_begin.shape[0]
     _, Hkv, bs, D = k_src.shape
     _check(lib().dgq_prefill_chunk_stats(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(src_block_tables),
                                          src_block_tables.shape[1], _ptr(chunk_begin), _ptr(chunk_end), B,
                                          int(max_seqlen), Hkv, D, bs, _ptr(window_stats), window_stats.shape[2],
-                                         _ptr(workspace), _nbytes(workspace), _stream(stream)),
+                                         PREFILL_V_VARIANCE if v_variance else 0, _ptr(workspace),
+                                         _nbytes(workspace), _stream(stream)),
            "dgq_prefill_chunk_stats")
 
 
 def dgq_prefill_finish(k_src, v_src, src_block_tables, seq_lens, max_seqlen, window_stats, block_tables, k_pool,
-                       v_pool, seg_table, workspace, stream=None, max_groups=MAX_SEG, min_var=0.0) -> None:
+                       v_pool, seg_table, workspace, stream=None, max_groups=MAX_SEG, min_var=0.0,
+                       v_seg_table=None) -> None:
     """Segmentation from window_stats and codes of every token [0, seq_lens[b]) into the INT8
-    pools / records (as dgq_compress_paged with the same settings would write them)."""
+    pools / records (as dgq_compress_paged with the same settings would write them).  With
+    v_seg_table (uint8 [B, Hkv, 128]): independent V segmentation, V's records there."""
     B = seq_lens.shape[0]
     _, Hkv, bs, D = k_src.shape
     opts = CompressOptions(int(max_groups), float(min_var))
@@ -264,8 +275,21 @@ def dgq_prefill_finish(k_src, v_src, src_block_tables, seq_lens, max_seqlen, win
                                     src_block_tables.shape[1], _ptr(seq_lens), B, int(max_seqlen), Hkv, D, bs,
                                     _ptr(window_stats), window_stats.shape[2], _ptr(block_tables),
                                     block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
-                                    _ptr(seg_table), ctypes.byref(opts), _ptr(workspace), _nbytes(workspace),
-                                    _stream(stream)), "dgq_prefill_finish")
+                                    _ptr(seg_table), _ptr(v_seg_table), ctypes.byref(opts), _ptr(workspace),
+                                    _nbytes(workspace), _stream(stream)), "dgq_prefill_finish")
+
+
+def dgq_paged_decode_attn_split(q, k_new, v_new, k_pool, v_pool, k_seg_table, v_seg_table, block_tables, seq_lens,
+                                max_seqlen, out, workspace, stream=None) -> None:
+    """dgq_paged_decode_attn over a cache with independent V segmentation (K's and V's record
+    tables as dgq_prefill_finish wrote them)."""
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    _check(lib().dgq_paged_decode_attn_split(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                             _ptr(k_seg_table), _ptr(v_seg_table), _ptr(block_tables),
+                                             _ptr(seq_lens), int(max_seqlen), B, Hq, Hkv, D, k_pool.shape[2],
+                                             block_tables.shape[1], k_pool.shape[0], _ptr(out), _ptr(workspace),
+                                             _nbytes(workspace), _stream(stream)), "dgq_paged_decode_attn_split")
 
 
 def _format_id(fmt) -> int:

@@ -60,7 +60,7 @@ constexpr int kTileSmem = 2 * kTileBytes;          // K tile + V tile
 constexpr int kParBytes = kTile * 16;              // fixed groups: a tile's (min0, scale0, min1, scale1) per token
 
 // Code formats of the decode kernel's instances.
-enum : int { kDecAffine = 0, kDecFp8 = 1, kDecFixed = 2 };
+enum : int { kDecAffine = 0, kDecFp8 = 1, kDecFixed = 2, kDecSplitV = 3 };
 
 // Bytes of one ring stage: the K and V tiles, and for fixed groups their K and V parameters.
 template <int Fmt>
@@ -76,6 +76,7 @@ struct AttnArgs {
     const uint8_t *kpool;
     const uint8_t *vpool;
     const dgq_seg_record *table;
+    const dgq_seg_record *vtable;  // independent V segmentation: V's records (K's are in `table`)
     const float4 *kpar;  // fixed groups: per-slot (min0, scale0, min1, scale1) of K and of V
     const float4 *vpar;
     const int32_t *bt;
@@ -279,8 +280,11 @@ __device__ __forceinline__ void next_piece(Piece &pz, const int32_t *s_tpre, con
 
 // Per-piece data staged in shared memory ahead of use: the segment record, the current token's
 // key and value and the group's query rows.
-constexpr int kPbRec = 0, kPbKnew = 128, kPbVnew = 384, kPbQ = 640;
-constexpr int kPieceBytes = kPbQ + 8 * 256;
+constexpr int kPbRec = 0, kPbKnew = 128, kPbVnew = 384, kPbQ = 640, kPbRecV = kPbQ + 8 * 256;
+
+// Bytes of one piece's staging buffer (plus V's own record with independent V segmentation).
+template <int Fmt>
+__host__ __device__ constexpr int piece_bytes() { return kPbRecV + (Fmt == kDecSplitV ? 128 : 0); }
 
 // Workspace header words used to hand the split to the combine kernel.
 constexpr int kHdrTiles = 0, kHdrCtas = 1;
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 {
     constexpr int kStage = stage_bytes<Fmt>();
     constexpr int kWarpSmem = kDepth * kStage;
+    constexpr int kPieceBytes = piece_bytes<Fmt>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
     uint8_t *pbuf = smem + kWarpsPerCta * kWarpSmem;                                 // [2][kPieceBytes]
@@ -360,8 +365,9 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     }
     auto stage_piece = [&](const Piece &pz, int buf) {  // thread 0 only
         uint8_t *dst = pbuf + buf * kPieceBytes;
-        mbar_arrive_expect_tx(&pbar[buf], (uint32_t)(kPbQ + 256 * G));
+        mbar_arrive_expect_tx(&pbar[buf], (uint32_t)(kPbQ + 256 * G + (Fmt == kDecSplitV ? 128 : 0)));
         bulk_load(dst + kPbRec, a.table + (int64_t)pz.b * Hkv + pz.h, 128, &pbar[buf]);
+        if constexpr (Fmt == kDecSplitV) bulk_load(dst + kPbRecV, a.vtable + (int64_t)pz.b * Hkv + pz.h, 128, &pbar[buf]);
         bulk_load(dst + kPbKnew, a.knew + ((int64_t)pz.b * Hkv + pz.h) * kD, 256, &pbar[buf]);
         bulk_load(dst + kPbVnew, a.vnew + ((int64_t)pz.b * Hkv + pz.h) * kD, 256, &pbar[buf]);
         bulk_load(dst + kPbQ, a.q + ((int64_t)pz.b * a.Hq + pz.h * G) * kD, (uint32_t)(256 * G), &pbar[buf]);
@@ -451,6 +457,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 
         // piece start (per warp): record word, Q fragments of head g = r, state
         const uint32_t recw = reinterpret_cast<const uint32_t *>(pb + kPbRec)[lane];
+        const uint32_t recw_v = Fmt == kDecSplitV ? reinterpret_cast<const uint32_t *>(pb + kPbRecV)[lane] : 0u;
         float qsum;
         {
             float qs = 0.0f;
@@ -494,10 +501,17 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
             const int32_t valid = min(kTile, cur.L - tok0);
             if (valid > 0) {
                 // segment constants (record words: start 2..6, k_min 7.., k_scale 12.., v_min 17.., v_scale 22..)
-                const int sg = Fmt != kDecAffine
-                                   ? 0
-                                   : __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
-                if (Fmt != kDecAffine && sg != seg) {  // decoded values reach the tensor cores: identity fold
+                // (independent V segmentation: K's segment sgk from `recw`, V's sgv from `recw_v`)
+                int sgk = 0, sgv = 0, sg = 0;
+                if constexpr (Fmt == kDecAffine) {
+                    sg = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
+                    sgk = sgv = sg;
+                } else if constexpr (Fmt == kDecSplitV) {
+                    sgk = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw <= tok0));
+                    sgv = __popc(__ballot_sync(0xffffffffu, lane >= 3 && lane <= 6 && (int32_t)recw_v <= tok0));
+                    sg = sgk * 8 + sgv;
+                }
+                if ((Fmt == kDecFp8 || Fmt == kDecFixed) && sg != seg) {  // decoded values: identity fold
                     seg = sg;
                     vflat = false;
                     ak = kLog2eOverSqrtD;
@@ -505,16 +519,17 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                     cv = 0.0f;
                 } else if (sg != seg) {
                     seg = sg;
-                    const float kmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 7 + sg));
-                    const float kscale = __uint_as_float(__shfl_sync(0xffffffffu, recw, 12 + sg));
-                    const float vmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 17 + sg));
-                    const float vsc = __uint_as_float(__shfl_sync(0xffffffffu, recw, 22 + sg));
+                    const uint32_t vw = Fmt == kDecSplitV ? recw_v : recw;
+                    const float kmin = __uint_as_float(__shfl_sync(0xffffffffu, recw, 7 + sgk));
+                    const float kscale = __uint_as_float(__shfl_sync(0xffffffffu, recw, 12 + sgk));
+                    const float vmin = __uint_as_float(__shfl_sync(0xffffffffu, vw, 17 + sgv));
+                    const float vsc = __uint_as_float(__shfl_sync(0xffffffffu, vw, 22 + sgv));
                     // a flat V segment (scale 0) decodes to v_min whatever its codes: it only feeds bsum
                     vflat = !(vsc > 0.0f);
                     ak = kscale * kLog2eOverSqrtD;
                     bk = (kmin - 1024.0f * kscale) * qsum * kLog2eOverSqrtD;
                     cv = vflat ? vmin : vmin - 1024.0f * vsc;
-                    if (!vflat && sg != vseg) {
+                    if (!vflat && sgv != vseg) {
                         if (vseg >= 0) {  // keep sigma * o invariant across the change of V scale
                             const float ratio = sigma / vsc;
 #pragma unroll
@@ -523,7 +538,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                                 for (int e = 0; e < 4; ++e) o[i][e] *= ratio;
                         }
                         sigma = vsc;
-                        vseg = sg;
+                        vseg = sgv;
                     }
                 }
 
@@ -832,7 +847,8 @@ namespace dgq {
 size_t attn_smem_bytes(int dec, int32_t B, int32_t G)
 {
     const int stage = dec == kDecFixed ? stage_bytes<kDecFixed>() : stage_bytes<kDecAffine>();
-    return 1024 + (size_t)kWarpsPerCta * kDepth * stage + 2 * kPieceBytes + 16 + (size_t)kWarpsPerCta * G * kPartStride * 4 +
+    const int piece = dec == kDecSplitV ? piece_bytes<kDecSplitV>() : piece_bytes<kDecAffine>();
+    return 1024 + (size_t)kWarpsPerCta * kDepth * stage + 2 * (size_t)piece + 16 + (size_t)kWarpsPerCta * G * kPartStride * 4 +
            8 * 4 + (size_t)(2 * B + 1) * 4;
 }
 
@@ -853,7 +869,8 @@ AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm)
 }
 
 cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const void *vnew, const uint8_t *kpool,
-                        const uint8_t *vpool, const dgq_seg_record *table, const float *kpar, const float *vpar,
+                        const uint8_t *vpool, const dgq_seg_record *table, const dgq_seg_record *vtable,
+                        const float *kpar, const float *vpar,
                         const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen, int32_t B, int32_t Hq,
                         int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks, void *out, void *ws, int nsm,
                         bool *map_failed, cudaStream_t stream)
@@ -869,6 +886,7 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
     a.kpool = kpool;
     a.vpool = vpool;
     a.table = table;
+    a.vtable = vtable;
     a.kpar = reinterpret_cast<const float4 *>(kpar);
     a.vpar = reinterpret_cast<const float4 *>(vpar);
     a.bt = bt;
@@ -886,14 +904,19 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
     a.num_blocks = num_blocks;
 
     // the kernel instance for the code format (the symmetric INT8 cache is an affine one)
-    const int dec = format == DGQ_FORMAT_FP8_E4M3 ? kDecFp8 : (format == DGQ_FORMAT_FIXED64 ? kDecFixed : kDecAffine);
+    const int dec = vtable != nullptr ? kDecSplitV
+                                      : (format == DGQ_FORMAT_FP8_E4M3 ? kDecFp8
+                                                                       : (format == DGQ_FORMAT_FIXED64 ? kDecFixed
+                                                                                                       : kDecAffine));
     void (*kern)(AttnArgs) = dec == kDecFp8 ? attn_kernel<kDecFp8>
-                                            : (dec == kDecFixed ? attn_kernel<kDecFixed> : attn_kernel<kDecAffine>);
+                             : dec == kDecFixed ? attn_kernel<kDecFixed>
+                             : dec == kDecSplitV ? attn_kernel<kDecSplitV>
+                                                 : attn_kernel<kDecAffine>;
 
     // per-device launch shape, computed once per (instance, device, shared-memory size)
-    static int cached_dev[3] = {-1, -1, -1};
-    static size_t cached_smem[3] = {0, 0, 0};
-    static int cached_occ[3] = {0, 0, 0};
+    static int cached_dev[4] = {-1, -1, -1, -1};
+    static size_t cached_smem[4] = {0, 0, 0, 0};
+    static int cached_occ[4] = {0, 0, 0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

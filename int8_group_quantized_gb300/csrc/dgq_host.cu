@@ -211,6 +211,31 @@ dgq_status dgq_paged_decode_attn(const void *q_bf16, const void *k_new_bf16, con
                                         num_blocks, out_bf16, workspace, workspace_bytes, cuda_stream);
 }
 
+namespace {
+dgq_status attn_impl(int32_t format, const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                     const uint8_t *k_pool, const uint8_t *v_pool, const dgq_seg_record *seg_table,
+                     const dgq_seg_record *v_seg_table, const float *k_group_params, const float *v_group_params,
+                     const int32_t *block_tables_dev, const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16, void *workspace,
+                     size_t workspace_bytes, void *cuda_stream);
+}  // namespace
+
+dgq_status dgq_paged_decode_attn_split(const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                                       const uint8_t *k_pool, const uint8_t *v_pool, const dgq_seg_record *k_seg_table,
+                                       const dgq_seg_record *v_seg_table, const int32_t *block_tables_dev,
+                                       const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16,
+                                       void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (!v_seg_table || !aligned16(v_seg_table)) return DGQ_ERR_INVALID_ARG;
+    return attn_impl(DGQ_FORMAT_DGQ, q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, k_seg_table, v_seg_table,
+                     nullptr, nullptr, block_tables_dev, seq_lens_dev, max_seqlen, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, out_bf16, workspace, workspace_bytes,
+                     cuda_stream);
+}
+
 dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, const void *k_new_bf16,
                                         const void *v_new_bf16, const uint8_t *k_pool, const uint8_t *v_pool,
                                         const dgq_seg_record *seg_table, const float *k_group_params,
@@ -219,6 +244,21 @@ dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, cons
                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                         int32_t block_size, int32_t max_blocks_per_seq, int32_t num_blocks,
                                         void *out_bf16, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    return attn_impl(format, q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table, nullptr, k_group_params,
+                     v_group_params, block_tables_dev, seq_lens_dev, max_seqlen, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, out_bf16, workspace, workspace_bytes,
+                     cuda_stream);
+}
+
+namespace {
+dgq_status attn_impl(int32_t format, const void *q_bf16, const void *k_new_bf16, const void *v_new_bf16,
+                     const uint8_t *k_pool, const uint8_t *v_pool, const dgq_seg_record *seg_table,
+                     const dgq_seg_record *v_seg_table, const float *k_group_params, const float *v_group_params,
+                     const int32_t *block_tables_dev, const int32_t *seq_lens_dev, int32_t max_seqlen, int32_t batch,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int32_t max_blocks_per_seq, int32_t num_blocks, void *out_bf16, void *workspace,
+                     size_t workspace_bytes, void *cuda_stream)
 {
     if (format != DGQ_FORMAT_DGQ && format != DGQ_FORMAT_FIXED64 && format != DGQ_FORMAT_SYM_INT8 &&
         format != DGQ_FORMAT_FP8_E4M3)
@@ -251,12 +291,14 @@ dgq_status dgq_paged_decode_attn_format(int32_t format, const void *q_bf16, cons
         return DGQ_ERR_WORKSPACE;
     bool map_failed = false;
     cudaError_t e = dgq::launch_attn(format, q_bf16, k_new_bf16, v_new_bf16, k_pool, v_pool, seg_table,
-                                     k_group_params, v_group_params, block_tables_dev, seq_lens_dev, max_seqlen,
-                                     batch, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq, num_blocks,
-                                     out_bf16, workspace, nsm, &map_failed, static_cast<cudaStream_t>(cuda_stream));
+                                     v_seg_table, k_group_params, v_group_params, block_tables_dev, seq_lens_dev,
+                                     max_seqlen, batch, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq,
+                                     num_blocks, out_bf16, workspace, nsm, &map_failed,
+                                     static_cast<cudaStream_t>(cuda_stream));
     if (map_failed) return DGQ_ERR_INVALID_ARG;
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
+}  // namespace
 
 size_t dgq_prefill_workspace_size(int32_t batch, int32_t num_kv_heads)
 {
@@ -295,9 +337,10 @@ dgq_status dgq_prefill_chunk_stats(const void *k_src_bf16, const void *v_src_bf1
                                    const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
                                    const int32_t *chunk_begin_dev, const int32_t *chunk_end_dev, int32_t batch,
                                    int32_t max_seqlen, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                   float *window_stats, int32_t max_windows, void *workspace, size_t workspace_bytes,
-                                   void *cuda_stream)
+                                   float *window_stats, int32_t max_windows, int32_t flags, void *workspace,
+                                   size_t workspace_bytes, void *cuda_stream)
 {
+    if (flags & ~DGQ_PREFILL_V_VARIANCE) return DGQ_ERR_INVALID_ARG;
     dgq_status st = prefill_checks(k_src_bf16, v_src_bf16, num_src_blocks, src_block_tables_dev,
                                    max_src_blocks_per_seq, batch, max_seqlen, num_kv_heads, head_dim, block_size,
                                    window_stats, max_windows, workspace, workspace_bytes);
@@ -310,8 +353,9 @@ dgq_status dgq_prefill_chunk_stats(const void *k_src_bf16, const void *v_src_bf1
                                  num_src_blocks};
     bool map_failed = false;
     const cudaError_t e = dgq::launch_prefill_stats(src, chunk_begin_dev, chunk_end_dev, batch, max_seqlen,
-                                                    num_kv_heads, block_size, window_stats, max_windows, workspace,
-                                                    nsm, &map_failed, static_cast<cudaStream_t>(cuda_stream));
+                                                    num_kv_heads, block_size, window_stats, max_windows,
+                                                    (flags & DGQ_PREFILL_V_VARIANCE) != 0, workspace, nsm,
+                                                    &map_failed, static_cast<cudaStream_t>(cuda_stream));
     if (map_failed) return DGQ_ERR_INVALID_ARG;
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
@@ -322,9 +366,10 @@ dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, in
                               int32_t head_dim, int32_t block_size, const float *window_stats, int32_t max_windows,
                               const int32_t *block_tables_dev, int32_t max_blocks_per_seq, uint8_t *k_pool,
                               uint8_t *v_pool, int32_t num_blocks, dgq_seg_record *seg_table,
-                              const dgq_compress_options *options, void *workspace, size_t workspace_bytes,
-                              void *cuda_stream)
+                              dgq_seg_record *v_seg_table, const dgq_compress_options *options, void *workspace,
+                              size_t workspace_bytes, void *cuda_stream)
 {
+    if (v_seg_table && !aligned16(v_seg_table)) return DGQ_ERR_INVALID_ARG;
     dgq::GroupSettings gs = {DGQ_MAX_SEG, 0.0f};
     if (options) {
         if (options->max_groups < 1 || options->max_groups > DGQ_MAX_SEG || !(options->min_var >= 0.0f) ||
@@ -352,7 +397,7 @@ dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, in
     bool map_failed = false;
     const cudaError_t e = dgq::launch_prefill_finish(
         src, seq_lens_dev, batch, max_seqlen, num_kv_heads, block_size, window_stats, max_windows, block_tables_dev,
-        max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, gs, workspace, nsm, &map_failed,
+        max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, v_seg_table, gs, workspace, nsm, &map_failed,
         static_cast<cudaStream_t>(cuda_stream));
     if (map_failed) return DGQ_ERR_INVALID_ARG;
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;

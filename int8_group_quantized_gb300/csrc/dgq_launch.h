@@ -48,9 +48,10 @@ struct AttnLayout {
 };
 AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm);
 // format: a dgq_format (DGQ and SYM_INT8 decode through the records; kpar / vpar are read for
-// FIXED64 only).
+// FIXED64 only).  vtable non-null (DGQ only): independent V segmentation, V's records there.
 cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const void *vnew, const uint8_t *kpool,
-                        const uint8_t *vpool, const dgq_seg_record *table, const float *kpar, const float *vpar,
+                        const uint8_t *vpool, const dgq_seg_record *table, const dgq_seg_record *vtable,
+                        const float *kpar, const float *vpar,
                         const int32_t *bt, const int32_t *seq_lens, int32_t max_seqlen, int32_t B, int32_t Hq,
                         int32_t Hkv, int32_t bs, int32_t max_blocks, int32_t num_blocks, void *out, void *ws, int nsm,
                         bool *map_failed, cudaStream_t stream);
@@ -71,12 +72,13 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32
 size_t prefill_workspace_bytes(int32_t B, int32_t Hkv);
 cudaError_t launch_prefill_stats(const SourceDesc &src, const int32_t *begin, const int32_t *end, int32_t B,
                                  int32_t max_seqlen, int32_t Hkv, int32_t bs, float *stats, int32_t max_windows,
-                                 void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+                                 bool v_variance, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+// vtable non-null: independent V segmentation (V's records there)
 cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens, int32_t B, int32_t max_seqlen,
                                   int32_t Hkv, int32_t bs, const float *stats, int32_t max_windows,
                                   const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
-                                  int32_t num_blocks, dgq_seg_record *table, GroupSettings gs, void *ws, int nsm,
-                                  bool *map_failed, cudaStream_t stream);
+                                  int32_t num_blocks, dgq_seg_record *table, dgq_seg_record *vtable,
+                                  GroupSettings gs, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query), or null.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

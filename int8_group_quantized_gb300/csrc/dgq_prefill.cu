@@ -38,7 +38,7 @@ constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfRingBytes = kPfWarps * kPfSlots * kWinBytes;
 constexpr int kSegThreads = 256;                  // segmentation CTA (one per pair)
 constexpr int32_t kMaxPrefillBatch = 8192;       // the library's per-call batch limit
-constexpr int kStatFloats = 8;                    // per window: mean, k min, k max, v min, v max, 0, 0, 0
+constexpr int kStatFloats = 8;  // per window: K mean variance, k min, k max, v min, v max, V mean variance, 0, 0
 
 struct PrefillArgs {
     TileSource src;
@@ -48,7 +48,8 @@ struct PrefillArgs {
     uint8_t *kpool, *vpool;
     float *stats;          // [B, Hkv, max_windows, 8]
     dgq_seg_record *table;
-    PairParams *params;    // [B * Hkv] quantiser parameters (workspace)
+    dgq_seg_record *vtable;  // independent V segmentation: V's records (null: one shared segmentation)
+    PairParams *params;    // [2][B * Hkv] quantiser parameters (workspace): K's (or shared), V's
     WsHeader *hdr;
     int32_t B, Hkv, bs, max_windows, max_blocks, num_blocks, max_seqlen;
     int32_t max_groups;
@@ -69,8 +70,54 @@ __device__ __forceinline__ void pf_range(const PrefillArgs &a, bool quant, int32
     w1 = (t1 + kWin - 1) / kWin;
 }
 
-// Statistics (quant == false) or codes (quant == true) of every window of the call.
-template <bool quant>
+// Mean variance of the tokens of a V tile, in the same balanced order as K's (window_stats).
+__device__ __forceinline__ float tile_var_mean(uint32_t tile, int32_t cnt)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = lane >> 1, hh = lane & 1;
+    __nv_bfloat162 mn2 = __float2bfloat162_rn(INFINITY), mx2 = __float2bfloat162_rn(-INFINITY);
+    float s = sum64<false>(tile, t, hh, 0, mn2, mx2);
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
+    const float mean = __fmul_rn(s, 0.0078125f);  // exact /128
+    float e = sum64<true>(tile, t, hh, mean, mn2, mx2);
+    e = __fadd_rn(e, __shfl_xor_sync(0xffffffffu, e, 1));
+    float var = __fmul_rn(e, 0.0078125f);
+    var = t < cnt ? var : 0.0f;
+#pragma unroll
+    for (int o = 2; o <= 16; o <<= 1) var = __fadd_rn(var, __shfl_xor_sync(0xffffffffu, var, o));
+    return __fdiv_rn(var, (float)cnt);
+}
+
+// Codes of one window tile when K and V have their own segments: as window_quant, with K's
+// segment looked up in pk and V's in pv.
+__device__ __forceinline__ void window_quant_split(uint8_t *kpool, uint8_t *vpool, int32_t Hkv, int32_t bs,
+                                                   int32_t h, int32_t t0, int32_t cnt, int32_t blk, uint32_t kt,
+                                                   uint32_t vt, const PairCache &pk, const PairCache &pv)
+{
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, sub = lane & 15;
+    const int sk = __popc(__ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pk.start <= t0));
+    const int sv = __popc(__ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pv.start <= t0));
+    const float kmn = __shfl_sync(0xffffffffu, pk.kmn, sk), kinv = __shfl_sync(0xffffffffu, pk.kinv, sk);
+    const float vmn = __shfl_sync(0xffffffffu, pv.vmn, sv), vinv = __shfl_sync(0xffffffffu, pv.vinv, sv);
+    const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + (t0 % bs)) * kD + sub * 8;
+    const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
+    const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int tt = 2 * i + half;
+        if (tt < cnt) {
+            const uint4 kq = ld_shared_v4(kt + tile_off(tt, sub));
+            const uint4 vq = ld_shared_v4(vt + tile_off(tt, sub));
+            __stcs(reinterpret_cast<uint2 *>(kpool + dst0 + tt * kD), encode8(kq, kmn, kinv2));
+            __stcs(reinterpret_cast<uint2 *>(vpool + dst0 + tt * kD), encode8(vq, vmn, vinv2));
+        }
+    }
+}
+
+// Statistics (quant == false) or codes (quant == true) of every window of the call; `split`:
+// statistics also take V's mean variance, codes use K's and V's own segments.
+template <bool quant, bool split>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_window_kernel(const __grid_constant__ PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -158,19 +205,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_window_kernel(const __g
         const int64_t pair = (int64_t)l.b * Hkv + l.h;
         if (!quant) {
             const WinStats s = window_stats(kt, vt, cnt);
+            const float vmean = split ? tile_var_mean(vt, cnt) : 0.0f;
             if (lane == 0) {
                 float4 *dst = reinterpret_cast<float4 *>(a.stats + (pair * a.max_windows + l.w) * kStatFloats);
                 __stcg(dst, make_float4(s.mean, s.kmn, s.kmx, s.vmn));
-                __stcg(dst + 1, make_float4(s.vmx, 0.0f, 0.0f, 0.0f));
+                __stcg(dst + 1, make_float4(s.vmx, vmean, 0.0f, 0.0f));
             }
         } else {
             const PairCache pc = load_params(a.params + pair);
             int32_t blk = -1;
             if (t0 / a.bs < a.max_blocks) blk = __ldg(a.bt + (int64_t)l.b * a.max_blocks + t0 / a.bs);
-            if ((uint32_t)blk < (uint32_t)a.num_blocks)
-                window_quant(a.kpool, a.vpool, Hkv, a.bs, l.h, t0, cnt, blk, kt, vt, pc);
-            else if (lane == 0)  // not a block of the pools: flagged, nothing written
+            if ((uint32_t)blk < (uint32_t)a.num_blocks) {
+                if (split)
+                    window_quant_split(a.kpool, a.vpool, Hkv, a.bs, l.h, t0, cnt, blk, kt, vt, pc,
+                                       load_params(a.params + (int64_t)a.B * Hkv + pair));
+                else
+                    window_quant(a.kpool, a.vpool, Hkv, a.bs, l.h, t0, cnt, blk, kt, vt, pc);
+            } else if (lane == 0) {  // not a block of the pools: flagged, nothing written
                 record_error(a.hdr, kErrBadBlock);
+            }
         }
         __syncwarp();  // the slot's reads are done before it is refilled
         issue(x + kPfSlots * nw, slot);
@@ -186,32 +239,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_window_kernel(const __g
     }
 }
 
-// Segmentation of pair blockIdx.x from its window statistics: record and quantiser parameters.
-__global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __grid_constant__ PrefillArgs a)
+// Boundaries of one pair, chosen by the whole CTA from the window means at float `slot` of each
+// window's statistics: at most k of them (the k largest jumps |m[w+1] - m[w]|, descending, the
+// earlier window first on ties; none between two windows below min_var).  Every thread keeps
+// the top four of its strided share of the windows, each warp reduces its lanes' lists to its
+// own top four, and warp 0 merges the warps' lists.  Returns the number placed; cut[] holds
+// the starts in windows, ascending (INT32_MAX past the last), in every thread.
+__device__ int cta_boundaries(const float *st, int32_t W, int k, float min_var, int slot, int32_t (&cut)[4])
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t pair = blockIdx.x, b = pair / a.Hkv;
-    int32_t L = __ldg(a.end + b);
-    if (L < 0 || L > a.max_seqlen) {
-        if (tid == 0) record_error(a.hdr, kErrBadLength);
-        L = 0;
-    }
-    const int32_t W = (L + kWin - 1) / kWin;
-    int k = L == 0 ? -1 : min(min(ngroups(L), a.max_groups), W) - 1;  // boundaries to place
-    const float *st = a.stats + (int64_t)pair * a.max_windows * kStatFloats;
     __shared__ float s_cj[kSegThreads / 32][4];
     __shared__ int32_t s_cw[kSegThreads / 32][4];
     __shared__ int32_t s_cut[4];
     __shared__ int s_k;
-    __shared__ float s_mm[kSegThreads / 32][4][kMaxSeg];
-
-    // (1) per-thread top four of (jump desc, window asc) over windows tid, tid + 256, ...
     float cj[4] = {-1.0f, -1.0f, -1.0f, -1.0f};
     int32_t cw[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
     if (k > 0) {
         for (int32_t w = tid; w + 1 < W; w += kSegThreads) {
-            const float m0 = __ldcg(st + (int64_t)w * kStatFloats), m1 = __ldcg(st + (int64_t)(w + 1) * kStatFloats);
-            if (!(m0 >= a.min_var || m1 >= a.min_var)) continue;  // two quiet windows stay together
+            const float m0 = __ldcg(st + (int64_t)w * kStatFloats + slot);
+            const float m1 = __ldcg(st + (int64_t)(w + 1) * kStatFloats + slot);
+            if (!(m0 >= min_var || m1 >= min_var)) continue;  // two quiet windows stay together
             const float j = fabsf(__fsub_rn(m1, m0));
             if (j > cj[3]) {  // windows arrive in increasing order: an equal jump keeps the earlier
                 cj[3] = j;
@@ -226,8 +273,7 @@ __global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __gr
             }
         }
     }
-    // (2) each warp: its top k by k rounds of arg-best over the lanes' list heads
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 4; ++r) {  // each warp: four rounds of arg-best over the lanes' list heads
         float j = cj[0];
         int32_t wv = cw[0];
 #pragma unroll
@@ -249,11 +295,10 @@ __global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __gr
         }
     }
     __syncthreads();
-    // (3) warp 0 merges the warps' lists (one candidate per lane) into the k boundaries
-    if (warp == 0) {
+    if (warp == 0) {  // merge: one candidate per lane, k rounds of arg-best
         float mj = s_cj[lane >> 2][lane & 3];
         int32_t mw = s_cw[lane >> 2][lane & 3];
-        int32_t cut[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
+        int32_t c4[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX};
         int kk = k < 0 ? 0 : k;
         for (int r = 0; r < kk; ++r) {
             float j = mj;
@@ -278,80 +323,138 @@ __global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __gr
             int32_t c = wv + 1;  // insertion into the sorted list of starts (in windows)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                if (c < cut[s]) {
-                    const int32_t t = cut[s];
-                    cut[s] = c;
+                if (c < c4[s]) {
+                    const int32_t t = c4[s];
+                    c4[s] = c;
                     c = t;
                 }
             }
         }
         if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s) s_cut[s] = cut[s];
+            for (int s = 0; s < 4; ++s) s_cut[s] = c4[s];
             s_k = k < 0 ? -1 : kk;
         }
     }
     __syncthreads();
-    k = s_k;
-    int32_t cut[4];
 #pragma unroll
     for (int s = 0; s < 4; ++s) cut[s] = s_cut[s];
+    const int res = s_k;
+    __syncthreads();  // the shared lists may be reused by the next call
+    return res;
+}
 
-    // (4) per-segment extremes (exact in any order)
-    float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
+// Per-segment extremes of one pair under cut[] (exact in any order), reduced over the CTA:
+// floats lo_slot (minima) and lo_slot + 1 (maxima) of each window's statistics.
+__device__ void cta_extremes(const float *st, int32_t W, const int32_t (&cut)[4], int lo_slot, float (&mn)[kMaxSeg],
+                             float (&mx)[kMaxSeg])
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float s_mm[kSegThreads / 32][2][kMaxSeg];
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
-        kmn[s] = INFINITY; kmx[s] = -INFINITY; vmn[s] = INFINITY; vmx[s] = -INFINITY;
+        mn[s] = INFINITY;
+        mx[s] = -INFINITY;
     }
     for (int32_t w = tid; w < W; w += kSegThreads) {
-        const float4 e = __ldcg(reinterpret_cast<const float4 *>(st + (int64_t)w * kStatFloats));
-        const float vx = __ldcg(st + (int64_t)w * kStatFloats + 4);
+        const float lo = __ldcg(st + (int64_t)w * kStatFloats + lo_slot);
+        const float hi = __ldcg(st + (int64_t)w * kStatFloats + lo_slot + 1);
         const int sg = (w >= cut[0]) + (w >= cut[1]) + (w >= cut[2]) + (w >= cut[3]);
 #pragma unroll
         for (int s = 0; s < kMaxSeg; ++s) {
             if (s == sg) {
-                kmn[s] = fminf(kmn[s], e.y); kmx[s] = fmaxf(kmx[s], e.z);
-                vmn[s] = fminf(vmn[s], e.w); vmx[s] = fmaxf(vmx[s], vx);
+                mn[s] = fminf(mn[s], lo);
+                mx[s] = fmaxf(mx[s], hi);
             }
         }
     }
 #pragma unroll
     for (int s = 0; s < kMaxSeg; ++s) {
-        kmn[s] = warp_min(kmn[s]); kmx[s] = warp_max(kmx[s]);
-        vmn[s] = warp_min(vmn[s]); vmx[s] = warp_max(vmx[s]);
+        mn[s] = warp_min(mn[s]);
+        mx[s] = warp_max(mx[s]);
     }
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kMaxSeg; ++s) {
-            s_mm[warp][0][s] = kmn[s]; s_mm[warp][1][s] = kmx[s];
-            s_mm[warp][2][s] = vmn[s]; s_mm[warp][3][s] = vmx[s];
+            s_mm[warp][0][s] = mn[s];
+            s_mm[warp][1][s] = mx[s];
         }
     }
     __syncthreads();
-    if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < kMaxSeg; ++s) {
-            for (int w = 1; w < kSegThreads / 32; ++w) {
-                kmn[s] = fminf(kmn[s], s_mm[w][0][s]); kmx[s] = fmaxf(kmx[s], s_mm[w][1][s]);
-                vmn[s] = fminf(vmn[s], s_mm[w][2][s]); vmx[s] = fmaxf(vmx[s], s_mm[w][3][s]);
-            }
+    for (int s = 0; s < kMaxSeg; ++s) {
+        for (int w = 0; w < kSegThreads / 32; ++w) {
+            mn[s] = fminf(mn[s], s_mm[w][0][s]);
+            mx[s] = fmaxf(mx[s], s_mm[w][1][s]);
         }
-        dgq_seg_record rec = {};
-        PairParams pp = {};
-        if (k >= 0) make_params(L, k, cut, kmn, kmx, vmn, vmx, rec, pp);
-        a.table[pair] = rec;
-        a.params[pair] = pp;
+    }
+    __syncthreads();
+}
+
+// Segmentation of pair blockIdx.x from its window statistics: record(s) and quantiser parameters.
+__global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __grid_constant__ PrefillArgs a)
+{
+    const int tid = threadIdx.x;
+    const int32_t pair = blockIdx.x, b = pair / a.Hkv;
+    const int64_t P = (int64_t)a.B * a.Hkv;
+    int32_t L = __ldg(a.end + b);
+    if (L < 0 || L > a.max_seqlen) {
+        if (tid == 0) record_error(a.hdr, kErrBadLength);
+        L = 0;
+    }
+    const int32_t W = (L + kWin - 1) / kWin;
+    const int k0 = L == 0 ? -1 : min(min(ngroups(L), a.max_groups), W) - 1;  // boundaries to place
+    const float *st = a.stats + (int64_t)pair * a.max_windows * kStatFloats;
+
+    int32_t cut[4];
+    const int k = cta_boundaries(st, W, k0, a.min_var, 0, cut);  // from K's variance
+    float kmn[kMaxSeg], kmx[kMaxSeg], vmn[kMaxSeg], vmx[kMaxSeg];
+    cta_extremes(st, W, cut, 1, kmn, kmx);
+    if (a.vtable == nullptr) {  // one segmentation, shared by K and V
+        cta_extremes(st, W, cut, 3, vmn, vmx);
+        if (tid == 0) {
+            dgq_seg_record rec = {};
+            PairParams pp = {};
+            if (k >= 0) make_params(L, k, cut, kmn, kmx, vmn, vmx, rec, pp);
+            a.table[pair] = rec;
+            a.params[pair] = pp;
+        }
+        return;
+    }
+    // independent V segmentation: V's boundaries from V's variance, each record keeps its tensor's
+    // fields (the other tensor's are 0)
+    int32_t vcut[4];
+    const int kv = cta_boundaries(st, W, k0, a.min_var, 5, vcut);
+    cta_extremes(st, W, vcut, 3, vmn, vmx);
+    if (tid == 0) {
+        dgq_seg_record rk = {}, rv = {};
+        PairParams pk = {}, pv = {};
+        if (k >= 0) {
+            make_params(L, k, cut, kmn, kmx, kmn, kmx, rk, pk);
+            make_params(L, kv, vcut, vmn, vmx, vmn, vmx, rv, pv);
+#pragma unroll
+            for (int s = 0; s < kMaxSeg; ++s) {
+                rk.v_min[s] = rk.v_scale[s] = 0.0f;
+                rv.k_min[s] = rv.k_scale[s] = 0.0f;
+            }
+            rk.v_inv_last = 0.0f;
+            rv.k_inv_last = 0.0f;
+        }
+        a.table[pair] = rk;
+        a.vtable[pair] = rv;
+        a.params[pair] = pk;
+        a.params[P + pair] = pv;
     }
 }
 
 size_t prefill_workspace_bytes(int32_t B, int32_t Hkv)
 {
-    return sizeof(WsHeader) + (size_t)B * Hkv * sizeof(PairParams);
+    return sizeof(WsHeader) + 2 * (size_t)B * Hkv * sizeof(PairParams);
 }
 
 static size_t prefill_smem(int32_t B) { return 1024 + kPfRingBytes + 8 * kPfSlots * kPfWarps + 4 * ((size_t)B + 1); }
 
-template <bool quant>
+template <bool quant, bool split>
 static cudaError_t launch_windows(const PrefillArgs &a, int nsm, cudaStream_t stream)
 {
     // the shared-memory limit is raised once per device, to what the largest batch needs
@@ -360,12 +463,12 @@ static cudaError_t launch_windows(const PrefillArgs &a, int nsm, cudaStream_t st
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev != ready_dev) {
-        e = cudaFuncSetAttribute(prefill_window_kernel<quant>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_window_kernel<quant, split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)prefill_smem(kMaxPrefillBatch));
         if (e != cudaSuccess) return e;
         ready_dev = dev;
     }
-    prefill_window_kernel<quant><<<nsm, kPfThreads, prefill_smem(a.B), stream>>>(a);
+    prefill_window_kernel<quant, split><<<nsm, kPfThreads, prefill_smem(a.B), stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -376,7 +479,7 @@ static bool prefill_args(const SourceDesc &src, int32_t B, int32_t max_seqlen, i
     a.begin = a.end = a.bt = nullptr;
     a.kpool = a.vpool = nullptr;
     a.stats = stats;
-    a.table = nullptr;
+    a.table = a.vtable = nullptr;
     a.hdr = static_cast<WsHeader *>(ws);
     a.params = reinterpret_cast<PairParams *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
     a.B = B;
@@ -392,21 +495,21 @@ static bool prefill_args(const SourceDesc &src, int32_t B, int32_t max_seqlen, i
 
 cudaError_t launch_prefill_stats(const SourceDesc &src, const int32_t *begin, const int32_t *end, int32_t B,
                                  int32_t max_seqlen, int32_t Hkv, int32_t bs, float *stats, int32_t max_windows,
-                                 void *ws, int nsm, bool *map_failed, cudaStream_t stream)
+                                 bool v_variance, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
 {
     PrefillArgs a;
     *map_failed = !prefill_args(src, B, max_seqlen, Hkv, bs, stats, max_windows, ws, a);
     if (*map_failed) return cudaErrorInvalidValue;
     a.begin = begin;
     a.end = end;
-    return launch_windows<false>(a, nsm, stream);
+    return v_variance ? launch_windows<false, true>(a, nsm, stream) : launch_windows<false, false>(a, nsm, stream);
 }
 
 cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens, int32_t B, int32_t max_seqlen,
                                   int32_t Hkv, int32_t bs, const float *stats, int32_t max_windows,
                                   const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
-                                  int32_t num_blocks, dgq_seg_record *table, GroupSettings gs, void *ws, int nsm,
-                                  bool *map_failed, cudaStream_t stream)
+                                  int32_t num_blocks, dgq_seg_record *table, dgq_seg_record *vtable,
+                                  GroupSettings gs, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
 {
     PrefillArgs a;
     *map_failed = !prefill_args(src, B, max_seqlen, Hkv, bs, const_cast<float *>(stats), max_windows, ws, a);
@@ -418,12 +521,13 @@ cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens
     a.vpool = vpool;
     a.num_blocks = num_blocks;
     a.table = table;
+    a.vtable = vtable;
     a.max_groups = gs.max_groups;
     a.min_var = gs.min_var;
     prefill_segment_kernel<<<(unsigned)(B * Hkv), kSegThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_windows<true>(a, nsm, stream);
+    return vtable ? launch_windows<true, true>(a, nsm, stream) : launch_windows<true, false>(a, nsm, stream);
 }
 
 }  // namespace dgq

@@ -163,19 +163,20 @@ def test_attn_format_rejects_bad_arguments_before_launch(L):
 def test_prefill_calls_reject_bad_arguments_before_launch(L):
     def stats(**kw):
         a = dict(k=FAKE, v=FAKE, nsrc=32, sbt=FAKE, msrc=19, beg=FAKE, end=FAKE, batch=2, max_seqlen=300, hkv=2,
-                 d=128, bs=16, st=FAKE, mw=19, ws=FAKE, wsb=1 << 20)
+                 d=128, bs=16, st=FAKE, mw=19, flags=0, ws=FAKE, wsb=1 << 20)
         a.update(kw)
         return L.dgq_prefill_chunk_stats(a["k"], a["v"], a["nsrc"], a["sbt"], a["msrc"], a["beg"], a["end"],
                                          a["batch"], a["max_seqlen"], a["hkv"], a["d"], a["bs"], a["st"], a["mw"],
-                                         a["ws"], a["wsb"], 0)
+                                         a["flags"], a["ws"], a["wsb"], 0)
 
     def finish(**kw):
         a = dict(k=FAKE, v=FAKE, nsrc=32, sbt=FAKE, msrc=19, lens=FAKE, batch=2, max_seqlen=300, hkv=2, d=128,
-                 bs=16, st=FAKE, mw=19, bt=FAKE, mb=19, kp=FAKE, vp=FAKE, nb=32, table=FAKE, ws=FAKE, wsb=1 << 20)
+                 bs=16, st=FAKE, mw=19, bt=FAKE, mb=19, kp=FAKE, vp=FAKE, nb=32, table=FAKE, vtable=None, ws=FAKE,
+                 wsb=1 << 20)
         a.update(kw)
         return L.dgq_prefill_finish(a["k"], a["v"], a["nsrc"], a["sbt"], a["msrc"], a["lens"], a["batch"],
                                     a["max_seqlen"], a["hkv"], a["d"], a["bs"], a["st"], a["mw"], a["bt"], a["mb"],
-                                    a["kp"], a["vp"], a["nb"], a["table"], None, a["ws"], a["wsb"], 0)
+                                    a["kp"], a["vp"], a["nb"], a["table"], a["vtable"], None, a["ws"], a["wsb"], 0)
     for call in (stats, finish):
         assert call(d=64) == UNSUPPORTED
         assert call(bs=48) == UNSUPPORTED
@@ -188,10 +189,19 @@ def test_prefill_calls_reject_bad_arguments_before_launch(L):
         assert call(ws=0) == WORKSPACE
         assert call(wsb=L.dgq_prefill_workspace_size(2, 2) - 1) == WORKSPACE
     assert stats(beg=0) == INVALID
+    assert stats(flags=2) == INVALID                     # unknown flag bits
+    assert finish(vtable=FAKE + 8) == INVALID            # misaligned V record table
     assert finish(lens=0) == INVALID
     assert finish(mb=18) == INVALID                          # destination table too short for 300 tokens
     assert finish(table=FAKE + 8) == INVALID
-    assert L.dgq_prefill_workspace_size(2, 2) == 256 + 2 * 2 * 128
+    assert L.dgq_prefill_workspace_size(2, 2) == 256 + 2 * 2 * 2 * 128
+
+    def split(vtable=FAKE, d=128):
+        return L.dgq_paged_decode_attn_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, vtable, FAKE, FAKE, 300, 2, 4, 2,
+                                             d, 16, 19, 32, FAKE, FAKE, 1 << 30, 0)
+    assert split(vtable=0) == INVALID
+    assert split(vtable=FAKE + 4) == INVALID
+    assert split(d=64) == UNSUPPORTED
 
 
 def test_workspace_size_is_monotone(L):

@@ -441,6 +441,10 @@ def run_ours(args):
     if not args.no_prefill:
         prefill = time_prefill(w, lens, cu, bt, layers, d_cu, d_bt, d_lens, max_seqlen, sp, comp_b,
                                max(2, min(args.steps, 5)))
+    split_v = None
+    if not args.no_prefill:
+        split_v = time_split_v(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, comp_b, ref0,
+                               max(2, min(args.steps, 5)))
     formats = None
     if not args.no_formats:
         formats = time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0,
@@ -499,6 +503,7 @@ def run_ours(args):
             "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
             "fidelity": fidelity,
             "prefill_two_phase": prefill,
+            "independent_v_segmentation": split_v,
             "formats": formats,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
@@ -682,6 +687,68 @@ def time_prefill(w, lens, cu, bt, layers, d_cu, d_bt, d_lens, max_seqlen, sp, co
             "records_identical_to_one_shot": same, "device_error": err,
             "what": "statistics per prefill chunk right after the chunk is written (L2-hot), then one "
                     "finishing pass; bytes as for compress (2 B read + 1 B written per K/V value)"}
+
+
+def time_split_v(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, comp_b, ref0, reps):
+    """Independent V segmentation (a group-selection variant) on the same workload, outside the
+    timed steps: each layer compressed in two phases from a bf16 paged copy of its K/V (one
+    statistics call over whole requests with V's variance, then the finish with a V record
+    table), then decoded by the split instance of the decode kernel; CUDA-event time per layer
+    over `reps` passes, and on rank 0 the GPU output of request 0 against fp64 attention over
+    the unquantised K/V."""
+    import numpy as np
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    dev = layers[0]["k"].device
+    B, Hkv, bs = w.batch, w.hkv, w.block_size
+    nb = layers[0]["kp"].shape[0]
+    bt = d_bt.cpu().numpy()
+    cu = d_cu.cpu().numpy()
+    blk = torch.from_numpy(np.concatenate([bt[b, np.arange(int(L)) // bs] for b, L in enumerate(lens)])
+                           .astype(np.int64)).to(dev)
+    slot = torch.from_numpy(np.concatenate([np.arange(int(L)) % bs for L in lens]).astype(np.int64)).to(dev)
+    rows = torch.from_numpy(np.concatenate([int(cu[b]) + np.arange(int(L)) for b, L in enumerate(lens)])
+                            .astype(np.int64)).to(dev)
+    ks = torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vs = torch.zeros_like(ks)
+    stats = torch.zeros((B, Hkv, (max_seqlen + 15) // 16, 8), dtype=torch.float32, device=dev)
+    ws = torch.zeros(dgq.dgq_prefill_workspace_size(B, Hkv), dtype=torch.uint8, device=dev)
+    vtab = torch.zeros_like(layers[0]["table"])
+    zeros = torch.zeros(B, dtype=torch.int32, device=dev)
+    t_st = t_fin = t_dec = 0.0
+    use = layers[:8]
+    for r in range(reps + 1):
+        for L in use:
+            ks[blk, :, slot, :] = L["k"][rows]
+            vs[blk, :, slot, :] = L["v"][rows]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record()
+            dgq.dgq_prefill_chunk_stats(ks, vs, d_bt, zeros, d_lens, max_seqlen, stats, ws, sp, v_variance=True)
+            ev[1].record()
+            dgq.dgq_prefill_finish(ks, vs, d_bt, d_lens, max_seqlen, stats, d_bt, L["kp"], L["vp"], L["table"], ws,
+                                   sp, v_seg_table=vtab)
+            ev[2].record()
+            dgq.dgq_paged_decode_attn_split(L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], vtab, d_bt,
+                                            d_lens, max_seqlen, L["out"], aws, sp)
+            ev[3].record()
+            torch.cuda.synchronize()
+            if r > 0:
+                t_st += ev[0].elapsed_time(ev[1])
+                t_fin += ev[1].elapsed_time(ev[2])
+                t_dec += ev[2].elapsed_time(ev[3])
+            if r == reps and L is use[0] and ref0 is not None:
+                fid = err_stats(out0(L), ref0["raw"])
+    n = reps * len(use)
+    st_us, fin_us, dec_us = t_st / n * 1e3, t_fin / n * 1e3, t_dec / n * 1e3
+    res = {"stats_us_per_layer": round(st_us, 2), "finish_us_per_layer": round(fin_us, 2),
+           "compress_gbs": round(comp_b / (st_us + fin_us) / 1e3, 1), "decode_us_per_layer": round(dec_us, 2),
+           "decode_gbs": round(dec_b / dec_us / 1e3, 1),
+           "device_error": dgq.dgq_workspace_error(ws, sp) or dgq.dgq_workspace_error(aws, sp),
+           "what": "statistics with V's variance over whole requests + finish with V's own segments; decode "
+                   "with both record tables"}
+    if ref0 is not None:
+        res["gpu_vs_unquantised"] = fid
+    return res
 
 
 def time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0, reps):

@@ -115,3 +115,43 @@ def test_misaligned_chunk_is_flagged():
     torch.cuda.synchronize()
     assert dgq.dgq_workspace_error(ws) == 6  # kErrBadLength
     assert not stats.any()
+
+
+def test_window_statistics_bit_exact():
+    """The statistics array itself against the oracle, window by window: K's and V's mean
+    variance (balanced fp32 sums, as the oracle fixes them) and the K/V extremes, bit for bit."""
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    import oracle
+    case = Case([37, 300, 1, 2100], hq=4, hkv=2, bs=16, seed=134)
+    dev = torch.device("cuda:0")
+    ks, vs, sbt = paged_source(case, seed=10)
+    d_ks = torch.from_numpy(ks.view(np.int16)).to(dev).view(torch.bfloat16)
+    d_vs = torch.from_numpy(vs.view(np.int16)).to(dev).view(torch.bfloat16)
+    W = (case.max_seqlen + 15) // 16
+    stats = torch.full((case.B, case.hkv, W, 8), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.zeros(dgq.dgq_prefill_workspace_size(case.B, case.hkv), dtype=torch.uint8, device=dev)
+    for beg, end in schedule_ragged(case.lens, 11):
+        dgq.dgq_prefill_chunk_stats(d_ks, d_vs, torch.from_numpy(sbt).to(dev),
+                                    torch.from_numpy(np.asarray(beg, np.int32)).to(dev),
+                                    torch.from_numpy(np.asarray(end, np.int32)).to(dev), case.max_seqlen, stats, ws,
+                                    v_variance=True)
+    torch.cuda.synchronize()
+    assert dgq.dgq_workspace_error(ws) == 0
+    got = stats.cpu().numpy()
+    for b in range(case.B):
+        L = int(case.lens[b])
+        rows = slice(int(case.cu[b]), int(case.cu[b + 1]))
+        for h in range(case.hkv):
+            k, v = case.k[rows, h], case.v[rows, h]
+            km = oracle.window_means(np.array([oracle.token_variance(r) for r in k], dtype=np.float32))
+            vm = oracle.window_means(np.array([oracle.token_variance(r) for r in v], dtype=np.float32))
+            kf = (k.astype(np.uint32) << 16).view(np.float32)
+            vf = (v.astype(np.uint32) << 16).view(np.float32)
+            nw = (L + 15) // 16
+            want = np.zeros((nw, 8), dtype=np.float32)
+            want[:, 0], want[:, 5] = km, vm
+            for w in range(nw):
+                want[w, 1], want[w, 2] = kf[16 * w:16 * w + 16].min(), kf[16 * w:16 * w + 16].max()
+                want[w, 3], want[w, 4] = vf[16 * w:16 * w + 16].min(), vf[16 * w:16 * w + 16].max()
+            assert np.array_equal(got[b, h, :nw].view(np.uint32), want.view(np.uint32)), (b, h)

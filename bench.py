@@ -222,6 +222,22 @@ class OracleSample:
         return self.dec_b * n, td, self.comp_b * n, tc
 
 
+def host_cpu():
+    """The host's CPU model and logical core count (the oracle baseline runs on one core)."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part") and not model:
+                    model = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return {"model": model or platform.processor() or "unknown", "arch": platform.machine(),
+            "nproc": os.cpu_count()}
+
+
 def max_over_ranks(values, device, world):
     """The slowest rank's value of each timing (a replica run is as fast as its slowest GPU)."""
     import torch
@@ -259,7 +275,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": "4 requests x 1 layer per step"},
         "compress_gbs": round(bc / tot_c / 1e9, 4),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -517,6 +534,7 @@ def run_ours(args):
                 a_, b_, c_, d_ = sample.run()
                 db, dt, cb, ct = db + a_, dt + b_, cb + c_, ct + d_
             line["cpu_baseline"] = {"value": round(db / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "host": host_cpu(),
                                     "sample": sample.desc + f", repeated for {dt + ct:.1f} s",
                                     "compress_gbs": round(cb / ct / 1e9, 4)}
         print(json.dumps(line), flush=True)

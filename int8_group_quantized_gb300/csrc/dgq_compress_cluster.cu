@@ -22,8 +22,13 @@
 //  * Twelve workers and one segmentation warp per CTA (127 registers a thread): measured on
 //    this GPU, 12 workers with 2 pair slots took 104 us per layer of the Llama-3-8B batch-32
 //    workload where 10 workers with 3 slots took 120 us.
-//  * Clusters of 4 (not 8): measured on this GPU, only 15 clusters of 8 CTAs fit at once
-//    (120 of 152 SMs), 36 of 4 (144).
+//  * Clusters of 4 or 2 CTAs (not 8: measured on this GPU, only 15 clusters of 8 CTAs fit at
+//    once, 120 of 152 SMs; 36 of 4, 144 SMs; 76 of 2, all 152).  Measured per layer: the
+//    Llama-3-8B batch (256 pairs of 128 windows) 105 us with clusters of 4 and 118 us with
+//    clusters of 2 (the last round of pairs leaves more of the GPU idle); the MHA batch (3200
+//    pairs of 16-128 windows) 743 us with 4 and 639 us with 2 (more, smaller clusters; each CTA
+//    gets a larger share of a short pair).  Calls with at least kManyPairs pairs take clusters
+//    of 2.
 // Every wait is bounded; a timeout records an error in the workspace header and the CTA skips
 // dependent work.
 #include "dgq_device.cuh"
@@ -35,16 +40,14 @@
 
 namespace dgq {
 
-constexpr int kCl = 4;                                   // CTAs per cluster
+constexpr int32_t kManyPairs = 1024;                     // from this many pairs on: clusters of 2
 constexpr int kCWorkers = 12;                            // worker warps per CTA (plus a segmentation warp)
 constexpr int kCThreads = (kCWorkers + 1) * 32;
 constexpr int kCRing = 2;                                // windows in flight per worker
 static_assert(kCRing == 2, "the worker loop alternates two ring slots");
 constexpr int kCRingBytes = kCWorkers * kCRing * kWinBytes;
 constexpr int kSlots = 2;                                // pairs a cluster holds at once
-constexpr int kSlotWin = 64;                             // windows of one pair per CTA
 constexpr int32_t kClusterMaxWin = 256;                  // pairs of at most 256 windows (4096 tokens)
-static_assert(kCl * kSlotWin >= kClusterMaxWin, "a CTA holds its share of the longest pair");
 static_assert(kClusterMaxWin == 8 * 32, "segment_small holds 8 windows per lane");
 
 struct ClusterArgs {
@@ -61,7 +64,9 @@ struct ClusterArgs {
     int32_t max_seqlen, num_blocks;  // for the device-side checks of lengths and block ids
 };
 
-struct ClusterSmem {
+// kSlotWin: windows of one pair per CTA (the longest pair split over the cluster's CTAs)
+template <int kSlotWin>
+struct ClusterSmemT {
     float mean[kSlots][kSlotWin];
     float4 mm[kSlots][kSlotWin];
     PairParams par[kSlots];
@@ -164,7 +169,8 @@ __device__ __forceinline__ PairCache load_params_smem(const PairParams *pp)
     return pc;
 }
 
-// Windows [lo, hi) of a pair of W windows held by CTA `r` of the cluster.
+// Windows [lo, hi) of a pair of W windows held by CTA `r` of a cluster of kCl CTAs.
+template <int kCl>
 __device__ __forceinline__ void cta_range(int32_t W, int32_t r, int32_t &lo, int32_t &hi)
 {
     lo = (W * r) / kCl;
@@ -187,8 +193,12 @@ struct CItem {
     PairCache pc;
 };
 
+template <int kCl>
 __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __grid_constant__ ClusterArgs a)
 {
+    constexpr int kSlotWin = kClusterMaxWin / kCl;
+    static_assert(kCl * kSlotWin == kClusterMaxWin, "a CTA holds its share of the longest pair");
+    using ClusterSmem = ClusterSmemT<kSlotWin>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);  // window tiles start on 1024-byte boundaries
     ClusterSmem *cs = reinterpret_cast<ClusterSmem *>(smem + kCRingBytes);
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
             if (lane == 0) record_error(a.hdr, kErrBadLength);
             c.L = 0;
         }
-        cta_range((c.L + kWin - 1) / kWin, rank, c.lo, c.hi);
+        cta_range<kCl>((c.L + kWin - 1) / kWin, rank, c.lo, c.hi);
     };
     auto aborted = [&]() { return *reinterpret_cast<volatile int32_t *>(&cs->abort) != 0; };
 
@@ -464,6 +474,43 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
 
 int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 
+template <int kCl>
+static cudaError_t launch_cluster_size(const ClusterArgs &a, cudaStream_t stream)
+{
+    const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmemT<kClusterMaxWin / kCl>);  // + alignment slack
+    static int cached_dev = -1, cached_clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dev != cached_dev) {
+        e = cudaFuncSetAttribute(compress_cluster_kernel<kCl>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(nsm / kCl * kCl));
+        int nclusters = 0;  // clusters that fit on the GPU at once (GPC boundaries)
+        e = cudaOccupancyMaxActiveClusters(&nclusters, compress_cluster_kernel<kCl>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (nclusters < 1) return cudaErrorInvalidConfiguration;
+        cached_dev = dev;
+        cached_clusters = nclusters;
+    }
+    cfg.gridDim = dim3((unsigned)(cached_clusters * kCl));  // one wave: every cluster resident
+    return cudaLaunchKernelEx(&cfg, compress_cluster_kernel<kCl>, a);
+}
+
 cudaError_t launch_compress_cluster(const SourceDesc &src, const int32_t *cu, int32_t B,
                                     int32_t max_seqlen, int32_t Hkv, int32_t bs, const int32_t *bt,
                                     int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
@@ -485,39 +532,7 @@ cudaError_t launch_compress_cluster(const SourceDesc &src, const int32_t *cu, in
     a.min_var = gs.min_var;
     a.max_seqlen = max_seqlen;
     a.num_blocks = num_blocks;
-
-    const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmem);  // + alignment slack
-    static int cached_dev = -1, cached_clusters = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kCThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (dev != cached_dev) {
-        e = cudaFuncSetAttribute(compress_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        int nsm = 0;
-        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3((unsigned)(nsm / kCl * kCl));
-        int nclusters = 0;  // clusters that fit on the GPU at once (GPC boundaries)
-        e = cudaOccupancyMaxActiveClusters(&nclusters, compress_cluster_kernel, &cfg);
-        if (e != cudaSuccess) return e;
-        if (nclusters < 1) return cudaErrorInvalidConfiguration;
-        cached_dev = dev;
-        cached_clusters = nclusters;
-    }
-    cfg.gridDim = dim3((unsigned)(cached_clusters * kCl));  // one wave: every cluster resident
-    return cudaLaunchKernelEx(&cfg, compress_cluster_kernel, a);
+    return (int64_t)B * Hkv >= kManyPairs ? launch_cluster_size<2>(a, stream) : launch_cluster_size<4>(a, stream);
 }
 
 }  // namespace dgq

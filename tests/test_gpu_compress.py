@@ -53,6 +53,15 @@ def test_many_short_pairs_cluster_path():
     run(Case(lens, hq=32, hkv=8, bs=16, seed=11))
 
 
+def test_many_pairs_two_cta_clusters():
+    # at least 1024 pairs: the cluster path uses clusters of two CTAs; ragged lengths up to the
+    # longest pair it takes, empty and one-token requests, shuffled blocks
+    rng = np.random.default_rng(2)
+    lens = rng.integers(1, 700, 130).tolist()
+    lens[3], lens[7], lens[11], lens[20] = 0, 1, 4096, 16
+    run(Case(lens, hq=16, hkv=8, bs=16, seed=13))
+
+
 def test_short_pairs_cluster_path_edges():
     # the longest pair the cluster path takes (4096 tokens = 256 windows), one-window pairs,
     # empty requests, a partial last window, block size 64

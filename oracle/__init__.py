@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_compress_ex.restype = None
         L.oracle_compress_split.argtypes = [P, P, P, i32, i32, i32, P, i32, i32, ctypes.c_float, P, P, P, P]
         L.oracle_compress_split.restype = None
+        L.oracle_append_split.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P, P]
+        L.oracle_append_split.restype = i32
         L.oracle_dequant_pair.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_int, P]
         L.oracle_dequant_pair.restype = None
         L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, P]
@@ -199,6 +201,19 @@ def append(k_new, v_new, block_size, block_tables, k_pool, v_pool, table):
     B, Hkv = k_new.shape[0], k_new.shape[1]
     return int(lib().oracle_append(_p(k_new), _p(v_new), B, Hkv, int(block_size), _p(bt), bt.shape[1],
                                    _p(k_pool), _p(v_pool), _p(table)))
+
+
+def append_split(k_new, v_new, block_size, block_tables, k_pool, v_pool, k_table, v_table):
+    """append with independent V segmentation: K's codes and record from k_table, V's from
+    v_table, in place.  Returns the number of pairs skipped for want of a block-table column."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    for a in (k_pool, v_pool, k_table, v_table):
+        assert a.flags["C_CONTIGUOUS"]
+    B, Hkv = k_new.shape[0], k_new.shape[1]
+    return int(lib().oracle_append_split(_p(k_new), _p(v_new), B, Hkv, int(block_size), _p(bt), bt.shape[1],
+                                         _p(k_pool), _p(v_pool), _p(k_table), _p(v_table)))
 
 
 def dequant_pair(pool, table, block_tables, b, h, L, which_v):

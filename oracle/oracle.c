@@ -487,6 +487,52 @@ int32_t oracle_append(const uint16_t *k_new, const uint16_t *v_new, int32_t B, i
     return skipped;
 }
 
+/* Decode-step append with independent V segmentation: as oracle_append, each tensor with its own
+ * record (K: k_table's K fields; V: v_table's V fields; a record with n_seg == 0 gets a first
+ * segment made of the new token's own values of that tensor).  The slot is taken from K's
+ * record (both records of a pair hold the same seq_len).  Returns the pairs skipped for want of
+ * a block-table column. */
+static void append_tensor(const uint16_t *x, oracle_seg *rec, int which_v, int32_t L, uint8_t *dst)
+{
+    float *mn0 = which_v ? rec->v_min : rec->k_min;
+    float *sc0 = which_v ? rec->v_scale : rec->k_scale;
+    float *inv = which_v ? &rec->v_inv_last : &rec->k_inv_last;
+    if (rec->n_seg == 0) {
+        float mn, mx;
+        segment_min_max(x, OR_D, 0, 1, &mn, &mx);
+        mn0[0] = mn;
+        segment_affine(mn, mx, &sc0[0], inv);
+        rec->n_seg = 1;
+        rec->start[0] = 0;
+    }
+    const int32_t s = rec->n_seg - 1;
+    for (int d = 0; d < OR_D; ++d) dst[d] = oracle_encode(bf16_to_float(x[d]), mn0[s], *inv);
+    rec->seq_len = L + 1;
+    for (int32_t i = rec->n_seg; i < OR_MAX_SEG; ++i) rec->start[i] = L + 1;
+}
+
+int32_t oracle_append_split(const uint16_t *k_new, const uint16_t *v_new, int32_t B, int32_t Hkv, int32_t bs,
+                            const int32_t *block_tables, int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool,
+                            oracle_seg *k_table, oracle_seg *v_table)
+{
+    int32_t skipped = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        for (int32_t h = 0; h < Hkv; ++h) {
+            oracle_seg *kr = &k_table[(int64_t)b * Hkv + h], *vr = &v_table[(int64_t)b * Hkv + h];
+            const int32_t L = kr->seq_len;
+            if (L / bs >= max_blocks) {
+                ++skipped;
+                continue;
+            }
+            const int64_t blk = block_tables[(int64_t)b * max_blocks + L / bs];
+            const int64_t dst = ((blk * Hkv + h) * bs + L % bs) * OR_D;
+            append_tensor(k_new + ((int64_t)b * Hkv + h) * OR_D, kr, 0, L, k_pool + dst);
+            append_tensor(v_new + ((int64_t)b * Hkv + h) * OR_D, vr, 1, L, v_pool + dst);
+        }
+    }
+    return skipped;
+}
+
 /* Dequantised value of one code, in fp64: min + q * scale. */
 static double dequant(uint8_t q, float mn, float scale)
 {

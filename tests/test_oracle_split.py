@@ -1,7 +1,8 @@
 """Pins for the oracle's independent V segmentation (a group-selection variant: V segmented by
 the same rule on its own variance).  Checks: identical K and V reduce to the shared path; the
 two tensors' roles swap with the inputs; planted variance steps in K and in V land as each
-tensor's own boundaries; each V segment's extremes encode to 0 and 255.  CPU only."""
+tensor's own boundaries; each V segment's extremes encode to 0 and 255; appending through split
+tables that carry the shared segmentation equals the shared append.  CPU only."""
 import numpy as np
 
 import oracle
@@ -102,3 +103,34 @@ def test_v_segment_extremes_encode_to_0_and_255():
         assert np.float32(x[seg].min()) == rec["v_min"][s]
         assert codes[seg][x[seg] == x[seg].min()].max() == 0
         assert codes[seg][x[seg] == x[seg].max()].min() == 255
+
+
+def test_split_append_equals_shared_append_on_shared_segments():
+    """Split tables that carry the shared segmentation (K's fields in one, V's in the other):
+    appending through them gives the shared append's codes and the same fields."""
+    lens, hkv, bs = [37, 300, 0, 2100], 2, 16
+    k, v = layer(lens, hkv, 5)
+    cu, bt, nb = paging(lens, bs)
+    bt = np.concatenate([bt, np.full((len(lens), 2), -1, dtype=np.int32)], axis=1)
+    for b, L in enumerate(lens):  # one more block per request for the appended tokens
+        n = (L + bs - 1) // bs
+        bt[b, n] = nb + b
+    nb += len(lens)
+    kp, vp, table = oracle.compress(k, v, cu, hkv, bs, bt, nb)
+    kt, vt = table.copy(), table.copy()
+    for f in ("v_min", "v_scale", "v_inv_last"):
+        kt[f] = 0
+    for f in ("k_min", "k_scale", "k_inv_last"):
+        vt[f] = 0
+    rng = np.random.default_rng(6)
+    skp, svp = kp.copy(), vp.copy()
+    for step in range(3):
+        kn = bf16_bits(rng.standard_normal((len(lens), hkv, D)).astype(np.float32) * 0.3)
+        vn = bf16_bits(rng.standard_normal((len(lens), hkv, D)).astype(np.float32) * 0.3)
+        assert oracle.append(kn, vn, bs, bt, kp, vp, table) == 0
+        assert oracle.append_split(kn, vn, bs, bt, skp, svp, kt, vt) == 0
+    assert np.array_equal(skp, kp) and np.array_equal(svp, vp)
+    for f in ("n_seg", "seq_len", "start", "k_min", "k_scale", "k_inv_last"):
+        assert np.array_equal(kt[f], table[f]), f
+    for f in ("n_seg", "seq_len", "start", "v_min", "v_scale", "v_inv_last"):
+        assert np.array_equal(vt[f], table[f]), f

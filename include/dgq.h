@@ -190,7 +190,7 @@ dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, in
  * variance and encoded with its own segments.  Statistics taken with DGQ_PREFILL_V_VARIANCE and
  * a non-NULL v_seg_table in dgq_prefill_finish select it: seg_table then receives K's records
  * (V fields 0) and v_seg_table V's (start, n_seg, v_min, v_scale, v_inv_last; K fields 0); decode
- * with dgq_paged_decode_attn_split.  dgq_append does not support it.
+ * with dgq_paged_decode_attn_split; append the decode steps' tokens with dgq_append_split.
  * workspace        >= dgq_prefill_workspace_size(batch, Hkv) bytes, zero-filled before first use.
  * The bf16 source (k_src, v_src, src block tables) is as for dgq_compress_paged.
  */
@@ -340,6 +340,17 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
                       dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 size_t dgq_append_workspace_size(void);
+
+/* dgq_append for a cache with independent V segmentation (dgq_prefill_finish with a v_seg_table):
+ * K's codes from k_seg_table's last K segment, V's from v_seg_table's last V segment, each record
+ * updated for its own tensor (a record with n_seg == 0 gets a segment made of the new token's
+ * values of that tensor).  Both records of a pair must hold the same seq_len; a pair whose two
+ * records disagree is left untouched and flagged in the workspace.  Arguments as dgq_append. */
+dgq_status dgq_append_split(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                            int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                            dgq_seg_record *k_seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream);
 
 /* ---------------------------------------------------------------------------------------
  * Comparison encodings: the same paged cache layout and the same decode kernel, with the

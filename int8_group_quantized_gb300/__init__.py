@@ -29,7 +29,7 @@ __all__ = [
     "dgq_append_workspace_size",
     "dgq_paged_decode_attn", "dgq_encode_format", "dgq_encode_format_workspace_size",
     "dgq_paged_decode_attn_format", "FORMATS", "dgq_prefill_workspace_size", "dgq_prefill_chunk_stats",
-    "dgq_prefill_finish", "dgq_paged_decode_attn_split",
+    "dgq_prefill_finish", "dgq_paged_decode_attn_split", "dgq_append_split",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.dgq_paged_decode_attn_split.restype = ctypes.c_int
         L.dgq_prefill_finish.restype = ctypes.c_int
         L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
+        L.dgq_append_split.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P, sz, P]
+        L.dgq_append_split.restype = ctypes.c_int
         L.dgq_append.restype = ctypes.c_int
         L.dgq_append_workspace_size.argtypes = []
         L.dgq_append_workspace_size.restype = sz
@@ -210,6 +212,16 @@ def dgq_append(k_new, v_new, block_size, block_tables, k_pool, v_pool, seg_table
     _check(lib().dgq_append(_ptr(k_new), _ptr(v_new), B, Hkv, D, int(block_size), _ptr(block_tables),
                             block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table),
                             _ptr(workspace), _nbytes(workspace), _stream(stream)), "dgq_append")
+
+
+def dgq_append_split(k_new, v_new, block_size, block_tables, k_pool, v_pool, k_seg_table, v_seg_table, workspace,
+                     stream=None) -> None:
+    """dgq_append for a cache with independent V segmentation (K's and V's record tables)."""
+    B, Hkv, D = k_new.shape
+    _check(lib().dgq_append_split(_ptr(k_new), _ptr(v_new), B, Hkv, D, int(block_size), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                  _ptr(k_seg_table), _ptr(v_seg_table), _ptr(workspace), _nbytes(workspace),
+                                  _stream(stream)), "dgq_append_split")
 
 
 def dgq_compress_paged(k_src, v_src, src_block_tables, cu_seqlens, max_seqlen, block_size, block_tables, k_pool,

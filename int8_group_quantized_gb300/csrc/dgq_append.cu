@@ -35,6 +35,7 @@ struct AppendArgs {
     uint8_t *kpool;
     uint8_t *vpool;
     uint32_t *table;     // records as words
+    uint32_t *vtable;    // independent V segmentation: V's records (null otherwise)
     WsHeader *hdr;
     int32_t pairs, Hkv, bs, max_blocks, num_blocks;
 };
@@ -143,9 +144,79 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_kernel(AppendA
     rec[lane] = nw;
 }
 
+// One tensor's new row (four values per lane) into slot `dst` with its own record, of which this
+// lane holds word w; returns the lane's updated record word.  As append_kernel, for the fields of
+// one tensor (K: k_min / k_scale / k_inv_last; V: the V fields).
+__device__ __forceinline__ uint32_t append_one(const float (&x)[4], uint32_t w, bool is_v, uint8_t *pool,
+                                               int64_t dst, int32_t L)
+{
+    const int lane = threadIdx.x & 31;
+    const int wmin = is_v ? kWVMin : kWKMin, wscale = is_v ? kWVScale : kWKScale, winv = is_v ? kWVInv : kWKInv;
+    const int32_t n_seg = (int32_t)__shfl_sync(0xffffffffu, w, kWN);
+    float mn, inv, scale = 0.0f, mx;
+    if (n_seg == 0) {  // the first token: a segment of its own
+        row_min_max(x, mn, mx);
+        affine(mn, mx, scale, inv);
+    } else {
+        mn = __uint_as_float(__shfl_sync(0xffffffffu, w, wmin + n_seg - 1));
+        inv = __uint_as_float(__shfl_sync(0xffffffffu, w, winv));
+    }
+    *reinterpret_cast<uint32_t *>(pool + dst) = encode4(x, mn, inv);
+    const int32_t n_new = n_seg == 0 ? 1 : n_seg;
+    uint32_t nw = w;
+    if (lane == kWN) nw = (uint32_t)n_new;
+    if (lane == kWLen) nw = (uint32_t)(L + 1);
+    if (lane >= kWStart && lane < kWStart + kMaxSeg) {
+        const int i = lane - kWStart;
+        if (i >= n_new) nw = (uint32_t)(L + 1);
+        else if (n_seg == 0) nw = 0u;  // start[0]
+    }
+    if (n_seg == 0) {
+        if (lane == wmin) nw = __float_as_uint(mn);
+        if (lane == wscale) nw = __float_as_uint(scale);
+        if (lane == winv) nw = __float_as_uint(inv);
+    }
+    return nw;
+}
+
+// Append with independent V segmentation: K's and V's codes each from their own record.
+__global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_split_kernel(AppendArgs a)
+{
+    pdl_wait_primary();  // records and pools as the previous kernel in the stream left them
+    const int lane = threadIdx.x & 31;
+    const int32_t pair = blockIdx.x * kAppendPairsPerCta + (threadIdx.x >> 5);
+    if (pair >= a.pairs) return;
+    const int32_t b = pair / a.Hkv, h = pair - b * a.Hkv;
+    uint32_t *krec = a.table + (int64_t)pair * 32, *vrec = a.vtable + (int64_t)pair * 32;
+    const uint32_t wk = krec[lane], wv = vrec[lane];
+    const int32_t L = (int32_t)__shfl_sync(0xffffffffu, wk, kWLen);
+    if (L != (int32_t)__shfl_sync(0xffffffffu, wv, kWLen)) {  // the two records disagree: untouched
+        if (lane == 0) record_error(a.hdr, kErrBadLength);
+        return;
+    }
+    if (L < 0 || L / a.bs >= a.max_blocks) {  // the block table has no column for slot L
+        if (lane == 0) record_error(a.hdr, kErrNoBlock);
+        return;
+    }
+    const int32_t blk = __ldg(a.bt + (int64_t)b * a.max_blocks + L / a.bs);
+    if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged, untouched
+        if (lane == 0) record_error(a.hdr, kErrBadBlock);
+        return;
+    }
+    const uint2 kw = __ldg(a.k_new + (int64_t)pair * 32 + lane);
+    const uint2 vw = __ldg(a.v_new + (int64_t)pair * 32 + lane);
+    const float kx[4] = {bf_lo_f(kw.x), bf_hi_f(kw.x), bf_lo_f(kw.y), bf_hi_f(kw.y)};
+    const float vx[4] = {bf_lo_f(vw.x), bf_hi_f(vw.x), bf_lo_f(vw.y), bf_hi_f(vw.y)};
+    const int64_t dst = (((int64_t)blk * a.Hkv + h) * a.bs + L % a.bs) * kD + lane * 4;
+    const uint32_t nk = append_one(kx, wk, false, a.kpool, dst, L);
+    const uint32_t nv = append_one(vx, wv, true, a.vpool, dst, L);
+    krec[lane] = nk;
+    vrec[lane] = nv;
+}
+
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
                           const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
-                          dgq_seg_record *table, void *ws, cudaStream_t stream)
+                          dgq_seg_record *table, dgq_seg_record *vtable, void *ws, cudaStream_t stream)
 {
     AppendArgs a;
     a.k_new = static_cast<const uint2 *>(k_new);
@@ -154,6 +225,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32
     a.kpool = kpool;
     a.vpool = vpool;
     a.table = reinterpret_cast<uint32_t *>(table);
+    a.vtable = reinterpret_cast<uint32_t *>(vtable);
     a.hdr = static_cast<WsHeader *>(ws);
     a.pairs = B * Hkv;
     a.Hkv = Hkv;
@@ -169,7 +241,7 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, append_kernel, a);
+    return vtable ? cudaLaunchKernelEx(&cfg, append_split_kernel, a) : cudaLaunchKernelEx(&cfg, append_kernel, a);
 }
 
 }  // namespace dgq

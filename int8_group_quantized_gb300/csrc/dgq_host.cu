@@ -167,10 +167,42 @@ dgq_status dgq_compress_paged(const void *k_src_bf16, const void *v_src_bf16, in
 
 size_t dgq_append_workspace_size(void) { return 256; }  // the workspace header alone
 
+namespace {
+dgq_status append_impl(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                       int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                       size_t workspace_bytes, void *cuda_stream);
+}  // namespace
+
 dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
                       int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
                       dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    return append_impl(k_new_bf16, v_new_bf16, batch, num_kv_heads, head_dim, block_size, block_tables_dev,
+                       max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, nullptr, workspace,
+                       workspace_bytes, cuda_stream);
+}
+
+dgq_status dgq_append_split(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                            int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                            dgq_seg_record *k_seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream)
+{
+    if (!v_seg_table || !aligned16(v_seg_table)) return DGQ_ERR_INVALID_ARG;
+    return append_impl(k_new_bf16, v_new_bf16, batch, num_kv_heads, head_dim, block_size, block_tables_dev,
+                       max_blocks_per_seq, k_pool, v_pool, num_blocks, k_seg_table, v_seg_table, workspace,
+                       workspace_bytes, cuda_stream);
+}
+
+namespace {
+dgq_status append_impl(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                       int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                       size_t workspace_bytes, void *cuda_stream)
 {
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
     if (batch <= 0 || batch > kMaxBatch || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -185,9 +217,11 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
         return DGQ_ERR_WORKSPACE;
     const cudaError_t e = dgq::launch_append(k_new_bf16, v_new_bf16, batch, num_kv_heads, block_size,
                                              block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
-                                             seg_table, workspace, static_cast<cudaStream_t>(cuda_stream));
+                                             seg_table, v_seg_table, workspace,
+                                             static_cast<cudaStream_t>(cuda_stream));
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
+}  // namespace
 
 size_t dgq_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seqlen)
 {

@@ -65,7 +65,7 @@ cudaError_t launch_format_encode(int32_t format, const void *k, const void *v, i
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
                           const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
-                          dgq_seg_record *table, void *ws, cudaStream_t stream);
+                          dgq_seg_record *table, dgq_seg_record *vtable, void *ws, cudaStream_t stream);
 
 // Compression in two phases for chunked prefill: window statistics of each request's chunk
 // [begin, end) from a bf16 paged cache, then segmentation and codes for whole requests.

@@ -120,6 +120,12 @@ def test_append_rejects_bad_arguments_before_launch(L):
     assert _append(L, max_blocks=0) == INVALID
     assert _append(L, ws=0) == WORKSPACE
     assert _append(L, wsb=255) == WORKSPACE
+    # the split variant needs V's record table
+    args = (FAKE, FAKE, 2, 2, 128, 16, FAKE, 19, FAKE, FAKE, 32, FAKE)
+    assert L.dgq_append_split(*args, 0, FAKE, 256, 0) == INVALID
+    assert L.dgq_append_split(*args, FAKE + 4, FAKE, 256, 0) == INVALID
+    assert L.dgq_append_split(FAKE, FAKE, 2, 2, 64, 16, FAKE, 19, FAKE, FAKE, 32, FAKE, FAKE, FAKE, 256,
+                              0) == UNSUPPORTED
 
 
 def _encode(L, **kw):

@@ -159,3 +159,47 @@ def test_v_variance_statistics_leave_the_shared_path_unchanged():
     torch.cuda.synchronize()
     assert dgq.dgq_workspace_error(ws) == 0
     assert_compress_equal(case, kp, vp, table, g_kp.cpu().numpy(), g_vp.cpu().numpy(), table_to_numpy(g_t))
+
+
+def test_split_append_matches_oracle_and_decodes():
+    """Three decode steps appended through both record tables (one empty request among them), then
+    the split decode over L + 3 tokens: pools and records bit-exact, attention within tolerance."""
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    case = Case([37, 300, 0, 2100, 129], hq=4, hkv=2, bs=16, seed=145, extra_blocks=8)
+    restructure_v(case, seed=145)
+    kp, vp, kt, vt = oracle.compress_split(case.k, case.v, case.cu, case.hkv, case.bs, case.bt, case.num_blocks)
+    run_split(case, schedule_uniform(case.lens, 512), src_seed=11)
+    # room for three more tokens per request: one of the unused blocks where a new block starts
+    bt = np.concatenate([case.bt, np.zeros((case.B, 1), dtype=np.int32)], axis=1)
+    used = {int(case.bt[b, i]) for b, L in enumerate(case.lens) for i in range((int(L) + case.bs - 1) // case.bs)}
+    free = iter(sorted(set(range(case.num_blocks)) - used))
+    for b, L in enumerate(case.lens):
+        for t in range(int(L), int(L) + 3):
+            if t % case.bs == 0:
+                bt[b, t // case.bs] = next(free)
+    case.bt = bt
+    dev = torch.device("cuda:0")
+    case.d_bt = torch.from_numpy(bt).to(dev)
+    ws = torch.zeros(dgq.dgq_append_workspace_size(), dtype=torch.uint8, device=dev)
+    rng = np.random.default_rng(146)
+    for step in range(3):
+        kn = bf16_bits_np(rng.standard_normal((case.B, case.hkv, D)).astype(np.float32) * 0.3)
+        vn = bf16_bits_np(rng.standard_normal((case.B, case.hkv, D)).astype(np.float32) * 0.3)
+        assert oracle.append_split(kn, vn, case.bs, bt, kp, vp, kt, vt) == 0
+        d_kn = torch.from_numpy(kn.view(np.int16)).to(dev).view(torch.bfloat16)
+        d_vn = torch.from_numpy(vn.view(np.int16)).to(dev).view(torch.bfloat16)
+        dgq.dgq_append_split(d_kn, d_vn, case.bs, case.d_bt, case.d_kp, case.d_vp, case.d_kt, case.d_vt, ws)
+    torch.cuda.synchronize()
+    assert dgq.dgq_workspace_error(ws) == 0
+    case.lens = case.lens + 3
+    case.d_lens = torch.from_numpy(case.lens).to(dev)
+    case.max_seqlen = int(case.lens.max())
+    assert_split_equal(case, (kp, vp, kt, vt), (case.d_kp.cpu().numpy(), case.d_vp.cpu().numpy(),
+                                                table_to_numpy(case.d_kt), table_to_numpy(case.d_vt)))
+    assert_attn_close(oracle_split_attn(case, kp, vp, kt, vt), gpu_split_attn(case))
+
+
+def bf16_bits_np(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)

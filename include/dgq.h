@@ -31,6 +31,11 @@
  *     failures (a wait that timed out) are recorded in the workspace and read with
  *     dgq_workspace_error.
  *   - bf16 values are IEEE bfloat16 bit patterns; fp32 is IEEE binary32.
+ *   - Host threads: the launchers keep the launch shape of each kernel (occupancy, shared-memory
+ *     limit) for the device they last ran on, in unsynchronised statics.  Calls from one host
+ *     thread at a time are safe on any number of devices; a process that calls from several
+ *     threads at once must serialise its calls (or keep every thread on one device after one
+ *     call has configured it).
  */
 #ifndef DGQ_H
 #define DGQ_H

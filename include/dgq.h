@@ -34,8 +34,7 @@
  *   - Host threads: the launchers keep the launch shape of each kernel (occupancy, shared-memory
  *     limit) for the device they last ran on, in unsynchronised statics.  Calls from one host
  *     thread at a time are safe on any number of devices; a process that calls from several
- *     threads at once must serialise its calls (or keep every thread on one device after one
- *     call has configured it).
+ *     threads at once must serialise its calls.
  */
 #ifndef DGQ_H
 #define DGQ_H

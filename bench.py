@@ -234,6 +234,9 @@ def host_cpu():
     except OSError:
         pass
     import platform
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+                 "0xd49": "Arm Neoverse N2"}  # /proc/cpuinfo "CPU part" of Arm server cores
+    model = arm_parts.get(model.lower(), model)
     return {"model": model or platform.processor() or "unknown", "arch": platform.machine(),
             "nproc": os.cpu_count()}
 

@@ -318,6 +318,11 @@ def run_ours(args):
     d_bt = torch.from_numpy(bt).to(dev)
     d_lens = torch.from_numpy(lens).to(dev)
     layers = []
+    # every layer's step inputs (q, k_new, v_new) and outputs in one buffer each, so that the
+    # end-to-end step moves them with one host-to-device and one device-to-host copy
+    n_q, n_kv = B * Hq * D, B * Hkv * D
+    step_in = torch.empty(nl * (n_q + 2 * n_kv), dtype=torch.bfloat16, device=dev)
+    step_out = torch.empty(nl * n_q, dtype=torch.bfloat16, device=dev)
     for l in range(nl):
         n, st, sg = synth.span_tables(w.seed, l, lens, Hkv, w.rule)
         tabs = tuple(torch.from_numpy(x).to(dev) for x in (n, st, sg))
@@ -325,9 +330,10 @@ def run_ours(args):
         v = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
         synth.dev_fill_layer(w.seed, synth.STREAM_K, l, d_cu, Hkv, tabs, T, k, sp)
         synth.dev_fill_layer(w.seed, synth.STREAM_V, l, d_cu, Hkv, tabs, T, v, sp)
-        q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-        kn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
-        vn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+        base = l * (n_q + 2 * n_kv)
+        q = step_in[base:base + n_q].view(B, Hq, D)
+        kn = step_in[base + n_q:base + n_q + n_kv].view(B, Hkv, D)
+        vn = step_in[base + n_q + n_kv:base + n_q + 2 * n_kv].view(B, Hkv, D)
         synth.dev_fill_heads(w.seed, synth.STREAM_Q, l, B, Hq, 1.0, q, sp)
         synth.dev_fill_heads(w.seed, synth.STREAM_KNEW, l, B, Hkv, 0.15, kn, sp)
         synth.dev_fill_heads(w.seed, synth.STREAM_VNEW, l, B, Hkv, 0.15, vn, sp)
@@ -336,7 +342,7 @@ def run_ours(args):
             kp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
             vp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
             table=torch.zeros((B, Hkv, REC), dtype=torch.uint8, device=dev),
-            out=torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)))
+            out=step_out[l * n_q:(l + 1) * n_q].view(B, Hq, D)))
     if args.paged_input:  # the same tokens in a bf16 paged cache laid out like the INT8 pools
         tok_blk = torch.from_numpy(np.concatenate(
             [bt[b, np.arange(int(L)) // bs] for b, L in enumerate(lens)]).astype(np.int64)).to(dev)
@@ -419,26 +425,18 @@ def run_ours(args):
     dec_b_step, comp_b_step = dec_b * nl, comp_b * nl
 
     # ---- end-to-end through the public API: per step the step's decode inputs (q, k_new, v_new
-    # of every layer) come from pinned host memory and the outputs go back to pinned host memory.
-    hq_in = [torch.empty_like(L["q"], device="cpu").pin_memory() for L in layers]
-    hk_in = [torch.empty_like(L["kn"], device="cpu").pin_memory() for L in layers]
-    hv_in = [torch.empty_like(L["vn"], device="cpu").pin_memory() for L in layers]
-    h_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
-    for i, L in enumerate(layers):
-        hq_in[i].copy_(L["q"])
-        hk_in[i].copy_(L["kn"])
-        hv_in[i].copy_(L["vn"])
-    h2d = sum(t.numel() * t.element_size() for t in hq_in + hk_in + hv_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # of every layer) come from pinned host memory in one copy and the outputs go back to pinned
+    # host memory in one copy.
+    h_in = torch.empty(step_in.shape, dtype=step_in.dtype, device="cpu").pin_memory()
+    h_out = torch.empty(step_out.shape, dtype=step_out.dtype, device="cpu").pin_memory()
+    h_in.copy_(step_in)
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        for i, L in enumerate(layers):
-            L["q"].copy_(hq_in[i], non_blocking=True)
-            L["kn"].copy_(hk_in[i], non_blocking=True)
-            L["vn"].copy_(hv_in[i], non_blocking=True)
+        step_in.copy_(h_in, non_blocking=True)
         decode_all()
-        for i, L in enumerate(layers):
-            h_out[i].copy_(L["out"], non_blocking=True)
+        h_out.copy_(step_out, non_blocking=True)
         append_all()
 
     for _ in range(max(3, args.warmup)):
@@ -518,8 +516,9 @@ def run_ours(args):
             "kernels": kernels,
             "e2e": {"value": round(world * dec_b_step / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "what": "decode step via the C ABI: host->device copy of q/k_new/v_new, 32-layer decode, "
-                            "device->host copy of the outputs, the step's token appended to every layer's cache"},
+                    "what": "decode step via the C ABI: one host->device copy of every layer's q/k_new/v_new, "
+                            "the decode of every layer, one device->host copy of the outputs, the step's token "
+                            "appended to every layer's cache"},
             "segments": {"n_seg_histogram": seg_hist, "over": "(request, KV head) pairs of layer 0"},
             "fidelity": fidelity,
             "prefill_two_phase": prefill,

@@ -838,6 +838,82 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
     if (!waited) pdl_wait_primary();
 }
 
+// The same merge with one warp per (pair, query head) item, for calls whose pairs are split over
+// few CTAs: the warp folds the pieces in CTA order (kCombineSlots in flight), adds the current
+// token and writes its four columns per lane; no shared memory and no block barrier.
+__global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine_warp_kernel(AttnArgs a)
+{
+    const int32_t G = a.G, Hkv = a.Hkv;
+    const int32_t items = a.B * Hkv * G;
+    const int lane = threadIdx.x & 31;
+    const int32_t nw = gridDim.x * kCombineWarps;
+    bool waited = false;
+    for (int32_t item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5); item < items; item += nw) {
+        const int32_t p = item / G, g = item - p * G;
+        const int32_t b = p / Hkv, h = p - b * Hkv;
+        // inputs of this call (not written by the main kernel): loaded before the wait
+        const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * a.Hq + h * G + g) * kD) + lane);
+        const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(a.knew + ((int64_t)b * Hkv + h) * kD) + lane);
+        const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(a.vnew + ((int64_t)b * Hkv + h) * kD) + lane);
+        if (!waited) {
+            pdl_wait_primary();
+            waited = true;
+        }
+        const int2 info = __ldcg(a.pair_info + p);
+        const int32_t cfirst = info.x, clast = info.y;
+        if (cfirst == clast) continue;  // finished inside the main kernel
+        const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
+        const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
+        const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
+        float M = -INFINITY, L = 0.0f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t base = cfirst; base <= clast; base += kCombineSlots) {
+            float mm[kCombineSlots], ll[kCombineSlots];
+            float4 oo[kCombineSlots];
+#pragma unroll
+            for (int i = 0; i < kCombineSlots; ++i) {
+                const int32_t cc = base + i;
+                mm[i] = -INFINITY;
+                ll[i] = 0.0f;
+                oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
+                    const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
+                    mm[i] = ml.x;
+                    ll[i] = ml.y;
+                    oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kCombineSlots; ++i) {  // in CTA order: online fold
+                const float Mn = fmaxf(M, mm[i]);
+                if (Mn == -INFINITY) continue;
+                const float fo = M == -INFINITY ? 0.0f : ex2(M - Mn);
+                const float fn = mm[i] == -INFINITY ? 0.0f : ex2(mm[i] - Mn);
+                L = L * fo + ll[i] * fn;
+                O.x = O.x * fo + oo[i].x * fn;
+                O.y = O.y * fo + oo[i].y * fn;
+                O.z = O.z * fo + oo[i].z * fn;
+                O.w = O.w * fo + oo[i].w * fn;
+                M = Mn;
+            }
+        }
+        // the current token's score, then this lane's columns 4 lane .. 4 lane + 3
+        float acc = bf16lo_to_f32(qv.x) * bf16lo_to_f32(kv.x);
+        acc = fmaf(bf16hi_to_f32(qv.x), bf16hi_to_f32(kv.x), acc);
+        acc = fmaf(bf16lo_to_f32(qv.y), bf16lo_to_f32(kv.y), acc);
+        acc = fmaf(bf16hi_to_f32(qv.y), bf16hi_to_f32(kv.y), acc);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const float sn = acc * kLog2eOverSqrtD;
+        uint2 res;
+        res.x = pack_bf16x2(finish(M, L, O.x, sn, bf16lo_to_f32(vv.x)), finish(M, L, O.y, sn, bf16hi_to_f32(vv.x)));
+        res.y = pack_bf16x2(finish(M, L, O.z, sn, bf16lo_to_f32(vv.y)), finish(M, L, O.w, sn, bf16hi_to_f32(vv.y)));
+        reinterpret_cast<uint2 *>(a.out + ((int64_t)b * a.Hq + h * G + g) * kD)[lane] = res;
+    }
+    if (!waited) pdl_wait_primary();
+}
+
 }  // namespace dgq
 
 // ---- host launcher ---------------------------------------------------------------------------
@@ -944,7 +1020,12 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
     // merge of shared pairs, chained with programmatic dependent launch
     cudaLaunchConfig_t cfg = {};
     const int64_t items = (int64_t)B * Hkv * G;
-    const int64_t cgrid = items < (int64_t)nsm * kCombineCtasPerSm ? items : (int64_t)nsm * kCombineCtasPerSm;
+    // pairs split over few CTAs (at least one pair per two CTAs): one warp per item; otherwise
+    // the four warps of a CTA share an item's pieces
+    const bool warp_merge = (int64_t)B * Hkv * 2 >= grid;
+    const int64_t per_cta = warp_merge ? kCombineWarps : 1;
+    const int64_t cneed = (items + per_cta - 1) / per_cta;
+    const int64_t cgrid = cneed < (int64_t)nsm * kCombineCtasPerSm ? cneed : (int64_t)nsm * kCombineCtasPerSm;
     cfg.gridDim = dim3((unsigned)cgrid);
     cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.dynamicSmemBytes = 0;
@@ -954,7 +1035,7 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+    return warp_merge ? cudaLaunchKernelEx(&cfg, combine_warp_kernel, a) : cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace dgq

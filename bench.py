@@ -276,7 +276,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * (tot_d + tot_c) / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": "4 requests x 1 layer per step"},
+        "config": {"workload": w.name, "sample": f"{min(4, len(lens))} requests x 1 layer per step"},
         "compress_gbs": round(bc / tot_c / 1e9, 4),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
                          "host": host_cpu()},

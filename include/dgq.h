@@ -114,7 +114,13 @@ typedef struct dgq_seg_record {
  * seg_table        [batch, Hkv] dgq_seg_record, device, written in full.
  * workspace        >= dgq_compress_workspace_size(batch, max_seqlen, num_kv_heads) bytes.
  * Inputs must be finite; requests may be empty (L = 0 writes a record with n_seg = 0).
- * The call launches one cooperative kernel; the whole GPU takes part in it.
+ * Finite values large enough to overflow the fp32 variance (|x| beyond about 2^62) give a
+ * window mean of +inf; the jump between two such adjacent windows is undefined (inf - inf) and
+ * is no boundary candidate, and a pair left with fewer candidates gets fewer segments.
+ * Kernel: when every request is at most 4096 tokens long, a non-cooperative kernel of
+ * thread-block clusters that each segment whole (request, head) pairs; otherwise one
+ * cooperative kernel with one block per SM, in which the whole GPU takes part (the call then
+ * needs the GPU to itself for its duration, as any cooperative launch).
  */
 dgq_status dgq_compress(const void *k_bf16, const void *v_bf16, int32_t total_tokens,
                         const int32_t *cu_seqlens_dev, int32_t batch, int32_t max_seqlen, int32_t num_kv_heads,

@@ -166,6 +166,11 @@ int32_t oracle_boundaries_ex(const float *means, int32_t W, int32_t L, int32_t m
             if (taken) continue;
             if (!(means[w] >= min_var || means[w + 1] >= min_var)) continue; /* both quiet */
             float jump = fabsf(means[w + 1] - means[w]);
+            /* READING: two adjacent windows whose fp32 variance overflowed (both means +inf)
+             * have no defined jump (inf - inf is NaN); such a pair of windows is no candidate,
+             * like two quiet windows, and a pair left with fewer candidates gets fewer segments.
+             * An overflowed window next to a finite one gives an infinite jump, which is one. */
+            if (jump != jump) continue;
             if (best < 0 || jump > best_jump) { /* strict: earlier window wins ties */
                 best = w;
                 best_jump = jump;

@@ -152,6 +152,76 @@ def test_boundaries_brute_force_tiny():
             assert got == _brute_force_starts(means, L_eff), (means, L_eff)
 
 
+_HUGE = Fraction(2) ** 200  # exceeds any sum of finite fp32 jumps (each < 2^129)
+
+
+def _brute_force_starts_nonfinite(means, L):
+    """Brute force for means that may be +inf: a jump between two infinite means (NaN) is no
+    candidate; an infinite jump outranks every finite total; the count is capped by the
+    candidates left.  Maximum total jump, then the lexicographically first subset."""
+    W = len(means)
+    k = min(oracle.ngroups(L), W) - 1
+    jumps = {}
+    for w in range(W - 1):
+        j = abs(np.float32(means[w + 1]) - np.float32(means[w]))
+        if not np.isnan(j):
+            jumps[w] = _HUGE if np.isinf(j) else Fraction(float(j))
+    k = min(k, len(jumps))
+    best = None
+    for subset in itertools.combinations(sorted(jumps), k):
+        key = (-sum(jumps[w] for w in subset), subset)
+        if best is None or key < best:
+            best = key
+    return [0] + [16 * (w + 1) for w in best[1]]
+
+
+def test_boundaries_skip_undefined_jumps():
+    # two adjacent overflowed windows: inf - inf has no value, so the cut goes to the infinite
+    # jump after them, not to the first (undefined) candidate
+    inf = np.float32(np.inf)
+    with np.errstate(invalid="ignore"):
+        assert oracle.boundaries(np.array([inf, inf, 1.0], np.float32), 40) == [0, 32]
+        # only undefined jumps: no candidate, one segment
+        assert oracle.boundaries(np.array([inf, inf], np.float32), 32) == [0]
+        # three segments wanted, two candidates (the jumps either side of an infinite run)
+        assert oracle.boundaries(np.array([1.0, inf, inf, inf, 2.0], np.float32), 3000) == [0, 16, 64]
+
+
+def test_boundaries_brute_force_with_overflowed_windows():
+    rng = np.random.default_rng(4)
+    with np.errstate(invalid="ignore"):
+        for trial in range(300):
+            W = int(rng.integers(1, 9))
+            L = 16 * (W - 1) + int(rng.integers(1, 17))
+            means = rng.integers(0, 3, W).astype(np.float32) if trial % 2 else rng.random(W).astype(np.float32)
+            means[rng.random(W) < 0.4] = np.inf
+            for L_eff in (L, L + 3000, L + 20000):
+                got = oracle.boundaries(means, L_eff)
+                assert got == _brute_force_starts_nonfinite(means, L_eff), (means, L_eff)
+
+
+def test_variance_overflow_closed_form():
+    # a row of +-a has mean 0 and variance a^2; for a = 2^60 every step is exact, for a = 2^63
+    # the squares (2^126) are finite but their fp32 sum (2^133) overflows, so the variance is +inf
+    row = np.where(np.arange(D) % 2 == 0, 1.0, -1.0).astype(np.float32)
+    assert oracle.token_variance(bf16_bits(row * np.float32(2.0 ** 60))) == np.float32(2.0 ** 120)
+    assert np.isposinf(oracle.token_variance(bf16_bits(row * np.float32(2.0 ** 63))))
+
+
+def test_overflowed_windows_cut_at_the_finite_edge():
+    # finite bf16 rows large enough to overflow the fp32 variance in windows 0..1, ordinary rows
+    # after: the only defined jump that is infinite is the one between windows 1 and 2
+    rng = np.random.default_rng(9)
+    L = 300
+    k = gauss_rows(rng, L, 0.1)
+    sign = np.where(rng.random((32, D)) < 0.5, -1.0, 1.0).astype(np.float32)
+    k[:32] = bf16_bits(sign * np.float32(2.0 ** 63))
+    rec, kc, _ = oracle.compress_pair(k, k)
+    assert rec["n_seg"] == 2 and list(rec["start"][:2]) == [0, 32]
+    # the overflowed segment holds two values: its codes are exactly 0 and 255
+    assert set(np.unique(kc[:32]).tolist()) == {0, 255}
+
+
 def test_single_window_is_one_segment():
     k = gauss_rows(np.random.default_rng(1), 16, 0.3)
     rec, _, _ = oracle.compress_pair(k, k)

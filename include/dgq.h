@@ -303,7 +303,12 @@ dgq_status dgq_paged_decode_attn_split(const void *q_bf16, const void *k_new_bf1
  *     each call clears the array's 256-byte header on the stream before it launches, so calls
  *     issued in order on one stream are safe, while calls that overlap on the GPU (several
  *     streams at once) race and give wrong results;
- *   - a device-side wait that timed out is not reported (there is no workspace to query).
+ *   - no device-side error is reported: a wait that timed out, a block id outside the pool or
+ *     a request longer than its block-table row is recorded in the array's header as in a
+ *     workspace, but the next call clears that header and no call reads it, so this entry
+ *     point returns DGQ_OK for them (the guarded accesses stay inside the caller's buffers as
+ *     with the regular entry point); a caller that needs those checks uses
+ *     dgq_paged_decode_attn with a workspace and dgq_workspace_error.
  */
 #define DGQ_NOALLOC_SCRATCH_BYTES (8u << 20)
 

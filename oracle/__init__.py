@@ -93,6 +93,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_paged_decode_attn.restype = None
         L.oracle_append.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P]
         L.oracle_append.restype = i32
+        L.oracle_resegment_flags.argtypes = [i32]
+        L.oracle_resegment_flags.restype = i32
+        L.oracle_append_resegment.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P, P, P, P, i32, i32,
+                                              ctypes.c_float, P]
+        L.oracle_append_resegment.restype = i32
         L.oracle_decode_attn_unquantised.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P]
         L.oracle_decode_attn_unquantised.restype = None
         for name in ("oracle_dequant_fixed64", "oracle_dequant_sym_int8", "oracle_dequant_fp8_e4m3"):
@@ -201,6 +206,36 @@ def append(k_new, v_new, block_size, block_tables, k_pool, v_pool, table):
     B, Hkv = k_new.shape[0], k_new.shape[1]
     return int(lib().oracle_append(_p(k_new), _p(v_new), B, Hkv, int(block_size), _p(bt), bt.shape[1],
                                    _p(k_pool), _p(v_pool), _p(table)))
+
+
+RESEG_WINDOW = 1   # the appended token completed a 16-token window
+RESEG_NGROUPS = 2  # the length crossed an n_groups threshold
+
+
+def resegment_flags(L: int) -> int:
+    """Trigger bits of appending token L (the cache grows from L to L + 1 tokens)."""
+    return int(lib().oracle_resegment_flags(int(L)))
+
+
+def append_resegment(k_new, v_new, block_size, block_tables, k_pool, v_pool, table, k_hist, v_hist, hist_cu,
+                     mask=RESEG_WINDOW | RESEG_NGROUPS, max_groups=MAX_SEG, min_var=0.0):
+    """append, then every request with a pair whose trigger bits meet `mask` compressed again from
+    its bf16 history (k_hist, v_hist packed [T, Hkv, 128] uint16 with its L + 1 tokens on rows
+    hist_cu[b] ..).  Pools and table in place.  Returns (flags [B, Hkv] int32, skipped)."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    kh = np.ascontiguousarray(k_hist, dtype=np.uint16)
+    vh = np.ascontiguousarray(v_hist, dtype=np.uint16)
+    cu = np.ascontiguousarray(hist_cu, dtype=np.int32)
+    for a in (k_pool, v_pool, table):
+        assert a.flags["C_CONTIGUOUS"]
+    B, Hkv = k_new.shape[0], k_new.shape[1]
+    flags = np.zeros((B, Hkv), dtype=np.int32)
+    skipped = lib().oracle_append_resegment(_p(k_new), _p(v_new), B, Hkv, int(block_size), _p(bt), bt.shape[1],
+                                            _p(k_pool), _p(v_pool), _p(table), _p(kh), _p(vh), _p(cu), int(mask),
+                                            int(max_groups), float(min_var), _p(flags))
+    return flags, int(skipped)
 
 
 def append_split(k_new, v_new, block_size, block_tables, k_pool, v_pool, k_table, v_table):

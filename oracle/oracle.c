@@ -46,6 +46,9 @@
  *   append         a first token alone: its min -> 0, max -> 255; in-range values give
  *                  the codes compress gives them when the segment keeps its min/max;
  *                  out-of-range values clamp to 0 / 255; flat segments give 0
+ *   re-segmentation trigger bits against the closed form of the length rule at every length
+ *                  edge; a re-segmented request equals a fresh compress of its grown history,
+ *                  the others equal the plain append; steps to 2048 and 16384 change the count
  */
 #include <math.h>
 #include <stdint.h>
@@ -534,6 +537,55 @@ int32_t oracle_append_split(const uint16_t *k_new, const uint16_t *v_new, int32_
             append_tensor(k_new + ((int64_t)b * Hkv + h) * OR_D, kr, 0, L, k_pool + dst);
             append_tensor(v_new + ((int64_t)b * Hkv + h) * OR_D, vr, 1, L, v_pool + dst);
         }
+    }
+    return skipped;
+}
+
+/* Re-segmentation triggers of a decode-step append, [DGQ] section 2.2 (the variance curve is
+ * analysed in real time as each new token is generated; segments come from jumps between
+ * 16-token window means) and section 3.2 (the segment count follows the length).  READING:
+ * appending token L -- the cache grows from L to L + 1 tokens -- completes a window when L + 1 is
+ * a multiple of 16 (a new window mean, hence a new candidate jump, exists: bit 1), and changes the
+ * segment count when n_groups(L + 1) != n_groups(L) (bit 2; by the rule this happens at
+ * L + 1 = 2048 and 16384, both also window ends).  A partial window adds no mean the segmentation
+ * of complete windows lacks, so no other length triggers. */
+int32_t oracle_resegment_flags(int32_t L)
+{
+    int32_t f = 0;
+    if ((L + 1) % OR_WIN == 0) f |= 1;
+    if (oracle_ngroups(L + 1) != oracle_ngroups(L)) f |= 2;
+    return f;
+}
+
+/* One decode step with re-segmentation: oracle_append of the step's token, then every request
+ * with a pair whose trigger bits (oracle_resegment_flags of its length before the append) meet
+ * `mask` is compressed again from its bf16 history -- oracle_compress_pair_ex over its L + 1
+ * tokens: new boundaries, new segment parameters, every code re-encoded and scattered through
+ * the block table.  READING: the INT8 cache cannot be re-segmented from its own codes (the
+ * segment extremes and the variance need the original values), so a re-segmentation redoes the
+ * method's compression of the whole request from the bf16 K/V a serving engine keeps (its bf16
+ * paged cache); [DGQ] section 2.2 gives no incremental form.
+ * k_hist, v_hist: packed [T, Hkv, 128] bf16, request b's L + 1 tokens on rows hist_cu[b] ..
+ * hist_cu[b + 1] - 1 (the last of them is the step's token).  flags_out [B, Hkv]: every pair's
+ * trigger bits.  Returns the pairs the append skipped for want of a block-table column. */
+int32_t oracle_append_resegment(const uint16_t *k_new, const uint16_t *v_new, int32_t B, int32_t Hkv, int32_t bs,
+                                const int32_t *block_tables, int32_t max_blocks, uint8_t *k_pool, uint8_t *v_pool,
+                                oracle_seg *table, const uint16_t *k_hist, const uint16_t *v_hist,
+                                const int32_t *hist_cu, int32_t mask, int32_t max_groups, float min_var,
+                                int32_t *flags_out)
+{
+    for (int64_t p = 0; p < (int64_t)B * Hkv; ++p) flags_out[p] = oracle_resegment_flags(table[p].seq_len);
+    const int32_t skipped = oracle_append(k_new, v_new, B, Hkv, bs, block_tables, max_blocks, k_pool, v_pool, table);
+    for (int32_t b = 0; b < B; ++b) {
+        int redo = 0;
+        for (int32_t h = 0; h < Hkv; ++h)
+            if (flags_out[(int64_t)b * Hkv + h] & mask) redo = 1;
+        if (!redo) continue;
+        /* the request's history, compressed as one request of its own */
+        const int32_t cu[2] = {0, hist_cu[b + 1] - hist_cu[b]};
+        const int64_t row0 = (int64_t)hist_cu[b] * Hkv * OR_D;
+        oracle_compress_ex(k_hist + row0, v_hist + row0, cu, 1, Hkv, bs, block_tables + (int64_t)b * max_blocks,
+                           max_blocks, max_groups, min_var, k_pool, v_pool, table + (int64_t)b * Hkv);
     }
     return skipped;
 }

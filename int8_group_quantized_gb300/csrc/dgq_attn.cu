@@ -558,8 +558,15 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                         ksc[n][1] = half2_bits(__uint_as_float(pw.w), __uint_as_float(pw.w));
                     }
                     const uint32_t hv = (uint32_t)(tr >> 2) * 8;
-                    const uint2 pa = ld_shared_v2(vpb + cq * 16 + hv), pb_ = ld_shared_v2(vpb + (cq + 4) * 16 + hv);
-                    const uint2 pc = ld_shared_v2(vpb + (cq + 8) * 16 + hv), pd = ld_shared_v2(vpb + (cq + 12) * 16 + hv);
+                    uint2 pa = ld_shared_v2(vpb + cq * 16 + hv), pb_ = ld_shared_v2(vpb + (cq + 4) * 16 + hv);
+                    uint2 pc = ld_shared_v2(vpb + (cq + 8) * 16 + hv), pd = ld_shared_v2(vpb + (cq + 12) * 16 + hv);
+                    if (valid < kTile) {  // slots past the end hold anything (NaN parameters too): their
+                        const uint2 z2 = make_uint2(0u, 0u);  // values become 0, so 0-weight rows add 0
+                        if (cq >= valid) pa = z2;
+                        if (cq + 4 >= valid) pb_ = z2;
+                        if (cq + 8 >= valid) pc = z2;
+                        if (cq + 12 >= valid) pd = z2;
+                    }
                     vmn_ab = half2_bits(__uint_as_float(pa.x), __uint_as_float(pb_.x));
                     vsc_ab = half2_bits(__uint_as_float(pa.y), __uint_as_float(pb_.y));
                     vmn_cd = half2_bits(__uint_as_float(pc.x), __uint_as_float(pd.x));
@@ -631,10 +638,21 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
                 if (!vflat) {
                     // rows cq, cq + 4, cq + 8, cq + 12, column tau(r)
                     const uint32_t vt = tile + kTileBytes;  // rows cq + 4i, column tau(r)
-                    const uint4 va = ld_shared_v4(vt + cq * kD + ((tr ^ cq) << 4));
-                    const uint4 vb = ld_shared_v4(vt + (cq + 4) * kD + ((tr ^ (cq + 4)) << 4));
-                    const uint4 vc = ld_shared_v4(vt + (cq + 8) * kD + ((tr ^ cq) << 4));
-                    const uint4 vd = ld_shared_v4(vt + (cq + 12) * kD + ((tr ^ (cq + 4)) << 4));
+                    uint4 va = ld_shared_v4(vt + cq * kD + ((tr ^ cq) << 4));
+                    uint4 vb = ld_shared_v4(vt + (cq + 4) * kD + ((tr ^ (cq + 4)) << 4));
+                    uint4 vc = ld_shared_v4(vt + (cq + 8) * kD + ((tr ^ cq) << 4));
+                    uint4 vd = ld_shared_v4(vt + (cq + 12) * kD + ((tr ^ (cq + 4)) << 4));
+                    if constexpr (Fmt == kDecFp8) {
+                        // slots past the end hold any byte, E4M3 NaN patterns too (0 * NaN would
+                        // reach the sums): their codes become +0
+                        if (valid < kTile) {
+                            const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+                            if (cq >= valid) va = z4;
+                            if (cq + 4 >= valid) vb = z4;
+                            if (cq + 8 >= valid) vc = z4;
+                            if (cq + 12 >= valid) vd = z4;
+                        }
+                    }
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
                         const uint32_t xab01 = prmt(word(va, wi), word(vb, wi), 0x5140);

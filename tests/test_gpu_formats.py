@@ -30,7 +30,7 @@ def e4m3_values() -> np.ndarray:
     return out
 
 
-def gpu_encode(case: Case, fmt: str):
+def gpu_encode(case: Case, fmt: str, fill=FILL, par_fill=-7.0):
     import torch
     import int8_group_quantized_gb300 as dgq
     dev = torch.device("cuda:0")
@@ -42,12 +42,12 @@ def gpu_encode(case: Case, fmt: str):
     case.d_bt = torch.from_numpy(case.bt).to(dev)
     case.d_lens = torch.from_numpy(case.lens).to(dev)
     shape = (case.num_blocks, case.hkv, case.bs, D)
-    case.d_kp = torch.full(shape, FILL, dtype=torch.uint8, device=dev)
-    case.d_vp = torch.full(shape, FILL, dtype=torch.uint8, device=dev)
+    case.d_kp = torch.full(shape, fill, dtype=torch.uint8, device=dev)
+    case.d_vp = torch.full(shape, fill, dtype=torch.uint8, device=dev)
     case.d_kpar = case.d_vpar = None
     if fmt == "fixed64":
-        case.d_kpar = torch.full((*shape[:3], 4), -7.0, dtype=torch.float32, device=dev)
-        case.d_vpar = torch.full((*shape[:3], 4), -7.0, dtype=torch.float32, device=dev)
+        case.d_kpar = torch.full((*shape[:3], 4), par_fill, dtype=torch.float32, device=dev)
+        case.d_vpar = torch.full((*shape[:3], 4), par_fill, dtype=torch.float32, device=dev)
     case.d_table = torch.full((case.B, case.hkv, 128), 0x5A, dtype=torch.uint8, device=dev)
     ws = torch.zeros(dgq.dgq_encode_format_workspace_size(case.B, case.hkv), dtype=torch.uint8, device=dev)
     dgq.dgq_encode_format(fmt, d_k, d_v, case.d_cu, case.max_seqlen, case.bs, case.d_bt, case.d_kp, case.d_vp,
@@ -177,3 +177,19 @@ def test_fp8_saturation_and_subnormals():
     case.k[0, 0, :16] = bits
     case.v[3, 0, 100:116] = bits
     check_encoding(case, "fp8_e4m3")
+
+
+@pytest.mark.parametrize("fmt", ["fixed64", "fp8_e4m3", "sym_int8"])
+@pytest.mark.parametrize("fill", [0x7F, 0xFF])
+def test_decode_ignores_whatever_lies_past_the_end(fmt, fill):
+    """Slots past each request's end are never written and may hold any bytes: E4M3 NaN patterns
+    (0x7F, 0xFF) in the codes and NaN in the fixed groups' parameters must not reach the output
+    (their softmax weight is 0, and 0 * NaN is NaN).  Ragged lengths leave partial tiles; G = 1 and
+    G = 4."""
+    for kw in (dict(lens=[37, 300, 1, 129, 250], hq=4, hkv=4, bs=16, seed=106),
+               dict(lens=[700, 65, 17, 3], hq=16, hkv=4, bs=64, seed=107)):
+        case = Case(**kw)
+        gpu_encode(case, fmt, fill=fill, par_fill=float("nan"))
+        got = gpu_attn_format(case, fmt)
+        assert np.isfinite(got).all()
+        assert_attn_close(oracle_attn_format(case, fmt), got)

@@ -236,6 +236,21 @@ dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, in
                               dgq_seg_record *v_seg_table, const dgq_compress_options *options, void *workspace,
                               size_t workspace_bytes, void *cuda_stream);
 
+/* dgq_prefill_finish restricted to the requests a re-segmentation selects: request b is segmented
+ * and encoded when (pair_flags[b][h] & flag_mask) != 0 for some head h (pair_flags [batch, Hkv]
+ * int32, device, e.g. as dgq_append_ex wrote them); the records, codes and window statistics of
+ * every other request are left untouched.  pair_flags == NULL selects every request
+ * (dgq_prefill_finish).  Other arguments as dgq_prefill_finish. */
+dgq_status dgq_prefill_finish_ex(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                                 const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                                 const int32_t *seq_lens_dev, int32_t batch, int32_t max_seqlen,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 const float *window_stats, int32_t max_windows, const int32_t *block_tables_dev,
+                                 int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                                 dgq_seg_record *seg_table, dgq_seg_record *v_seg_table,
+                                 const dgq_compress_options *options, const int32_t *pair_flags,
+                                 int32_t flag_mask, void *workspace, size_t workspace_bytes, void *cuda_stream);
+
 /* ---------------------------------------------------------------------------------------
  * dgq_paged_decode_attn -- one decode step of grouped-query attention over the INT8
  * paged cache plus the step's own (unquantised) key and value.
@@ -331,8 +346,8 @@ dgq_status dgq_paged_decode_attn_noalloc(const void *q_bf16, const void *k_new_b
  * inv), 0), 255) with inv = k_inv_last / v_inv_last of the record (the compress quantiser's
  * two IEEE steps; values outside the segment's range clamp, and the segment's min and scale,
  * hence every code already stored, stay as they are).  Boundaries are not revisited (that
- * needs the bf16 history); a caller that keeps it can re-run dgq_compress, e.g. when L
- * crosses an n_groups threshold (2048, 16384).  A record with n_seg == 0 gets a first
+ * needs the bf16 history): dgq_append_ex reports when a re-segmentation is due and
+ * dgq_prefill_finish_ex performs it from the caller's bf16 history.  A record with n_seg == 0 gets a first
  * segment made of the new token alone (its min/max over the 128 values, as in compress).
  * The record's seq_len and its start entries past the last segment become L + 1.
  *
@@ -355,6 +370,34 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
                       dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 size_t dgq_append_workspace_size(void);
+
+/* ---------------------------------------------------------------------------------------
+ * Re-segmentation after appends.  [DGQ] section 2.2 analyses the variance curve as each new
+ * token is generated (segments come from jumps between 16-token window means) and section 3.2
+ * ties the segment count to the length.  dgq_append keeps the boundaries; these two calls let a
+ * caller that keeps the bf16 history (its bf16 paged cache) re-run the segmentation when it
+ * changes:
+ *   DGQ_RESEG_WINDOW   appending token L completed a 16-token window ((L + 1) % 16 == 0): a new
+ *                      window mean, hence a new candidate jump, exists;
+ *   DGQ_RESEG_NGROUPS  the length reached a threshold of the n_groups rule (L + 1 = 2048 or
+ *                      16384; for every L >= 16384 the rule gives 5), so the segment count changes.
+ * A step with re-segmentation: dgq_append_ex (flags per pair); the step's bf16 K/V written into
+ * the bf16 paged history (the caller's own cache write); dgq_prefill_chunk_stats over the window
+ * each flagged request just completed ([L + 1 - 16, L + 1); an empty range for the others); then
+ * dgq_prefill_finish_ex with the flags, which segments and re-encodes exactly the flagged
+ * requests from their whole bf16 history (records and every code), as dgq_compress_paged of the
+ * L + 1 tokens would, and leaves every other request untouched.
+ */
+#define DGQ_RESEG_WINDOW 1
+#define DGQ_RESEG_NGROUPS 2
+
+/* dgq_append, and in resegment_flags ([batch, Hkv] int32, device, written for every pair; NULL:
+ * none) each pair's DGQ_RESEG_* bits for the token it appended (0 for a pair left untouched). */
+dgq_status dgq_append_ex(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                         int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                         dgq_seg_record *seg_table, int32_t *resegment_flags, void *workspace,
+                         size_t workspace_bytes, void *cuda_stream);
 
 /* dgq_append for a cache with independent V segmentation (dgq_prefill_finish with a v_seg_table):
  * K's codes from k_seg_table's last K segment, V's from v_seg_table's last V segment, each record

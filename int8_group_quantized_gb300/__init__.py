@@ -29,7 +29,8 @@ __all__ = [
     "dgq_append_workspace_size",
     "dgq_paged_decode_attn", "dgq_encode_format", "dgq_encode_format_workspace_size",
     "dgq_paged_decode_attn_format", "FORMATS", "dgq_prefill_workspace_size", "dgq_prefill_chunk_stats",
-    "dgq_prefill_finish", "dgq_paged_decode_attn_split", "dgq_append_split",
+    "dgq_prefill_finish", "dgq_paged_decode_attn_split", "dgq_append_split", "dgq_append_ex",
+    "dgq_prefill_finish_ex", "RESEG_WINDOW", "RESEG_NGROUPS",
     "dgq_attn_workspace_size", "dgq_workspace_init", "dgq_workspace_error", "BlockPool",
     "seg_record_dtype",
 ]
@@ -86,11 +87,16 @@ def lib() -> ctypes.CDLL:
         L.dgq_prefill_chunk_stats.restype = ctypes.c_int
         L.dgq_prefill_finish.argtypes = [P, P, i32, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, i32, P,
                                          P, P, P, sz, P]
+        L.dgq_prefill_finish_ex.argtypes = [P, P, i32, P, i32, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, i32,
+                                            P, P, P, P, i32, P, sz, P]
+        L.dgq_prefill_finish_ex.restype = ctypes.c_int
         L.dgq_paged_decode_attn_split.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                   i32, P, P, sz, P]
         L.dgq_paged_decode_attn_split.restype = ctypes.c_int
         L.dgq_prefill_finish.restype = ctypes.c_int
         L.dgq_append.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, sz, P]
+        L.dgq_append_ex.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P, sz, P]
+        L.dgq_append_ex.restype = ctypes.c_int
         L.dgq_append_split.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, i32, P, P, P, sz, P]
         L.dgq_append_split.restype = ctypes.c_int
         L.dgq_append.restype = ctypes.c_int
@@ -214,6 +220,21 @@ def dgq_append(k_new, v_new, block_size, block_tables, k_pool, v_pool, seg_table
                             _ptr(workspace), _nbytes(workspace), _stream(stream)), "dgq_append")
 
 
+RESEG_WINDOW = 1   # dgq_append_ex: the appended token completed a 16-token window
+RESEG_NGROUPS = 2  # the length reached a threshold of the n_groups rule (2048, 16384)
+
+
+def dgq_append_ex(k_new, v_new, block_size, block_tables, k_pool, v_pool, seg_table, resegment_flags, workspace,
+                  stream=None) -> None:
+    """dgq_append, writing each pair's re-segmentation bits into resegment_flags (int32 CUDA tensor
+    [B, Hkv], or None)."""
+    B, Hkv, D = k_new.shape
+    _check(lib().dgq_append_ex(_ptr(k_new), _ptr(v_new), B, Hkv, D, int(block_size), _ptr(block_tables),
+                               block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(seg_table),
+                               _ptr(resegment_flags), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dgq_append_ex")
+
+
 def dgq_append_split(k_new, v_new, block_size, block_tables, k_pool, v_pool, k_seg_table, v_seg_table, workspace,
                      stream=None) -> None:
     """dgq_append for a cache with independent V segmentation (K's and V's record tables)."""
@@ -289,6 +310,23 @@ def dgq_prefill_finish(k_src, v_src, src_block_tables, seq_lens, max_seqlen, win
                                     block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
                                     _ptr(seg_table), _ptr(v_seg_table), ctypes.byref(opts), _ptr(workspace),
                                     _nbytes(workspace), _stream(stream)), "dgq_prefill_finish")
+
+
+def dgq_prefill_finish_ex(k_src, v_src, src_block_tables, seq_lens, max_seqlen, window_stats, block_tables, k_pool,
+                          v_pool, seg_table, workspace, pair_flags, flag_mask=RESEG_WINDOW | RESEG_NGROUPS,
+                          stream=None, max_groups=MAX_SEG, min_var=0.0, v_seg_table=None) -> None:
+    """dgq_prefill_finish for the requests with a pair whose pair_flags (int32 CUDA tensor [B, Hkv],
+    e.g. from dgq_append_ex) meet flag_mask; every other request is left untouched."""
+    B = seq_lens.shape[0]
+    _, Hkv, bs, D = k_src.shape
+    opts = CompressOptions(int(max_groups), float(min_var))
+    _check(lib().dgq_prefill_finish_ex(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(src_block_tables),
+                                       src_block_tables.shape[1], _ptr(seq_lens), B, int(max_seqlen), Hkv, D, bs,
+                                       _ptr(window_stats), window_stats.shape[2], _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                       _ptr(seg_table), _ptr(v_seg_table), ctypes.byref(opts), _ptr(pair_flags),
+                                       int(flag_mask), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "dgq_prefill_finish_ex")
 
 
 def dgq_paged_decode_attn_split(q, k_new, v_new, k_pool, v_pool, k_seg_table, v_seg_table, block_tables, seq_lens,

@@ -36,9 +36,17 @@ struct AppendArgs {
     uint8_t *vpool;
     uint32_t *table;     // records as words
     uint32_t *vtable;    // independent V segmentation: V's records (null otherwise)
+    int32_t *flags;      // re-segmentation bits per pair (null: not reported)
     WsHeader *hdr;
     int32_t pairs, Hkv, bs, max_blocks, num_blocks;
 };
+
+// Re-segmentation bits of appending token L: a 16-token window completed, or the length reached a
+// threshold of the n_groups rule.
+__device__ __forceinline__ int32_t reseg_bits(int32_t L)
+{
+    return (((L + 1) % kWin == 0) ? DGQ_RESEG_WINDOW : 0) | (ngroups(L + 1) != ngroups(L) ? DGQ_RESEG_NGROUPS : 0);
+}
 
 __device__ __forceinline__ float bf_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -92,14 +100,21 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_kernel(AppendA
     const int32_t n_seg = (int32_t)__shfl_sync(0xffffffffu, w, kWN);
     const int32_t L = (int32_t)__shfl_sync(0xffffffffu, w, kWLen);
     if (L < 0 || L / a.bs >= a.max_blocks) {  // the block table has no column for slot L
-        if (lane == 0) record_error(a.hdr, kErrNoBlock);
+        if (lane == 0) {
+            record_error(a.hdr, kErrNoBlock);
+            if (a.flags) a.flags[pair] = 0;
+        }
         return;
     }
     const int32_t blk = __ldg(a.bt + (int64_t)b * a.max_blocks + L / a.bs);
     if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged, untouched
-        if (lane == 0) record_error(a.hdr, kErrBadBlock);
+        if (lane == 0) {
+            record_error(a.hdr, kErrBadBlock);
+            if (a.flags) a.flags[pair] = 0;
+        }
         return;
     }
+    if (a.flags && lane == 0) a.flags[pair] = reseg_bits(L);
     const uint2 kw = __ldg(a.k_new + (int64_t)pair * 32 + lane);
     const uint2 vw = __ldg(a.v_new + (int64_t)pair * 32 + lane);
     const float kx[4] = {bf_lo_f(kw.x), bf_hi_f(kw.x), bf_lo_f(kw.y), bf_hi_f(kw.y)};
@@ -190,17 +205,19 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_split_kernel(A
     uint32_t *krec = a.table + (int64_t)pair * 32, *vrec = a.vtable + (int64_t)pair * 32;
     const uint32_t wk = krec[lane], wv = vrec[lane];
     const int32_t L = (int32_t)__shfl_sync(0xffffffffu, wk, kWLen);
+    int err = kErrNone;
+    int32_t blk = -1;
     if (L != (int32_t)__shfl_sync(0xffffffffu, wv, kWLen)) {  // the two records disagree: untouched
-        if (lane == 0) record_error(a.hdr, kErrBadLength);
-        return;
+        err = kErrBadLength;
+    } else if (L < 0 || L / a.bs >= a.max_blocks) {  // the block table has no column for slot L
+        err = kErrNoBlock;
+    } else {
+        blk = __ldg(a.bt + (int64_t)b * a.max_blocks + L / a.bs);
+        if ((uint32_t)blk >= (uint32_t)a.num_blocks) err = kErrBadBlock;  // not a block of the pools
     }
-    if (L < 0 || L / a.bs >= a.max_blocks) {  // the block table has no column for slot L
-        if (lane == 0) record_error(a.hdr, kErrNoBlock);
-        return;
-    }
-    const int32_t blk = __ldg(a.bt + (int64_t)b * a.max_blocks + L / a.bs);
-    if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged, untouched
-        if (lane == 0) record_error(a.hdr, kErrBadBlock);
+    if (a.flags && lane == 0) a.flags[pair] = err == kErrNone ? reseg_bits(L) : 0;
+    if (err != kErrNone) {  // flagged, untouched
+        if (lane == 0) record_error(a.hdr, err);
         return;
     }
     const uint2 kw = __ldg(a.k_new + (int64_t)pair * 32 + lane);
@@ -216,9 +233,11 @@ __global__ void __launch_bounds__(kAppendPairsPerCta * 32) append_split_kernel(A
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
                           const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
-                          dgq_seg_record *table, dgq_seg_record *vtable, void *ws, cudaStream_t stream)
+                          dgq_seg_record *table, dgq_seg_record *vtable, int32_t *flags, void *ws,
+                          cudaStream_t stream)
 {
     AppendArgs a;
+    a.flags = flags;
     a.k_new = static_cast<const uint2 *>(k_new);
     a.v_new = static_cast<const uint2 *>(v_new);
     a.bt = bt;

@@ -14,6 +14,17 @@ constexpr int kWin = 16;    // variance window (tokens)
 constexpr int kMaxSeg = 5;  // segments per (request, KV head)
 
 // Every workspace starts with this 256-byte header.
+// n_groups(L), the length rule of the DGQ article (section 3.2): 2 below 2048 tokens, 3 below
+// 16384, else min(5, floor(log2(L / 1024)) + 2), which is 5 for every L >= 16384.
+__device__ __forceinline__ int32_t ngroups(int32_t L)
+{
+    if (L < 2048) return 2;
+    if (L < 16384) return 3;
+    // floor(log2(L / 1024)) = floor(log2(L)) - 10 for integer L >= 1024
+    const int32_t g = (31 - __clz(L)) - 10 + 2;
+    return g < 5 ? g : 5;
+}
+
 struct WsHeader {
     uint32_t error;        // first device-side error code (0 = none)
     uint32_t path;         // compress: which kernel path the last call took (kPath*), for tests

@@ -171,9 +171,21 @@ namespace {
 dgq_status append_impl(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
                        int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
                        int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
-                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, int32_t *flags, void *workspace,
                        size_t workspace_bytes, void *cuda_stream);
 }  // namespace
+
+dgq_status dgq_append_ex(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
+                         int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                         dgq_seg_record *seg_table, int32_t *resegment_flags, void *workspace,
+                         size_t workspace_bytes, void *cuda_stream)
+{
+    if (resegment_flags && !aligned16(resegment_flags)) return DGQ_ERR_INVALID_ARG;
+    return append_impl(k_new_bf16, v_new_bf16, batch, num_kv_heads, head_dim, block_size, block_tables_dev,
+                       max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, nullptr, resegment_flags,
+                       workspace, workspace_bytes, cuda_stream);
+}
 
 dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
@@ -181,7 +193,7 @@ dgq_status dgq_append(const void *k_new_bf16, const void *v_new_bf16, int32_t ba
                       dgq_seg_record *seg_table, void *workspace, size_t workspace_bytes, void *cuda_stream)
 {
     return append_impl(k_new_bf16, v_new_bf16, batch, num_kv_heads, head_dim, block_size, block_tables_dev,
-                       max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, nullptr, workspace,
+                       max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, nullptr, nullptr, workspace,
                        workspace_bytes, cuda_stream);
 }
 
@@ -193,15 +205,15 @@ dgq_status dgq_append_split(const void *k_new_bf16, const void *v_new_bf16, int3
 {
     if (!v_seg_table || !aligned16(v_seg_table)) return DGQ_ERR_INVALID_ARG;
     return append_impl(k_new_bf16, v_new_bf16, batch, num_kv_heads, head_dim, block_size, block_tables_dev,
-                       max_blocks_per_seq, k_pool, v_pool, num_blocks, k_seg_table, v_seg_table, workspace,
-                       workspace_bytes, cuda_stream);
+                       max_blocks_per_seq, k_pool, v_pool, num_blocks, k_seg_table, v_seg_table, nullptr,
+                       workspace, workspace_bytes, cuda_stream);
 }
 
 namespace {
 dgq_status append_impl(const void *k_new_bf16, const void *v_new_bf16, int32_t batch, int32_t num_kv_heads,
                        int32_t head_dim, int32_t block_size, const int32_t *block_tables_dev,
                        int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
-                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, void *workspace,
+                       dgq_seg_record *seg_table, dgq_seg_record *v_seg_table, int32_t *flags, void *workspace,
                        size_t workspace_bytes, void *cuda_stream)
 {
     if (head_dim != DGQ_HEAD_DIM || !block_size_ok(block_size)) return DGQ_ERR_UNSUPPORTED;
@@ -217,7 +229,7 @@ dgq_status append_impl(const void *k_new_bf16, const void *v_new_bf16, int32_t b
         return DGQ_ERR_WORKSPACE;
     const cudaError_t e = dgq::launch_append(k_new_bf16, v_new_bf16, batch, num_kv_heads, block_size,
                                              block_tables_dev, max_blocks_per_seq, k_pool, v_pool, num_blocks,
-                                             seg_table, v_seg_table, workspace,
+                                             seg_table, v_seg_table, flags, workspace,
                                              static_cast<cudaStream_t>(cuda_stream));
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }
@@ -403,7 +415,25 @@ dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, in
                               dgq_seg_record *v_seg_table, const dgq_compress_options *options, void *workspace,
                               size_t workspace_bytes, void *cuda_stream)
 {
+    return dgq_prefill_finish_ex(k_src_bf16, v_src_bf16, num_src_blocks, src_block_tables_dev,
+                                 max_src_blocks_per_seq, seq_lens_dev, batch, max_seqlen, num_kv_heads, head_dim,
+                                 block_size, window_stats, max_windows, block_tables_dev, max_blocks_per_seq, k_pool,
+                                 v_pool, num_blocks, seg_table, v_seg_table, options, nullptr, 0, workspace,
+                                 workspace_bytes, cuda_stream);
+}
+
+dgq_status dgq_prefill_finish_ex(const void *k_src_bf16, const void *v_src_bf16, int32_t num_src_blocks,
+                                 const int32_t *src_block_tables_dev, int32_t max_src_blocks_per_seq,
+                                 const int32_t *seq_lens_dev, int32_t batch, int32_t max_seqlen,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 const float *window_stats, int32_t max_windows, const int32_t *block_tables_dev,
+                                 int32_t max_blocks_per_seq, uint8_t *k_pool, uint8_t *v_pool, int32_t num_blocks,
+                                 dgq_seg_record *seg_table, dgq_seg_record *v_seg_table,
+                                 const dgq_compress_options *options, const int32_t *pair_flags,
+                                 int32_t flag_mask, void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
     if (v_seg_table && !aligned16(v_seg_table)) return DGQ_ERR_INVALID_ARG;
+    if (pair_flags && !aligned16(pair_flags)) return DGQ_ERR_INVALID_ARG;
     dgq::GroupSettings gs = {DGQ_MAX_SEG, 0.0f};
     if (options) {
         if (options->max_groups < 1 || options->max_groups > DGQ_MAX_SEG || !(options->min_var >= 0.0f) ||
@@ -431,8 +461,8 @@ dgq_status dgq_prefill_finish(const void *k_src_bf16, const void *v_src_bf16, in
     bool map_failed = false;
     const cudaError_t e = dgq::launch_prefill_finish(
         src, seq_lens_dev, batch, max_seqlen, num_kv_heads, block_size, window_stats, max_windows, block_tables_dev,
-        max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, v_seg_table, gs, workspace, nsm, &map_failed,
-        static_cast<cudaStream_t>(cuda_stream));
+        max_blocks_per_seq, k_pool, v_pool, num_blocks, seg_table, v_seg_table, gs, pair_flags, flag_mask,
+        workspace, nsm, &map_failed, static_cast<cudaStream_t>(cuda_stream));
     if (map_failed) return DGQ_ERR_INVALID_ARG;
     return e == cudaSuccess ? DGQ_OK : DGQ_ERR_CUDA;
 }

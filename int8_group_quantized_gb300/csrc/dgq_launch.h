@@ -65,7 +65,8 @@ cudaError_t launch_format_encode(int32_t format, const void *k, const void *v, i
 
 cudaError_t launch_append(const void *k_new, const void *v_new, int32_t B, int32_t Hkv, int32_t bs,
                           const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool, int32_t num_blocks,
-                          dgq_seg_record *table, dgq_seg_record *vtable, void *ws, cudaStream_t stream);
+                          dgq_seg_record *table, dgq_seg_record *vtable, int32_t *flags, void *ws,
+                          cudaStream_t stream);
 
 // Compression in two phases for chunked prefill: window statistics of each request's chunk
 // [begin, end) from a bf16 paged cache, then segmentation and codes for whole requests.
@@ -78,7 +79,8 @@ cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens
                                   int32_t Hkv, int32_t bs, const float *stats, int32_t max_windows,
                                   const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
                                   int32_t num_blocks, dgq_seg_record *table, dgq_seg_record *vtable,
-                                  GroupSettings gs, void *ws, int nsm, bool *map_failed, cudaStream_t stream);
+                                  GroupSettings gs, const int32_t *sel, int32_t sel_mask, void *ws, int nsm,
+                                  bool *map_failed, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point query), or null.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -50,18 +50,32 @@ struct PrefillArgs {
     dgq_seg_record *table;
     dgq_seg_record *vtable;  // independent V segmentation: V's records (null: one shared segmentation)
     PairParams *params;    // [2][B * Hkv] quantiser parameters (workspace): K's (or shared), V's
+    const int32_t *sel;    // finish: per-pair flags selecting the requests to encode (null: all)
+    int32_t sel_mask;
     WsHeader *hdr;
     int32_t B, Hkv, bs, max_windows, max_blocks, num_blocks, max_seqlen;
     int32_t max_groups;
     float min_var;
 };
 
+// Whether the finish encodes request b: always without selection flags, else when a flag of one
+// of its pairs meets the mask.
+__device__ __forceinline__ bool pf_selected(const PrefillArgs &a, int32_t b)
+{
+    if (a.sel == nullptr) return true;
+    int32_t any = 0;
+    for (int32_t h = 0; h < a.Hkv; ++h) any |= __ldg(a.sel + (int64_t)b * a.Hkv + h);
+    return (any & a.sel_mask) != 0;
+}
+
 // Windows of request b in this call: [w0, w1).  Statistics: the chunk's windows; codes: all of
-// the request's.  A range that the call's sizes cannot hold is flagged and dropped.
+// the request's (none when the finish does not select it).  A range that the call's sizes cannot
+// hold is flagged and dropped.
 __device__ __forceinline__ void pf_range(const PrefillArgs &a, bool quant, int32_t b, int32_t &w0, int32_t &w1)
 {
-    const int32_t t0 = quant ? 0 : __ldg(a.begin + b), t1 = __ldg(a.end + b);
     w0 = w1 = 0;
+    if (quant && !pf_selected(a, b)) return;
+    const int32_t t0 = quant ? 0 : __ldg(a.begin + b), t1 = __ldg(a.end + b);
     if (t0 < 0 || t1 < t0 || t1 > a.max_seqlen || (t0 & (kWin - 1)) != 0) {
         if (t1 != t0) record_error(a.hdr, kErrBadLength);
         return;
@@ -397,6 +411,7 @@ __global__ void __launch_bounds__(kSegThreads) prefill_segment_kernel(const __gr
     const int tid = threadIdx.x;
     const int32_t pair = blockIdx.x, b = pair / a.Hkv;
     const int64_t P = (int64_t)a.B * a.Hkv;
+    if (!pf_selected(a, b)) return;  // a request the call does not select keeps its record
     int32_t L = __ldg(a.end + b);
     if (L < 0 || L > a.max_seqlen) {
         if (tid == 0) record_error(a.hdr, kErrBadLength);
@@ -482,6 +497,8 @@ static bool prefill_args(const SourceDesc &src, int32_t B, int32_t max_seqlen, i
     a.table = a.vtable = nullptr;
     a.hdr = static_cast<WsHeader *>(ws);
     a.params = reinterpret_cast<PairParams *>(static_cast<uint8_t *>(ws) + sizeof(WsHeader));
+    a.sel = nullptr;
+    a.sel_mask = 0;
     a.B = B;
     a.Hkv = Hkv;
     a.bs = bs;
@@ -509,11 +526,14 @@ cudaError_t launch_prefill_finish(const SourceDesc &src, const int32_t *seq_lens
                                   int32_t Hkv, int32_t bs, const float *stats, int32_t max_windows,
                                   const int32_t *bt, int32_t max_blocks, uint8_t *kpool, uint8_t *vpool,
                                   int32_t num_blocks, dgq_seg_record *table, dgq_seg_record *vtable,
-                                  GroupSettings gs, void *ws, int nsm, bool *map_failed, cudaStream_t stream)
+                                  GroupSettings gs, const int32_t *sel, int32_t sel_mask, void *ws, int nsm,
+                                  bool *map_failed, cudaStream_t stream)
 {
     PrefillArgs a;
     *map_failed = !prefill_args(src, B, max_seqlen, Hkv, bs, const_cast<float *>(stats), max_windows, ws, a);
     if (*map_failed) return cudaErrorInvalidValue;
+    a.sel = sel;
+    a.sel_mask = sel_mask;
     a.end = seq_lens;
     a.bt = bt;
     a.max_blocks = max_blocks;

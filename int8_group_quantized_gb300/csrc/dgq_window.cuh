@@ -25,15 +25,6 @@ struct alignas(16) PairParams {
 };
 static_assert(sizeof(PairParams) == 128, "PairParams is 128 bytes");
 
-__device__ __forceinline__ int32_t ngroups(int32_t L)
-{
-    if (L < 2048) return 2;
-    if (L < 16384) return 3;
-    // floor(log2(L / 1024)) = floor(log2(L)) - 10 for integer L >= 1024
-    const int32_t g = (31 - __clz(L)) - 10 + 2;
-    return g < 5 ? g : 5;
-}
-
 
 // ---- warp reductions ------------------------------------------------------------------------
 

@@ -126,6 +126,11 @@ def test_append_rejects_bad_arguments_before_launch(L):
     assert L.dgq_append_split(*args, FAKE + 4, FAKE, 256, 0) == INVALID
     assert L.dgq_append_split(FAKE, FAKE, 2, 2, 64, 16, FAKE, 19, FAKE, FAKE, 32, FAKE, FAKE, FAKE, 256,
                               0) == UNSUPPORTED
+    # the variant that reports re-segmentation bits: same checks, plus an aligned flags array
+    assert L.dgq_append_ex(*args, FAKE + 4, FAKE, 256, 0) == INVALID
+    assert L.dgq_append_ex(FAKE, FAKE, 2, 2, 64, 16, FAKE, 19, FAKE, FAKE, 32, FAKE, FAKE, FAKE, 256,
+                           0) == UNSUPPORTED
+    assert L.dgq_append_ex(*args, FAKE, 0, 256, 0) == WORKSPACE
 
 
 def _encode(L, **kw):
@@ -200,6 +205,13 @@ def test_prefill_calls_reject_bad_arguments_before_launch(L):
     assert finish(lens=0) == INVALID
     assert finish(mb=18) == INVALID                          # destination table too short for 300 tokens
     assert finish(table=FAKE + 8) == INVALID
+
+    def finish_ex(flags=FAKE, d=128, ws=FAKE):
+        return L.dgq_prefill_finish_ex(FAKE, FAKE, 32, FAKE, 19, FAKE, 2, 300, 2, d, 16, FAKE, 19, FAKE, 19, FAKE,
+                                       FAKE, 32, FAKE, None, None, flags, 3, ws, 1 << 20, 0)
+    assert finish_ex(flags=FAKE + 4) == INVALID           # misaligned flags
+    assert finish_ex(d=64) == UNSUPPORTED
+    assert finish_ex(ws=0) == WORKSPACE
     assert L.dgq_prefill_workspace_size(2, 2) == 256 + 2 * 2 * 2 * 128
 
     def split(vtable=FAKE, d=128):

@@ -1,5 +1,5 @@
-"""Builds libdgq.so in-tree with nvcc for sm_103a (one -gencode, three translation units
-compiled in parallel).  Used by ``__graft_entry__.build()`` and by the binding when the
+"""Builds libdgq.so in-tree with nvcc for sm_103a (one -gencode; the eight translation units
+of csrc/ compiled in parallel).  Used by ``__graft_entry__.build()`` and by the binding when the
 library is missing or older than its sources."""
 from __future__ import annotations
 

@@ -765,6 +765,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
     __shared__ float4 s_o[kCombineWarps][32];
     __shared__ float s_sn;
+    if (blockIdx.x == 0 && tid == 0) a.hdr->path = kPathBlockMerge;  // which merge ran (tests read it)
 
     bool waited = false;
     for (int32_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -865,6 +866,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
     const int32_t items = a.B * Hkv * G;
     const int lane = threadIdx.x & 31;
     const int32_t nw = gridDim.x * kCombineWarps;
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->path = kPathWarpMerge;  // which merge ran (tests read it)
     bool waited = false;
     for (int32_t item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5); item < items; item += nw) {
         const int32_t p = item / G, g = item - p * G;

@@ -13,7 +13,6 @@ constexpr int kD = 128;     // head dimension
 constexpr int kWin = 16;    // variance window (tokens)
 constexpr int kMaxSeg = 5;  // segments per (request, KV head)
 
-// Every workspace starts with this 256-byte header.
 // n_groups(L), the length rule of the DGQ article (section 3.2): 2 below 2048 tokens, 3 below
 // 16384, else min(5, floor(log2(L / 1024)) + 2), which is 5 for every L >= 16384.
 __device__ __forceinline__ int32_t ngroups(int32_t L)
@@ -25,9 +24,10 @@ __device__ __forceinline__ int32_t ngroups(int32_t L)
     return g < 5 ? g : 5;
 }
 
+// Every workspace starts with this 256-byte header.
 struct WsHeader {
     uint32_t error;        // first device-side error code (0 = none)
-    uint32_t path;         // compress: which kernel path the last call took (kPath*), for tests
+    uint32_t path;         // which kernel path the last call took (kPath*), for tests
     uint32_t done_ctas;    // CTAs finished in the current call (compress)
     uint32_t pad[61];
 };
@@ -46,7 +46,7 @@ enum : uint32_t {
 };
 
 // WsHeader::path values
-enum : uint32_t { kPathGrid = 1, kPathClusterWhole = 2 };
+enum : uint32_t { kPathGrid = 1, kPathClusterWhole = 2, kPathBlockMerge = 3, kPathWarpMerge = 4 };
 
 // Upper bound on spin iterations of any wait (each iteration sleeps or polls ~tens of ns;
 // ~2^26 iterations is seconds, far beyond any legitimate wait).

@@ -105,3 +105,19 @@ def test_arbitrary_codes_and_records():
     d_table = torch.from_numpy(table.view(np.uint8).reshape(case.B, case.hkv, 128).copy()).to(dev)
     got = case.gpu_attn(table=d_table, kp=torch.from_numpy(kp).to(dev), vp=torch.from_numpy(vp).to(dev))
     assert_attn_close(ref, got)
+
+
+MERGE_BLOCK, MERGE_WARP = 3, 4  # word 1 of the decode workspace header: the merge kernel that ran
+
+
+@pytest.mark.parametrize("lens,hq,hkv,expect", [
+    # 256 pairs of 13 tiles over at most 3 CTAs per SM: at least one pair per two decode CTAs, so
+    # the one-warp-per-item merge runs, and each pair is split over two or three CTAs
+    ([200] * 128, 8, 2, MERGE_WARP),
+    # 16 pairs of 188 tiles: each split over dozens of CTAs, merged by whole CTAs
+    ([3000] * 8, 8, 2, MERGE_BLOCK),
+])
+def test_both_merge_kernels_with_split_pairs(lens, hq, hkv, expect):
+    case = Case(lens, hq=hq, hkv=hkv, bs=16, seed=61 + len(lens))
+    compress_and_attend(case)
+    assert int(case.d_aws[4:8].cpu().numpy().view(np.uint32)[0]) == expect

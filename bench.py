@@ -4,15 +4,17 @@
 One step = dgq_compress of every layer's K/V (bf16 -> uint8 codes in paged blocks plus
 segment records), dgq_paged_decode_attn over every layer's INT8 cache, then dgq_append of the
 step's own key and value into every layer's cache, for one
-synthetic workload (default: the Llama-3-8B-shaped decode batch, 32 layers, 32 requests of
-2048 tokens, Hq 32 / Hkv 8, block size 16).  Inputs are generated on the GPU by the seeded
-generator before timing and stay resident in HBM; each layer has its own buffers, so one
-step touches far more than L2 (no flush needed).
+synthetic workload (default: the largest, the MHA high-concurrency decode batch, 32 layers, 100
+requests of 256..2048 tokens, Hq = Hkv = 32, block size 16, shuffled blocks).  Inputs are
+generated on the GPU by the seeded generator before timing and stay resident in HBM; each layer
+has its own buffers, so one step touches far more than L2 (no flush needed).  After the main
+line's measurements, the other workloads (2, 4, 5, 5p) are set up and timed the same way for a
+per-workload table (`other_workloads`).
 
 Prints ONE JSON line (rank 0).  `value` is decode-attention algorithmic GB/s over all ranks;
 `compress_gbs` the same for dgq_compress.  `--impl reference` times the CPU oracle instead.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3] [--impl ours|reference]
 """
 from __future__ import annotations
 
@@ -40,7 +42,10 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="2", help="workload id: 1..5 or 5p")
+    ap.add_argument("--config", default="3", help="workload id: 1..5 or 5p (default 3, the largest: MHA, "
+                    "100 requests)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-workload table (workloads 2, 4, 5, 5p timed after the main line)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
@@ -126,49 +131,117 @@ def ncu_traffic(kernel_src, workload_name):
 
 
 class ClockSampler:
+    """SM clock, power and throttle reasons sampled while the timed region runs (read-only
+    queries).  NVML through ctypes every 20 ms when the driver's NVML library loads (the GPU
+    picked by its PCI bus id), else `nvidia-smi -lms 50`."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}  # nvmlClocksEventReason* masks
 
     def __init__(self, dev_index):
         self.proc = None
         self.dev = dev_index
+        self.thread = None
+        self.samples = []
+        self.smax = None
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.dev)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML device for that bus id")
+        except Exception:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.dev), ctypes.byref(h)) != 0:
+                return None, None
+        return nv, h
+
+    def _poll(self, nv, h):
+        import ctypes
+        clk, mw, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag:
+            ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0  # NVML_CLOCK_SM
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            get_reasons(h, ctypes.byref(reasons))
+            if ok:
+                self.samples.append((float(clk.value), mw.value / 1e3, int(reasons.value)))
+            time.sleep(0.02)
 
     def start(self):
+        import threading
+        try:
+            import ctypes
+            nv, h = self._nvml_handle()
+            if nv is not None:
+                mx = ctypes.c_uint()
+                if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                    self.smax = float(mx.value)
+                self.stop_flag = False
+                self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+                self.thread.start()
+                t0 = time.time()
+                while not self.samples and time.time() - t0 < 2.0:  # the first sample is in
+                    time.sleep(0.005)
+                self.source = "nvml, 20 ms"
+                return
+        except Exception:
+            self.thread = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 50 ms"
         except Exception:
             self.proc = None
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            return None
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
+        sm, reasons, smax, power = [], set(), self.smax, []
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=2)
+            for mhz, w, bits in self.samples:
+                sm.append(mhz)
+                power.append(w)
+                for n, b in self.REASON_BITS.items():
+                    if bits & b:
+                        reasons.add(n)
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                return None
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax = float(f[2])
+                    power.append(float(f[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "sm_mhz_min": min(sm),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": round(max(power), 1) if power else None,
+                "source": self.source}
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -287,39 +360,19 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------ GPU path
 
-def run_ours(args):
+def setup_layers(w, lens, bt, nb, cu, dev, sp, nl, paged_input=False):
+    """Every layer's inputs drawn on the GPU by the seeded generator (K/V, the step's q / k_new /
+    v_new), and its own zeroed INT8 pools and records.  The step inputs of all layers sit in one
+    buffer and the outputs in another, so that an end-to-end step moves each with one copy."""
     import numpy as np
     import torch
-    import torch.distributed as dist
-
-    import int8_group_quantized_gb300 as dgq
     import synth
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dgq.lib()
-
-    w, lens, bt, nb, cu = workload(args.config)
-    B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
-    bt, nb = with_append_room(bt, nb, lens, bs, APPEND_ROOM)
-    if args.layers:
-        nl = min(nl, args.layers)
+    B, Hq, Hkv, bs = w.batch, w.hq, w.hkv, w.block_size
     T = int(cu[-1])
-    max_seqlen = int(lens.max())
-    stream = torch.cuda.current_stream()
-    sp = stream.cuda_stream
-
     d_cu = torch.from_numpy(cu).to(dev)
     d_bt = torch.from_numpy(bt).to(dev)
     d_lens = torch.from_numpy(lens).to(dev)
     layers = []
-    # every layer's step inputs (q, k_new, v_new) and outputs in one buffer each, so that the
-    # end-to-end step moves them with one host-to-device and one device-to-host copy
     n_q, n_kv = B * Hq * D, B * Hkv * D
     step_in = torch.empty(nl * (n_q + 2 * n_kv), dtype=torch.bfloat16, device=dev)
     step_out = torch.empty(nl * n_q, dtype=torch.bfloat16, device=dev)
@@ -343,7 +396,7 @@ def run_ours(args):
             vp=torch.zeros((nb, Hkv, bs, D), dtype=torch.uint8, device=dev),
             table=torch.zeros((B, Hkv, REC), dtype=torch.uint8, device=dev),
             out=step_out[l * n_q:(l + 1) * n_q].view(B, Hq, D)))
-    if args.paged_input:  # the same tokens in a bf16 paged cache laid out like the INT8 pools
+    if paged_input:  # the same tokens in a bf16 paged cache laid out like the INT8 pools
         tok_blk = torch.from_numpy(np.concatenate(
             [bt[b, np.arange(int(L)) // bs] for b, L in enumerate(lens)]).astype(np.int64)).to(dev)
         tok_slot = torch.from_numpy(np.concatenate(
@@ -353,27 +406,148 @@ def run_ours(args):
                 src = torch.zeros((nb, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
                 src[tok_blk, :, tok_slot, :] = L[name]
                 L[name + "_src"] = src
+    return layers, step_in, step_out, d_cu, d_bt, d_lens
+
+
+class StepFns:
+    """The three phases of a step over every layer, through the C ABI binding."""
+
+    def __init__(self, dgq, layers, d_cu, d_bt, d_lens, max_seqlen, bs, cws, aws, pws, sp, paged_input=False):
+        self.__dict__.update(dgq=dgq, layers=layers, d_cu=d_cu, d_bt=d_bt, d_lens=d_lens, ms=max_seqlen, bs=bs,
+                             cws=cws, aws=aws, pws=pws, sp=sp, paged=paged_input)
+
+    def compress_all(self):
+        dgq = self.dgq
+        for L in self.layers:
+            if self.paged:
+                dgq.dgq_compress_paged(L["k_src"], L["v_src"], self.d_bt, self.d_cu, self.ms, self.bs, self.d_bt,
+                                       L["kp"], L["vp"], L["table"], self.cws, self.sp)
+            else:
+                dgq.dgq_compress(L["k"], L["v"], self.d_cu, self.ms, self.bs, self.d_bt, L["kp"], L["vp"], L["table"],
+                                 self.cws, self.sp)
+
+    def decode_all(self):
+        for L in self.layers:
+            self.dgq.dgq_paged_decode_attn(L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], self.d_bt,
+                                           self.d_lens, self.ms, L["out"], self.aws, self.sp)
+
+    def append_all(self):  # the step's own token of every layer into its cache
+        for L in self.layers:
+            self.dgq.dgq_append(L["kn"], L["vn"], self.bs, self.d_bt, L["kp"], L["vp"], L["table"], self.pws,
+                                self.sp)
+
+
+def time_other_workload(cfg, dev, sp, peak, steps=5, warmup=2):
+    """Compress and decode of every layer of another workload, timed like the main run (CUDA
+    events on the launching stream around each phase; inputs resident in HBM, each layer its own
+    buffers), for the per-workload table.  Frees everything before it returns."""
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    w, lens, bt, nb, cu = workload(cfg)
+    B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
+    ms = int(lens.max())
+    layers, step_in, step_out, d_cu, d_bt, d_lens = setup_layers(w, lens, bt, nb, cu, dev, sp, nl)
+    cws = torch.zeros(dgq.dgq_compress_workspace_size(B, ms, Hkv), dtype=torch.uint8, device=dev)
+    aws = torch.zeros(dgq.dgq_attn_workspace_size(B, Hq, Hkv, ms), dtype=torch.uint8, device=dev)
+    fn = StepFns(dgq, layers, d_cu, d_bt, d_lens, ms, bs, cws, aws, None, sp)
+    for _ in range(warmup):
+        fn.compress_all()
+        fn.decode_all()
+    torch.cuda.synchronize()
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    stream = torch.cuda.current_stream()
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fn.compress_all()
+        e1.record(stream)
+        fn.decode_all()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    comp_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
+    dec_ms = sum(b.elapsed_time(c) for _, b, c in ev)
+    err = dgq.dgq_workspace_error(cws, sp) or dgq.dgq_workspace_error(aws, sp)
+    dec_b, comp_b = algorithmic_bytes(w, lens)
+    dec_us, comp_us = dec_ms / (steps * nl) * 1e3, comp_ms / (steps * nl) * 1e3
+    del layers, step_in, step_out, cws, aws, fn
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "layers": nl, "steps": steps, "warmup": warmup,
+            "decode_us_per_layer": round(dec_us, 2), "decode_gbs": round(dec_b / dec_us / 1e3, 1),
+            "decode_frac_of_peak": round(dec_b / dec_us / 1e3 / peak, 4),
+            "compress_us_per_layer": round(comp_us, 2), "compress_gbs": round(comp_b / comp_us / 1e3, 1),
+            "compress_frac_of_peak": round(comp_b / comp_us / 1e3 / peak, 4),
+            "compress_kernel": "compress_cluster_kernel" if ms <= 4096 else "compress_kernel",
+            "decode_bytes_per_layer": dec_b, "compress_bytes_per_layer": comp_b, "device_error": err}
+
+
+def time_compress_e2e(w, layers, d_cu, d_bt, max_seqlen, bs, cws, sp, comp_b, nlayers=4, reps=3):
+    """Compression end to end through the C ABI: per layer, the bf16 K/V come from pinned host
+    memory (one copy each), dgq_compress writes the layer's pools and records, and the records go
+    back to pinned host memory; CUDA events around `nlayers` layers, `reps` passes after one warm
+    pass.  Context for the compress figure: in serving, K/V are produced on the GPU by prefill and
+    never cross the host link (the device-resident figure is compress_gbs)."""
+    import torch
+    import int8_group_quantized_gb300 as dgq
+    use = layers[:nlayers]
+    h_k = torch.empty(use[0]["k"].shape, dtype=torch.bfloat16).pin_memory()
+    h_v = torch.empty_like(h_k).pin_memory()
+    h_k.copy_(use[0]["k"])
+    h_v.copy_(use[0]["v"])
+    d_k, d_v = torch.empty_like(use[0]["k"]), torch.empty_like(use[0]["v"])
+    h_tab = torch.empty((len(use),) + tuple(use[0]["table"].shape), dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for r in range(reps + 1):
+        if r == 1:
+            ev[0].record(stream)
+        for i, L in enumerate(use):
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            dgq.dgq_compress(d_k, d_v, d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"], cws, sp)
+            h_tab[i].copy_(L["table"], non_blocking=True)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / (reps * len(use))
+    h2d = 2 * h_k.numel() * 2
+    d2h = h_tab[0].numel()
+    return {"value": round(comp_b / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "us_per_layer": round(ms * 1e3, 2),
+            "h2d_bytes_per_layer": h2d, "d2h_bytes_per_layer": d2h, "layers": len(use), "reps": reps,
+            "what": "dgq_compress with the layer's bf16 K/V copied from pinned host memory and its records "
+                    "copied back, per layer; GB/s over compression's algorithmic bytes"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import int8_group_quantized_gb300 as dgq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dgq.lib()
+
+    w, lens, bt, nb, cu = workload(args.config)
+    B, Hq, Hkv, bs, nl = w.batch, w.hq, w.hkv, w.block_size, w.layers
+    bt, nb = with_append_room(bt, nb, lens, bs, APPEND_ROOM)
+    if args.layers:
+        nl = min(nl, args.layers)
+    max_seqlen = int(lens.max())
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    layers, step_in, step_out, d_cu, d_bt, d_lens = setup_layers(w, lens, bt, nb, cu, dev, sp, nl,
+                                                                  args.paged_input)
     cws = torch.zeros(dgq.dgq_compress_workspace_size(B, max_seqlen, Hkv), dtype=torch.uint8, device=dev)
     aws = torch.zeros(dgq.dgq_attn_workspace_size(B, Hq, Hkv, max_seqlen), dtype=torch.uint8, device=dev)
     pws = torch.zeros(dgq.dgq_append_workspace_size(), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
-
-    def compress_all():
-        for L in layers:
-            if args.paged_input:
-                dgq.dgq_compress_paged(L["k_src"], L["v_src"], d_bt, d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"],
-                                       L["table"], cws, sp)
-            else:
-                dgq.dgq_compress(L["k"], L["v"], d_cu, max_seqlen, bs, d_bt, L["kp"], L["vp"], L["table"], cws, sp)
-
-    def decode_all():
-        for L in layers:
-            dgq.dgq_paged_decode_attn(L["q"], L["kn"], L["vn"], L["kp"], L["vp"], L["table"], d_bt, d_lens,
-                                      max_seqlen, L["out"], aws, sp)
-
-    def append_all():  # the step's own token of every layer into its cache
-        for L in layers:
-            dgq.dgq_append(L["kn"], L["vn"], bs, d_bt, L["kp"], L["vp"], L["table"], pws, sp)
+    fn = StepFns(dgq, layers, d_cu, d_bt, d_lens, max_seqlen, bs, cws, aws, pws, sp, args.paged_input)
+    compress_all, decode_all, append_all = fn.compress_all, fn.decode_all, fn.append_all
 
     for _ in range(args.warmup):
         compress_all()
@@ -409,6 +583,9 @@ def run_ours(args):
     comp_ms = sum(e0.elapsed_time(e1) for e0, e1, _, _ in evs)
     dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2, _ in evs)
     app_ms = sum(e2.elapsed_time(e3) for _, _, e2, e3 in evs)
+    if clk:
+        clk["timed_region_ms"] = round(total_ms, 2)
+        clk["ms_x_median_mhz"] = round(total_ms * clk["sm_mhz"], 1)
     # parity spot check outside the timed region (layer 0 compressed again: the appends above
     # have grown its records)
     dgq.dgq_compress(layers[0]["k"], layers[0]["v"], d_cu, max_seqlen, bs, d_bt, layers[0]["kp"],
@@ -451,7 +628,8 @@ def run_ours(args):
     a1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
-
+    del h_in, h_out
+    comp_e2e = time_compress_e2e(w, layers, d_cu, d_bt, max_seqlen, bs, cws, sp, comp_b) if rank == 0 else None
 
     ref0 = request0_reference(w, lens, layers[0]) if rank == 0 else None
     fidelity = fidelity_check(w, layers[0], ref0) if rank == 0 else None
@@ -470,12 +648,20 @@ def run_ours(args):
 
     total_ms, comp_ms, dec_ms, app_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, app_ms, e2e_ms], dev,
                                                               world)
+    peak, peak_src = measured_peak()
+    others = None
+    if world == 1 and not args.no_others:  # the other workloads, each with every layer resident
+        del layers, step_in, step_out, fn, compress_all, decode_all, append_all
+        torch.cuda.empty_cache()
+        others = {}
+        for cfg in ("2", "4", "5", "5p"):
+            if cfg != str(args.config):
+                others[cfg] = time_other_workload(cfg, dev, sp, peak)
 
     if rank == 0:
         K = args.steps
         dec_gbs = replica_gbs(dec_b_step, K, world, dec_ms)
         comp_gbs = replica_gbs(comp_b_step, K, world, comp_ms)
-        peak, peak_src = measured_peak()
         dec_launch_us = dec_ms / (K * nl) * 1e3
         comp_launch_us = comp_ms / (K * nl) * 1e3
         app_launch_us = app_ms / (K * nl) * 1e3
@@ -524,6 +710,8 @@ def run_ours(args):
             "prefill_two_phase": prefill,
             "independent_v_segmentation": split_v,
             "formats": formats,
+            "compress_e2e": comp_e2e,
+            "other_workloads": others,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,
             "device_error": err,

@@ -473,6 +473,7 @@ def time_other_workload(cfg, dev, sp, peak, steps=5, warmup=2):
     return {"workload": w.name, "layers": nl, "steps": steps, "warmup": warmup,
             "decode_us_per_layer": round(dec_us, 2), "decode_gbs": round(dec_b / dec_us / 1e3, 1),
             "decode_frac_of_peak": round(dec_b / dec_us / 1e3 / peak, 4),
+            "decode_token_heads_per_s": round(sum(int(L) + 1 for L in lens) * Hq / (dec_us / 1e6), 1),
             "compress_us_per_layer": round(comp_us, 2), "compress_gbs": round(comp_b / comp_us / 1e3, 1),
             "compress_frac_of_peak": round(comp_b / comp_us / 1e3 / peak, 4),
             "compress_kernel": "compress_cluster_kernel" if ms <= 4096 else "compress_kernel",

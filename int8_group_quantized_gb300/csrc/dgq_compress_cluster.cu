@@ -16,7 +16,8 @@
 //    quantiser parameters into every CTA of the cluster and arrives on each CTA's "ready"
 //    mbarrier.  No step goes through L2 or a grid barrier.
 //  * Workers quantise a pair once its parameters are ready, re-reading its K/V (read a few
-//    microseconds earlier, so from L2; the re-read carries an evict-first hint), and meanwhile
+//    microseconds earlier, so from L2; the re-read carries an evict-first hint and takes the
+//    CTA's windows in the reverse of their first-read order), and meanwhile
 //    compute statistics of at most kSlots - 1 later pairs: a cluster holds at most kSlots pairs
 //    (2 MB) between first read and re-read, the whole GPU about 70 MB.
 //  * Twelve workers and one segmentation warp per CTA (127 registers a thread): measured on
@@ -361,7 +362,9 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 }
                 it.kind = ab ? 2 : 1;
                 it.j = qc.j;
-                it.t0 = qc.i * kWin;
+                // the CTA's windows of the pair are re-read last-read first, while they are the
+                // likeliest still to be in L2 (measured 1.4% faster on the MHA batch)
+                it.t0 = (qc.lo + qc.hi - 1 - qc.i) * kWin;
                 it.cnt = min(kWin, qc.L - it.t0);
                 it.h = qc.h;
                 if (!ab) {

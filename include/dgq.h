@@ -31,10 +31,10 @@
  *     failures (a wait that timed out) are recorded in the workspace and read with
  *     dgq_workspace_error.
  *   - bf16 values are IEEE bfloat16 bit patterns; fp32 is IEEE binary32.
- *   - Host threads: the launchers keep the launch shape of each kernel (occupancy, shared-memory
- *     limit) for the device they last ran on, in unsynchronised statics.  Calls from one host
- *     thread at a time are safe on any number of devices; a process that calls from several
- *     threads at once must serialise its calls.
+ *   - Host threads: each launcher keeps the launch shape of its kernel (occupancy, shared-memory
+ *     limit) for the device it last ran on, per host thread; host threads share no library
+ *     state, so calls from several threads at once are safe (each on its own stream and
+ *     workspace, as above), on any number of devices.
  */
 #ifndef DGQ_H
 #define DGQ_H

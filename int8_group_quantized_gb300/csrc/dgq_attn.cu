@@ -66,6 +66,7 @@ enum : int { kDecAffine = 0, kDecFp8 = 1, kDecFixed = 2, kDecSplitV = 3 };
 template <int Fmt>
 __host__ __device__ constexpr int stage_bytes() { return kTileSmem + (Fmt == kDecFixed ? 2 * kParBytes : 0); }
 constexpr int kPartStride = 132;                   // floats per (piece, head) partial: m, l, pad, pad, O[128]
+constexpr int32_t kMaxGroup = 8;                   // largest query-head group the entry points accept
 constexpr float kLog2eOverSqrtD = 0.12751743074570180f;  // log2(e) / sqrt(128)
 constexpr float kLazyRescale = 8.0f;               // log2 units
 
@@ -1009,17 +1010,24 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
                              : dec == kDecSplitV ? attn_kernel<kDecSplitV>
                                                  : attn_kernel<kDecAffine>;
 
-    // per-device launch shape, computed once per (instance, device, shared-memory size)
-    static int cached_dev[4] = {-1, -1, -1, -1};
-    static size_t cached_smem[4] = {0, 0, 0, 0};
-    static int cached_occ[4] = {0, 0, 0, 0};
+    // per-device launch shape, computed once per (instance, device, shared-memory size) and host
+    // thread; the kernel's shared-memory limit is raised once per device and host thread to what
+    // the largest call needs (every thread sets the same value, so none lowers it under another)
+    static thread_local int limit_dev[4] = {-1, -1, -1, -1};
+    static thread_local int cached_dev[4] = {-1, -1, -1, -1};
+    static thread_local size_t cached_smem[4] = {0, 0, 0, 0};
+    static thread_local int cached_occ[4] = {0, 0, 0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const size_t smem = attn_smem_bytes(dec, B, G);
-    if (dev != cached_dev[dec] || smem != cached_smem[dec]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev != limit_dev[dec]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_smem_bytes(dec, kMaxCallBatch, kMaxGroup));
         if (e != cudaSuccess) return e;
+        limit_dev[dec] = dev;
+    }
+    if (dev != cached_dev[dec] || smem != cached_smem[dec]) {
         int occ = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAttnThreads, smem);
         if (e != cudaSuccess) return e;

@@ -880,15 +880,18 @@ cudaError_t launch_compress(const SourceDesc &src, const int32_t *cu, int32_t B,
     a.max_groups = gs.max_groups;
     a.min_var = gs.min_var;
 
-    // per-device launch set-up, done once per (device, shared-memory size)
-    static int cached_dev = -1;
-    static size_t cached_smem = 0;
+    // per-device launch set-up, done once per (device, shared-memory size) and host thread; the
+    // kernel's shared-memory limit is raised to what the largest call needs (the same value from
+    // every host thread, so none lowers it under another)
+    static thread_local int cached_dev = -1;
+    static thread_local size_t cached_smem = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const size_t smem = compress_smem_bytes(B);
     if (dev != cached_dev || smem != cached_smem) {
-        e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)compress_smem_bytes(kMaxCallBatch));
         if (e != cudaSuccess) return e;
         int occ = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kThreads, smem);

@@ -481,7 +481,7 @@ template <int kCl>
 static cudaError_t launch_cluster_size(const ClusterArgs &a, cudaStream_t stream)
 {
     const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmemT<kClusterMaxWin / kCl>);  // + alignment slack
-    static int cached_dev = -1, cached_clusters = 0;
+    static thread_local int cached_dev = -1, cached_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -16,7 +16,7 @@ static_assert(sizeof(dgq_seg_record) == 128, "dgq_seg_record must be 128 bytes")
 namespace dgq {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static thread_local PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
         void *p = nullptr;
@@ -31,7 +31,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 
 namespace {
 
-constexpr int32_t kMaxBatch = 8192;  // per-call limit (the kernels keep per-request prefixes on chip)
+constexpr int32_t kMaxBatch = dgq::kMaxCallBatch;  // per-call limit (the kernels keep per-request prefixes on chip)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

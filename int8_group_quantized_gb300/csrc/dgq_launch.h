@@ -10,6 +10,11 @@
 
 namespace dgq {
 
+// Requests per call the entry points accept (the kernels keep per-request prefixes on chip).  A
+// kernel's dynamic shared-memory limit is a property of the kernel shared by every host thread, so
+// the launchers raise it once, to what a call of this many requests needs, and never lower it.
+constexpr int32_t kMaxCallBatch = 8192;
+
 // Group-selection settings passed to both compress kernels (see dgq_compress_options).
 struct GroupSettings {
     int32_t max_groups;

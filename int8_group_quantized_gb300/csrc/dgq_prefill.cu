@@ -37,7 +37,6 @@ constexpr int kPfSlots = 1;                       // windows in flight per warp
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfRingBytes = kPfWarps * kPfSlots * kWinBytes;
 constexpr int kSegThreads = 256;                  // segmentation CTA (one per pair)
-constexpr int32_t kMaxPrefillBatch = 8192;       // the library's per-call batch limit
 constexpr int kStatFloats = 8;  // per window: K mean variance, k min, k max, v min, v max, V mean variance, 0, 0
 
 struct PrefillArgs {
@@ -473,13 +472,13 @@ template <bool quant, bool split>
 static cudaError_t launch_windows(const PrefillArgs &a, int nsm, cudaStream_t stream)
 {
     // the shared-memory limit is raised once per device, to what the largest batch needs
-    static int ready_dev = -1;
+    static thread_local int ready_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev != ready_dev) {
         e = cudaFuncSetAttribute(prefill_window_kernel<quant, split>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)prefill_smem(kMaxPrefillBatch));
+                                 (int)prefill_smem(kMaxCallBatch));
         if (e != cudaSuccess) return e;
         ready_dev = dev;
     }

@@ -61,6 +61,7 @@ def test_compress_rejects_bad_arguments_before_launch(L):
     assert _compress(L, table=0) == INVALID
     assert _compress(L, k=FAKE + 2) == INVALID           # misaligned
     assert _compress(L, batch=0) == INVALID
+    assert _compress(L, batch=8193) == INVALID            # above the per-call limit of 8192 requests
     assert _compress(L, max_seqlen=305) == INVALID       # > max_blocks * bs
     assert _compress(L, T=-1) == INVALID
     assert _compress(L, ws=0) == WORKSPACE

@@ -23,11 +23,19 @@ def _prefix(x, cu, lens):
 
 @pytest.mark.parametrize("mask", [oracle.RESEG_WINDOW | oracle.RESEG_NGROUPS, oracle.RESEG_NGROUPS])
 def test_appends_with_resegmentation_match_oracle(mask):
+    o_tab, redone = run_resegment_steps([2040, 300, 1000, 16380, 5, 2047, 0], 2, 16, 10, 51, mask)
+    assert redone == (3 if mask == oracle.RESEG_NGROUPS else 5)  # the steps did re-segment
+    assert o_tab[0, 0]["n_seg"] == 3 and o_tab[3, 0]["n_seg"] == 5  # 2048 and 16384 crossed
+
+
+def run_resegment_steps(lens0, Hkv, bs, steps, seed, mask):
+    """`steps` decode steps with re-segmentation on the GPU, each checked against the oracle;
+    then the one-shot compress of the grown history.  Returns the oracle's final records and the
+    number of request re-segmentations."""
     import torch
     import int8_group_quantized_gb300 as dgq
     dev = torch.device("cuda:0")
-    lens0 = np.array([2040, 300, 1000, 16380, 5, 2047, 0], dtype=np.int32)
-    Hkv, bs, steps, seed = 2, 16, 10, 51
+    lens0 = np.asarray(lens0, dtype=np.int32)
     full = lens0 + steps
     cu = configs.cu_seqlens(full)
     tabs = synth.span_tables(seed, 0, full, Hkv, synth.RULE_U)
@@ -105,8 +113,7 @@ def test_appends_with_resegmentation_match_oracle(mask):
         assert g_tab.tobytes() == o_tab.tobytes(), s
         assert np.array_equal(kp.cpu().numpy(), o_kp) and np.array_equal(vp.cpu().numpy(), o_vp), s
         redone += int(((o_flags & mask).max(axis=1) > 0).sum())
-    assert redone == (3 if mask == oracle.RESEG_NGROUPS else 5)  # the steps did re-segment
-    assert o_tab[0, 0]["n_seg"] == 3 and o_tab[3, 0]["n_seg"] == 5  # 2048 and 16384 crossed
+    final_tab = o_tab.copy()
 
     # the whole grown history through the one-shot compress from the paged cache
     grown = lens0 + steps
@@ -121,3 +128,4 @@ def test_appends_with_resegmentation_match_oracle(mask):
     assert dgq.dgq_workspace_error(cws) == 0
     assert table_to_numpy(table).tobytes() == f_tab.tobytes()
     assert np.array_equal(kp.cpu().numpy(), f_kp) and np.array_equal(vp.cpu().numpy(), f_vp)
+    return final_tab, redone

@@ -9,12 +9,19 @@
 // K+V), a pair's segmentation needs no grid-wide step: clusters of kCl CTAs take whole pairs
 // round-robin, and the kCl CTAs of a cluster split each pair's windows.
 //  * Workers (per-warp two-window rings filled by TMA, as in the grid-wide kernel) compute
-//    window statistics into their CTA's shared memory and arrive, with cluster-scope release,
-//    on an mbarrier of the pair's owner CTA (owners rotate through the cluster).
-//  * The owner's segmentation warp reads the pair's statistics from the kCl CTAs through
-//    distributed shared memory in one round, segments the pair, writes the record, stores the
-//    quantiser parameters into every CTA of the cluster and arrives on each CTA's "ready"
-//    mbarrier.  No step goes through L2 or a grid barrier.
+//    window statistics and send them straight into the shared memory of the pair's owner CTA
+//    (owners rotate through the cluster) with asynchronous remote stores that complete bytes on
+//    the owner's mbarrier (st.async ... mbarrier::complete_tx); the owner arms that barrier with
+//    the pair's byte count.  Every worker also arrives on that barrier once it is done with the
+//    pair's statistics (even with no window of the pair), so a phase completes only after every
+//    worker has moved past the pair and so has taken the parameters of the pair that last used
+//    the slot; that arrival is relaxed, as it publishes no data.  Measured on this GPU, a
+//    cluster-scope release arrive per worker and pair (the data in the worker's own shared
+//    memory) waited for the worker's outstanding code stores and cost 5-6% of the kernel.
+//  * The owner's segmentation warp reads the pair's statistics from its own shared memory,
+//    segments the pair, writes the record, stores the quantiser parameters into every CTA of
+//    the cluster and arrives on each CTA's "ready" mbarrier.  No step goes through L2 or a grid
+//    barrier.
 //  * Workers quantise a pair once its parameters are ready, re-reading its K/V (read a few
 //    microseconds earlier, so from L2; the re-read carries an evict-first hint and takes the
 //    CTA's windows in the reverse of their first-read order), and meanwhile
@@ -65,13 +72,11 @@ struct ClusterArgs {
     int32_t max_seqlen, num_blocks;  // for the device-side checks of lengths and block ids
 };
 
-// kSlotWin: windows of one pair per CTA (the longest pair split over the cluster's CTAs)
-template <int kSlotWin>
-struct ClusterSmemT {
-    float mean[kSlots][kSlotWin];
-    float4 mm[kSlots][kSlotWin];
+struct ClusterSmem {
+    float mean[kSlots][kClusterMaxWin];  // owner side: statistics of every window of an owned pair
+    float4 mm[kSlots][kClusterMaxWin];
     PairParams par[kSlots];
-    uint64_t stats_done[kSlots];  // owner side: arrivals of every worker of the cluster
+    uint64_t stats_done[kSlots];  // owner side: the pair's statistics have all landed (byte count)
     uint64_t ready[kSlots];       // parameters of the slot's pair are in par[]
     uint64_t full[kCWorkers][kCRing];  // a worker's ring slot holds its window
     int32_t abort;
@@ -130,27 +135,44 @@ __device__ __forceinline__ bool test_wait_cluster(uint64_t *bar, uint32_t parity
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ float ld_remote_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 ld_remote_f4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
 __device__ __forceinline__ void st_remote_u4(uint32_t addr, uint4 v)
 {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
 }
+// Asynchronous stores into another CTA's shared memory, each completing its bytes on an mbarrier
+// of that CTA (both addresses from mapa).  They need no fence: the owner observes them through
+// the barrier's phase.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w)), "r"(bar)
+                 : "memory");
+}
+// Arrival without release on another CTA's mbarrier: a worker tells the owner that it is done
+// with a pair's statistics (its data travel by st.async and complete on their own).
+__device__ __forceinline__ void remote_arrive_relaxed(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// The owner arms its statistics barrier: its own arrival and the bytes to expect (no release:
+// it publishes nothing).
+__device__ __forceinline__ void arm_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+constexpr uint32_t kStatBytes = 4 + 16;  // per window: mean (fp32) and extremes (float4)
+
 __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -197,9 +219,6 @@ struct CItem {
 template <int kCl>
 __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __grid_constant__ ClusterArgs a)
 {
-    constexpr int kSlotWin = kClusterMaxWin / kCl;
-    static_assert(kCl * kSlotWin == kClusterMaxWin, "a CTA holds its share of the longest pair");
-    using ClusterSmem = ClusterSmemT<kSlotWin>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);  // window tiles start on 1024-byte boundaries
     ClusterSmem *cs = reinterpret_cast<ClusterSmem *>(smem + kCRingBytes);
@@ -211,7 +230,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
 
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&cs->stats_done[s], kCl * kCWorkers);
+            // every worker of the cluster and the owner arrive; the workers' bytes complete too
+            mbar_init(&cs->stats_done[s], kCl * kCWorkers + 1);
             mbar_init(&cs->ready[s], 1);
         }
         for (int w = 0; w < kCWorkers; ++w)
@@ -260,6 +280,10 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
         for (int32_t q = 0; q * kCl + rank < nj; ++q) {
             const int32_t j = q * kCl + rank;
             const int32_t qs = q % kSlots;
+            PairCursor pc;
+            pair_of(j, pc, geo);
+            const int32_t W = (pc.L + kWin - 1) / kWin;
+            if (lane == 0) arm_expect_tx(&cs->stats_done[qs], (uint32_t)W * kStatBytes);
             bool ok = true;
             for (uint32_t it = 0; !try_wait_cluster(&cs->stats_done[qs], (uint32_t)(q / kSlots) & 1u);) {
                 if (++it >= kSpinLimit || aborted()) {
@@ -275,15 +299,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 }
                 break;
             }
-            PairCursor pc;
-            pair_of(j, pc, geo);
-            const int32_t W = (pc.L + kWin - 1) / kWin;
             const int32_t p = clu + j * ncl;
             const int slot = j % kSlots;
             dgq_seg_record rec = {};
             PairParams pp = {};
             if (W > 0) {
-                // the pair's window statistics from the kCl CTAs, lane i holding windows 8i .. 8i+7
+                // the pair's window statistics, sent here by the cluster's workers; lane i holds
+                // windows 8i .. 8i+7
                 float m[8];
                 float4 mm[8];
 #pragma unroll
@@ -292,10 +314,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                     m[i] = 0.0f;
                     mm[i] = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
                     if (w < W) {
-                        const int32_t r = ((w + 1) * kCl + W - 1) / W - 1;  // CTA holding window w
-                        const int32_t idx = w - (W * r) / kCl;
-                        m[i] = ld_remote_f32(map_rank(&cs->mean[slot][idx], (uint32_t)r));
-                        mm[i] = ld_remote_f4(map_rank(&cs->mm[slot][idx], (uint32_t)r));
+                        m[i] = cs->mean[qs][w];
+                        mm[i] = cs->mm[qs][w];
                     }
                 }
                 int k = min(min(ngroups(pc.L), a.max_groups), W) - 1;
@@ -333,11 +353,11 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 c.i = c.lo + warp;
             }
         };
-        // the arrival a worker owes pair j's owner once its statistics of pair j are done
+        // the arrival a worker owes pair j's owner once it is done with pair j's statistics
         auto arrive_stats = [&](int32_t j) {
             if (lane == 0) {
                 const int32_t q = j / kCl;
-                remote_arrive(map_rank(&cs->stats_done[q % kSlots], (uint32_t)(j % kCl)));
+                remote_arrive_relaxed(map_rank(&cs->stats_done[q % kSlots], (uint32_t)(j % kCl)));
             }
         };
 
@@ -392,7 +412,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 }
                 it.kind = 0;
                 it.j = sc.j;
-                it.idx = sc.i - sc.lo;
+                it.idx = sc.i;  // window within the pair
                 it.t0 = sc.i * kWin;
                 it.cnt = min(kWin, sc.L - it.t0);
                 it.last = sc.i + kCWorkers >= sc.hi;
@@ -423,11 +443,14 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
             const uint32_t kt = ring + slot * kWinBytes, vt = kt + kTileBytes;
             if (it.kind == 0) {
                 const WinStats s = window_stats(kt, vt, it.cnt);
-                if (lane == 0) {
-                    cs->mean[it.j % kSlots][it.idx] = s.mean;
-                    cs->mm[it.j % kSlots][it.idx] = make_float4(s.kmn, s.kmx, s.vmn, s.vmx);
+                if (lane == 0) {  // into the owner's shared memory, completing bytes on its barrier
+                    const uint32_t owner = (uint32_t)(it.j % kCl);
+                    const int qs = (it.j / kCl) % kSlots;
+                    const uint32_t bar = map_rank(&cs->stats_done[qs], owner);
+                    st_async_f32(map_rank(&cs->mean[qs][it.idx], owner), s.mean, bar);
+                    st_async_f4(map_rank(&cs->mm[qs][it.idx], owner), make_float4(s.kmn, s.kmx, s.vmn, s.vmx), bar);
                 }
-                if (it.last) arrive_stats(it.j);  // after this lane's writes (release, cluster scope)
+                if (it.last) arrive_stats(it.j);
             } else if (it.kind == 1) {
                 if ((uint32_t)it.blk < (uint32_t)a.num_blocks)
                     window_quant(a.kpool, a.vpool, a.Hkv, a.bs, it.h, it.t0, it.cnt, it.blk, kt, vt, it.pc);
@@ -480,7 +503,7 @@ int32_t cluster_compress_max_seqlen() { return kClusterMaxWin * kWin; }
 template <int kCl>
 static cudaError_t launch_cluster_size(const ClusterArgs &a, cudaStream_t stream)
 {
-    const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmemT<kClusterMaxWin / kCl>);  // + alignment slack
+    const size_t smem = 1024 + (size_t)kCRingBytes + sizeof(ClusterSmem);  // + alignment slack
     static thread_local int cached_dev = -1, cached_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

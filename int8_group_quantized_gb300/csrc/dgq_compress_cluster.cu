@@ -110,10 +110,6 @@ __device__ __forceinline__ uint32_t map_rank(const void *p, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void remote_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -134,12 +130,6 @@ __device__ __forceinline__ bool test_wait_cluster(uint64_t *bar, uint32_t parity
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
-}
-__device__ __forceinline__ void st_remote_u4(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
 }
 // Asynchronous stores into another CTA's shared memory, each completing its bytes on an mbarrier
 // of that CTA (both addresses from mapa).  They need no fence: the owner observes them through
@@ -163,6 +153,14 @@ __device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t ba
 __device__ __forceinline__ void remote_arrive_relaxed(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrival on another CTA's mbarrier that also announces bytes still to come by st.async (no
+// release: the bytes themselves complete the phase).
+__device__ __forceinline__ void remote_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
 }
 // The owner arms its statistics barrier: its own arrival and the bytes to expect (no release:
 // it publishes nothing).
@@ -325,13 +323,18 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                 make_params(pc.L, k, cut, kmn, kmx, vmn, vmx, rec, pp);  // same values in every lane
             }
             if (lane == 0) a.table[p] = rec;
-            // parameters into every CTA of the cluster (lane r < kCl serves CTA r), then its ready
+            // parameters into every CTA of the cluster (lane r < kCl serves CTA r): the arrival on
+            // its "ready" barrier announces 128 bytes, which the asynchronous stores complete
             if (lane < kCl) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(&pp);
                 const uint32_t dst = map_rank(&cs->par[slot], (uint32_t)lane);
+                const uint32_t bar = map_rank(&cs->ready[slot], (uint32_t)lane);
+                remote_arrive_expect_tx(bar, (uint32_t)sizeof(PairParams));
 #pragma unroll
-                for (int i = 0; i < 8; ++i) st_remote_u4(dst + 16 * i, src[i]);
-                remote_arrive(map_rank(&cs->ready[slot], (uint32_t)lane));
+                for (int i = 0; i < 8; ++i)
+                    st_async_f4(dst + 16 * i, make_float4(__uint_as_float(src[i].x), __uint_as_float(src[i].y),
+                                                          __uint_as_float(src[i].z), __uint_as_float(src[i].w)),
+                                bar);
             }
             __syncwarp();
         }

@@ -757,6 +757,8 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 constexpr int kCombineWarps = 4;
 constexpr int kCombineSlots = 8;    // pieces one warp keeps in flight per round
 constexpr int kCombineCtasPerSm = 8;
+// combine_kernel reads the current value and writes the output with one thread per dimension
+static_assert(kCombineWarps * 32 == kD, "the block merge has exactly one thread per head dimension");
 
 __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine_kernel(AttnArgs a)
 {

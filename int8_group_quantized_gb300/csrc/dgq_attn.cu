@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         int32_t blk = 0;
         if (k < nmine) {
             const TileLoc c = locate_tile(xw0 + kWarpsPerCta * k, s_tpre, s_len, B);
-            if (c.L > 0) blk = __ldg(a.bt + (int64_t)c.b * a.max_blocks + c.j / per_blk);
+            if (c.L > 0) blk = __ldg(a.bt + (int64_t)c.b * a.max_blocks + pow2_div(c.j, per_blk));
             if ((uint32_t)blk >= (uint32_t)a.num_blocks) {  // not a block of the pools: flagged,
                 record_error(a.hdr, kErrBadBlock);          // and block 0 read instead
                 blk = 0;
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         }
         const int32_t blk = __shfl_sync(0xffffffffu, bq_cur, (kn - kb) & 31);
         if (kn < nmine && ic.L > 0) {
-            const int64_t row0 = ((int64_t)blk * Hkv + ic.h) * a.bs + (ic.j % per_blk) * kTile;
+            const int64_t row0 = ((int64_t)blk * Hkv + ic.h) * a.bs + pow2_mod(ic.j, per_blk) * kTile;
             const uint8_t *kp = a.kpool + row0 * kD;
             const uint8_t *vp = a.vpool + row0 * kD;
             // whole 128-byte rows: lane l copies 16-byte column l % 8 of rows 4i + l / 8, stored

@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
                         cur_slot = qc.slot;
                     }
                     it.pc = params;
-                    it.blk = __ldg(a.bt + (int64_t)qc.loc.b * a.max_blocks + (qc.loc.wi * kWin) / a.bs);
+                    it.blk = __ldg(a.bt + (int64_t)qc.loc.b * a.max_blocks + pow2_div(qc.loc.wi * kWin, a.bs));
                     it.h = qc.loc.h;
                 }
             } else if (sc.w >= 0 && (qc.w < 0 || sc.m <= qc.m || sc.w < qc.w + kAhead)) {

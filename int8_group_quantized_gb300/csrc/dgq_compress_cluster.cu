@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                         pc_j = qc.j;
                     }
                     it.pc = params;
-                    it.blk = __ldg(a.bt + (int64_t)qc.b * a.max_blocks + it.t0 / a.bs);
+                    it.blk = __ldg(a.bt + (int64_t)qc.b * a.max_blocks + pow2_div(it.t0, a.bs));
                     if (lane == 0) {
                         fence_proxy_async_smem();  // the slot's earlier reads come before the copy
                         load_window(ring + slot * kWinBytes, full + slot, a.src, qc.b, qc.h, qc.c0, it.t0,

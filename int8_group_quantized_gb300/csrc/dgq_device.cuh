@@ -24,6 +24,11 @@ __device__ __forceinline__ int32_t ngroups(int32_t L)
     return g < 5 ? g : 5;
 }
 
+// Block sizes are powers of two (16, 32 or 64 tokens, checked on the host), so the block and the
+// slot of a token index t >= 0 come from a shift and a mask instead of an integer division.
+__device__ __forceinline__ int32_t pow2_div(int32_t t, int32_t n) { return t >> (__ffs(n) - 1); }
+__device__ __forceinline__ int32_t pow2_mod(int32_t t, int32_t n) { return t & (n - 1); }
+
 // Every workspace starts with this 256-byte header.
 struct WsHeader {
     uint32_t error;        // first device-side error code (0 = none)

@@ -113,7 +113,7 @@ __device__ __forceinline__ void window_quant_split(uint8_t *kpool, uint8_t *vpoo
     const int sv = __popc(__ballot_sync(0xffffffffu, lane >= 1 && lane < kMaxSeg && pv.start <= t0));
     const float kmn = __shfl_sync(0xffffffffu, pk.kmn, sk), kinv = __shfl_sync(0xffffffffu, pk.kinv, sk);
     const float vmn = __shfl_sync(0xffffffffu, pv.vmn, sv), vinv = __shfl_sync(0xffffffffu, pv.vinv, sv);
-    const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + (t0 % bs)) * kD + sub * 8;
+    const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + pow2_mod(t0, bs)) * kD + sub * 8;
     const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
     const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
 #pragma unroll
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_window_kernel(const __g
         } else {
             const PairCache pc = load_params(a.params + pair);
             int32_t blk = -1;
-            if (t0 / a.bs < a.max_blocks) blk = __ldg(a.bt + (int64_t)l.b * a.max_blocks + t0 / a.bs);
+            if (pow2_div(t0, a.bs) < a.max_blocks) blk = __ldg(a.bt + (int64_t)l.b * a.max_blocks + pow2_div(t0, a.bs));
             if ((uint32_t)blk < (uint32_t)a.num_blocks) {
                 if (split)
                     window_quant_split(a.kpool, a.vpool, Hkv, a.bs, l.h, t0, cnt, blk, kt, vt, pc,

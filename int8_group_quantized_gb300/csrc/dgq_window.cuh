@@ -144,14 +144,14 @@ __device__ __forceinline__ void load_window(uint32_t dst, uint64_t *bar, const T
         tma_load_4d_hint(dst, &s.k, 0, 0, h, c0 + t0, smem_u32(bar), pol);
         tma_load_4d_hint(dst + kTileBytes, &s.v, 0, 0, h, c0 + t0, smem_u32(bar), pol);
     } else {
-        int32_t blk = __ldg(s.bt + (int64_t)b * s.max_blocks + t0 / s.bs);
+        int32_t blk = __ldg(s.bt + (int64_t)b * s.max_blocks + pow2_div(t0, s.bs));
         if ((uint32_t)blk >= (uint32_t)s.num_blocks) {
             record_error(hdr, kErrBadBlock);
             blk = 0;
         }
         mbar_arrive_expect_tx(bar, kWinBytes);
-        tma_load_5d_hint(dst, &s.k, 0, 0, t0 % s.bs, h, blk, smem_u32(bar), pol);
-        tma_load_5d_hint(dst + kTileBytes, &s.v, 0, 0, t0 % s.bs, h, blk, smem_u32(bar), pol);
+        tma_load_5d_hint(dst, &s.k, 0, 0, pow2_mod(t0, s.bs), h, blk, smem_u32(bar), pol);
+        tma_load_5d_hint(dst + kTileBytes, &s.v, 0, 0, pow2_mod(t0, s.bs), h, blk, smem_u32(bar), pol);
     }
 }
 
@@ -347,7 +347,7 @@ __device__ __forceinline__ void window_quant(uint8_t *kpool, uint8_t *vpool, int
     const int s = __popc(ballot);
     const float kmn = __shfl_sync(0xffffffffu, pc.kmn, s), kinv = __shfl_sync(0xffffffffu, pc.kinv, s);
     const float vmn = __shfl_sync(0xffffffffu, pc.vmn, s), vinv = __shfl_sync(0xffffffffu, pc.vinv, s);
-    const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + (t0 % bs)) * kD + sub * 8;
+    const int64_t dst0 = (((int64_t)blk * Hkv + h) * bs + pow2_mod(t0, bs)) * kD + sub * 8;
     const uint64_t kinv2 = f2_pack(__float_as_uint(kinv), __float_as_uint(kinv));
     const uint64_t vinv2 = f2_pack(__float_as_uint(vinv), __float_as_uint(vinv));
 #pragma unroll

@@ -714,8 +714,10 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         const int d = tid;  // thread d owns output column d
         const float vn = bf16lo_to_f32((uint32_t)reinterpret_cast<const uint16_t *>(pb + kPbVnew)[d]);
         uint16_t *orow = a.out + ((int64_t)cur.b * a.Hq + cur.h * G) * kD + d;
-        const int32_t cfirst = owner(cur.fp, T, ncta);
-        const int32_t clast = owner(cur.fp + cur.ntl - 1, T, ncta);
+        // CTAs holding the pair's first and last tiles (this CTA unless the pair leaves its slice;
+        // the division only for such pairs)
+        const int32_t cfirst = cur.fp >= c0 ? cta : owner(cur.fp, T, ncta);
+        const int32_t clast = cur.fp + cur.ntl <= c1 ? cta : owner(cur.fp + cur.ntl - 1, T, ncta);
         for (int g = 0; g < G; ++g) {
             float M = -INFINITY, L = 0.0f, O = 0.0f;
 #pragma unroll

@@ -9,11 +9,13 @@
 // GPU design.
 //  * Work: every (request, KV head) pair is cut into 16-token tiles (a tile never crosses a
 //    block, since block sizes are multiples of 16, nor a segment, since segment starts are);
-//    all tiles of all pairs form one flat list and each persistent CTA takes an equal
-//    contiguous slice of it, so mixed lengths and a single long request balance alike.  The
-//    four warps of a CTA take every fourth tile of the slice and combine their softmax states
-//    in shared memory wherever the slice crosses from one pair to the next.  A CTA's part of a
-//    pair is a "piece".  A pair inside one CTA is finished there; the pieces of a pair shared by
+//    all tiles of all pairs form one flat list and each persistent CTA takes a contiguous
+//    slice of it, so mixed lengths and a single long request balance alike.  The slices are
+//    equal in cost, a pair costing its tiles plus a fixed charge for the end of a piece
+//    (measured on this GPU: with slices equal in tiles, CTAs over many short pairs ran up to
+//    16% longer than the mean and set the kernel's time).  The four warps of a CTA take every
+//    fourth tile of the slice and combine their softmax states in shared memory wherever the
+//    slice crosses from one pair to the next.  A CTA's part of a pair is a "piece".  A pair inside one CTA is finished there; the pieces of a pair shared by
 //    several CTAs go to a small combine kernel chained with programmatic dependent launch, which
 //    folds them in a fixed order (bitwise reproducible on a given GPU) with the current token.
 //    The next pieces' record, query rows and current key/value are staged in shared memory by
@@ -69,6 +71,7 @@ constexpr int kPartStride = 132;                   // floats per (piece, head) p
 constexpr int32_t kMaxGroup = 8;                   // largest query-head group the entry points accept
 constexpr float kLog2eOverSqrtD = 0.12751743074570180f;  // log2(e) / sqrt(128)
 constexpr float kLazyRescale = 8.0f;               // log2 units
+constexpr int32_t kPieceCost = 10;                 // tile times a piece's end costs a CTA (measured)
 
 struct AttnArgs {
     const uint16_t *q;
@@ -85,6 +88,7 @@ struct AttnArgs {
     uint16_t *out;
     WsHeader *hdr;
     int2 *pair_info;  // per pair: first and last CTA holding a piece of it
+    int32_t *held;    // per CTA of the main kernel: 1 when its slice holds tiles
     float *part;
     int32_t B, Hq, Hkv, G, bs, max_blocks, num_blocks;
 };
@@ -218,15 +222,42 @@ __device__ __forceinline__ void advance(TileLoc &c, const int32_t *s_len, int32_
     }
 }
 
-// CTA owning flat tile x when T tiles are split evenly over n CTAs
-__device__ __forceinline__ int32_t owner(int32_t x, int32_t T, int32_t n)
+// The CTAs split the flat tile list evenly by cost, not by tiles: each pair costs its tiles plus
+// kPieceCost, what the end of a piece (the warps' wait for the piece's last tile, the merge, the
+// staging of the next piece) takes in tile times of a CTA.  Pair p's tiles sit at cost positions
+// x + kPieceCost (p + 1) (x its flat tile index) and CTA c of n takes the tiles whose positions
+// fall in [C c / n, C (c + 1) / n), C = T + kPieceCost * pairs.
+
+// Tiles whose cost position is below q (q in [0, C]); s_tpre: tile prefix over requests [B + 1].
+__device__ __forceinline__ int32_t tile_at(int64_t q, const int32_t *s_tpre, const int32_t *s_len, int32_t B,
+                                           int32_t Hkv)
 {
-    return (int32_t)((((int64_t)x + 1) * n - 1) / T);
+    const int64_t kh = (int64_t)kPieceCost * Hkv;
+    int32_t lo = 0, hi = B;  // the last request whose cost range starts at or below q (B: the end)
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (s_tpre[mid] + kh * mid <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    if (lo == B) return s_tpre[B];
+    const int32_t ntl = tiles_of(s_len[lo]);
+    const int32_t r = (int32_t)(q - (s_tpre[lo] + kh * lo));  // < Hkv * (ntl + kPieceCost)
+    const int32_t u = ntl + kPieceCost;
+    const int32_t h = r / u;
+    const int32_t j = r - h * u - kPieceCost;  // < ntl
+    return s_tpre[lo] + h * ntl + max(0, j);
 }
 
-__device__ __forceinline__ bool owns_tiles(int32_t w, int32_t T, int32_t n)
+// Workspace header word: 1 when every CTA of the main kernel holds tiles.  That is so when each
+// CTA's cost range is longer than kPieceCost: runs of positions without a tile are at most
+// kPieceCost long.
+constexpr int kHdrAllHeld = 0;
+
+// CTA holding flat tile x of pair p
+__device__ __forceinline__ int32_t owner(int32_t x, int32_t p, int64_t C, int32_t n)
 {
-    return ((int64_t)(w + 1) * T) / n > ((int64_t)w * T) / n;
+    const int64_t pos = (int64_t)x + (int64_t)kPieceCost * (p + 1);
+    return (int32_t)(((pos + 1) * n - 1) / C);
 }
 
 // Final softmax merge with the current token: (O + p_new v_new) / (L + p_new), where (M, L, O)
@@ -287,8 +318,6 @@ constexpr int kPbRec = 0, kPbKnew = 128, kPbVnew = 384, kPbQ = 640, kPbRecV = kP
 template <int Fmt>
 __host__ __device__ constexpr int piece_bytes() { return kPbRecV + (Fmt == kDecSplitV ? 128 : 0); }
 
-// Workspace header words used to hand the split to the combine kernel.
-constexpr int kHdrTiles = 0, kHdrCtas = 1;
 
 template <int Fmt>
 __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnArgs a)
@@ -341,13 +370,12 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
     __syncthreads();
 
     const int32_t T = s_tpre[B];
+    const int64_t C = (int64_t)T + (int64_t)kPieceCost * B * Hkv;  // total cost
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
-    if (cta == 0 && tid == 0) {
-        a.hdr->pad[kHdrTiles] = (uint32_t)T;
-        a.hdr->pad[kHdrCtas] = (uint32_t)ncta;
-    }
-    const int32_t c0 = (int32_t)(((int64_t)T * cta) / ncta);
-    const int32_t c1 = (int32_t)(((int64_t)T * (cta + 1)) / ncta);
+    const int32_t c0 = tile_at(C * cta / ncta, s_tpre, s_len, B, Hkv);
+    const int32_t c1 = tile_at(C * (cta + 1) / ncta, s_tpre, s_len, B, Hkv);
+    if (tid == 0) a.held[cta] = c0 < c1 ? 1 : 0;  // read by the merge kernels
+    if (cta == 0 && tid == 0) a.hdr->pad[kHdrAllHeld] = C / ncta > kPieceCost ? 1u : 0u;
     if (c0 >= c1) return;  // the whole CTA: no barrier follows for it
 
     const int r = lane >> 2, cq = lane & 3;
@@ -716,8 +744,8 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
         uint16_t *orow = a.out + ((int64_t)cur.b * a.Hq + cur.h * G) * kD + d;
         // CTAs holding the pair's first and last tiles (this CTA unless the pair leaves its slice;
         // the division only for such pairs)
-        const int32_t cfirst = cur.fp >= c0 ? cta : owner(cur.fp, T, ncta);
-        const int32_t clast = cur.fp + cur.ntl <= c1 ? cta : owner(cur.fp + cur.ntl - 1, T, ncta);
+        const int32_t cfirst = cur.fp >= c0 ? cta : owner(cur.fp, p, C, ncta);
+        const int32_t clast = cur.fp + cur.ntl <= c1 ? cta : owner(cur.fp + cur.ntl - 1, p, C, ncta);
         for (int g = 0; g < G; ++g) {
             float M = -INFINITY, L = 0.0f, O = 0.0f;
 #pragma unroll
@@ -752,13 +780,13 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 }
 
 // Merge of the pieces of every pair that several CTAs share, after the main kernel
-// (programmatic dependent launch).  One item per (pair, query head); a grid of at most 8 CTAs
-// per SM walks the items, so the whole merge is one wave of small CTAs that can already be
-// resident while the main kernel runs.  Pieces are folded in CTA order and the current token
+// (programmatic dependent launch).  One item per (pair, query head); a grid of at most 4 CTAs
+// per SM walks the items (at 128 registers a thread the slot arrays below stay in registers),
+// and these small CTAs can already be resident while the main kernel runs.  Pieces are folded in CTA order and the current token
 // is added last, as in the single-piece path; all pieces of an item are fetched in one round.
 constexpr int kCombineWarps = 4;
 constexpr int kCombineSlots = 8;    // pieces one warp keeps in flight per round
-constexpr int kCombineCtasPerSm = 8;
+constexpr int kCombineCtasPerSm = 4;  // 128 registers a thread: the slot arrays stay in registers
 // combine_kernel reads the current value and writes the output with one thread per dimension
 static_assert(kCombineWarps * 32 == kD, "the block merge has exactly one thread per head dimension");
 
@@ -787,9 +815,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
         const int2 info = __ldcg(a.pair_info + p);
         const int32_t cfirst = info.x, clast = info.y;
         if (cfirst == clast) continue;  // finished inside the main kernel
-        const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
-        const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
-        const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
+        const bool all_held = __ldcg(&a.hdr->pad[kHdrAllHeld]) != 0;  // no slot is empty
 
         // warp w folds slots cfirst + w, + 4, ...: per slot its (m, l) and this lane's 4 columns of O
         float m_w = -INFINITY, l_w = 0.0f;
@@ -803,12 +829,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
                 mm[i] = -INFINITY;
                 ll[i] = 0.0f;
                 oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
+                if (cc <= clast) {
                     const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
                     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
                     mm[i] = ml.x;
                     ll[i] = ml.y;
                     oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+                }
+            }
+            // the slot of a CTA whose slice is empty holds stale data (no piece of this call
+            // writes it): dropped
+            if (!all_held) {
+#pragma unroll
+                for (int i = 0; i < kCombineSlots; ++i) {
+                    const int32_t cc = base + i * kCombineWarps;
+                    if (cc <= clast && __ldcg(a.held + cc) == 0) {
+                        mm[i] = -INFINITY;
+                        ll[i] = 0.0f;
+                        oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
             }
 #pragma unroll
@@ -887,9 +926,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
         const int2 info = __ldcg(a.pair_info + p);
         const int32_t cfirst = info.x, clast = info.y;
         if (cfirst == clast) continue;  // finished inside the main kernel
-        const int32_t T = (int32_t)__ldcg(&a.hdr->pad[kHdrTiles]);
-        const int32_t ncta = (int32_t)__ldcg(&a.hdr->pad[kHdrCtas]);
-        const bool all_own = T >= ncta;  // every CTA holds at least one tile: no slot is empty
+        const bool all_held = __ldcg(&a.hdr->pad[kHdrAllHeld]) != 0;  // no slot is empty
         float M = -INFINITY, L = 0.0f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int32_t base = cfirst; base <= clast; base += kCombineSlots) {
@@ -901,12 +938,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineCtasPerSm) combine
                 mm[i] = -INFINITY;
                 ll[i] = 0.0f;
                 oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (cc <= clast && (all_own || owns_tiles(cc, T, ncta))) {
+                if (cc <= clast) {
                     const float *src = a.part + ((int64_t)(p + cc) * G + g) * kPartStride;
                     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src));
                     mm[i] = ml.x;
                     ll[i] = ml.y;
                     oo[i] = __ldcg(reinterpret_cast<const float4 *>(src + 4) + lane);
+                }
+            }
+            // the slot of a CTA whose slice is empty holds stale data (no piece of this call
+            // writes it): dropped
+            if (!all_held) {
+#pragma unroll
+                for (int i = 0; i < kCombineSlots; ++i) {
+                    const int32_t cc = base + i;
+                    if (cc <= clast && __ldcg(a.held + cc) == 0) {
+                        mm[i] = -INFINITY;
+                        ll[i] = 0.0f;
+                        oo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
             }
 #pragma unroll
@@ -963,6 +1013,8 @@ AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm)
     size_t off = sizeof(WsHeader);
     l.off_count = off;  // per-pair piece range (int2)
     off = (off + P * 8 + 255) & ~size_t(255);
+    l.off_held = off;  // per CTA of the main kernel (int32)
+    off = (off + (size_t)attn_max_ctas(nsm) * 4 + 255) & ~size_t(255);
     l.off_part = off;
     off += (P + (size_t)attn_max_ctas(nsm)) * G * kPartStride * 4;
     l.total = (off + 255) & ~size_t(255);
@@ -995,6 +1047,7 @@ cudaError_t launch_attn(int32_t format, const void *q, const void *knew, const v
     a.out = static_cast<uint16_t *>(out);
     a.hdr = reinterpret_cast<WsHeader *>(base);
     a.pair_info = reinterpret_cast<int2 *>(base + l.off_count);
+    a.held = reinterpret_cast<int32_t *>(base + l.off_held);
     a.part = reinterpret_cast<float *>(base + l.off_part);
     a.B = B;
     a.Hq = Hq;

@@ -49,7 +49,7 @@ cudaError_t launch_compress_cluster(const SourceDesc &src, const int32_t *cu, in
                                     dgq_seg_record *table, void *ws, GroupSettings gs, cudaStream_t stream);
 
 struct AttnLayout {
-    size_t off_count, off_part, total;
+    size_t off_count, off_held, off_part, total;
 };
 AttnLayout attn_layout(int32_t batch, int32_t Hq, int32_t Hkv, int nsm);
 // format: a dgq_format (DGQ and SYM_INT8 decode through the records; kpar / vpar are read for

@@ -121,3 +121,38 @@ def test_both_merge_kernels_with_split_pairs(lens, hq, hkv, expect):
     case = Case(lens, hq=hq, hkv=hkv, bs=16, seed=61 + len(lens))
     compress_and_attend(case)
     assert int(case.d_aws[4:8].cpu().numpy().view(np.uint32)[0]) == expect
+
+
+def _empty_slices(lens, hkv, ncta, piece_cost=10):
+    """CTAs of the decode kernel whose slice holds no tile when the flat tile list (16-token tiles,
+    at least one per pair) is split evenly by cost, a pair costing its tiles plus piece_cost: a
+    model of the launch layout, used only to show that a case reaches the path it is meant for."""
+    tiles = [max(1, -(-int(L) // 16)) for L in lens for _ in range(hkv)]
+    C = sum(tiles) + piece_cost * len(tiles)
+    starts, pos = [], 0  # cost position of every tile
+    for n in tiles:
+        starts.extend(range(pos + piece_cost, pos + piece_cost + n))
+        pos += piece_cost + n
+    held = set(((p + 1) * ncta - 1) // C for p in starts)
+    return ncta - len(held)
+
+
+@pytest.mark.parametrize("B,lmax,expect", [
+    (150, 100, MERGE_WARP),   # 300 short pairs: one pair per two CTAs or more, warp merge
+    (100, 200, MERGE_BLOCK),  # 200 short pairs: fewer, block merge
+])
+def test_split_pairs_around_empty_slices(B, lmax, expect):
+    # Many short pairs: the per-piece charge of the cost split exceeds some CTAs' share of the
+    # total cost, so those CTAs hold no tile although the tiles outnumber the CTAs; the merges must
+    # skip their slots.  Word 3 of the decode workspace header is 0 when some slice is empty.
+    import torch
+    lens = np.random.default_rng(B).integers(0, lmax + 1, B).astype(np.int32)
+    hkv = 2
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    ncta = min(3 * nsm, B * hkv * -(-int(lens.max()) // 16))
+    assert sum(hkv * max(1, -(-int(L) // 16)) for L in lens) >= ncta
+    assert _empty_slices(lens, hkv, ncta) > 0
+    case = Case(lens, hq=8, hkv=hkv, bs=16, seed=90 + B)
+    compress_and_attend(case)
+    words = case.d_aws[:16].cpu().numpy().view(np.uint32)
+    assert int(words[1]) == expect and int(words[3]) == 0

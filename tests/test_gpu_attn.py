@@ -123,7 +123,7 @@ def test_both_merge_kernels_with_split_pairs(lens, hq, hkv, expect):
     assert int(case.d_aws[4:8].cpu().numpy().view(np.uint32)[0]) == expect
 
 
-def _empty_slices(lens, hkv, ncta, piece_cost=10):
+def _empty_slices(lens, hkv, ncta, piece_cost):
     """CTAs of the decode kernel whose slice holds no tile when the flat tile list (16-token tiles,
     at least one per pair) is split evenly by cost, a pair costing its tiles plus piece_cost: a
     model of the launch layout, used only to show that a case reaches the path it is meant for."""
@@ -151,7 +151,7 @@ def test_split_pairs_around_empty_slices(B, lmax, expect):
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     ncta = min(3 * nsm, B * hkv * -(-int(lens.max()) // 16))
     assert sum(hkv * max(1, -(-int(L) // 16)) for L in lens) >= ncta
-    assert _empty_slices(lens, hkv, ncta) > 0
+    assert _empty_slices(lens, hkv, ncta, piece_cost=10) > 0  # the kernel's charge per piece end
     case = Case(lens, hq=8, hkv=hkv, bs=16, seed=90 + B)
     compress_and_attend(case)
     words = case.d_aws[:16].cpu().numpy().view(np.uint32)

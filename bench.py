@@ -480,6 +480,45 @@ def time_other_workload(cfg, dev, sp, peak, steps=5, warmup=2):
             "decode_bytes_per_layer": dec_b, "compress_bytes_per_layer": comp_b, "device_error": err}
 
 
+def time_graph_step(dgq, layers, d_cu, d_bt, d_lens, max_seqlen, bs, cws, aws, pws, paged, dec_b, comp_b, peak,
+                    steps, warmup=3):
+    """The step (compress, decode, append of every layer) captured into three CUDA graphs, one per
+    phase, and replayed: the same launches as the main run without the per-launch host and
+    submission cost.  Timed like the main run (CUDA events around each phase's replay)."""
+    import torch
+    s = torch.cuda.Stream()
+    fn = StepFns(dgq, layers, d_cu, d_bt, d_lens, max_seqlen, bs, cws, aws, pws, s.cuda_stream, paged)
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for phase in (fn.compress_all, fn.decode_all, fn.append_all):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            phase()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        for i, g in enumerate(graphs):
+            e[i].record(cur)
+            g.replay()
+        e[3].record(cur)
+    torch.cuda.synchronize()
+    err = dgq.dgq_workspace_error(cws) or dgq.dgq_workspace_error(aws) or dgq.dgq_workspace_error(pws)
+    nl = len(layers)
+    us = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / (steps * nl) * 1e3 for i in range(3)]
+    return {"what": "each phase of the step (every layer's launches) captured into one CUDA graph and replayed; "
+                    "CUDA events around each replay",
+            "steps": steps, "compress_us_per_layer": round(us[0], 2),
+            "compress_gbs": round(comp_b / us[0] / 1e3, 1), "decode_us_per_layer": round(us[1], 2),
+            "decode_gbs": round(dec_b / us[1] / 1e3, 1), "decode_frac_of_peak": round(dec_b / us[1] / 1e3 / peak, 4),
+            "append_us_per_layer": round(us[2], 2), "device_error": int(err)}
+
+
 def time_compress_e2e(w, layers, d_cu, d_bt, max_seqlen, bs, cws, sp, comp_b, nlayers=4, reps=3):
     """Compression end to end through the C ABI: per layer, the bf16 K/V come from pinned host
     memory (one copy each), dgq_compress writes the layer's pools and records, and the records go
@@ -669,9 +708,13 @@ def run_ours(args):
         formats = time_formats(w, lens, layers, d_cu, d_bt, d_lens, max_seqlen, aws, sp, dec_b, ref0,
                                max(3, min(args.steps, 10)))
 
+    peak, peak_src = measured_peak()
+    graph = None
+    if rank == 0:
+        graph = time_graph_step(dgq, layers, d_cu, d_bt, d_lens, max_seqlen, bs, cws, aws, pws, args.paged_input,
+                                dec_b, comp_b, peak, max(5, min(args.steps, 20)))
     total_ms, comp_ms, dec_ms, app_ms, e2e_ms = max_over_ranks([total_ms, comp_ms, dec_ms, app_ms, e2e_ms], dev,
                                                               world)
-    peak, peak_src = measured_peak()
     others = None
     if world == 1 and not args.no_others:  # the other workloads, each with every layer resident
         del layers, step_in, step_out, fn, compress_all, decode_all, append_all
@@ -735,6 +778,7 @@ def run_ours(args):
             "independent_v_segmentation": split_v,
             "formats": formats,
             "compress_e2e": comp_e2e,
+            "graph": graph,
             "other_workloads": others,
             "gpu_launches": 4 * nl * K,  # per layer: compress, attention, merge, append
             "clocks": clk,

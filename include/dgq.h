@@ -35,6 +35,13 @@
  *     limit) for the device it last ran on, per host thread; host threads share no library
  *     state, so calls from several threads at once are safe (each on its own stream and
  *     workspace, as above), on any number of devices.
+ *   - CUDA graphs: every compute call (compress, decode, append, the prefill calls, the
+ *     comparison formats) enqueues only kernel launches and workspace memsets on its stream,
+ *     with no host synchronisation, so it may be captured into a graph on a capturing stream;
+ *     a replay does what the call does.  Make one call on the device and host thread first
+ *     (outside the capture) so that the launcher's per-device setup is done; the decode merge's
+ *     programmatic dependent launch becomes a programmatic edge of the graph.
+ *     dgq_workspace_error reads the workspace back and synchronises: not inside a capture.
  */
 #ifndef DGQ_H
 #define DGQ_H

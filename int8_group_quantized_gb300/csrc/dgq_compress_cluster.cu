@@ -25,8 +25,9 @@
 //  * Workers quantise a pair once its parameters are ready, re-reading its K/V (read a few
 //    microseconds earlier, so from L2; the re-read carries an evict-first hint and takes the
 //    CTA's windows in the reverse of their first-read order), and meanwhile
-//    compute statistics of at most kSlots - 1 later pairs: a cluster holds at most kSlots pairs
-//    (2 MB) between first read and re-read, the whole GPU about 70 MB.
+//    compute statistics of the next pair (kSlots - 1 later pairs; with clusters of 2 at most two
+//    windows per worker of it, see stats_ahead): a cluster holds at most kSlots pairs (2 MB)
+//    between first read and re-read, the whole GPU about 70 MB.
 //  * Twelve workers and one segmentation warp per CTA (127 registers a thread): measured on
 //    this GPU, 12 workers with 2 pair slots took 104 us per layer of the Llama-3-8B batch-32
 //    workload where 10 workers with 3 slots took 120 us.
@@ -56,6 +57,15 @@ static_assert(kCRing == 2, "the worker loop alternates two ring slots");
 constexpr int kCRingBytes = kCWorkers * kCRing * kWinBytes;
 constexpr int kSlots = 2;                                // pairs a cluster holds at once
 constexpr int32_t kClusterMaxWin = 256;                  // pairs of at most 256 windows (4096 tokens)
+
+// Statistics of the next pair run at most this many windows per worker ahead of the pair being
+// quantised.  Clusters of 2 (calls with many pairs, mostly short: DRAM-bound) keep the read-ahead
+// short so that more of the quantisation's re-read still finds its windows in L2 (measured on the
+// MHA batch, per layer: 579 us without a cap, 561 with 2 windows, 566 with 3, 595 with 1).
+// Clusters of 4 (few long pairs: latency-bound) need the read-ahead to cover segmentation and
+// take no cap (2 windows measured 13% slower on the Llama-shaped batch).
+template <int kCl>
+__host__ __device__ constexpr int32_t stats_ahead() { return kCl == 2 ? 2 : kClusterMaxWin; }
 static_assert(kClusterMaxWin == 8 * 32, "segment_small holds 8 windows per lane");
 
 struct ClusterArgs {
@@ -413,6 +423,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_cluster_kernel(const __
                     start_pair(sc, sgeo, sc.j + 1);
                     continue;
                 }
+                if (sc.j > qc.j && sc.i >= sc.lo + warp + stats_ahead<kCl>() * kCWorkers)
+                    return false;  // far enough ahead: quantisation of pair qc.j comes first
                 it.kind = 0;
                 it.j = sc.j;
                 it.idx = sc.i;  // window within the pair

@@ -10,7 +10,8 @@
 // GPU design: one persistent cooperative kernel, one CTA per SM: 10 worker warps, an
 // arrival warp and a segmentation warp.
 //  * The flat list of all 16-token windows of all (request, head) pairs, in (request, head,
-//    window) order, is cut into chunks of kChunk windows (256 MB of bf16 K+V).  Workers
+//    window) order, is cut into chunks of 128-256 MB of bf16 K+V (at least four of the call's
+//    longest pairs; see kChunkMax).  Workers
 //    compute window statistics (variance mean; K and V min/max, also folded into aggregates
 //    of 64 windows with exact order-preserving integer atomics) for their CTA's share of
 //    each chunk.  Quantisation range m holds the pairs whose last window lies in chunk m; it
@@ -19,10 +20,11 @@
 //    chunk's statistics (one release store per CTA and chunk, to a word of its own, so CTAs
 //    may run several chunks apart), and only waits for the other CTAs when it is about to
 //    quantise range m.  Meanwhile its workers keep computing statistics of later chunks, up
-//    to kAhead windows (three chunks) past their quantisation position, so that they keep
-//    streaming while a range is segmented.  Measured on this GPU (one 131072-token request;
-//    64 requests of 128-32768 tokens): 64 MB chunks with a 128 MB lead took 340 / 790 us per
-//    layer, 256 MB chunks with a 768 MB lead 232 / 664 us.  Most second reads then come from
+//    to a lead of 512-768 MB past their quantisation position, so that they keep streaming
+//    while a range is segmented.  Measured on this GPU (one 131072-token request; 64 requests
+//    of 128-32768 tokens): 64 MB chunks with a 128 MB lead took 340 / 790 us per layer, 256 MB
+//    chunks with a 768 MB lead 232 / 655 us, 128 MB chunks with a 512 MB lead 251 / 629 us
+//    (long pairs want the larger chunks, shorter ones the smaller).  Most second reads come from
 //    DRAM rather than L2 (they carry an evict-first hint); fewer segmentation stalls matter
 //    more here than L2 reuse.
 //  * Under full HBM load every dependent round trip through L2 costs microseconds, so all
@@ -58,8 +60,13 @@ constexpr int kThreads = (kWorkers + 2) * 32;
 constexpr int kRing = 2;                   // windows in flight per worker
 static_assert(kRing == 2, "the worker loop alternates two ring slots");
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
-constexpr int32_t kChunk = 32768;          // windows per chunk: 256 MB of K+V
-constexpr int32_t kAhead = 98304;          // statistics may lead quantisation by this many windows
+// Windows per chunk, chosen per call: at least four of the call's longest pairs, between 16384
+// and kChunkMax (128 to 256 MB of K+V); statistics may lead quantisation by max(65536 windows,
+// three chunks).  Measured per layer (one 131072-token request / 64 requests of 128-32768
+// tokens, us): 256 MB chunks with a 768 MB lead 232 / 655; 128 MB with 512 MB 251 / 629; 128 MB
+// with 384 MB 260 / 643; 192 MB with 576 MB 282 / 640; 512 MB with 1 GB 271 / 690.
+constexpr int32_t kChunkMax = 32768;
+constexpr int32_t kChunkMin = 16384;
 constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for
 
 struct CompressArgs {
@@ -77,6 +84,7 @@ struct CompressArgs {
     uint4 *agg;  // per 64 flat windows: ~enc(k min), enc(k max), ~enc(v min), enc(v max); 0 = empty
     int32_t B, Hkv, bs, max_blocks, cap;
     int32_t max_seqlen, num_blocks;  // for the device-side checks of lengths and block ids
+    int32_t chunk, ahead;  // windows per chunk; statistics' lead over quantisation, in windows
     int32_t max_groups;  // group-selection settings
     float min_var;
 };
@@ -504,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
     if (tid == 0) ctl->last = 0;
     const int32_t Wtot = s_wpre[B];
     if (blockIdx.x == 0 && tid == 0) a.hdr->path = kPathGrid;
-    const int32_t M = (Wtot + kChunk - 1) / kChunk;  // chunks (and quantisation ranges)
+    const int32_t chunk = a.chunk;
+    const int32_t M = (Wtot + chunk - 1) / chunk;  // chunks (and quantisation ranges)
     const int32_t ncta = gridDim.x, cta = blockIdx.x;
 
     // empty requests: a record with n_seg = 0
@@ -518,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
     }
 
     // end of the pairs completed by chunk m (the first window of the pair holding window
-    // min((m+1) kChunk, Wtot), or Wtot)
+    // min((m+1) chunk, Wtot), or Wtot)
     auto qend = [&](int32_t m) -> int32_t {
-        const int32_t E = (int32_t)min((int64_t)(m + 1) * kChunk, (int64_t)Wtot);
+        const int32_t E = (int32_t)min((int64_t)(m + 1) * chunk, (int64_t)Wtot);
         if (E >= Wtot) return Wtot;
         return E - locate(E, s_wpre, a.cu, B).wi;
     };
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
     };
     // this CTA's share of chunk m's statistics / of range m's quantisation
     auto stats_share = [&](int32_t m, int32_t &lo, int32_t &hi) {
-        split(m * kChunk, (int32_t)min((int64_t)(m + 1) * kChunk, (int64_t)Wtot), lo, hi);
+        split(m * chunk, (int32_t)min((int64_t)(m + 1) * chunk, (int64_t)Wtot), lo, hi);
     };
     auto quant_share = [&](int32_t m, int32_t &lo, int32_t &hi) {
         split(m == 0 ? 0 : qend(m - 1), qend(m), lo, hi);
@@ -696,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(const __grid_cons
                     it.blk = __ldg(a.bt + (int64_t)qc.loc.b * a.max_blocks + pow2_div(qc.loc.wi * kWin, a.bs));
                     it.h = qc.loc.h;
                 }
-            } else if (sc.w >= 0 && (qc.w < 0 || sc.m <= qc.m || sc.w < qc.w + kAhead)) {
+            } else if (sc.w >= 0 && (qc.w < 0 || sc.m <= qc.m || sc.w < qc.w + a.ahead)) {
                 it.kind = 0;
                 it.w = sc.w;
                 it.m = sc.m;
@@ -817,16 +826,16 @@ namespace dgq {
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Pairs that can overlap one CTA's share of a quantisation range: a range holds at most
-// kChunk + (windows of the longest pair) - 1 windows, and a share of n windows overlaps at
+// kChunkMax + (windows of the longest pair) - 1 windows, and a share of n windows overlaps at
 // most n + 1 pairs.
 static int32_t params_cap(int32_t max_seqlen, int nsm)
 {
     const int64_t wpair = (max_seqlen + kWin - 1) / kWin;
-    return (int32_t)((kChunk + wpair + nsm - 1) / nsm + 2);
+    return (int32_t)((kChunkMax + wpair + nsm - 1) / nsm + 2);
 }
 
 // The layout does not depend on the SM count: nsm * params_cap(.., nsm) is at most
-// kChunk + wpair + 3 * nsm pairs for any nsm <= kMaxSms.
+// kChunkMax + wpair + 3 * nsm pairs for any nsm <= kMaxSms.
 CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv)
 {
     CompressLayout l;
@@ -835,7 +844,7 @@ CompressLayout compress_layout(int32_t batch, int32_t max_seqlen, int32_t Hkv)
     const size_t Wmax = P * wpair;
     size_t off = sizeof(WsHeader);
     l.off_prog = off; off = align256(off + kMaxSms * 4);
-    l.off_params = off; off = align256(off + 2 * (kChunk + wpair + 3 * kMaxSms) * sizeof(PairParams));
+    l.off_params = off; off = align256(off + 2 * (kChunkMax + wpair + 3 * kMaxSms) * sizeof(PairParams));
     l.off_mean = off; off = align256(off + (Wmax + 4) * 4);  // +4: quad reads past the end
     l.off_mm = off; off = align256(off + Wmax * 16);
     l.off_agg = off; off = align256(off + (Wmax / kAgg + 1) * 16);
@@ -878,6 +887,11 @@ cudaError_t launch_compress(const SourceDesc &src, const int32_t *cu, int32_t B,
     a.max_seqlen = max_seqlen;
     a.num_blocks = num_blocks;
     a.max_groups = gs.max_groups;
+    {
+        const int32_t wpair = (max_seqlen + kWin - 1) / kWin;
+        a.chunk = 4 * wpair > kChunkMin ? (4 * wpair < kChunkMax ? 4 * wpair : kChunkMax) : kChunkMin;
+        a.ahead = 3 * a.chunk > 65536 ? 3 * a.chunk : 65536;
+    }
     a.min_var = gs.min_var;
 
     // per-device launch set-up, done once per (device, shared-memory size) and host thread; the

@@ -22,10 +22,11 @@
 //    quantise range m.  Meanwhile its workers keep computing statistics of later chunks, up
 //    to a lead of 512-768 MB past their quantisation position, so that they keep streaming
 //    while a range is segmented; within that lead a worker takes statistics before
-//    quantisation.  Measured on this GPU (one 131072-token request; 64 requests
-//    of 128-32768 tokens): 64 MB chunks with a 128 MB lead took 340 / 790 us per layer, 256 MB
-//    chunks with a 768 MB lead 232 / 655 us, 128 MB chunks with a 512 MB lead 251 / 629 us
-//    (long pairs want the larger chunks, shorter ones the smaller).  Most second reads come from
+//    quantisation.  Measured on this GPU with quantisation first (one 131072-token request; 64
+//    requests of 128-32768 tokens): 64 MB chunks with a 128 MB lead took 340 / 790 us per layer,
+//    256 MB chunks with a 768 MB lead 232 / 655 us, 128 MB chunks with a 512 MB lead 251 / 629 us
+//    (long pairs want the larger chunks, shorter ones the smaller); with statistics first the
+//    chosen rule takes 235 / 601 us, and smaller chunks or leads stay slower.  Most second reads come from
 //    DRAM rather than L2 (they carry an evict-first hint); fewer segmentation stalls matter
 //    more here than L2 reuse.
 //  * Under full HBM load every dependent round trip through L2 costs microseconds, so all
@@ -63,9 +64,11 @@ static_assert(kRing == 2, "the worker loop alternates two ring slots");
 constexpr int kRingBytes = kWorkers * kRing * kWinBytes;
 // Windows per chunk, chosen per call: at least four of the call's longest pairs, between 16384
 // and kChunkMax (128 to 256 MB of K+V); statistics may lead quantisation by max(65536 windows,
-// three chunks).  Measured per layer (one 131072-token request / 64 requests of 128-32768
-// tokens, us): 256 MB chunks with a 768 MB lead 232 / 655; 128 MB with 512 MB 251 / 629; 128 MB
-// with 384 MB 260 / 643; 192 MB with 576 MB 282 / 640; 512 MB with 1 GB 271 / 690.
+// three chunks).  Measured per layer with quantisation first (one 131072-token request / 64
+// requests of 128-32768 tokens, us): 256 MB chunks with a 768 MB lead 232 / 655; 128 MB with
+// 512 MB 251 / 629; 128 MB with 384 MB 260 / 643; 192 MB with 576 MB 282 / 640; 512 MB with 1 GB
+// 271 / 690.  With statistics first, 128 MB chunks with a 384 MB lead took 267 / 618, with a
+// 256 MB lead 282 / 654, and 64 MB chunks 370-379 / 716-733.
 constexpr int32_t kChunkMax = 32768;
 constexpr int32_t kChunkMin = 16384;
 constexpr int kMaxSms = 256;               // largest grid the workspace layout provides for

@@ -15,9 +15,10 @@
 //    (measured on this GPU: with slices equal in tiles, CTAs over many short pairs ran up to
 //    16% longer than the mean and set the kernel's time).  The four warps of a CTA take every
 //    fourth tile of the slice and combine their softmax states in shared memory wherever the
-//    slice crosses from one pair to the next.  A CTA's part of a pair is a "piece".  A pair inside one CTA is finished there; the pieces of a pair shared by
-//    several CTAs go to a small combine kernel chained with programmatic dependent launch, which
-//    folds them in a fixed order (bitwise reproducible on a given GPU) with the current token.
+//    slice crosses from one pair to the next.  A CTA's part of a pair is a "piece".  A pair
+//    inside one CTA is finished there; the pieces of a pair shared by several CTAs go to a
+//    small combine kernel chained with programmatic dependent launch, which folds them in a
+//    fixed order (bitwise reproducible on a given GPU) with the current token.
 //    The next pieces' record, query rows and current key/value are staged in shared memory by
 //    bulk copies while the current piece streams, so a piece boundary waits on no global load.
 //  * Loads: each warp copies its tiles' K and V rows with cp.async (whole 128-byte rows, four
@@ -782,8 +783,11 @@ __global__ void __launch_bounds__(kAttnThreads, kMaxCtasPerSm) attn_kernel(AttnA
 // Merge of the pieces of every pair that several CTAs share, after the main kernel
 // (programmatic dependent launch).  One item per (pair, query head); a grid of at most 4 CTAs
 // per SM walks the items (at 128 registers a thread the slot arrays below stay in registers),
-// and these small CTAs can already be resident while the main kernel runs.  Pieces are folded in CTA order and the current token
-// is added last, as in the single-piece path; all pieces of an item are fetched in one round.
+// and these small CTAs can already be resident while the main kernel runs.  The pieces are
+// folded in a fixed order and the current token is added last, as in the single-piece path:
+// the warp merge folds an item's pieces in CTA order, kCombineSlots loads in flight per round;
+// the block merge gives warp w the pieces of CTAs cfirst + w, + 4, ... (in that order,
+// kCombineSlots per round) and then folds the four warps' states in warp order.
 constexpr int kCombineWarps = 4;
 constexpr int kCombineSlots = 8;    // pieces one warp keeps in flight per round
 constexpr int kCombineCtasPerSm = 4;  // 128 registers a thread: the slot arrays stay in registers
